@@ -1,0 +1,223 @@
+"""ctypes binding of libfused_ce_tvd.so (declared in include/fused_ce_tvd.h).
+
+Argument marshalling only: tensors become device pointers, row strides and
+dtype codes; outputs are allocated with torch when the caller passes none;
+the work is launched on the current torch CUDA stream.  Every step of the
+computation runs in the library's CUDA kernels.  There is no fallback: if
+the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _build
+
+FCT_F32, FCT_BF16 = 0, 1
+FCT_DEV_TARGET_OUT_OF_RANGE = 0x1
+IGNORE_INDEX = -100
+
+_lock = threading.Lock()
+_lib = None
+
+EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "ce_forward", "ce_backward",
+           "fct_status_string", "fct_set_forward_cluster", "fct_version")
+
+
+class FctError(RuntimeError):
+    """A non-zero fct_status returned by the library."""
+
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load (building first if needed) the shared library and declare its ABI."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        lib = ctypes.CDLL(path or _build.build())
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.fused_ce_tvd_forward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                             vp, vp, vp, vp, vp, vp, vp]
+        lib.fused_ce_tvd_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                              vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
+        lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
+        lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
+        for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "ce_forward", "ce_backward"):
+            getattr(lib, f).restype = i32
+        lib.fct_status_string.argtypes = [i32]
+        lib.fct_status_string.restype = ctypes.c_char_p
+        lib.fct_set_forward_cluster.argtypes = [i32]
+        lib.fct_set_forward_cluster.restype = i32
+        lib.fct_version.argtypes = []
+        lib.fct_version.restype = i32
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    return load().fct_status_string(int(status)).decode()
+
+
+def set_forward_cluster(ctas_per_row: int) -> int:
+    """CTAs per row of the fused forward (1, 2, 4, 8; 0 = automatic)."""
+    prev = load().fct_set_forward_cluster(int(ctas_per_row))
+    if prev < 0:
+        raise ValueError("ctas_per_row must be 0, 1, 2, 4 or 8")
+    return prev
+
+
+def version() -> int:
+    return load().fct_version()
+
+
+# ------------------------------------------------------------------ marshalling
+
+def _ptr(t: torch.Tensor | None) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr() if t is not None else None)
+
+
+def _logits(x: torch.Tensor, name: str):
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError(f"{name} must be (BT, V) with unit stride along V")
+    code = {torch.float32: FCT_F32, torch.bfloat16: FCT_BF16}.get(x.dtype)
+    if code is None:
+        raise TypeError(f"{name}: dtype {x.dtype} is not float32 or bfloat16")
+    ld = x.stride(0) if x.shape[0] > 1 else x.shape[1]
+    return code, max(int(ld), int(x.shape[1]))
+
+
+def _rows(x: torch.Tensor, n: int, name: str, dtype=torch.float32) -> torch.Tensor:
+    if not x.is_cuda or x.dtype != dtype or x.dim() != 1 or x.numel() != n or (n > 1 and x.stride(0) != 1):
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} vector of {n} values")
+    return x
+
+
+def _upstream(g, BT: int, device, name: str):
+    """(tensor, grad_stride): a per-row fp32 vector, or one value broadcast."""
+    if not torch.is_tensor(g):
+        g = torch.tensor([float(g)], device=device, dtype=torch.float32)
+    if g.numel() == 1:
+        g = g.reshape(1).to(device=device, dtype=torch.float32)
+        return g, 0
+    return _rows(g, BT, name), 1
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise FctError(rc, what)
+
+
+def _out(x, n, device, name):
+    if x is None:
+        return torch.empty(n, device=device, dtype=torch.float32)
+    return _rows(x, n, name)
+
+
+# ------------------------------------------------------------------ entry points
+
+def fused_ce_tvd_forward(student, teacher, target, ignore_index=IGNORE_INDEX, *, ce=None,
+                         tvd=None, student_lse=None, teacher_lse=None, sigma=None,
+                         dev_status=None, stream=None):
+    """Per-row (ce, tvd, student_lse, teacher_lse, sigma), all fp32 (BT,)."""
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    BT, V = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                                             (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
+    rc = load().fused_ce_tvd_forward(_ptr(student), ld_s, _ptr(teacher), ld_t, code,
+                                     _ptr(target), BT, V, int(ignore_index), *map(_ptr, outs),
+                                     _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_ce_tvd_forward")
+    return tuple(outs)
+
+
+def fused_ce_tvd_backward(student, teacher, target, student_lse, teacher_lse, sigma,
+                          grad_ce, grad_tvd, ignore_index=IGNORE_INDEX, *, grad_student=None,
+                          inplace=False, dev_status=None, stream=None):
+    """Gradient of sum_r grad_ce[r]*ce[r] + grad_tvd[r]*tvd[r] w.r.t. the student.
+
+    ``inplace=True`` writes it over ``student`` and returns ``student``.
+    """
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    BT, V = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    for x, n in ((student_lse, "student_lse"), (teacher_lse, "teacher_lse"), (sigma, "sigma")):
+        _rows(x, BT, n)
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    stride = max(stride_ce, stride_tvd)
+    if inplace:
+        grad_student = student
+    elif grad_student is None:
+        grad_student = torch.empty_like(student)
+    code_g, ld_g = _logits(grad_student, "grad_student")
+    if code_g != code or grad_student.shape != student.shape:
+        raise ValueError("grad_student must match the student's shape and dtype")
+    rc = load().fused_ce_tvd_backward(_ptr(student), ld_s, _ptr(teacher), ld_t, code,
+                                      _ptr(target), BT, V, int(ignore_index), _ptr(student_lse),
+                                      _ptr(teacher_lse), _ptr(sigma), _ptr(gce), _ptr(gtvd),
+                                      stride, _ptr(grad_student), ld_g, _ptr(dev_status),
+                                      _stream(stream))
+    _check(rc, "fused_ce_tvd_backward")
+    return grad_student
+
+
+def ce_forward(logits, target, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,
+               dev_status=None, stream=None):
+    """Per-row (ce, lse) of plain cross-entropy, fp32 (BT,)."""
+    code, ld = _logits(logits, "logits")
+    BT, V = logits.shape
+    _rows(target, BT, "target", torch.int64)
+    ce = _out(ce, BT, logits.device, "ce")
+    lse = _out(lse, BT, logits.device, "lse")
+    rc = load().ce_forward(_ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index),
+                           _ptr(ce), _ptr(lse), _ptr(dev_status), _stream(stream))
+    _check(rc, "ce_forward")
+    return ce, lse
+
+
+def ce_backward(logits, target, lse, grad_ce, ignore_index=IGNORE_INDEX, *, grad_logits=None,
+                inplace=False, dev_status=None, stream=None):
+    """Gradient of sum_r grad_ce[r]*ce[r] w.r.t. the logits."""
+    code, ld = _logits(logits, "logits")
+    BT, V = logits.shape
+    _rows(target, BT, "target", torch.int64)
+    _rows(lse, BT, "lse")
+    gce, stride = _upstream(grad_ce, BT, logits.device, "grad_ce")
+    if inplace:
+        grad_logits = logits
+    elif grad_logits is None:
+        grad_logits = torch.empty_like(logits)
+    code_g, ld_g = _logits(grad_logits, "grad_logits")
+    if code_g != code or grad_logits.shape != logits.shape:
+        raise ValueError("grad_logits must match the logits' shape and dtype")
+    rc = load().ce_backward(_ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index),
+                            _ptr(lse), _ptr(gce), stride, _ptr(grad_logits), ld_g,
+                            _ptr(dev_status), _stream(stream))
+    _check(rc, "ce_backward")
+    return grad_logits

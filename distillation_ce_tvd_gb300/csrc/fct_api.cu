@@ -1,0 +1,262 @@
+// C ABI of libfused_ce_tvd.so: argument checks, launch planning, dispatch.
+// The operations themselves are described in include/fused_ce_tvd.h.
+#include <atomic>
+#include <mutex>
+
+#include "fct_internal.h"
+
+namespace {
+
+struct DeviceInfo {
+  int sms = 0;
+  int l2_bytes = 0;
+  int major = 0, minor = 0;
+  bool ok = false;
+};
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+std::atomic<int> g_cluster_override{0};
+
+// Properties of the calling thread's current device, queried once.
+int current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return FCT_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= 64) return FCT_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ok) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.l2_bytes, cudaDevAttrL2CacheSize, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return FCT_ERR_CUDA;
+    }
+    d.ok = true;
+  }
+  *out = d;
+  // The kernels are built for sm_103a only.
+  if (d.major != 10 || d.minor != 3) return FCT_ERR_UNSUPPORTED;
+  return FCT_OK;
+}
+
+size_t elem_size(int dtype) { return dtype == FCT_BF16 ? 2 : 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte range [lo, hi) covered by a (rows, cols) matrix with row stride ld.
+struct Range {
+  uintptr_t lo, hi;
+};
+Range mat_range(const void* p, int64_t rows, int64_t ld, int64_t cols, size_t e) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + static_cast<uintptr_t>(((rows - 1) * ld + cols) * static_cast<int64_t>(e))};
+}
+Range vec_range(const void* p, int64_t n, size_t e) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + static_cast<uintptr_t>(n * static_cast<int64_t>(e))};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+int check_logits(const void* x, int64_t ld, int dtype, int64_t V) {
+  if (x == nullptr) return FCT_ERR_INVALID_ARG;
+  if (ld < V) return FCT_ERR_INVALID_ARG;
+  if (!aligned(x, elem_size(dtype))) return FCT_ERR_ALIGNMENT;
+  return FCT_OK;
+}
+
+bool vec_ok(const void* x, int64_t ld, int dtype) {
+  return aligned(x, 16) && ((ld * static_cast<int64_t>(elem_size(dtype))) % 16) == 0;
+}
+
+int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
+  if (dtype != FCT_F32 && dtype != FCT_BF16) return FCT_ERR_UNSUPPORTED;
+  if (V <= 0) return FCT_ERR_INVALID_ARG;
+  if (target == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(target, 8)) return FCT_ERR_ALIGNMENT;
+  (void)BT;
+  return FCT_OK;
+}
+
+// Rows in flight and CTAs per row for the two-pass fused forward.  The
+// second pass re-reads each row from L2, so the rows in flight times the
+// bytes of a student+teacher row must stay well inside L2; rows are split
+// over a cluster of C CTAs until every SM still gets at least one CTA.
+// Depends on V, the element type and the device only (never on BT), so
+// results do not depend on how the rows are batched.
+fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec) {
+  fct::FwdPlan plan{vec, 1, 0};
+  if (!tvd) return plan;  // one pass: nothing to keep in L2
+  const double row_bytes = 2.0 * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
+  const double budget = 0.45 * static_cast<double>(d.l2_bytes);
+  int64_t fit = static_cast<int64_t>(budget / row_bytes);
+  if (fit < 1) fit = 1;
+  int C = g_cluster_override.load();
+  if (C == 0) {
+    C = 1;
+    while (C < 8 && fit * C < d.sms) C *= 2;
+  }
+  int64_t per_sm = (fit * C) / d.sms;
+  if (per_sm < 1) per_sm = 1;
+  if (per_sm > 4) per_sm = 4;
+  plan.cluster = C;
+  plan.slots = static_cast<int>((d.sms * per_sm) / C);
+  if (plan.slots < 1) plan.slots = 1;
+  return plan;
+}
+
+int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t ld_t,
+                 int dtype, const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
+                 float* ce, float* tvd, float* lse_s, float* lse_t, float* sigma,
+                 int32_t* dev_status, void* stream) {
+  const bool fused = (tvd != nullptr);
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  int rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
+  if (fused && (rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
+  float* outs[5] = {ce, lse_s, tvd, lse_t, sigma};
+  const int n_out = fused ? 5 : 2;
+  for (int i = 0; i < n_out; ++i) {
+    if (outs[i] == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(outs[i], 4)) return FCT_ERR_ALIGNMENT;
+  }
+  if (dev_status && !aligned(dev_status, 4)) return FCT_ERR_ALIGNMENT;
+  const size_t e = elem_size(dtype);
+  Range ins[3] = {mat_range(student, BT, ld_s, V, e),
+                  fused ? mat_range(teacher, BT, ld_t, V, e) : Range{0, 0},
+                  vec_range(target, BT, 8)};
+  for (int i = 0; i < n_out; ++i) {
+    const Range r = vec_range(outs[i], BT, 4);
+    for (int j = 0; j < 3; ++j)
+      if (overlap(r, ins[j])) return FCT_ERR_INVALID_ARG;
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlap(r, vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
+  }
+
+  DeviceInfo d;
+  if ((rc = current_device(&d)) != FCT_OK) return rc;
+  const bool vec = vec_ok(student, ld_s, dtype) && (!fused || vec_ok(teacher, ld_t, dtype));
+  fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
+                 ce, tvd, lse_s, lse_t, sigma, dev_status};
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec);
+  if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
+int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t ld_t,
+                  int dtype, const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
+                  const float* lse_s, const float* lse_t, const float* sigma,
+                  const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
+                  void* grad, int64_t ld_g, int32_t* dev_status, void* stream) {
+  const bool fused = (teacher != nullptr) || (lse_t != nullptr);
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  int rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
+  if (fused && (rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
+  const float* rows[5] = {lse_s, grad_ce, lse_t, sigma, grad_tvd};
+  const int n_rows = fused ? 5 : 2;
+  for (int i = 0; i < n_rows; ++i) {
+    if (rows[i] == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(rows[i], 4)) return FCT_ERR_ALIGNMENT;
+  }
+  if (dev_status && !aligned(dev_status, 4)) return FCT_ERR_ALIGNMENT;
+  const size_t e = elem_size(dtype);
+  const Range g = mat_range(grad, BT, ld_g, V, e);
+  const bool inplace = (grad == student);
+  if (inplace && ld_g != ld_s) return FCT_ERR_INVALID_ARG;
+  if (!inplace && overlap(g, mat_range(student, BT, ld_s, V, e))) return FCT_ERR_INVALID_ARG;
+  if (fused && overlap(g, mat_range(teacher, BT, ld_t, V, e))) return FCT_ERR_INVALID_ARG;
+  if (overlap(g, vec_range(target, BT, 8))) return FCT_ERR_INVALID_ARG;
+  for (int i = 0; i < n_rows; ++i) {
+    const int64_t n = (i == 1 || i == 4) ? (grad_stride ? BT : 1) : BT;
+    if (overlap(g, vec_range(rows[i], n, 4))) return FCT_ERR_INVALID_ARG;
+  }
+
+  DeviceInfo d;
+  if ((rc = current_device(&d)) != FCT_OK) return rc;
+  const bool vec = vec_ok(student, ld_s, dtype) && vec_ok(grad, ld_g, dtype) &&
+                   (!fused || vec_ok(teacher, ld_t, dtype));
+  fct::BwdArgs a{student, fused ? teacher : nullptr, ld_s, ld_t, dtype, target, BT, V,
+                 ignore_index, lse_s, lse_t, sigma, grad_ce, grad_tvd, grad_stride,
+                 grad, ld_g, dev_status};
+  if (fct::launch_backward(a, vec, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fused_ce_tvd_forward(const void* student, int64_t ld_student, const void* teacher,
+                         int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
+                         int64_t V, int64_t ignore_index, float* ce, float* tvd,
+                         float* student_lse, float* teacher_lse, float* sigma,
+                         int32_t* dev_status, void* stream) {
+  if (teacher == nullptr || tvd == nullptr || teacher_lse == nullptr || sigma == nullptr)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  return forward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                      ignore_index, ce, tvd, student_lse, teacher_lse, sigma, dev_status, stream);
+}
+
+int fused_ce_tvd_backward(const void* student, int64_t ld_student, const void* teacher,
+                          int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                          int64_t BT, int64_t V, int64_t ignore_index, const float* student_lse,
+                          const float* teacher_lse, const float* sigma, const float* grad_ce,
+                          const float* grad_tvd, int64_t grad_stride, void* grad_student,
+                          int64_t ld_grad, int32_t* dev_status, void* stream) {
+  if (teacher == nullptr || teacher_lse == nullptr || sigma == nullptr || grad_tvd == nullptr)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  return backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                       ignore_index, student_lse, teacher_lse, sigma, grad_ce, grad_tvd,
+                       grad_stride, grad_student, ld_grad, dev_status, stream);
+}
+
+int ce_forward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target, int64_t BT,
+               int64_t V, int64_t ignore_index, float* ce, float* lse, int32_t* dev_status,
+               void* stream) {
+  return forward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, ce, nullptr,
+                      lse, nullptr, nullptr, dev_status, stream);
+}
+
+int ce_backward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target,
+                int64_t BT, int64_t V, int64_t ignore_index, const float* lse,
+                const float* grad_ce, int64_t grad_stride, void* grad_logits, int64_t ld_grad,
+                int32_t* dev_status, void* stream) {
+  return backward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, lse, nullptr,
+                       nullptr, grad_ce, nullptr, grad_stride, grad_logits, ld_grad, dev_status,
+                       stream);
+}
+
+const char* fct_status_string(int status) {
+  switch (status) {
+    case FCT_OK: return "FCT_OK";
+    case FCT_ERR_INVALID_ARG: return "FCT_ERR_INVALID_ARG: invalid argument";
+    case FCT_ERR_UNSUPPORTED: return "FCT_ERR_UNSUPPORTED: unsupported dtype or device";
+    case FCT_ERR_ALIGNMENT: return "FCT_ERR_ALIGNMENT: pointer not aligned to its element size";
+    case FCT_ERR_CUDA: return "FCT_ERR_CUDA: CUDA runtime or launch error";
+    default: return "unknown fct_status";
+  }
+}
+
+int fct_set_forward_cluster(int ctas_per_row) {
+  if (ctas_per_row != 0 && ctas_per_row != 1 && ctas_per_row != 2 && ctas_per_row != 4 &&
+      ctas_per_row != 8)
+    return -1;
+  return g_cluster_override.exchange(ctas_per_row);
+}
+
+int fct_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,180 @@
+// Backward kernels of the fused CE + TVD loss and of plain cross-entropy.
+//
+// Method: PR #1384 analysis, section "Backward Pass": with p = softmax(s),
+// q = softmax(t) and sign_v = sign(p_v - q_v),
+//   d ce / d s_v  = p_v - 1[v == target]
+//   d tvd / d s_v = 0.5 * p_v * (sign_v - sigma)     (softmax Jacobian of 0.5*sign)
+// and the kernel reloads both rows, recomputes p, q and the sign from the
+// saved lse values, and writes
+//   grad_v = grad_ce * p_v + grad_tvd * 0.5 * p_v * (sign_v - sigma) - grad_ce * 1[v == target],
+// with zero rows for ignore_index and a zero subgradient at ties.
+//
+// GB300 mapping: a pure stream (2 reads + 1 write per element) cut into
+// units of (row, 1024 vectors); a persistent grid of resident CTAs walks the
+// units.  Per element the coefficient of p takes one of three per-row
+// values picked by the sign, so the inner loop is two ex2, one subtract, two
+// selects and one multiply.  Each element is read and then written by the
+// same thread, which makes grad_student == student (in place) safe.
+#include "fct_common.cuh"
+#include "fct_internal.h"
+
+namespace fct {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kUnroll = 4;
+constexpr int64_t kSeg = int64_t(kThreads) * kUnroll;  // vectors per unit
+
+template <typename T, int VE, bool kTvd>
+__global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
+  const T* S = static_cast<const T*>(a.student);
+  const T* Tt = static_cast<const T*>(a.teacher);
+  T* G = static_cast<T*>(a.grad);
+  const int64_t nvec = a.V / VE;
+  const int64_t tail0 = nvec * VE;
+  const int64_t nseg = nvec > 0 ? (nvec + kSeg - 1) / kSeg : 1;
+  const int64_t units = a.BT * nseg;
+  const uint64_t drop = policy_evict_first();
+
+  for (int64_t unit = blockIdx.x; unit < units; unit += gridDim.x) {
+    const int64_t row = unit / nseg;
+    const int64_t seg = unit - row * nseg;
+    const bool last_seg = (seg == nseg - 1);
+    const int64_t v0 = seg * kSeg;
+    const int64_t v1 = min(nvec, v0 + kSeg);
+    const int64_t tg = a.target[row];
+    const T* srow = S + row * a.ld_s;
+    const T* trow = kTvd ? Tt + row * a.ld_t : nullptr;
+    T* grow = G + row * a.ld_g;
+
+    const bool ignored = (tg == a.ignore_index);
+    if (ignored || tg < 0 || tg >= a.V) {
+      // Ignored rows get a zero gradient; out-of-range targets get NaN and
+      // raise the status bit.  Neither reads the logits.
+      const float fill = ignored ? 0.f : __uint_as_float(0x7fc00000u);
+      if (!ignored && seg == 0 && threadIdx.x == 0 && a.dev_status)
+        atomicOr(a.dev_status, FCT_DEV_TARGET_OUT_OF_RANGE);
+      float f[VE];
+#pragma unroll
+      for (int j = 0; j < VE; ++j) f[j] = fill;
+      for (int64_t i = v0 + threadIdx.x; i < v1; i += kThreads) store_vec<T, VE>(grow + i * VE, f, drop);
+      if (last_seg && tail0 + threadIdx.x < a.V) Elem<T>::store1(grow + tail0 + threadIdx.x, fill);
+      continue;
+    }
+
+    const float gce = a.grad_ce[row * a.grad_stride];
+    const float ns2 = -(a.lse_s[row] * kLog2e);
+    float nt2 = 0.f, c_pos = gce, c_neg = gce, c_zero = gce;
+    if constexpr (kTvd) {
+      const float gtvd = a.grad_tvd[row * a.grad_stride];
+      const float sg = a.sigma[row];
+      const float h = 0.5f * gtvd;
+      nt2 = -(a.lse_t[row] * kLog2e);
+      c_pos = gce + h * (1.f - sg);   // sign = +1
+      c_neg = gce + h * (-1.f - sg);  // sign = -1
+      c_zero = gce - h * sg;          // tie
+    }
+
+    auto grad_of = [&](const float (&xs)[VE], const float (&xt)[VE], int64_t base, float (&g)[VE]) {
+#pragma unroll
+      for (int j = 0; j < VE; ++j) {
+        const float p = ex2(fmaf(xs[j], kLog2e, ns2));
+        float c = gce;
+        if constexpr (kTvd) {
+          const float q = ex2(fmaf(xt[j], kLog2e, nt2));
+          const float d = p - q;
+          c = (d > 0.f) ? c_pos : ((d < 0.f) ? c_neg : c_zero);
+        }
+        g[j] = p * c;
+      }
+      const int64_t off = tg - base;
+      if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+#pragma unroll
+        for (int j = 0; j < VE; ++j)
+          if (j == off) g[j] -= gce;
+      }
+    };
+
+    int64_t i = v0 + threadIdx.x;
+    if (i + (kUnroll - 1) * kThreads < v1) {  // full unit: all loads first
+      uint4 rs[kUnroll], rt[kUnroll];
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        rs[k] = load_raw<T, VE>(srow + (i + k * kThreads) * VE, drop);
+        if constexpr (kTvd) rt[k] = load_raw<T, VE>(trow + (i + k * kThreads) * VE, drop);
+      }
+#pragma unroll
+      for (int k = 0; k < kUnroll; ++k) {
+        float xs[VE], xt[VE], g[VE];
+        unpack_raw<T, VE>(rs[k], xs);
+        if constexpr (kTvd) unpack_raw<T, VE>(rt[k], xt);
+        grad_of(xs, xt, (i + k * kThreads) * VE, g);
+        store_vec<T, VE>(grow + (i + k * kThreads) * VE, g, drop);
+      }
+    } else {
+      for (; i < v1; i += kThreads) {
+        float xs[VE], xt[VE], g[VE];
+        unpack_raw<T, VE>(load_raw<T, VE>(srow + i * VE, drop), xs);
+        if constexpr (kTvd) unpack_raw<T, VE>(load_raw<T, VE>(trow + i * VE, drop), xt);
+        grad_of(xs, xt, i * VE, g);
+        store_vec<T, VE>(grow + i * VE, g, drop);
+      }
+    }
+    if (last_seg && tail0 + threadIdx.x < a.V) {
+      const int64_t v = tail0 + threadIdx.x;
+      float xs[1] = {Elem<T>::load1(srow + v)}, xt[1] = {0.f}, g[1];
+      if constexpr (kTvd) xt[0] = Elem<T>::load1(trow + v);
+      // one element: reuse the vector code with VE = 1 semantics
+      const float p = ex2(fmaf(xs[0], kLog2e, ns2));
+      float c = gce;
+      if constexpr (kTvd) {
+        const float q = ex2(fmaf(xt[0], kLog2e, nt2));
+        const float d = p - q;
+        c = (d > 0.f) ? c_pos : ((d < 0.f) ? c_neg : c_zero);
+      }
+      g[0] = p * c;
+      if (v == tg) g[0] -= gce;
+      Elem<T>::store1(grow + v, g[0]);
+    }
+  }
+}
+
+template <typename T, int VE, bool kTvd>
+int blocks_per_sm() {
+  static int cached = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, backward_kernel<T, VE, kTvd>, kThreads, 0) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      n = 1;
+    }
+    return n > 0 ? n : 1;
+  }();
+  return cached;
+}
+
+template <typename T, int VE, bool kTvd>
+cudaError_t go(const BwdArgs& a, int sms, cudaStream_t st) {
+  const int64_t nvec = a.V / VE;
+  const int64_t nseg = nvec > 0 ? (nvec + kSeg - 1) / kSeg : 1;
+  const int64_t units = a.BT * nseg;
+  int64_t grid = int64_t(sms) * blocks_per_sm<T, VE, kTvd>();
+  if (grid > units) grid = units;
+  backward_kernel<T, VE, kTvd><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st) {
+  const bool tvd = a.teacher != nullptr;
+  if (a.dtype == FCT_BF16) {
+    if (tvd) return vec ? go<bf16_t, 8, true>(a, sms, st) : go<bf16_t, 1, true>(a, sms, st);
+    return vec ? go<bf16_t, 8, false>(a, sms, st) : go<bf16_t, 1, false>(a, sms, st);
+  }
+  if (tvd) return vec ? go<float, 4, true>(a, sms, st) : go<float, 1, true>(a, sms, st);
+  return vec ? go<float, 4, false>(a, sms, st) : go<float, 1, false>(a, sms, st);
+}
+
+}  // namespace fct

@@ -1,0 +1,225 @@
+// Device helpers shared by the fused CE + TVD kernels (sm_103a).
+//
+// Everything works in base 2: a logit x enters the exponentials as
+// x * log2(e), so every exponential is one ex2 (MUFU) after one FFMA.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fct {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- math
+
+// 2^x on the special-function unit (flushes denormal results to zero).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Running (max, sum) state of a log-sum-exp in base 2:
+//   m2 = max_v x_v*log2(e)  (rounded product),  s = sum_v 2^(x_v*log2(e) - m2).
+// lse2 = m2 + log2(s), and the natural lse = lse2 * ln 2.
+struct Lse2 {
+  float m2;
+  float s;
+};
+
+__device__ __forceinline__ Lse2 lse2_empty() { return Lse2{-INFINITY, 0.f}; }
+
+// Merge of two partial states.  Commutative bit for bit (max and the sum of
+// two products are), so butterfly reductions leave every lane identical.
+__device__ __forceinline__ Lse2 lse2_merge(Lse2 a, Lse2 b) {
+  const float m = fmaxf(a.m2, b.m2);
+  const float sa = (a.m2 == -INFINITY) ? 0.f : a.s * ex2(a.m2 - m);
+  const float sb = (b.m2 == -INFINITY) ? 0.f : b.s * ex2(b.m2 - m);
+  return Lse2{m, sa + sb};
+}
+
+// Natural-log lse of a finished state.
+__device__ __forceinline__ float lse2_finish(Lse2 a) {
+  return (a.m2 + log2f(a.s)) * kLn2;
+}
+
+// Fold N values into a running state: rescale once per group if the group
+// raises the maximum, then add the group's exponentials.
+template <int N>
+__device__ __forceinline__ void lse2_update(Lse2& st, const float (&x)[N]) {
+  float vm = x[0];
+#pragma unroll
+  for (int j = 1; j < N; ++j) vm = fmaxf(vm, x[j]);
+  const float m2n = vm * kLog2e;
+  if (m2n > st.m2) {
+    st.s *= ex2(st.m2 - m2n);
+    st.m2 = m2n;
+  }
+  const float neg = -st.m2;
+  float acc = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) acc += ex2(fmaf(x[j], kLog2e, neg));
+  st.s += acc;
+}
+
+// ---------------------------------------------------------------- memory
+
+// L2 eviction-priority policies for the cache_hint loads below.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// 16-byte global load that skips L1 and tags the L2 line with `pol`.
+__device__ __forceinline__ uint4 ld16(const void* ptr, uint64_t pol) {
+  uint4 r;
+  asm volatile(
+      "ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(ptr), "l"(pol));
+  return r;
+}
+
+// 16-byte global store that skips L1 and tags the L2 line with `pol`.
+__device__ __forceinline__ void st16(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile(
+      "st.global.L1::no_allocate.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+      :
+      : "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+      : "memory");
+}
+
+// Element-type traits.  A "vector" is the 16 bytes one thread moves at once:
+// 8 bf16 or 4 fp32 values.  The scalar path (VE == 1) serves rows whose
+// pointers or strides are not 16-byte aligned.
+struct bf16_t {
+  uint16_t bits;
+};
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float load1(const float* p) { return *p; }
+  __device__ __forceinline__ static void unpack(uint4 w, float (&x)[4]) {
+    x[0] = __uint_as_float(w.x);
+    x[1] = __uint_as_float(w.y);
+    x[2] = __uint_as_float(w.z);
+    x[3] = __uint_as_float(w.w);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&x)[4]) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]),
+                      __float_as_uint(x[2]), __float_as_uint(x[3]));
+  }
+  __device__ __forceinline__ static void store1(float* p, float v) { *p = v; }
+  static constexpr uint32_t kNanBits = 0x7fc00000u;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  // cvt.rn.bf16x2.f32 d, a, b puts a in the upper half and b in the lower.
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+template <>
+struct Elem<bf16_t> {
+  static constexpr int kVec = 8;
+  __device__ __forceinline__ static float load1(const bf16_t* p) {
+    const unsigned short b = *reinterpret_cast<const unsigned short*>(p);
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+  }
+  __device__ __forceinline__ static void unpack(uint4 w, float (&x)[8]) {
+    x[0] = __uint_as_float(w.x << 16);
+    x[1] = __uint_as_float(w.x & 0xffff0000u);
+    x[2] = __uint_as_float(w.y << 16);
+    x[3] = __uint_as_float(w.y & 0xffff0000u);
+    x[4] = __uint_as_float(w.z << 16);
+    x[5] = __uint_as_float(w.z & 0xffff0000u);
+    x[6] = __uint_as_float(w.w << 16);
+    x[7] = __uint_as_float(w.w & 0xffff0000u);
+  }
+  __device__ __forceinline__ static uint4 pack(const float (&x)[8]) {
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]),
+                      pack_bf16x2(x[4], x[5]), pack_bf16x2(x[6], x[7]));
+  }
+  __device__ __forceinline__ static void store1(bf16_t* p, float v) {
+    const uint32_t two = pack_bf16x2(v, 0.f);
+    *reinterpret_cast<unsigned short*>(p) = static_cast<unsigned short>(two & 0xffffu);
+  }
+  static constexpr uint32_t kNanBits = 0x7fc0u;
+};
+
+// Load VE consecutive elements starting at element `p` as floats.
+template <typename T, int VE>
+__device__ __forceinline__ void load_vec(const T* p, uint64_t pol, float (&x)[VE]) {
+  if constexpr (VE == 1) {
+    x[0] = Elem<T>::load1(p);
+  } else {
+    static_assert(VE == Elem<T>::kVec, "a vector is 16 bytes");
+    Elem<T>::unpack(ld16(p, pol), x);
+  }
+}
+
+// Raw 16-byte (or one-element) load, unpacked later: keeps the registers of
+// several loads in flight at 4 per vector instead of VE floats.
+template <typename T, int VE>
+__device__ __forceinline__ uint4 load_raw(const T* p, uint64_t pol) {
+  if constexpr (VE == 1) {
+    uint4 r;
+    r.x = __float_as_uint(Elem<T>::load1(p));
+    r.y = r.z = r.w = 0u;
+    return r;
+  } else {
+    static_assert(VE == Elem<T>::kVec, "a vector is 16 bytes");
+    return ld16(p, pol);
+  }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void unpack_raw(uint4 r, float (&x)[VE]) {
+  if constexpr (VE == 1) {
+    x[0] = __uint_as_float(r.x);
+  } else {
+    Elem<T>::unpack(r, x);
+  }
+}
+
+template <typename T, int VE>
+__device__ __forceinline__ void store_vec(T* p, const float (&x)[VE], uint64_t pol) {
+  if constexpr (VE == 1) {
+    Elem<T>::store1(p, x[0]);
+  } else {
+    st16(p, Elem<T>::pack(x), pol);
+  }
+}
+
+// ---------------------------------------------------------------- warp
+
+__device__ __forceinline__ Lse2 shfl_xor(Lse2 a, int m) {
+  return Lse2{__shfl_xor_sync(0xffffffffu, a.m2, m), __shfl_xor_sync(0xffffffffu, a.s, m)};
+}
+
+__device__ __forceinline__ Lse2 warp_merge(Lse2 a) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) a = lse2_merge(a, shfl_xor(a, m));
+  return a;
+}
+
+__device__ __forceinline__ float warp_sum(float a) {
+#pragma unroll
+  for (int m = 16; m >= 1; m >>= 1) a += __shfl_xor_sync(0xffffffffu, a, m);
+  return a;
+}
+
+}  // namespace fct

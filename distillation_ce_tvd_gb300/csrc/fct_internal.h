@@ -1,0 +1,53 @@
+// Internal launch interface between the C ABI (fct_api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fused_ce_tvd.h"
+
+namespace fct {
+
+struct FwdArgs {
+  const void* student;
+  const void* teacher;  // unused by the plain cross-entropy forward
+  int64_t ld_s, ld_t;
+  int dtype;
+  const int64_t* target;
+  int64_t BT, V, ignore_index;
+  float* ce;
+  float* tvd;  // nullptr selects the plain cross-entropy forward
+  float* lse_s;
+  float* lse_t;
+  float* sigma;
+  int32_t* dev_status;
+};
+
+struct FwdPlan {
+  bool vec;     // 16-byte vector path (pointers and strides aligned)
+  int cluster;  // CTAs per row: 1, 2, 4 or 8
+  int slots;    // rows in flight across the GPU (clusters launched), 0 = as many as fit
+};
+
+struct BwdArgs {
+  const void* student;
+  const void* teacher;  // nullptr selects the plain cross-entropy backward
+  int64_t ld_s, ld_t;
+  int dtype;
+  const int64_t* target;
+  int64_t BT, V, ignore_index;
+  const float* lse_s;
+  const float* lse_t;
+  const float* sigma;
+  const float* grad_ce;
+  const float* grad_tvd;
+  int64_t grad_stride;
+  void* grad;
+  int64_t ld_g;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
+cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st);
+
+}  // namespace fct

@@ -1,0 +1,152 @@
+/*
+ * fused_ce_tvd.h -- C ABI of libfused_ce_tvd.so, the GB300 (sm_103a) fused
+ * cross-entropy + total-variation-distance distillation loss.
+ *
+ * The method is the one described in "[Liger-Kernel] Liger-Kernel:
+ * Cross-Entropy와 Total Variation Distance를 하나로 융합하여 성능을
+ * 극대화하다" (an analysis of linkedin/Liger-Kernel PR #1384, "fused CE + TV
+ * distance kernel"), cited below as "PR #1384 analysis".  For one row of
+ * student logits s and teacher logits t over a vocabulary of V entries:
+ *
+ *   p = softmax(s), q = softmax(t)
+ *   ce    = lse(s) - s[target]
+ *   tvd   = 0.5 * sum_v |p_v - q_v|
+ *   sigma = sum_v p_v * sign(p_v - q_v)            (sign(0) = 0)
+ *   d(grad_ce*ce + grad_tvd*tvd)/ds_v
+ *         = grad_ce*(p_v - 1[v==target]) + grad_tvd*0.5*p_v*(sign_v - sigma)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All array arguments are DEVICE pointers, owned by the caller.  The
+ *    library allocates nothing and keeps no state between calls.
+ *  - Logit matrices are row-major (BT, V) with a row stride `ld` (in
+ *    elements, ld >= V).  Student and teacher share one element type.
+ *  - `target` is int64 (BT,).  A row whose target equals `ignore_index`
+ *    contributes nothing: its ce, tvd, lse and sigma outputs are written as 0
+ *    and its gradient row as 0.  A target outside [0, V) that is not
+ *    ignore_index sets FCT_DEV_TARGET_OUT_OF_RANGE in *dev_status; that row's
+ *    ce is NaN and its gradient row is NaN, the other outputs are computed.
+ *  - Per-row outputs and inputs (ce, tvd, lse, sigma, grad_ce, grad_tvd) are
+ *    fp32 arrays of BT values.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    are asynchronous and stream-ordered; none synchronises the host.
+ *  - `dev_status` may be NULL.  Otherwise it points to one device int32 that
+ *    kernels OR error bits into (never cleared by the library); read it after
+ *    synchronising the stream.  No kernel traps or asserts.
+ *  - The return value is a fct_status.  Argument errors are detected on the
+ *    host before any launch and leave every output untouched.  A launch
+ *    failure returns FCT_ERR_CUDA (the CUDA error is left for
+ *    cudaGetLastError to report again).
+ *  - BT == 0 is a valid no-op.  Rows are independent: splitting BT into
+ *    contiguous blocks across calls (or processes) gives bitwise the same
+ *    results as one call.
+ */
+#ifndef FUSED_CE_TVD_H_
+#define FUSED_CE_TVD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { FCT_F32 = 0, FCT_BF16 = 1 } fct_dtype;
+
+typedef enum {
+  FCT_OK = 0,
+  FCT_ERR_INVALID_ARG = 1, /* null pointer, negative size, ld < V, bad aliasing */
+  FCT_ERR_UNSUPPORTED = 2, /* unknown dtype, no sm_103a device */
+  FCT_ERR_ALIGNMENT = 3,   /* pointer not aligned to its element size */
+  FCT_ERR_CUDA = 4         /* a CUDA runtime call or kernel launch failed */
+} fct_status;
+
+/* Bits OR-ed into *dev_status by the kernels. */
+#define FCT_DEV_TARGET_OUT_OF_RANGE 0x1
+
+/*
+ * Forward of the fused loss (PR #1384 analysis, "Forward Pass": step 1 is the
+ * per-row log-sum-exp of student and teacher, step 2 the TVD and sigma
+ * reductions, closed by the five per-row stores).
+ *
+ *   student, teacher : (BT, V) logits, element type `dtype`, strides ld_*.
+ *   target           : (BT,) int64.
+ *   ce, tvd, student_lse, teacher_lse, sigma : (BT,) fp32 outputs; none may
+ *                      overlap another output or an input.
+ *
+ * The saved state needed by the backward is student_lse, teacher_lse and
+ * sigma (O(BT)); no (BT, V) buffer is written.
+ */
+int fused_ce_tvd_forward(const void* student, int64_t ld_student,
+                         const void* teacher, int64_t ld_teacher,
+                         fct_dtype dtype, const int64_t* target, int64_t BT,
+                         int64_t V, int64_t ignore_index, float* ce,
+                         float* tvd, float* student_lse, float* teacher_lse,
+                         float* sigma, int32_t* dev_status, void* stream);
+
+/*
+ * Backward of the fused loss (PR #1384 analysis, "Backward Pass": reload the
+ * student and teacher rows, recompute p, q and the sign from the saved lse
+ * values, and combine both terms with the saved sigma).
+ *
+ *   student_lse, teacher_lse, sigma : (BT,) fp32, as written by
+ *                      fused_ce_tvd_forward for the same logits.
+ *   grad_ce, grad_tvd : upstream gradients; grad_stride = 1 reads BT values,
+ *                      grad_stride = 0 broadcasts element 0 to every row.
+ *   grad_student     : (BT, V) output, element type `dtype`, stride ld_grad.
+ *                      grad_student == student with ld_grad == ld_student
+ *                      computes the gradient IN PLACE over the student
+ *                      logits; any other overlap with an input is
+ *                      FCT_ERR_INVALID_ARG.
+ *
+ * bf16 gradients are rounded once, to nearest even, from fp32.
+ */
+int fused_ce_tvd_backward(const void* student, int64_t ld_student,
+                          const void* teacher, int64_t ld_teacher,
+                          fct_dtype dtype, const int64_t* target, int64_t BT,
+                          int64_t V, int64_t ignore_index,
+                          const float* student_lse, const float* teacher_lse,
+                          const float* sigma, const float* grad_ce,
+                          const float* grad_tvd, int64_t grad_stride,
+                          void* grad_student, int64_t ld_grad,
+                          int32_t* dev_status, void* stream);
+
+/*
+ * Cross-entropy alone: the CE half of "Forward Pass" (one log-sum-exp pass,
+ * ce = lse - logits[target]).  ce, lse: (BT,) fp32 outputs.
+ */
+int ce_forward(const void* logits, int64_t ld, fct_dtype dtype,
+               const int64_t* target, int64_t BT, int64_t V,
+               int64_t ignore_index, float* ce, float* lse,
+               int32_t* dev_status, void* stream);
+
+/*
+ * Cross-entropy gradient alone: grad_ce*(p_v - 1[v==target]), the first of
+ * the "Backward Pass" identities.  grad_logits may equal logits (with
+ * ld_grad == ld) for an in-place gradient.
+ */
+int ce_backward(const void* logits, int64_t ld, fct_dtype dtype,
+                const int64_t* target, int64_t BT, int64_t V,
+                int64_t ignore_index, const float* lse, const float* grad_ce,
+                int64_t grad_stride, void* grad_logits, int64_t ld_grad,
+                int32_t* dev_status, void* stream);
+
+/* Human-readable name of a fct_status value (static storage). */
+const char* fct_status_string(int status);
+
+/*
+ * Tuning knob (no counterpart in the method's description): number of CTAs
+ * (1, 2, 4 or 8, one thread-block cluster) that share one row in the fused
+ * forward.  0 restores the automatic choice, which depends only on V, the
+ * element type and the device, never on BT.  Process-wide; returns the
+ * previous value, or -1 for an invalid argument.
+ */
+int fct_set_forward_cluster(int ctas_per_row);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int fct_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSED_CE_TVD_H_ */

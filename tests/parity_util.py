@@ -1,0 +1,92 @@
+"""Element-by-element comparison of the CUDA path against the CPU oracle.
+
+Tolerances (from the problem statement; their derivation is in the design
+notes):
+  * per-row ce, tvd, student_lse, teacher_lse: abs 2e-4 for bf16 logits,
+    abs 1e-5 for fp32 logits;
+  * sigma: the same, widened by 2 * (oracle probability mass of the row's
+    near-ties), because a sign flip at an element with |p - q| < 1e-7 is
+    allowed and moves sigma by at most 2 p_v;
+  * gradient: abs 1e-6 + rel 2e-3, widened at a row with near-ties by
+    |grad_tvd| * 0.5 * p_v * (2 [v is a near-tie] + 2 * near-tie mass),
+    the most a set of allowed sign flips can move element v.
+Ignored rows must be exactly zero on both sides.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+
+TIE_EPS = 1e-7
+
+
+def row_atol(dtype) -> float:
+    return 2e-4 if dtype == torch.bfloat16 else 1e-5
+
+
+def to_host_rows(x: torch.Tensor, rows) -> torch.Tensor:
+    return x[rows].cpu() if rows is not None else x.cpu()
+
+
+def tie_info(s_rows, t_rows):
+    """Per row: boolean near-tie mask, near-tie mass and the oracle's p."""
+    masks, mass, probs = [], [], []
+    for r in range(s_rows.shape[0]):
+        p, q = oracle.row_probs(s_rows, t_rows, r)
+        m = np.abs(p - q) < TIE_EPS
+        masks.append(m)
+        mass.append(float(p[m].sum()))
+        probs.append(p)
+    return masks, np.array(mass), probs
+
+
+def check_forward(dtype, target, got: dict, ref: dict, tie_mass, ignore_index=-100,
+                  what=""):
+    """got/ref: dict of per-row arrays (ce, tvd, student_lse, teacher_lse, sigma)."""
+    atol = row_atol(dtype)
+    tg = np.asarray(target)
+    ign = tg == ignore_index
+    for k in ("ce", "tvd", "student_lse", "teacher_lse", "sigma"):
+        g = np.asarray(got[k], np.float64)
+        r = np.asarray(ref[k], np.float64)
+        assert np.all(g[ign] == 0.0), f"{what}{k}: ignored rows must be exactly 0"
+        nan_r = np.isnan(r)
+        assert np.array_equal(np.isnan(g), nan_r), f"{what}{k}: NaN pattern differs"
+        tol = atol + (2.0 * tie_mass if k == "sigma" else 0.0)
+        err = np.abs(g - r)
+        err[nan_r] = 0.0
+        bad = np.nonzero(err > tol)[0]
+        assert bad.size == 0, (f"{what}{k}: {bad.size} rows out of tolerance, worst row "
+                               f"{bad[np.argmax(err[bad])]}: got {g[bad[0]]!r} ref {r[bad[0]]!r} "
+                               f"err {err[bad].max():.3e} tol {np.atleast_1d(tol)[0]:.3e}")
+
+
+def check_grad(got: np.ndarray, ref: np.ndarray, grad_tvd_rows, tie_masks, tie_mass, probs,
+               target, ignore_index=-100, what=""):
+    """got: gradient rows as fp64 (from bf16/fp32); ref: the oracle's fp64 rows."""
+    tg = np.asarray(target)
+    gtvd = np.asarray(grad_tvd_rows, np.float64)
+    for r in range(ref.shape[0]):
+        g, f = got[r], ref[r]
+        if tg[r] == ignore_index:
+            assert np.all(g == 0.0), f"{what}row {r}: ignored row gradient must be exactly 0"
+            continue
+        if np.isnan(f).all():
+            assert np.isnan(g).all(), f"{what}row {r}: out-of-range target row must be NaN"
+            continue
+        tol = 1e-6 + 2e-3 * np.abs(f)
+        if tie_mass[r] > 0.0:
+            tol = tol + abs(gtvd[r]) * 0.5 * probs[r] * (2.0 * tie_masks[r] + 2.0 * tie_mass[r])
+        err = np.abs(g - f)
+        bad = np.nonzero(err > tol)[0]
+        assert bad.size == 0, (f"{what}row {r}: {bad.size} elements out of tolerance; v={bad[0]} "
+                               f"got {g[bad[0]]!r} ref {f[bad[0]]!r} tol {tol[bad[0]]:.3e}")
+
+
+def oracle_rows(s_rows, t_rows, tg_rows, gce_rows, gtvd_rows, ignore_index=-100):
+    ref = oracle.fused_ce_tvd_forward(s_rows, t_rows, tg_rows, ignore_index)
+    grad, _ = oracle.fused_ce_tvd_backward(s_rows, t_rows, tg_rows, gce_rows, gtvd_rows,
+                                           ignore_index)
+    return ref, grad

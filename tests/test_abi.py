@@ -1,0 +1,136 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/fused_ce_tvd.h declares, and rejects bad arguments on the host
+before any CUDA call (no compute is launched here)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from distillation_ce_tvd_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fused_ce_tvd.h")
+
+OK, INVALID, UNSUPPORTED, ALIGN = 0, 1, 2, 3
+FAKE = 0x7F0000000000  # a 256-byte aligned address that is never dereferenced
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return binding.load()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "ce_forward", "ce_backward",
+              "fct_status_string"):
+        assert n in names
+    assert set(names) == set(binding.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    for n in declared_functions():
+        assert n in exported, n
+        assert getattr(lib, n) is not None
+
+
+def test_header_compiles_as_c():
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings_and_version(lib):
+    for code in range(5):
+        assert binding.status_string(code).startswith("FCT_")
+    assert "unknown" in binding.status_string(99)
+    assert binding.version() >= 100
+
+
+def test_cluster_knob(lib):
+    assert lib.fct_set_forward_cluster(3) == -1
+    prev = lib.fct_set_forward_cluster(4)
+    assert lib.fct_set_forward_cluster(prev) == 4
+
+
+def fwd(lib, **kw):
+    a = dict(s=FAKE, ld_s=128, t=FAKE + (1 << 30), ld_t=128, dtype=1, tg=FAKE + (2 << 30), BT=4,
+             V=100, ign=-100, ce=FAKE + (3 << 30), tvd=FAKE + (3 << 30) + 4096,
+             ls=FAKE + (3 << 30) + 8192, lt=FAKE + (3 << 30) + 12288,
+             sg=FAKE + (3 << 30) + 16384, st=None, stream=None)
+    a.update(kw)
+    return lib.fused_ce_tvd_forward(a["s"], a["ld_s"], a["t"], a["ld_t"], a["dtype"], a["tg"],
+                                    a["BT"], a["V"], a["ign"], a["ce"], a["tvd"], a["ls"], a["lt"],
+                                    a["sg"], a["st"], a["stream"])
+
+
+def bwd(lib, **kw):
+    base = FAKE + (4 << 30)
+    a = dict(s=FAKE, ld_s=128, t=FAKE + (1 << 30), ld_t=128, dtype=1, tg=FAKE + (2 << 30), BT=4,
+             V=100, ign=-100, ls=base, lt=base + 4096, sg=base + 8192, gce=base + 12288,
+             gtvd=base + 16384, gs=1, g=FAKE + (5 << 30), ld_g=128, st=None, stream=None)
+    a.update(kw)
+    return lib.fused_ce_tvd_backward(a["s"], a["ld_s"], a["t"], a["ld_t"], a["dtype"], a["tg"],
+                                     a["BT"], a["V"], a["ign"], a["ls"], a["lt"], a["sg"], a["gce"],
+                                     a["gtvd"], a["gs"], a["g"], a["ld_g"], a["st"], a["stream"])
+
+
+def test_forward_argument_checks(lib):
+    assert fwd(lib, BT=0) == OK
+    assert fwd(lib, BT=0, s=None, t=None) == OK
+    assert fwd(lib, BT=-1) == INVALID
+    assert fwd(lib, V=0) == INVALID
+    assert fwd(lib, dtype=7) == UNSUPPORTED
+    assert fwd(lib, s=None) == INVALID
+    assert fwd(lib, t=None) == INVALID
+    assert fwd(lib, tg=None) == INVALID
+    assert fwd(lib, sg=None) == INVALID
+    assert fwd(lib, ld_s=99) == INVALID
+    assert fwd(lib, ld_t=50) == INVALID
+    assert fwd(lib, s=FAKE + 1) == ALIGN            # bf16 needs 2-byte alignment
+    assert fwd(lib, dtype=0, s=FAKE + 2) == ALIGN   # fp32 needs 4
+    assert fwd(lib, tg=FAKE + (2 << 30) + 4) == ALIGN
+    assert fwd(lib, tvd=FAKE + (3 << 30)) == INVALID            # two outputs alias
+    assert fwd(lib, ce=FAKE + 64) == INVALID                     # output inside the student
+    assert fwd(lib, sg=FAKE + (2 << 30) + 8) == INVALID          # output inside the targets
+
+
+def test_backward_argument_checks(lib):
+    assert bwd(lib, BT=0) == OK
+    assert bwd(lib, BT=-3) == INVALID
+    assert bwd(lib, dtype=2) == UNSUPPORTED
+    assert bwd(lib, gs=2) == INVALID
+    assert bwd(lib, g=None) == INVALID
+    assert bwd(lib, ld_g=10) == INVALID
+    assert bwd(lib, g=FAKE, ld_g=256) == INVALID                  # in place needs the same ld
+    assert bwd(lib, g=FAKE + 256) == INVALID                     # partial overlap with student
+    assert bwd(lib, g=FAKE + (1 << 30)) == INVALID               # over the teacher
+    assert bwd(lib, g=FAKE + (5 << 30) + 1) == ALIGN
+    assert bwd(lib, gce=FAKE + (5 << 30) + 64) == INVALID        # grad_ce inside grad
+    assert bwd(lib, lt=None) == INVALID
+
+
+def test_ce_argument_checks(lib):
+    assert lib.ce_forward(FAKE, 128, 1, FAKE + (2 << 30), 0, 100, -100, None, None, None, None) == OK
+    assert lib.ce_forward(FAKE, 128, 1, FAKE + (2 << 30), 4, 100, -100, None,
+                          FAKE + (3 << 30), None, None) == INVALID
+    assert lib.ce_backward(FAKE, 128, 5, FAKE + (2 << 30), 4, 100, -100, FAKE + (3 << 30),
+                           FAKE + (3 << 30) + 64, 1, FAKE + (4 << 30), 128, None, None) == UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+    x = torch.zeros(2, 8)
+    with pytest.raises(ValueError):
+        binding.fused_ce_tvd_forward(x, x, torch.zeros(2, dtype=torch.int64))

@@ -1,0 +1,279 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU fp64 oracle."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from distillation_ce_tvd_gb300 import binding, workloads
+from parity_util import (check_forward, check_grad, oracle_rows, tie_info, to_host_rows)
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+    yield
+    binding.set_forward_cluster(0)
+
+
+def run(w, cluster=0, inplace=False, stream=None):
+    """Forward + backward of a workload on the GPU; returns host copies."""
+    prev = binding.set_forward_cluster(cluster)
+    try:
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ce, tvd, ls, lt, sg = binding.fused_ce_tvd_forward(
+            w.student, w.teacher, w.target, w.ignore_index, dev_status=status, stream=stream)
+        s_in = w.student.clone() if inplace else w.student
+        grad = binding.fused_ce_tvd_backward(
+            s_in, w.teacher, w.target, ls, lt, sg, w.grad_ce, w.grad_tvd, w.ignore_index,
+            inplace=inplace, dev_status=status, stream=stream)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_forward_cluster(prev)
+    fwd = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
+    return fwd, grad, int(status.item())
+
+
+def compare(w, fwd, grad, rows=None, what=""):
+    """Check the given rows (all when None) against the oracle."""
+    s = to_host_rows(w.student, rows)
+    t = to_host_rows(w.teacher, rows)
+    tg = to_host_rows(w.target, rows).numpy()
+    gce = to_host_rows(w.grad_ce, rows).numpy()
+    gtvd = to_host_rows(w.grad_tvd, rows).numpy()
+    ref, ref_grad = oracle_rows(s, t, tg, gce, gtvd, w.ignore_index)
+    masks, mass, probs = tie_info(s, t)
+    got = {k: to_host_rows(v, rows).numpy() for k, v in fwd.items()}
+    check_forward(w.student.dtype, tg, got, ref, mass, w.ignore_index, what)
+    g = to_host_rows(grad, rows).double().numpy()
+    check_grad(g, ref_grad, gtvd, masks, mass, probs, tg, w.ignore_index, what)
+    return ref
+
+
+def exact_tie_rows(w):
+    return torch.nonzero((w.student == w.teacher).all(dim=1)).flatten()
+
+
+def assert_exact_ties(w, fwd):
+    rows = exact_tie_rows(w)
+    rows = rows[w.target[rows] != w.ignore_index]
+    if rows.numel():
+        assert torch.all(fwd["tvd"][rows] == 0) and torch.all(fwd["sigma"][rows] == 0)
+
+
+# ------------------------------------------------------------------ small, all rows
+
+def test_tiny_workload_all_rows_and_fixture():
+    with open(os.path.join(HERE, "golden", "tiny_bt8_v32_f32.json")) as f:
+        d = json.load(f)
+    w = workloads.make("tiny_bt8_v32_f32", "cpu")
+    w = workloads.Workload(w.name, w.student.to(DEV), w.teacher.to(DEV), w.target.to(DEV),
+                           w.grad_ce.to(DEV), w.grad_tvd.to(DEV))
+    fwd, grad, st = run(w)
+    assert st == 0
+    compare(w, fwd, grad)
+    np.testing.assert_allclose(fwd["tvd"].cpu().numpy(), d["forward"]["tvd"], atol=1e-5)
+    np.testing.assert_allclose(grad.cpu().double().numpy(), d["grad_student"], atol=1e-6, rtol=2e-3)
+    assert fwd["tvd"][3].item() == 0.0 and fwd["sigma"][3].item() == 0.0
+    assert torch.all(grad[5] == 0)
+
+
+@pytest.mark.parametrize("name,rows,V", [
+    ("bt1024_v32000_bf16", 96, 32000),
+    ("bt1024_v32000_bf16", 64, 32000 + 5),        # ragged tail, misaligned row stride
+    ("bt1024_v151936_bf16", 48, 151936),
+    ("bt8192_v151936_bf16", 48, 151936),
+    ("bt4096_v256000_f32", 24, 256000),
+    ("bt4096_v256000_f32", 24, 4099),              # fp32 ragged
+])
+def test_recipes_reduced_rows_all_rows(name, rows, V):
+    w = workloads.make(name, DEV, rows=rows, V=V, seed=11)
+    fwd, grad, st = run(w)
+    assert st == 0
+    compare(w, fwd, grad, what=f"{name}[{rows}x{V}] ")
+    assert_exact_ties(w, fwd)
+
+
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_every_cluster_size(cluster, dtype):
+    w = workloads.make("bt4096_v256000_f32", DEV, rows=40, V=20011, dtype=dtype, seed=5)
+    fwd, grad, st = run(w, cluster=cluster)
+    assert st == 0
+    compare(w, fwd, grad, what=f"C={cluster} ")
+    assert_exact_ties(w, fwd)
+
+
+# ------------------------------------------------------------------ full sizes, sampled rows
+
+FULL = ["bt1024_v32000_bf16", "bt1024_v151936_bf16", "bt8192_v151936_bf16", "bt4096_v256000_f32"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled_rows_and_properties(name):
+    w = workloads.make(name, DEV)
+    fwd, grad, st = run(w)
+    assert st == 0
+    BT = w.BT
+    g = torch.Generator().manual_seed(123)
+    sample = torch.randperm(BT, generator=g)[:40]
+    ign = torch.nonzero(w.target == w.ignore_index).flatten().cpu()[:4]
+    ties = exact_tie_rows(w).cpu()[:4]
+    rows = torch.unique(torch.cat([sample, ign, ties, torch.tensor([0, BT - 1])]))
+    compare(w, fwd, grad, rows=rows.to(DEV), what=f"{name} ")
+    # properties that hold at every row
+    keep = w.target != w.ignore_index
+    assert torch.all(fwd["tvd"] >= 0) and torch.all(fwd["tvd"] <= 1 + 1e-6)
+    assert torch.all(fwd["sigma"].abs() <= 1 + 1e-5)
+    rowmax = w.student.float().amax(dim=1)
+    assert torch.all(fwd["student_lse"][keep] >= rowmax[keep] - 1e-5)
+    assert torch.all(fwd["ce"][keep] >= -1e-4)
+    for k in fwd:
+        assert torch.all(fwd[k][~keep] == 0)
+    assert torch.all(grad[~keep] == 0)
+    assert torch.isfinite(grad).all()
+    assert_exact_ties(w, fwd)
+
+
+# ------------------------------------------------------------------ edge cases
+
+@pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 17, 1023])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_small_and_ragged_vocab(V, dtype):
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=13, V=V, dtype=dtype, seed=V)
+    fwd, grad, st = run(w)
+    assert st == 0
+    compare(w, fwd, grad, what=f"V={V} ")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_padded_and_misaligned_rows(dtype):
+    base = workloads.make("bt1024_v32000_bf16", DEV, rows=21, V=3000, dtype=dtype, seed=2)
+    for pad, off in ((0, 1), (40, 0), (13, 3)):
+        ld = 3000 + pad + off
+        S = torch.full((21, ld + off), 77.0, device=DEV, dtype=dtype)
+        Tt = torch.full((21, ld + off), -55.0, device=DEV, dtype=dtype)
+        s = S.view(-1)[off:off + 21 * ld].view(21, ld)[:, :3000]
+        t = Tt.view(-1)[off:off + 21 * ld].view(21, ld)[:, :3000]
+        s.copy_(base.student)
+        t.copy_(base.teacher)
+        w = workloads.Workload(base.name, s, t, base.target, base.grad_ce, base.grad_tvd)
+        fwd, grad, st = run(w)
+        assert st == 0
+        compare(w, fwd, grad, what=f"pad={pad} off={off} ")
+
+
+def test_empty_batch_is_a_no_op():
+    s = torch.empty(0, 100, device=DEV, dtype=torch.bfloat16)
+    tg = torch.empty(0, device=DEV, dtype=torch.int64)
+    out = binding.fused_ce_tvd_forward(s, s.clone(), tg)
+    assert all(o.numel() == 0 for o in out)
+    g = binding.fused_ce_tvd_backward(s, s.clone(), tg, *out[2:], out[0], out[0])
+    assert g.numel() == 0
+
+
+def test_all_rows_ignored_and_out_of_range_target():
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=6, V=500, seed=4)
+    w.target[:] = -100
+    fwd, grad, st = run(w)
+    assert st == 0 and all(torch.all(v == 0) for v in fwd.values()) and torch.all(grad == 0)
+    w.target[:] = torch.tensor([3, 500, -100, -1, 7, 499], device=DEV)
+    fwd, grad, st = run(w)
+    assert st == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+    compare(w, fwd, grad, what="oob ")
+    assert torch.isnan(fwd["ce"][1]) and torch.isnan(fwd["ce"][3])
+    assert torch.isnan(grad[1].float()).all() and torch.isnan(grad[3].float()).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_inplace_matches_out_of_place(dtype):
+    w = workloads.make("bt1024_v151936_bf16", DEV, rows=17, V=12345, dtype=dtype, seed=8)
+    _, g1, _ = run(w)
+    _, g2, _ = run(w, inplace=True)
+    assert torch.equal(g1, g2)
+
+
+def test_broadcast_upstream_gradient():
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=9, V=777, seed=3)
+    fwd, _, _ = run(w)
+    ls, lt, sg = fwd["student_lse"], fwd["teacher_lse"], fwd["sigma"]
+    a = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, ls, lt, sg, 0.25, 1.5)
+    b = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, ls, lt, sg,
+                                      torch.full((9,), 0.25, device=DEV),
+                                      torch.full((9,), 1.5, device=DEV))
+    assert torch.equal(a, b)
+
+
+def test_row_blocks_are_bitwise_independent():
+    w = workloads.make("bt8192_v151936_bf16", DEV, rows=64, V=151936, seed=21)
+    fwd, grad, _ = run(w)
+    for lo, hi in ((0, 1), (1, 30), (30, 64)):
+        sub = workloads.Workload(w.name, w.student[lo:hi], w.teacher[lo:hi], w.target[lo:hi],
+                                 w.grad_ce[lo:hi], w.grad_tvd[lo:hi])
+        f2, g2, _ = run(sub)
+        for k in fwd:
+            assert torch.equal(fwd[k][lo:hi], f2[k]), k
+        assert torch.equal(grad[lo:hi], g2)
+
+
+def test_non_default_stream():
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=33, V=32000, seed=6)
+    ref_fwd, ref_grad, _ = run(w)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        fwd, grad, _ = run(w, stream=s)
+    for k in fwd:
+        assert torch.equal(fwd[k], ref_fwd[k])
+    assert torch.equal(grad, ref_grad)
+
+
+def test_repeat_runs_are_deterministic():
+    w = workloads.make("bt4096_v256000_f32", DEV, rows=20, V=65536, seed=9)
+    a, ga, _ = run(w)
+    b, gb, _ = run(w)
+    for k in a:
+        assert torch.equal(a[k], b[k])
+    assert torch.equal(ga, gb)
+
+
+# ------------------------------------------------------------------ CE subset, autograd
+
+@pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 151936), (torch.float32, 32003), (torch.bfloat16, 5)])
+def test_ce_subset(dtype, V):
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=24, V=V, dtype=dtype, seed=12)
+    w.target[2] = -100
+    ce, lse = binding.ce_forward(w.student, w.target)
+    g = binding.ce_backward(w.student, w.target, lse, w.grad_ce)
+    gi = binding.ce_backward(w.student.clone(), w.target, lse, w.grad_ce, inplace=True)
+    torch.cuda.synchronize()
+    assert torch.equal(g, gi)
+    s = w.student.cpu()
+    tg = w.target.cpu().numpy()
+    ref = oracle.ce_forward(s, tg)
+    ref_g, _ = oracle.ce_backward(s, tg, w.grad_ce.cpu().numpy())
+    atol = 2e-4 if dtype == torch.bfloat16 else 1e-5
+    np.testing.assert_allclose(ce.cpu().numpy(), ref["ce"], atol=atol, rtol=0)
+    np.testing.assert_allclose(lse.cpu().numpy(), ref["lse"], atol=atol, rtol=0)
+    err = np.abs(g.cpu().double().numpy() - ref_g)
+    assert np.all(err <= 1e-6 + 2e-3 * np.abs(ref_g))
+
+
+def test_autograd_wrapper_matches_direct_calls():
+    from distillation_ce_tvd_gb300.autograd import fused_ce_tvd_loss
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=16, V=4000, seed=14)
+    s = w.student.clone().requires_grad_(True)
+    ce, tvd = fused_ce_tvd_loss(s, w.teacher, w.target)
+    (ce * w.grad_ce + tvd * w.grad_tvd).sum().backward()
+    fwd, grad, _ = run(w)
+    assert torch.equal(ce.detach(), fwd["ce"]) and torch.equal(tvd.detach(), fwd["tvd"])
+    assert torch.equal(s.grad, grad)
