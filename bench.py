@@ -32,7 +32,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from distillation_ce_tvd_gb300 import binding, workloads  # noqa: E402
+from distillation_ce_tvd_gb300 import binding, sharding, workloads  # noqa: E402
 
 METRIC = "fused CE+TVD fwd+bwd tokens/s and HBM GB/s (% of peak), V=151936 bf16, 1 GB300"
 DEFAULT_WORKLOAD = "bt8192_v151936_bf16"
@@ -131,15 +131,6 @@ def dist_setup():
     return world, rank, local
 
 
-def max_over_ranks(x: float, world: int) -> float:
-    if world == 1:
-        return x
-    import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -227,19 +218,25 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--cluster", type=int, default=0,
+                    help="CTAs per row in the fused forward (0 = automatic)")
     args = ap.parse_args()
 
-    world, rank, local = dist_setup()
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        # the oracle runs on rank 0's host cores only; other ranks exit at once
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
         return
+    world, rank, local = dist_setup()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
-    w = workloads.make(args.workload, dev, rows=args.rows)
+    binding.set_forward_cluster(args.cluster)
+    # each rank holds its own batch of the workload (weak scaling, no exchange)
+    seed = workloads.WORKLOADS[args.workload]["seed"] + 1000 * rank
+    w = workloads.make(args.workload, dev, rows=args.rows, seed=seed)
     BT, V = w.BT, w.V
     elem = w.student.element_size()
     ce = torch.empty(BT, device=dev)
@@ -287,7 +284,7 @@ def main():
     total_ms = start.elapsed_time(end)
     fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
     bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    ms = max_over_ranks(total_ms / K, world)
+    ms = sharding.max_over_ranks(total_ms / K, world, dev)
     value = world * BT / (ms * 1e-3)
 
     nbytes = algorithmic_bytes(BT, V, elem)
@@ -341,7 +338,7 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize(dev)
-        e2e_ms = max_over_ranks(a.elapsed_time(b) / E, world)
+        e2e_ms = sharding.max_over_ranks(a.elapsed_time(b) / E, world, dev)
         e2e = {"value": world * BT / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                "steps": E}
@@ -360,6 +357,7 @@ def main():
             "config": {"workload": args.workload, "BT": BT, "V": V,
                        "logit_dtype": "bf16" if elem == 2 else "f32",
                        "parallelism": f"replicas{world}" if world > 1 else "single",
+                       "forward_ctas_per_row": args.cluster or "auto",
                        "l2": "no flush: each step streams 12.4 GB, far above the 129 MB L2"
                        if args.rows is None else "reduced rows"},
             "hbm_gbs": step_gbs,

@@ -9,7 +9,10 @@ notes):
     allowed and moves sigma by at most 2 p_v;
   * gradient: abs 1e-6 + rel 2e-3, widened at a row with near-ties by
     |grad_tvd| * 0.5 * p_v * (2 [v is a near-tie] + 2 * near-tie mass),
-    the most a set of allowed sign flips can move element v.
+    the most a set of allowed sign flips can move element v.  A bf16
+    gradient adds half a bf16 ulp of the reference value: rel 2e-3 is finer
+    than bf16's unit roundoff (2^-8), so even the correctly rounded result
+    could not meet it; fp32 gradients get no such allowance.
 Ignored rows must be exactly zero on both sides.
 """
 from __future__ import annotations
@@ -63,8 +66,21 @@ def check_forward(dtype, target, got: dict, ref: dict, tie_mass, ignore_index=-1
                                f"err {err[bad].max():.3e} tol {np.atleast_1d(tol)[0]:.3e}")
 
 
+def bf16_half_ulp(x):
+    """Half a bf16 ulp at |x| (bf16 keeps 8 significant bits)."""
+    a = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 8)
+
+
+def grad_tol(ref: np.ndarray, out_dtype) -> np.ndarray:
+    tol = 1e-6 + 2e-3 * np.abs(ref)
+    if out_dtype == torch.bfloat16:
+        tol = tol + bf16_half_ulp(np.abs(ref) * (1 + 2e-3) + 1e-6)
+    return tol
+
+
 def check_grad(got: np.ndarray, ref: np.ndarray, grad_tvd_rows, tie_masks, tie_mass, probs,
-               target, ignore_index=-100, what=""):
+               target, ignore_index=-100, what="", out_dtype=torch.float32):
     """got: gradient rows as fp64 (from bf16/fp32); ref: the oracle's fp64 rows."""
     tg = np.asarray(target)
     gtvd = np.asarray(grad_tvd_rows, np.float64)
@@ -76,7 +92,7 @@ def check_grad(got: np.ndarray, ref: np.ndarray, grad_tvd_rows, tie_masks, tie_m
         if np.isnan(f).all():
             assert np.isnan(g).all(), f"{what}row {r}: out-of-range target row must be NaN"
             continue
-        tol = 1e-6 + 2e-3 * np.abs(f)
+        tol = grad_tol(f, out_dtype)
         if tie_mass[r] > 0.0:
             tol = tol + abs(gtvd[r]) * 0.5 * probs[r] * (2.0 * tie_masks[r] + 2.0 * tie_mass[r])
         err = np.abs(g - f)

@@ -8,7 +8,8 @@ import torch
 
 import oracle
 from distillation_ce_tvd_gb300 import binding, workloads
-from parity_util import (check_forward, check_grad, oracle_rows, tie_info, to_host_rows)
+from parity_util import (check_forward, check_grad, grad_tol, oracle_rows, tie_info,
+                         to_host_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -55,7 +56,7 @@ def compare(w, fwd, grad, rows=None, what=""):
     got = {k: to_host_rows(v, rows).numpy() for k, v in fwd.items()}
     check_forward(w.student.dtype, tg, got, ref, mass, w.ignore_index, what)
     g = to_host_rows(grad, rows).double().numpy()
-    check_grad(g, ref_grad, gtvd, masks, mass, probs, tg, w.ignore_index, what)
+    check_grad(g, ref_grad, gtvd, masks, mass, probs, tg, w.ignore_index, what, grad.dtype)
     return ref
 
 
@@ -82,7 +83,7 @@ def test_tiny_workload_all_rows_and_fixture():
     assert st == 0
     compare(w, fwd, grad)
     np.testing.assert_allclose(fwd["tvd"].cpu().numpy(), d["forward"]["tvd"], atol=1e-5)
-    np.testing.assert_allclose(grad.cpu().double().numpy(), d["grad_student"], atol=1e-6, rtol=2e-3)
+    np.testing.assert_allclose(grad.cpu().double().numpy(), d["grad_student"], atol=1e-6, rtol=2e-3)  # fp32
     assert fwd["tvd"][3].item() == 0.0 and fwd["sigma"][3].item() == 0.0
     assert torch.all(grad[5] == 0)
 
@@ -265,7 +266,7 @@ def test_ce_subset(dtype, V):
     np.testing.assert_allclose(ce.cpu().numpy(), ref["ce"], atol=atol, rtol=0)
     np.testing.assert_allclose(lse.cpu().numpy(), ref["lse"], atol=atol, rtol=0)
     err = np.abs(g.cpu().double().numpy() - ref_g)
-    assert np.all(err <= 1e-6 + 2e-3 * np.abs(ref_g))
+    assert np.all(err <= grad_tol(ref_g, dtype))
 
 
 def test_autograd_wrapper_matches_direct_calls():
