@@ -1,6 +1,7 @@
 // C ABI of libfused_ce_tvd.so: argument checks, launch planning, dispatch.
 // The operations themselves are described in include/fused_ce_tvd.h.
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "fct_internal.h"
@@ -89,7 +90,13 @@ int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
 // Depends on V, the element type and the device only (never on BT), so
 // results do not depend on how the rows are batched.
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec) {
-  fct::FwdPlan plan{vec, 1, 0};
+  fct::FwdPlan plan{vec, 1, 0, 512};
+  // FCT_FWD_THREADS=1024 selects the 1024-thread CTA (tuning experiments).
+  static const int threads = [] {
+    const char* e = std::getenv("FCT_FWD_THREADS");
+    return (e && std::atoi(e) == 1024) ? 1024 : 512;
+  }();
+  plan.threads = threads;
   if (!tvd) return plan;  // one pass: nothing to keep in L2
   const double row_bytes = 2.0 * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
   const double budget = 0.45 * static_cast<double>(d.l2_bytes);

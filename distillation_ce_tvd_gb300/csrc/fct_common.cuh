@@ -64,6 +64,78 @@ __device__ __forceinline__ void lse2_update(Lse2& st, const float (&x)[N]) {
   st.s += acc;
 }
 
+// ---------------------------------------------------------------- packed fp32 pairs
+//
+// sm_100+ executes two fp32 operations per lane in one instruction
+// (fma/add/mul .f32x2), each lane rounded exactly like the scalar form.
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 A, B, C, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
+      "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 A, B, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t"
+      "add.rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
+// (pp, qp) += (p, q) when p > q; (pn, qn) += (p, q) when p < q; ties add
+// nothing.  Then sum|p - q| = (pp - qp) + (qn - pn) and
+// sum p*sign(p - q) = pp - pn, with sign(0) = 0 exactly.
+__device__ __forceinline__ void tvd_split(float p, float q, float2& pos, float2& neg) {
+  asm("{\n\t.reg .pred gt, lt;\n\t.reg .b64 PQ, A;\n\t"
+      "setp.gt.f32 gt, %4, %5;\n\tsetp.lt.f32 lt, %4, %5;\n\t"
+      "mov.b64 PQ, {%4, %5};\n\t"
+      "mov.b64 A, {%0, %1};\n\t@gt add.rn.f32x2 A, A, PQ;\n\tmov.b64 {%0, %1}, A;\n\t"
+      "mov.b64 A, {%2, %3};\n\t@lt add.rn.f32x2 A, A, PQ;\n\tmov.b64 {%2, %3}, A;\n\t}"
+      : "+f"(pos.x), "+f"(pos.y), "+f"(neg.x), "+f"(neg.y)
+      : "f"(p), "f"(q));
+}
+
+// Running base-2 log-sum-exp state with two partial sums (summed by add2).
+struct Lse2x {
+  float m2;
+  float2 s;
+};
+
+__device__ __forceinline__ Lse2x lse2x_empty() { return Lse2x{-INFINITY, make_float2(0.f, 0.f)}; }
+
+__device__ __forceinline__ Lse2 lse2x_fold(Lse2x a) { return Lse2{a.m2, a.s.x + a.s.y}; }
+
+// Fold N (even) values: one rescale if the group raises the maximum, then
+// N/2 packed FMAs for the exponents, N ex2, N/2 packed adds.
+template <int N>
+__device__ __forceinline__ void lse2x_update(Lse2x& st, const float (&x)[N]) {
+  static_assert(N % 2 == 0, "pairs");
+  float vm = fmaxf(x[0], x[1]);
+#pragma unroll
+  for (int j = 2; j < N; ++j) vm = fmaxf(vm, x[j]);
+  const float m2n = vm * kLog2e;
+  if (m2n > st.m2) {
+    const float sc = ex2(st.m2 - m2n);
+    st.s.x *= sc;
+    st.s.y *= sc;
+    st.m2 = m2n;
+  }
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+  const float2 nm = make_float2(-st.m2, -st.m2);
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const float2 a = fma2(make_float2(x[j], x[j + 1]), L2, nm);
+    st.s = add2(st.s, make_float2(ex2(a.x), ex2(a.y)));
+  }
+}
+
 // ---------------------------------------------------------------- memory
 
 // L2 eviction-priority policies for the cache_hint loads below.
@@ -95,6 +167,26 @@ __device__ __forceinline__ void st16(void* ptr, uint4 v, uint64_t pol) {
       :
       : "l"(ptr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
       : "memory");
+}
+
+// Asynchronous 16-byte global -> shared copy (per thread, no registers),
+// tagged with an L2 eviction policy; completion is tracked per thread with
+// commit/wait groups.
+__device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;"
+               :
+               : "r"(smem_dst), "l"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // Element-type traits.  A "vector" is the 16 bytes one thread moves at once:

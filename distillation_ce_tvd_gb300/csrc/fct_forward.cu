@@ -12,11 +12,19 @@
 //     CTAs exchange only scalar partials, through distributed shared memory.
 //   * Step 1 reads the row from HBM with an L2 evict_last hint; step 2
 //     re-reads the same bytes, which are still in L2 because the number of
-//     rows in flight (clusters on the GPU) times the row size is kept well
-//     under the L2 capacity by the choice of C.  HBM therefore sees each
-//     logit about once, and no (BT, V) buffer is ever written.
-//   * The grid is persistent: one cluster per slot the GPU can hold, looping
-//     over rows, so the launch is sized by the SM count, not by BT.
+//     rows in flight (clusters on the GPU) times the row size is kept under
+//     the L2 capacity.  HBM therefore sees each logit about once, and no
+//     (BT, V) buffer is ever written.
+//   * Every thread streams its own vectors through a private ring of
+//     kStages 16-byte slots per tensor in shared memory, filled by
+//     cp.async D steps ahead.  The feed runs on across the step-1/step-2
+//     boundary and into the next row, so loads stay in flight while the CTA
+//     reduces; no thread ever reads another thread's slot, so the ring needs
+//     no barrier.
+//   * Step 2 keeps four packed sums per thread: (sum p, sum q) over p > q and
+//     over p < q.  Then sum|p - q| = (P+ - Q+) + (Q- - P-) and
+//     sigma = P+ - P-, and ties contribute to neither (zero subgradient).
+//   * The grid is persistent: one cluster per row slot, looping over rows.
 //   * Student and teacher go through the very same code, so a row whose
 //     teacher equals its student bit for bit gets p == q everywhere and
 //     tvd = sigma = 0 exactly.
@@ -31,9 +39,7 @@ namespace fct {
 
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 8;  // 16-byte loads in flight per thread and row
+constexpr int kMaxWarps = 32;
 
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
@@ -43,7 +49,9 @@ __device__ __forceinline__ void cluster_sync_all() {
 // Block-wide merge of two Lse2 states.  Every warp folds the per-warp
 // partials in the same order, so every thread ends with identical values.
 // `buf` must not be rewritten before the next __syncthreads of the caller.
+template <int NT>
 __device__ __forceinline__ void block_merge2(Lse2& a, Lse2& b, float4* buf) {
+  constexpr int kWarps = NT / 32;
   a = warp_merge(a);
   b = warp_merge(b);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -54,7 +62,9 @@ __device__ __forceinline__ void block_merge2(Lse2& a, Lse2& b, float4* buf) {
   b = warp_merge(Lse2{w.z, w.w});
 }
 
+template <int NT>
 __device__ __forceinline__ void block_sum2(float& x, float& y, float2* buf) {
+  constexpr int kWarps = NT / 32;
   x = warp_sum(x);
   y = warp_sum(y);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -65,167 +75,319 @@ __device__ __forceinline__ void block_sum2(float& x, float& y, float2* buf) {
   y = warp_sum(w.y);
 }
 
-// Step-1 streaming over vectors [vb, ve) of one row (and of the teacher row
-// when kTvd): thread i takes vectors vb+i, vb+i+kThreads, ...
-template <typename T, int VE, bool kTvd>
-__device__ __forceinline__ void lse_pass(const T* s, const T* t, int64_t vb, int64_t ve,
-                                         uint64_t pol, Lse2& a, Lse2& b) {
-  int64_t i = vb + threadIdx.x;
-  for (; i + (kUnroll - 1) * kThreads < ve; i += kUnroll * kThreads) {
-    uint4 rs[kUnroll], rt[kUnroll];
+// The C CTAs of a cluster fold their step-1 partials in rank order.
+template <int C>
+__device__ __forceinline__ void cluster_merge2(Lse2& a, Lse2& b, float4* part) {
+  if constexpr (C > 1) {
+    if (threadIdx.x == 0) *part = make_float4(a.m2, a.s, b.m2, b.s);
+    cluster_sync_all();
+    cg::cluster_group cl = cg::this_cluster();
+    a = lse2_empty();
+    b = lse2_empty();
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      rs[k] = load_raw<T, VE>(s + (i + k * kThreads) * VE, pol);
-      if constexpr (kTvd) rt[k] = load_raw<T, VE>(t + (i + k * kThreads) * VE, pol);
+    for (int r = 0; r < C; ++r) {
+      const float4 w = *cl.map_shared_rank(part, r);
+      a = lse2_merge(a, Lse2{w.x, w.y});
+      b = lse2_merge(b, Lse2{w.z, w.w});
     }
+  }
+}
+
+// Rank 0 (thread 0) folds the step-2 partials of the C CTAs in rank order.
+template <int C>
+__device__ __forceinline__ void cluster_sum2(float& x, float& y, float2* part, int rank) {
+  if constexpr (C > 1) {
+    if (threadIdx.x == 0) *part = make_float2(x, y);
+    cluster_sync_all();
+    if (rank == 0 && threadIdx.x == 0) {
+      cg::cluster_group cl = cg::this_cluster();
+      x = 0.f;
+      y = 0.f;
 #pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      float x[VE];
-      unpack_raw<T, VE>(rs[k], x);
-      lse2_update(a, x);
-      if constexpr (kTvd) {
-        unpack_raw<T, VE>(rt[k], x);
-        lse2_update(b, x);
+      for (int r = 0; r < C; ++r) {
+        const float2 w = *cl.map_shared_rank(part, r);
+        x += w.x;
+        y += w.y;
       }
     }
   }
-  for (; i < ve; i += kThreads) {
-    float x[VE];
-    unpack_raw<T, VE>(load_raw<T, VE>(s + i * VE, pol), x);
-    lse2_update(a, x);
-    if constexpr (kTvd) {
-      unpack_raw<T, VE>(load_raw<T, VE>(t + i * VE, pol), x);
-      lse2_update(b, x);
-    }
-  }
 }
 
-// p and q of one element pair folded into (sum |p - q|, sum p*sign(p - q)).
-__device__ __forceinline__ void tvd_accum(float xs, float xt, float ns2, float nt2,
-                                          float& abs_sum, float& sig) {
+// One element pair of step 2, scalar form (tails and the unaligned path).
+__device__ __forceinline__ void tvd_accum1(float xs, float xt, float ns2, float nt2,
+                                           float2& pos, float2& neg) {
   const float p = ex2(fmaf(xs, kLog2e, ns2));
   const float q = ex2(fmaf(xt, kLog2e, nt2));
-  const float d = p - q;
-  abs_sum += fabsf(d);
-  sig += (d > 0.f) ? p : ((d < 0.f) ? -p : 0.f);
+  tvd_split(p, q, pos, neg);
 }
 
-template <typename T, int VE>
-__device__ __forceinline__ void tvd_pass(const T* s, const T* t, int64_t vb, int64_t ve,
-                                         uint64_t pol, float ns2, float nt2,
-                                         float& abs_sum, float& sig) {
-  int64_t i = vb + threadIdx.x;
-  for (; i + (kUnroll - 1) * kThreads < ve; i += kUnroll * kThreads) {
-    uint4 rs[kUnroll], rt[kUnroll];
-#pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      rs[k] = load_raw<T, VE>(s + (i + k * kThreads) * VE, pol);
-      rt[k] = load_raw<T, VE>(t + (i + k * kThreads) * VE, pol);
-    }
-#pragma unroll
-    for (int k = 0; k < kUnroll; ++k) {
-      float xs[VE], xt[VE];
-      unpack_raw<T, VE>(rs[k], xs);
-      unpack_raw<T, VE>(rt[k], xt);
-      float a = 0.f, g = 0.f;
-#pragma unroll
-      for (int j = 0; j < VE; ++j) tvd_accum(xs[j], xt[j], ns2, nt2, a, g);
-      abs_sum += a;
-      sig += g;
-    }
+template <bool kTvd>
+__device__ __forceinline__ void write_row(const FwdArgs& p, int64_t row, int64_t tg, float lse_s,
+                                          float lse_t, float abs_sum, float sig, float s_at_tg) {
+  p.lse_s[row] = lse_s;
+  if constexpr (kTvd) {
+    p.tvd[row] = 0.5f * abs_sum;
+    p.lse_t[row] = lse_t;
+    p.sigma[row] = sig;
   }
-  for (; i < ve; i += kThreads) {
-    float xs[VE], xt[VE];
-    unpack_raw<T, VE>(load_raw<T, VE>(s + i * VE, pol), xs);
-    unpack_raw<T, VE>(load_raw<T, VE>(t + i * VE, pol), xt);
-    float a = 0.f, g = 0.f;
-#pragma unroll
-    for (int j = 0; j < VE; ++j) tvd_accum(xs[j], xt[j], ns2, nt2, a, g);
-    abs_sum += a;
-    sig += g;
+  if (tg < 0 || tg >= p.V) {
+    p.ce[row] = __uint_as_float(0x7fc00000u);
+    if (p.dev_status) atomicOr(p.dev_status, FCT_DEV_TARGET_OUT_OF_RANGE);
+  } else {
+    p.ce[row] = lse_s - s_at_tg;
   }
 }
 
-// One row per cluster of C CTAs; kTvd = false is the plain cross-entropy
-// forward (student only, ce and lse outputs).
-template <typename T, int VE, int C, bool kTvd>
-__global__ void __launch_bounds__(kThreads, 1) forward_kernel(FwdArgs p) {
-  __shared__ float4 red_lse[kWarps];
-  __shared__ float2 red_sum[kWarps];
-  __shared__ float4 part_lse;  // this CTA's step-1 partial, read by its peers
-  __shared__ float2 part_sum;  // this CTA's step-2 partial, read by rank 0
+template <bool kTvd>
+__device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
+  p.ce[row] = 0.f;
+  p.lse_s[row] = 0.f;
+  if constexpr (kTvd) {
+    p.tvd[row] = 0.f;
+    p.lse_t[row] = 0.f;
+    p.sigma[row] = 0.f;
+  }
+}
 
-  const T* __restrict__ S = static_cast<const T*>(p.student);
-  const T* __restrict__ Tt = static_cast<const T*>(p.teacher);
+// ===================================================================== pipelined path
+//
+// Per thread, the sequence of 16-byte steps is: for each non-ignored row of
+// this cluster (rows cluster_id, cluster_id + n_clusters, ...), step 1's n_my
+// vectors, then (fused loss only) step 2's n_my vectors.  Both the feed and
+// the consumer walk this same sequence; the feed runs kStages steps ahead.
+
+template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
+struct Pipe {
+  static constexpr int kPasses = kTvd ? 2 : 1;
+  static constexpr int kTensors = kTvd ? 2 : 1;
+
+  // feed cursor
+  int64_t row;
+  int64_t k;
+  int pass;
+  // fixed per thread
+  int64_t n_my;      // vectors of this thread in each pass of a row
+  int64_t first_v;   // vector index of this thread's first vector in the row
+  uint32_t ring;     // shared address of slot 0 for this thread
+  uint64_t keep, drop;
+
+  __device__ __forceinline__ static uint32_t slot_addr(uint32_t ring, int slot, int tensor) {
+    return ring + static_cast<uint32_t>((slot * kTensors + tensor) * NT * 16);
+  }
+
+  __device__ __forceinline__ int64_t next_row(const FwdArgs& p, int64_t r, int64_t n_clusters) const {
+    r += n_clusters;
+    while (r < p.BT && p.target[r] == p.ignore_index) r += n_clusters;
+    return r;
+  }
+
+  // Issue the copies of the next step of the sequence into `slot`, then
+  // commit one group (empty once the sequence is exhausted).
+  __device__ __forceinline__ void feed(const FwdArgs& p, int slot, int64_t n_clusters) {
+    if (row < p.BT && n_my > 0) {
+      const int64_t v = first_v + k * NT;
+      const uint64_t pol = pass == 0 ? keep : drop;
+      const T* s = static_cast<const T*>(p.student) + row * p.ld_s + v * VE;
+      cp_async16(slot_addr(ring, slot, 0), s, pol);
+      if constexpr (kTvd) {
+        const T* t = static_cast<const T*>(p.teacher) + row * p.ld_t + v * VE;
+        cp_async16(slot_addr(ring, slot, 1), t, pol);
+      }
+      if (++k == n_my) {
+        k = 0;
+        if (++pass == kPasses) {
+          pass = 0;
+          row = next_row(p, row, n_clusters);
+        }
+      }
+    }
+    cp_async_commit();
+  }
+};
+
+template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
+__global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
+  using P = Pipe<T, VE, C, kTvd, NT, kStages>;
+  extern __shared__ __align__(16) uint4 ring_mem[];
+  __shared__ float4 red_lse[kMaxWarps];
+  __shared__ float2 red_sum[kMaxWarps];
+  __shared__ float4 part_lse;
+  __shared__ float2 part_sum;
+
   const int rank = (C > 1) ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
   const int64_t cluster_id = blockIdx.x / C;
   const int64_t n_clusters = gridDim.x / C;
-
   const int64_t nvec = p.V / VE;
   const int64_t tail0 = nvec * VE;
   const int64_t per = (nvec + C - 1) / C;
   const int64_t vb = min(nvec, rank * per);
   const int64_t ve = min(nvec, vb + per);
+  const int64_t span = ve - vb;
+  const int tid = threadIdx.x;
   const bool owns_tail = (rank == C - 1);
 
-  const uint64_t keep = policy_evict_last();
-  const uint64_t drop = policy_evict_first();
+  P pipe;
+  pipe.n_my = (span > tid) ? (span - tid + NT - 1) / NT : 0;
+  pipe.first_v = vb + tid;
+  pipe.ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_mem)) + tid * 16;
+  pipe.keep = policy_evict_last();
+  pipe.drop = policy_evict_first();
+  pipe.k = 0;
+  pipe.pass = 0;
+  pipe.row = cluster_id;
+  while (pipe.row < p.BT && p.target[pipe.row] == p.ignore_index) pipe.row += n_clusters;
+
+  // this thread's slots: ring_mem[(slot * kTensors + tensor) * NT + tid]
+  const uint4* mine = ring_mem + tid;
+
+  // prologue: kStages steps in flight
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) pipe.feed(p, s, n_clusters);
+  int slot = 0;
+
+  const T* S = static_cast<const T*>(p.student);
+  const T* Tt = static_cast<const T*>(p.teacher);
 
   for (int64_t row = cluster_id; row < p.BT; row += n_clusters) {
     const int64_t tg = p.target[row];
     if (tg == p.ignore_index) {
-      if (rank == 0 && threadIdx.x == 0) {
-        p.ce[row] = 0.f;
-        p.lse_s[row] = 0.f;
-        if constexpr (kTvd) {
-          p.tvd[row] = 0.f;
-          p.lse_t[row] = 0.f;
-          p.sigma[row] = 0.f;
-        }
-      }
-      continue;  // uniform over the whole cluster: no barrier is skipped unevenly
+      if (rank == 0 && tid == 0) write_ignored<kTvd>(p, row);
+      continue;  // uniform over the cluster; the feed skips this row too
     }
     const T* srow = S + row * p.ld_s;
     const T* trow = kTvd ? Tt + row * p.ld_t : nullptr;
 
     // ---- step 1: log-sum-exp of both rows
+    Lse2x a = lse2x_empty(), b = lse2x_empty();
+    for (int64_t k = 0; k < pipe.n_my; ++k) {
+      cp_async_wait<kStages - 1>();
+      float x[VE];
+      unpack_raw<T, VE>(mine[(slot * P::kTensors) * NT], x);
+      lse2x_update(a, x);
+      if constexpr (kTvd) {
+        unpack_raw<T, VE>(mine[(slot * P::kTensors + 1) * NT], x);
+        lse2x_update(b, x);
+      }
+      pipe.feed(p, slot, n_clusters);
+      slot = (slot + 1 == kStages) ? 0 : slot + 1;
+    }
+    Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
+    if (owns_tail && tail0 + tid < p.V) {
+      float xs[1] = {Elem<T>::load1(srow + tail0 + tid)};
+      lse2_update(fa, xs);
+      if constexpr (kTvd) {
+        float xt[1] = {Elem<T>::load1(trow + tail0 + tid)};
+        lse2_update(fb, xt);
+      }
+    }
+    block_merge2<NT>(fa, fb, red_lse);
+    cluster_merge2<C>(fa, fb, &part_lse);
+    const float lse_s = lse2_finish(fa);
+
+    if constexpr (!kTvd) {
+      if (rank == 0 && tid == 0) {
+        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
+        write_row<false>(p, row, tg, lse_s, 0.f, 0.f, 0.f, s_tg);
+      }
+      // peers may still read part_lse; warps may still read red_lse
+      if constexpr (C > 1) {
+        cluster_sync_all();
+      } else {
+        __syncthreads();
+      }
+    } else {
+      const float lse_t = lse2_finish(fb);
+      // The backward recomputes p and q from the stored lse values with this
+      // same expression (x*log2e - lse*log2e, one FMA, then ex2), so both
+      // kernels see bit-identical p and q.
+      const float ns2 = -(lse_s * kLog2e);
+      const float nt2 = -(lse_t * kLog2e);
+      const float2 L2 = make_float2(kLog2e, kLog2e);
+      const float2 nst = make_float2(ns2, nt2);
+
+      // ---- step 2: split sums of (p, q) by the sign of p - q
+      float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
+      for (int64_t k = 0; k < pipe.n_my; ++k) {
+        cp_async_wait<kStages - 1>();
+        float xs[VE], xt[VE];
+        unpack_raw<T, VE>(mine[(slot * P::kTensors) * NT], xs);
+        unpack_raw<T, VE>(mine[(slot * P::kTensors + 1) * NT], xt);
+#pragma unroll
+        for (int j = 0; j < VE; ++j) {
+          const float2 e = fma2(make_float2(xs[j], xt[j]), L2, nst);
+          tvd_split(ex2(e.x), ex2(e.y), pos, neg);
+        }
+        pipe.feed(p, slot, n_clusters);
+        slot = (slot + 1 == kStages) ? 0 : slot + 1;
+      }
+      if (owns_tail && tail0 + tid < p.V) {
+        tvd_accum1(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid), ns2,
+                   nt2, pos, neg);
+      }
+      float abs_sum = (pos.x - pos.y) + (neg.y - neg.x);
+      float sig = pos.x - neg.x;
+      block_sum2<NT>(abs_sum, sig, red_sum);
+      cluster_sum2<C>(abs_sum, sig, &part_sum, rank);
+      if (rank == 0 && tid == 0) {
+        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
+        write_row<true>(p, row, tg, lse_s, lse_t, abs_sum, sig, s_tg);
+      }
+    }
+  }
+  cp_async_wait_all();
+  // No CTA may leave while a peer can still read its shared memory.
+  if constexpr (C > 1) cluster_sync_all();
+}
+
+// ===================================================================== scalar path
+//
+// Rows whose pointers or strides are not 16-byte aligned: plain element
+// loads, same arithmetic and reductions.
+
+constexpr int kScalarThreads = 512;
+
+template <typename T, int C, bool kTvd>
+__global__ void __launch_bounds__(kScalarThreads, 1) forward_scalar(FwdArgs p) {
+  constexpr int NT = kScalarThreads;
+  __shared__ float4 red_lse[kMaxWarps];
+  __shared__ float2 red_sum[kMaxWarps];
+  __shared__ float4 part_lse;
+  __shared__ float2 part_sum;
+
+  const int rank = (C > 1) ? static_cast<int>(cg::this_cluster().block_rank()) : 0;
+  const int64_t cluster_id = blockIdx.x / C;
+  const int64_t n_clusters = gridDim.x / C;
+  const int64_t per = (p.V + C - 1) / C;
+  const int64_t vb = min(p.V, rank * per);
+  const int64_t ve = min(p.V, vb + per);
+  const T* S = static_cast<const T*>(p.student);
+  const T* Tt = static_cast<const T*>(p.teacher);
+
+  for (int64_t row = cluster_id; row < p.BT; row += n_clusters) {
+    const int64_t tg = p.target[row];
+    if (tg == p.ignore_index) {
+      if (rank == 0 && threadIdx.x == 0) write_ignored<kTvd>(p, row);
+      continue;
+    }
+    const T* srow = S + row * p.ld_s;
+    const T* trow = kTvd ? Tt + row * p.ld_t : nullptr;
     Lse2 a = lse2_empty(), b = lse2_empty();
-    lse_pass<T, VE, kTvd>(srow, trow, vb, ve, kTvd ? keep : drop, a, b);
-    if (owns_tail && tail0 + threadIdx.x < p.V) {
-      float xs[1] = {Elem<T>::load1(srow + tail0 + threadIdx.x)};
+    for (int64_t v = vb + threadIdx.x; v < ve; v += NT) {
+      float xs[1] = {Elem<T>::load1(srow + v)};
       lse2_update(a, xs);
       if constexpr (kTvd) {
-        float xt[1] = {Elem<T>::load1(trow + tail0 + threadIdx.x)};
+        float xt[1] = {Elem<T>::load1(trow + v)};
         lse2_update(b, xt);
       }
     }
-    block_merge2(a, b, red_lse);
-    if constexpr (C > 1) {
-      if (threadIdx.x == 0) part_lse = make_float4(a.m2, a.s, b.m2, b.s);
-      cluster_sync_all();
-      cg::cluster_group cl = cg::this_cluster();
-      a = lse2_empty();
-      b = lse2_empty();
-#pragma unroll
-      for (int r = 0; r < C; ++r) {  // same order in every CTA: identical results
-        const float4 w = *cl.map_shared_rank(&part_lse, r);
-        a = lse2_merge(a, Lse2{w.x, w.y});
-        b = lse2_merge(b, Lse2{w.z, w.w});
-      }
-    }
+    block_merge2<NT>(a, b, red_lse);
+    cluster_merge2<C>(a, b, &part_lse);
     const float lse_s = lse2_finish(a);
-
     if constexpr (!kTvd) {
       if (rank == 0 && threadIdx.x == 0) {
-        p.lse_s[row] = lse_s;
-        if (tg < 0 || tg >= p.V) {
-          p.ce[row] = __uint_as_float(0x7fc00000u);
-          if (p.dev_status) atomicOr(p.dev_status, FCT_DEV_TARGET_OUT_OF_RANGE);
-        } else {
-          p.ce[row] = lse_s - Elem<T>::load1(srow + tg);
-        }
+        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
+        write_row<false>(p, row, tg, lse_s, 0.f, 0.f, 0.f, s_tg);
       }
-      // Peers may still read part_lse and warps may still read red_lse.
       if constexpr (C > 1) {
         cluster_sync_all();
       } else {
@@ -233,58 +395,33 @@ __global__ void __launch_bounds__(kThreads, 1) forward_kernel(FwdArgs p) {
       }
     } else {
       const float lse_t = lse2_finish(b);
-      // The backward recomputes p and q from the stored lse values with this
-      // same expression, so both passes see bit-identical p and q.
       const float ns2 = -(lse_s * kLog2e);
       const float nt2 = -(lse_t * kLog2e);
-
-      // ---- step 2: sum |p - q| and sigma
-      float abs_sum = 0.f, sig = 0.f;
-      tvd_pass<T, VE>(srow, trow, vb, ve, drop, ns2, nt2, abs_sum, sig);
-      if (owns_tail && tail0 + threadIdx.x < p.V) {
-        tvd_accum(Elem<T>::load1(srow + tail0 + threadIdx.x),
-                  Elem<T>::load1(trow + tail0 + threadIdx.x), ns2, nt2, abs_sum, sig);
-      }
-      block_sum2(abs_sum, sig, red_sum);
-      if constexpr (C > 1) {
-        if (threadIdx.x == 0) part_sum = make_float2(abs_sum, sig);
-        cluster_sync_all();
-        if (rank == 0 && threadIdx.x == 0) {
-          cg::cluster_group cl = cg::this_cluster();
-          abs_sum = 0.f;
-          sig = 0.f;
-#pragma unroll
-          for (int r = 0; r < C; ++r) {
-            const float2 w = *cl.map_shared_rank(&part_sum, r);
-            abs_sum += w.x;
-            sig += w.y;
-          }
-        }
-      }
+      float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
+      for (int64_t v = vb + threadIdx.x; v < ve; v += NT)
+        tvd_accum1(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v), ns2, nt2, pos, neg);
+      float abs_sum = (pos.x - pos.y) + (neg.y - neg.x);
+      float sig = pos.x - neg.x;
+      block_sum2<NT>(abs_sum, sig, red_sum);
+      cluster_sum2<C>(abs_sum, sig, &part_sum, rank);
       if (rank == 0 && threadIdx.x == 0) {
-        p.tvd[row] = 0.5f * abs_sum;
-        p.lse_s[row] = lse_s;
-        p.lse_t[row] = lse_t;
-        p.sigma[row] = sig;
-        if (tg < 0 || tg >= p.V) {
-          p.ce[row] = __uint_as_float(0x7fc00000u);
-          if (p.dev_status) atomicOr(p.dev_status, FCT_DEV_TARGET_OUT_OF_RANGE);
-        } else {
-          p.ce[row] = lse_s - Elem<T>::load1(srow + tg);
-        }
+        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
+        write_row<true>(p, row, tg, lse_s, lse_t, abs_sum, sig, s_tg);
       }
     }
   }
-  // No CTA may leave while a peer can still read its shared memory.
   if constexpr (C > 1) cluster_sync_all();
 }
 
-template <typename T, int VE, int C, bool kTvd>
-cudaError_t launch(const FwdArgs& a, int n_clusters, cudaStream_t stream) {
+// ===================================================================== launch
+
+template <typename K>
+cudaError_t launch_cluster(K kernel, int C, int nt, size_t smem, int n_clusters,
+                           const FwdArgs& a, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(n_clusters * C));
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.blockDim = dim3(nt);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -293,47 +430,76 @@ cudaError_t launch(const FwdArgs& a, int n_clusters, cudaStream_t stream) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, forward_kernel<T, VE, C, kTvd>, a);
+  return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-template <typename T, int VE, int C, bool kTvd>
-int max_clusters() {
-  static int cached = [] {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(C * 64);
-    cfg.blockDim = dim3(kThreads);
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = C;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, forward_kernel<T, VE, C, kTvd>, &cfg) != cudaSuccess) {
+template <typename K>
+int max_clusters(K kernel, int C, int nt, size_t smem) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(C * 64);
+  cfg.blockDim = dim3(nt);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  return n > 0 ? n : 1;
+}
+
+// One (kernel, configuration) instance: shared-memory opt-in and the
+// occupancy query are done once per process.
+template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
+cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
+  constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * NT * 16;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, NT, kStages>;
+  static int n_max = [&] {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmem)) != cudaSuccess) {
       cudaGetLastError();
-      n = 0;
+      return -1;
     }
-    return n;
+    return max_clusters(kernel, C, NT, kSmem);
   }();
-  return cached;
+  if (n_max < 0) return cudaErrorInvalidConfiguration;
+  int n = n_max;
+  if (n_slots > 0 && n > n_slots) n = n_slots;
+  if (n > a.BT) n = static_cast<int>(a.BT);
+  return launch_cluster(kernel, C, NT, kSmem, n, a, st);
 }
 
-template <typename T, int VE, bool kTvd>
-cudaError_t dispatch_c(const FwdArgs& a, int C, int n_slots, cudaStream_t st) {
-  auto go = [&](auto cc) -> cudaError_t {
-    constexpr int CC = decltype(cc)::value;
-    int n = max_clusters<T, VE, CC, kTvd>();
-    if (n <= 0) n = 1;
-    if (n_slots > 0 && n > n_slots) n = n_slots;
-    if (n > a.BT) n = static_cast<int>(a.BT);
-    return launch<T, VE, CC, kTvd>(a, n, st);
-  };
-  switch (C) {
-    case 1: return go(std::integral_constant<int, 1>{});
-    case 2: return go(std::integral_constant<int, 2>{});
-    case 4: return go(std::integral_constant<int, 4>{});
-    default: return go(std::integral_constant<int, 8>{});
+template <typename T, int C, bool kTvd>
+cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
+  auto kernel = forward_scalar<T, C, kTvd>;
+  static int n_max = max_clusters(kernel, C, kScalarThreads, 0);
+  int n = n_max;
+  if (n_slots > 0 && n > n_slots) n = n_slots;
+  if (n > a.BT) n = static_cast<int>(a.BT);
+  return launch_cluster(kernel, C, kScalarThreads, 0, n, a, st);
+}
+
+template <typename T, int C, bool kTvd>
+cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  constexpr int VE = Elem<T>::kVec;
+  if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
+  if (plan.threads == 1024) return run_pipelined<T, VE, C, kTvd, 1024, 4>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, 512, 8>(a, plan.slots, st);
+}
+
+template <typename T, bool kTvd>
+cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  switch (plan.cluster) {
+    case 1: return run<T, 1, kTvd>(a, plan, st);
+    case 2: return run<T, 2, kTvd>(a, plan, st);
+    case 4: return run<T, 4, kTvd>(a, plan, st);
+    default: return run<T, 8, kTvd>(a, plan, st);
   }
 }
 
@@ -341,19 +507,9 @@ cudaError_t dispatch_c(const FwdArgs& a, int C, int n_slots, cudaStream_t st) {
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   if (a.dtype == FCT_BF16) {
-    if (a.tvd) {
-      return plan.vec ? dispatch_c<bf16_t, 8, true>(a, plan.cluster, plan.slots, st)
-                      : dispatch_c<bf16_t, 1, true>(a, plan.cluster, plan.slots, st);
-    }
-    return plan.vec ? dispatch_c<bf16_t, 8, false>(a, plan.cluster, plan.slots, st)
-                    : dispatch_c<bf16_t, 1, false>(a, plan.cluster, plan.slots, st);
+    return a.tvd ? run_c<bf16_t, true>(a, plan, st) : run_c<bf16_t, false>(a, plan, st);
   }
-  if (a.tvd) {
-    return plan.vec ? dispatch_c<float, 4, true>(a, plan.cluster, plan.slots, st)
-                    : dispatch_c<float, 1, true>(a, plan.cluster, plan.slots, st);
-  }
-  return plan.vec ? dispatch_c<float, 4, false>(a, plan.cluster, plan.slots, st)
-                  : dispatch_c<float, 1, false>(a, plan.cluster, plan.slots, st);
+  return a.tvd ? run_c<float, true>(a, plan, st) : run_c<float, false>(a, plan, st);
 }
 
 }  // namespace fct
