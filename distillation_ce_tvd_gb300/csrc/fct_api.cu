@@ -85,21 +85,22 @@ int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
 
 // Rows in flight and CTAs per row for the two-pass fused forward.  The
 // second pass re-reads each row from L2, so the rows in flight times the
-// bytes of a student+teacher row must stay well inside L2; rows are split
+// bytes of a student+teacher row must stay inside L2 (80%: measured on
+// GB300, one CTA per row at V = 151936 bf16 beats splitting rows); rows are split
 // over a cluster of C CTAs until every SM still gets at least one CTA.
 // Depends on V, the element type and the device only (never on BT), so
 // results do not depend on how the rows are batched.
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec) {
-  fct::FwdPlan plan{vec, 1, 0, 512};
-  // FCT_FWD_THREADS=1024 selects the 1024-thread CTA (tuning experiments).
-  static const int threads = [] {
-    const char* e = std::getenv("FCT_FWD_THREADS");
-    return (e && std::atoi(e) == 1024) ? 1024 : 512;
+  fct::FwdPlan plan{vec, 1, 0, false};
+  // FCT_FWD_PACKED=1 selects packed f32x2 arithmetic (tuning experiments).
+  static const bool packed = [] {
+    const char* e = std::getenv("FCT_FWD_PACKED");
+    return e && std::atoi(e) == 1;
   }();
-  plan.threads = threads;
+  plan.packed = packed;
   if (!tvd) return plan;  // one pass: nothing to keep in L2
   const double row_bytes = 2.0 * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
-  const double budget = 0.45 * static_cast<double>(d.l2_bytes);
+  const double budget = 0.80 * static_cast<double>(d.l2_bytes);
   int64_t fit = static_cast<int64_t>(budget / row_bytes);
   if (fit < 1) fit = 1;
   int C = g_cluster_override.load();

@@ -102,6 +102,37 @@ __device__ __forceinline__ void tvd_split(float p, float q, float2& pos, float2&
       : "f"(p), "f"(q));
 }
 
+// Scalar form of tvd_split: four predicated adds instead of two packed ones.
+__device__ __forceinline__ void tvd_split_scalar(float p, float q, float2& pos, float2& neg) {
+  asm("{\n\t.reg .pred gt, lt;\n\t"
+      "setp.gt.f32 gt, %4, %5;\n\tsetp.lt.f32 lt, %4, %5;\n\t"
+      "@gt add.f32 %0, %0, %4;\n\t@gt add.f32 %1, %1, %5;\n\t"
+      "@lt add.f32 %2, %2, %4;\n\t@lt add.f32 %3, %3, %5;\n\t}"
+      : "+f"(pos.x), "+f"(pos.y), "+f"(neg.x), "+f"(neg.y)
+      : "f"(p), "f"(q));
+}
+
+// max(a, b, c) in one instruction (sm_100+).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+template <int N>
+__device__ __forceinline__ float vec_max(const float (&x)[N]) {
+  if constexpr (N == 8) {
+    return max3(max3(x[0], x[1], x[2]), max3(x[3], x[4], x[5]), fmaxf(x[6], x[7]));
+  } else if constexpr (N == 4) {
+    return max3(x[0], x[1], fmaxf(x[2], x[3]));
+  } else {
+    float m = x[0];
+#pragma unroll
+    for (int j = 1; j < N; ++j) m = fmaxf(m, x[j]);
+    return m;
+  }
+}
+
 // Running base-2 log-sum-exp state with two partial sums (summed by add2).
 struct Lse2x {
   float m2;
@@ -114,25 +145,31 @@ __device__ __forceinline__ Lse2 lse2x_fold(Lse2x a) { return Lse2{a.m2, a.s.x + 
 
 // Fold N (even) values: one rescale if the group raises the maximum, then
 // N/2 packed FMAs for the exponents, N ex2, N/2 packed adds.
-template <int N>
+template <bool kPacked, int N>
 __device__ __forceinline__ void lse2x_update(Lse2x& st, const float (&x)[N]) {
   static_assert(N % 2 == 0, "pairs");
-  float vm = fmaxf(x[0], x[1]);
-#pragma unroll
-  for (int j = 2; j < N; ++j) vm = fmaxf(vm, x[j]);
-  const float m2n = vm * kLog2e;
+  const float m2n = vec_max(x) * kLog2e;
   if (m2n > st.m2) {
     const float sc = ex2(st.m2 - m2n);
     st.s.x *= sc;
     st.s.y *= sc;
     st.m2 = m2n;
   }
-  const float2 L2 = make_float2(kLog2e, kLog2e);
-  const float2 nm = make_float2(-st.m2, -st.m2);
+  if constexpr (kPacked) {
+    const float2 L2 = make_float2(kLog2e, kLog2e);
+    const float2 nm = make_float2(-st.m2, -st.m2);
 #pragma unroll
-  for (int j = 0; j < N; j += 2) {
-    const float2 a = fma2(make_float2(x[j], x[j + 1]), L2, nm);
-    st.s = add2(st.s, make_float2(ex2(a.x), ex2(a.y)));
+    for (int j = 0; j < N; j += 2) {
+      const float2 a = fma2(make_float2(x[j], x[j + 1]), L2, nm);
+      st.s = add2(st.s, make_float2(ex2(a.x), ex2(a.y)));
+    }
+  } else {
+    const float nm = -st.m2;
+#pragma unroll
+    for (int j = 0; j < N; j += 2) {
+      st.s.x += ex2(fmaf(x[j], kLog2e, nm));
+      st.s.y += ex2(fmaf(x[j + 1], kLog2e, nm));
+    }
   }
 }
 

@@ -151,53 +151,65 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 
 // ===================================================================== pipelined path
 //
-// Per thread, the sequence of 16-byte steps is: for each non-ignored row of
-// this cluster (rows cluster_id, cluster_id + n_clusters, ...), step 1's n_my
-// vectors, then (fused loss only) step 2's n_my vectors.  Both the feed and
-// the consumer walk this same sequence; the feed runs kStages steps ahead.
+// Per thread, the sequence of steps is: for each non-ignored row of this
+// cluster (rows cluster_id, cluster_id + n_clusters, ...), step 1's n_my
+// vectors, then (fused loss only) step 2's n_my vectors, two vectors
+// (NT vectors apart) per step.  Both the feed and the consumer walk this
+// same sequence; the feed runs kStages steps ahead.
 
-template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
-struct Pipe {
+constexpr int kPerStep = 2;  // vectors per tensor moved by one step
+
+template <typename T, int VE, bool kTvd, int NT, int kStages>
+struct Feed {
   static constexpr int kPasses = kTvd ? 2 : 1;
   static constexpr int kTensors = kTvd ? 2 : 1;
+  static constexpr uint32_t kSlotBytes = kTensors * kPerStep * NT * 16;
+  static constexpr int64_t kStride = int64_t(NT) * 16;  // bytes between a thread's vectors
 
-  // feed cursor
+  const char* sp;  // student bytes of the current step's first vector
+  const char* tp;  // teacher bytes of the current step's first vector
   int64_t row;
-  int64_t k;
-  int pass;
-  // fixed per thread
-  int64_t n_my;      // vectors of this thread in each pass of a row
-  int64_t first_v;   // vector index of this thread's first vector in the row
-  uint32_t ring;     // shared address of slot 0 for this thread
+  int32_t q;       // step within the pass
+  int32_t pass;
+  int32_t n_my, n_steps;
+  int64_t first_byte;  // byte offset of this thread's first vector within a row
+  uint32_t ring;       // shared address of this thread's 16 bytes in slot 0
   uint64_t keep, drop;
 
-  __device__ __forceinline__ static uint32_t slot_addr(uint32_t ring, int slot, int tensor) {
-    return ring + static_cast<uint32_t>((slot * kTensors + tensor) * NT * 16);
+  __device__ __forceinline__ void seek_row(const FwdArgs& p) {
+    sp = static_cast<const char*>(p.student) + (row * p.ld_s) * int64_t(sizeof(T)) + first_byte;
+    if constexpr (kTvd)
+      tp = static_cast<const char*>(p.teacher) + (row * p.ld_t) * int64_t(sizeof(T)) + first_byte;
   }
 
-  __device__ __forceinline__ int64_t next_row(const FwdArgs& p, int64_t r, int64_t n_clusters) const {
-    r += n_clusters;
-    while (r < p.BT && p.target[r] == p.ignore_index) r += n_clusters;
-    return r;
+  __device__ __forceinline__ void next_row(const FwdArgs& p, int64_t n_clusters) {
+    row += n_clusters;
+    while (row < p.BT && p.target[row] == p.ignore_index) row += n_clusters;
+    if (row < p.BT) seek_row(p);
   }
 
-  // Issue the copies of the next step of the sequence into `slot`, then
-  // commit one group (empty once the sequence is exhausted).
+  // Issue the next step's copies into `slot` and commit one group (an
+  // empty group once this thread's sequence is exhausted).
   __device__ __forceinline__ void feed(const FwdArgs& p, int slot, int64_t n_clusters) {
-    if (row < p.BT && n_my > 0) {
-      const int64_t v = first_v + k * NT;
+    if (row < p.BT) {
       const uint64_t pol = pass == 0 ? keep : drop;
-      const T* s = static_cast<const T*>(p.student) + row * p.ld_s + v * VE;
-      cp_async16(slot_addr(ring, slot, 0), s, pol);
+      const uint32_t dst = ring + slot * kSlotBytes;
+      const bool two = (2 * q + 1) < n_my;
+      cp_async16(dst, sp, pol);
+      if (two) cp_async16(dst + NT * 16, sp + kStride, pol);
       if constexpr (kTvd) {
-        const T* t = static_cast<const T*>(p.teacher) + row * p.ld_t + v * VE;
-        cp_async16(slot_addr(ring, slot, 1), t, pol);
+        cp_async16(dst + 2 * NT * 16, tp, pol);
+        if (two) cp_async16(dst + 3 * NT * 16, tp + kStride, pol);
       }
-      if (++k == n_my) {
-        k = 0;
+      sp += 2 * kStride;
+      if constexpr (kTvd) tp += 2 * kStride;
+      if (++q == n_steps) {
+        q = 0;
         if (++pass == kPasses) {
           pass = 0;
-          row = next_row(p, row, n_clusters);
+          next_row(p, n_clusters);
+        } else {
+          seek_row(p);
         }
       }
     }
@@ -205,9 +217,10 @@ struct Pipe {
   }
 };
 
-template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
+template <typename T, int VE, int C, bool kTvd, int NT, int kStages, bool kPacked>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
-  using P = Pipe<T, VE, C, kTvd, NT, kStages>;
+  using F = Feed<T, VE, kTvd, NT, kStages>;
+  static_assert((kStages & (kStages - 1)) == 0, "power-of-two ring");
   extern __shared__ __align__(16) uint4 ring_mem[];
   __shared__ float4 red_lse[kMaxWarps];
   __shared__ float2 red_sum[kMaxWarps];
@@ -226,27 +239,29 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   const int tid = threadIdx.x;
   const bool owns_tail = (rank == C - 1);
 
-  P pipe;
-  pipe.n_my = (span > tid) ? (span - tid + NT - 1) / NT : 0;
-  pipe.first_v = vb + tid;
-  pipe.ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_mem)) + tid * 16;
-  pipe.keep = policy_evict_last();
-  pipe.drop = policy_evict_first();
-  pipe.k = 0;
-  pipe.pass = 0;
-  pipe.row = cluster_id;
-  while (pipe.row < p.BT && p.target[pipe.row] == p.ignore_index) pipe.row += n_clusters;
+  F f;
+  f.n_my = (span > tid) ? static_cast<int32_t>((span - tid + NT - 1) / NT) : 0;
+  f.n_steps = (f.n_my + 1) / 2;
+  f.first_byte = (vb + tid) * 16;
+  f.ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_mem)) + tid * 16;
+  f.keep = policy_evict_last();
+  f.drop = policy_evict_first();
+  f.q = 0;
+  f.pass = 0;
+  f.row = cluster_id;
+  while (f.row < p.BT && p.target[f.row] == p.ignore_index) f.row += n_clusters;
+  if (f.n_my == 0) f.row = p.BT;  // nothing to stream: only empty groups
+  if (f.row < p.BT) f.seek_row(p);
 
-  // this thread's slots: ring_mem[(slot * kTensors + tensor) * NT + tid]
+  // this thread's 16-byte cell of (slot, tensor, u): mine[((slot*kTensors + tensor)*2 + u)*NT]
   const uint4* mine = ring_mem + tid;
-
-  // prologue: kStages steps in flight
 #pragma unroll
-  for (int s = 0; s < kStages; ++s) pipe.feed(p, s, n_clusters);
+  for (int s = 0; s < kStages; ++s) f.feed(p, s, n_clusters);
   int slot = 0;
 
   const T* S = static_cast<const T*>(p.student);
   const T* Tt = static_cast<const T*>(p.teacher);
+  const int n_steps = f.n_steps, n_my = f.n_my;
 
   for (int64_t row = cluster_id; row < p.BT; row += n_clusters) {
     const int64_t tg = p.target[row];
@@ -259,17 +274,27 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
-    for (int64_t k = 0; k < pipe.n_my; ++k) {
+    for (int q = 0; q < n_steps; ++q) {
       cp_async_wait<kStages - 1>();
+      const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
+      const bool two = (2 * q + 1) < n_my;
       float x[VE];
-      unpack_raw<T, VE>(mine[(slot * P::kTensors) * NT], x);
-      lse2x_update(a, x);
-      if constexpr (kTvd) {
-        unpack_raw<T, VE>(mine[(slot * P::kTensors + 1) * NT], x);
-        lse2x_update(b, x);
+      unpack_raw<T, VE>(cell[0], x);
+      lse2x_update<kPacked>(a, x);
+      if (two) {
+        unpack_raw<T, VE>(cell[NT], x);
+        lse2x_update<kPacked>(a, x);
       }
-      pipe.feed(p, slot, n_clusters);
-      slot = (slot + 1 == kStages) ? 0 : slot + 1;
+      if constexpr (kTvd) {
+        unpack_raw<T, VE>(cell[2 * NT], x);
+        lse2x_update<kPacked>(b, x);
+        if (two) {
+          unpack_raw<T, VE>(cell[3 * NT], x);
+          lse2x_update<kPacked>(b, x);
+        }
+      }
+      f.feed(p, slot, n_clusters);
+      slot = (slot + 1) & (kStages - 1);
     }
     Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
     if (owns_tail && tail0 + tid < p.V) {
@@ -302,23 +327,32 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       // kernels see bit-identical p and q.
       const float ns2 = -(lse_s * kLog2e);
       const float nt2 = -(lse_t * kLog2e);
-      const float2 L2 = make_float2(kLog2e, kLog2e);
-      const float2 nst = make_float2(ns2, nt2);
 
       // ---- step 2: split sums of (p, q) by the sign of p - q
       float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
-      for (int64_t k = 0; k < pipe.n_my; ++k) {
-        cp_async_wait<kStages - 1>();
+      auto step2 = [&](uint4 ws, uint4 wt) {
         float xs[VE], xt[VE];
-        unpack_raw<T, VE>(mine[(slot * P::kTensors) * NT], xs);
-        unpack_raw<T, VE>(mine[(slot * P::kTensors + 1) * NT], xt);
+        unpack_raw<T, VE>(ws, xs);
+        unpack_raw<T, VE>(wt, xt);
 #pragma unroll
         for (int j = 0; j < VE; ++j) {
-          const float2 e = fma2(make_float2(xs[j], xt[j]), L2, nst);
-          tvd_split(ex2(e.x), ex2(e.y), pos, neg);
+          if constexpr (kPacked) {
+            const float2 e = fma2(make_float2(xs[j], xt[j]), make_float2(kLog2e, kLog2e),
+                                  make_float2(ns2, nt2));
+            tvd_split(ex2(e.x), ex2(e.y), pos, neg);
+          } else {
+            tvd_split_scalar(ex2(fmaf(xs[j], kLog2e, ns2)), ex2(fmaf(xt[j], kLog2e, nt2)), pos,
+                             neg);
+          }
         }
-        pipe.feed(p, slot, n_clusters);
-        slot = (slot + 1 == kStages) ? 0 : slot + 1;
+      };
+      for (int q = 0; q < n_steps; ++q) {
+        cp_async_wait<kStages - 1>();
+        const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
+        step2(cell[0], cell[2 * NT]);
+        if ((2 * q + 1) < n_my) step2(cell[NT], cell[3 * NT]);
+        f.feed(p, slot, n_clusters);
+        slot = (slot + 1) & (kStages - 1);
       }
       if (owns_tail && tail0 + tid < p.V) {
         tvd_accum1(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid), ns2,
@@ -456,10 +490,10 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per process.
-template <typename T, int VE, int C, bool kTvd, int NT, int kStages>
+template <typename T, int VE, int C, bool kTvd, int NT, int kStages, bool kPacked>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
-  constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * NT * 16;
-  auto kernel = forward_pipelined<T, VE, C, kTvd, NT, kStages>;
+  constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, NT, kStages, kPacked>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
@@ -489,8 +523,8 @@ template <typename T, int C, bool kTvd>
 cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr int VE = Elem<T>::kVec;
   if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
-  if (plan.threads == 1024) return run_pipelined<T, VE, C, kTvd, 1024, 4>(a, plan.slots, st);
-  return run_pipelined<T, VE, C, kTvd, 512, 8>(a, plan.slots, st);
+  if (plan.packed) return run_pipelined<T, VE, C, kTvd, 512, 4, true>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, 512, 4, false>(a, plan.slots, st);
 }
 
 template <typename T, bool kTvd>

@@ -27,7 +27,7 @@ struct FwdPlan {
   bool vec;     // 16-byte vector path (pointers and strides aligned)
   int cluster;  // CTAs per row: 1, 2, 4 or 8
   int slots;    // rows in flight across the GPU (clusters launched), 0 = as many as fit
-  int threads;  // CTA size of the pipelined path: 512 or 1024
+  bool packed;  // packed f32x2 arithmetic in the pipelined path
 };
 
 struct BwdArgs {
