@@ -6,8 +6,13 @@
 One step = the whole hot path over one batch: the fused forward (two-pass
 log-sum-exp, TVD and sigma) and the fused backward (gradient w.r.t. the
 student logits), through the C ABI, on inputs already resident in HBM.
-The default workload is BT = 8192 rows of V = 151936 bf16 logits.  Each
-step reads 12.4 GB, far more than L2, so L2 needs no flush between steps.
+The workload's upstream gradients are per-row constants known before the
+forward, so the headline step (``--path single``) is the single-launch
+forward + backward; ``--path two`` times the separate forward and backward
+launches, and each run also times the other path for comparison.  Both
+write bit-identical outputs.  The default workload is BT = 8192 rows of
+V = 151936 bf16 logits; a step streams at least 7.4 GB, far more than L2, so
+L2 needs no flush between steps.
 
 Under torchrun every rank runs the full per-rank workload on its own GPU
 (rows are independent, so there is no collective on the data path) and
@@ -38,6 +43,9 @@ METRIC = "fused CE+TVD fwd+bwd tokens/s and HBM GB/s (% of peak), V=151936 bf16,
 DEFAULT_WORKLOAD = "bt8192_v151936_bf16"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = ["fct_common.cuh", "fct_forward.cu", "fct_backward.cu"]
+# Algorithmic bytes per launch (per-row scalars ignored): the forward reads
+# student + teacher once (2 V e per row); the backward and the single-launch
+# forward + backward read both and write the gradient (3 V e per row).
 
 
 # ---------------------------------------------------------------- helpers
@@ -57,12 +65,6 @@ def measured_peaks() -> dict:
             d = json.load(f)
         return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
     return {"hbm_gbs": 6800.0, "source": "fallback"}
-
-
-def algorithmic_bytes(BT: int, V: int, elem: int) -> dict:
-    """Minimum HBM bytes per launch: forward reads student + teacher once,
-    backward reads both and writes the gradient (per-row scalars ignored)."""
-    return {"forward": 2 * BT * V * elem, "backward": 3 * BT * V * elem}
 
 
 class ClockSampler:
@@ -214,10 +216,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--rows", type=int, default=None, help="override BT (profiling)")
+    ap.add_argument("--path", default="single", choices=["single", "two"],
+                    help="headline step: one fused forward+backward launch, or the forward "
+                         "and backward launches")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-other", action="store_true", help="skip timing the other path")
     ap.add_argument("--cluster", type=int, default=0,
                     help="CTAs per row in the fused forward (0 = automatic)")
     args = ap.parse_args()
@@ -247,52 +253,71 @@ def main():
     grad = torch.empty_like(w.student)
     stream = torch.cuda.current_stream(dev)
 
-    def step():
+    def fwd():
         binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, w.ignore_index, ce=ce, tvd=tvd,
                                      student_lse=ls, teacher_lse=lt, sigma=sg, stream=stream)
+
+    def bwd():
         binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, ls, lt, sg, w.grad_ce,
                                       w.grad_tvd, w.ignore_index, grad_student=grad, stream=stream)
 
+    def single():
+        binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                              w.grad_tvd, w.ignore_index, ce=ce, tvd=tvd,
+                                              student_lse=ls, teacher_lse=lt, sigma=sg,
+                                              grad_student=grad, stream=stream)
+
+    # the launches of one step of each path, with the algorithmic bytes of each launch
+    paths = {
+        "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
+        "single": [("forward_backward", single, 3 * BT * V * elem)],
+    }
+
+    def time_path(name, K, sampler=None):
+        launches = paths[name]
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(launches) + 1)]
+              for _ in range(K)]
+        if sampler:
+            sampler.__enter__()
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record(stream)
+        for k in range(K):
+            ev[k][0].record(stream)
+            for i, (_, fn, _) in enumerate(launches):
+                fn()
+                ev[k][i + 1].record(stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        if sampler:
+            sampler.__exit__(None, None, None)
+        per = {}
+        for i, (kname, _, nbytes) in enumerate(launches):
+            kms = sum(ev[k][i].elapsed_time(ev[k][i + 1]) for k in range(K)) / K
+            per[kname] = {"ms": kms, "gbs": nbytes / (kms * 1e-3) / 1e9, "bytes": nbytes}
+        ms = sharding.max_over_ranks(start.elapsed_time(end) / K, world, dev)
+        return ms, per
+
     for _ in range(args.warmup):
-        step()
+        for name in paths:
+            for _, fn, _ in paths[name]:
+                fn()
     torch.cuda.synchronize(dev)
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     clocks = ClockSampler(local) if not args.no_clocks else None
-    if clocks:
-        clocks.__enter__()
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
-    start.record(stream)
-    for k in range(K):
-        e0, e1, e2 = ev[k]
-        e0.record(stream)
-        binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, w.ignore_index, ce=ce, tvd=tvd,
-                                     student_lse=ls, teacher_lse=lt, sigma=sg, stream=stream)
-        e1.record(stream)
-        binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, ls, lt, sg, w.grad_ce,
-                                      w.grad_tvd, w.ignore_index, grad_student=grad, stream=stream)
-        e2.record(stream)
-    end.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    if clocks:
-        clocks.__exit__(None, None, None)
-    total_ms = start.elapsed_time(end)
-    fwd_ms = sum(ev[k][0].elapsed_time(ev[k][1]) for k in range(K)) / K
-    bwd_ms = sum(ev[k][1].elapsed_time(ev[k][2]) for k in range(K)) / K
-    ms = sharding.max_over_ranks(total_ms / K, world, dev)
+    ms, kernels = time_path(args.path, K, clocks)
     value = world * BT / (ms * 1e-3)
+    other_name = "two" if args.path == "single" else "single"
+    other = None
+    if not args.no_other:
+        oms, okern = time_path(other_name, K)
+        other = {"path": other_name, "ms_per_step": oms, "value": world * BT / (oms * 1e-3),
+                 "kernels": okern}
 
-    nbytes = algorithmic_bytes(BT, V, elem)
     peaks = measured_peaks()
-    kernels = {
-        "forward": {"ms": fwd_ms, "gbs": nbytes["forward"] / (fwd_ms * 1e-3) / 1e9},
-        "backward": {"ms": bwd_ms, "gbs": nbytes["backward"] / (bwd_ms * 1e-3) / 1e9},
-    }
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     traffic = None
     if os.path.exists(PROFILE_SUMMARY):
@@ -302,7 +327,10 @@ def main():
         if (ent and prof.get("source_hash") == kernel_source_hash()
                 and prof.get("workload") == args.workload):
             traffic = ent["bytes_per_launch_full"]
-    step_gbs = (nbytes["forward"] + nbytes["backward"]) / (ms * 1e-3) / 1e9
+    # the metric's GB/s: bytes a step must move at minimum, over the step time
+    step_bytes = sum(b for _, _, b in paths[args.path])
+    step_gbs = step_bytes / (ms * 1e-3) / 1e9
+    two_bytes = sum(b for _, _, b in paths["two"])
 
     # ---- end to end through the public API: pinned host inputs in, per-row loss out
     e2e = None
@@ -323,7 +351,8 @@ def main():
             w.target.copy_(htg, non_blocking=True)
             w.grad_ce.copy_(hgc, non_blocking=True)
             w.grad_tvd.copy_(hgt, non_blocking=True)
-            step()
+            for _, fn, _ in paths[args.path]:
+                fn()
             out_ce.copy_(ce, non_blocking=True)
             out_tvd.copy_(tvd, non_blocking=True)
 
@@ -356,18 +385,23 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": args.workload, "BT": BT, "V": V,
                        "logit_dtype": "bf16" if elem == 2 else "f32",
+                       "path": args.path,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "forward_ctas_per_row": args.cluster or "auto",
-                       "l2": "no flush: each step streams 12.4 GB, far above the 129 MB L2"
+                       "l2": "no flush: each step streams >= 7.4 GB, far above the 129 MB L2"
                        if args.rows is None else "reduced rows"},
+            # GB/s of the bytes a step must move (3 V e per row in one launch) and the
+            # same step time against the two-launch minimum (5 V e per row)
             "hbm_gbs": step_gbs,
             "hbm_frac": step_gbs / peaks["hbm_gbs"],
+            "two_launch_equivalent_gbs": two_bytes / (ms * 1e-3) / 1e9,
             "kernels": kernels,
             "roofline": {"bound": "hbm", "kernel": dom, "achieved": k["gbs"],
                          "peak": peaks["hbm_gbs"], "peak_source": peaks["source"],
                          "unit": "GB/s", "frac": k["gbs"] / peaks["hbm_gbs"],
                          "traffic": traffic},
-            "gpu_launches": 2 * K,
+            "gpu_launches": len(paths[args.path]) * K,
+            "other_path": other,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary() if clocks else None,

@@ -22,8 +22,9 @@ IGNORE_INDEX = -100
 _lock = threading.Lock()
 _lib = None
 
-EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "ce_forward", "ce_backward",
-           "fct_status_string", "fct_set_forward_cluster", "fct_version")
+EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
+           "ce_forward", "ce_backward", "fct_status_string", "fct_set_forward_cluster",
+           "fct_version")
 
 
 class FctError(RuntimeError):
@@ -46,9 +47,13 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                              vp, vp, vp, vp, vp, vp, vp]
         lib.fused_ce_tvd_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                               vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
+        lib.fused_ce_tvd_forward_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                                      vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
+                                                      vp, vp]
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
-        for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "ce_forward", "ce_backward"):
+        for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
+                  "ce_forward", "ce_backward"):
             getattr(lib, f).restype = i32
         lib.fct_status_string.argtypes = [i32]
         lib.fct_status_string.restype = ctypes.c_char_p
@@ -185,6 +190,45 @@ def fused_ce_tvd_backward(student, teacher, target, student_lse, teacher_lse, si
                                       _stream(stream))
     _check(rc, "fused_ce_tvd_backward")
     return grad_student
+
+
+def fused_ce_tvd_forward_backward(student, teacher, target, grad_ce, grad_tvd,
+                                  ignore_index=IGNORE_INDEX, *, ce=None, tvd=None,
+                                  student_lse=None, teacher_lse=None, sigma=None,
+                                  grad_student=None, inplace=False, dev_status=None,
+                                  stream=None):
+    """Forward and backward in one launch, given the upstream gradients.
+
+    Returns (ce, tvd, student_lse, teacher_lse, sigma, grad_student); the
+    results equal fused_ce_tvd_forward followed by fused_ce_tvd_backward.
+    """
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    BT, V = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    stride = max(stride_ce, stride_tvd)
+    outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                                             (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
+    if inplace:
+        grad_student = student
+    elif grad_student is None:
+        grad_student = torch.empty_like(student)
+    code_g, ld_g = _logits(grad_student, "grad_student")
+    if code_g != code or grad_student.shape != student.shape:
+        raise ValueError("grad_student must match the student's shape and dtype")
+    rc = load().fused_ce_tvd_forward_backward(
+        _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V, int(ignore_index),
+        _ptr(gce), _ptr(gtvd), stride, *map(_ptr, outs), _ptr(grad_student), ld_g,
+        _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_ce_tvd_forward_backward")
+    return (*outs, grad_student)
 
 
 def ce_forward(logits, target, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,

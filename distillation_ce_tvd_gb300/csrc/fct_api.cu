@@ -151,7 +151,7 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
   if ((rc = current_device(&d)) != FCT_OK) return rc;
   const bool vec = vec_ok(student, ld_s, dtype) && (!fused || vec_ok(teacher, ld_t, dtype));
   fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
-                 ce, tvd, lse_s, lse_t, sigma, dev_status};
+                 ce, tvd, lse_s, lse_t, sigma, dev_status, nullptr, 0, nullptr, nullptr, 0};
   const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec);
   if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
@@ -203,9 +203,88 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
   return FCT_OK;
 }
 
+// Single-launch forward + backward: the checks of both calls, plus no
+// overlap between the gradient and the per-row outputs.
+int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t ld_t,
+                          int dtype, const int64_t* target, int64_t BT, int64_t V,
+                          int64_t ignore_index, const float* grad_ce, const float* grad_tvd,
+                          int64_t grad_stride, float* ce, float* tvd, float* lse_s, float* lse_t,
+                          float* sigma, void* grad, int64_t ld_g, int32_t* dev_status,
+                          void* stream) {
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  int rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
+  if ((rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
+  if (grad_ce == nullptr || grad_tvd == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(grad_ce, 4) || !aligned(grad_tvd, 4)) return FCT_ERR_ALIGNMENT;
+  float* outs[5] = {ce, tvd, lse_s, lse_t, sigma};
+  for (int i = 0; i < 5; ++i) {
+    if (outs[i] == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(outs[i], 4)) return FCT_ERR_ALIGNMENT;
+  }
+  if (dev_status && !aligned(dev_status, 4)) return FCT_ERR_ALIGNMENT;
+  const size_t e = elem_size(dtype);
+  const Range rs = mat_range(student, BT, ld_s, V, e), rt = mat_range(teacher, BT, ld_t, V, e);
+  const Range rtg = vec_range(target, BT, 8), g = mat_range(grad, BT, ld_g, V, e);
+  const int64_t n_up = grad_stride ? BT : 1;
+  const Range rgc = vec_range(grad_ce, n_up, 4), rgt = vec_range(grad_tvd, n_up, 4);
+  const bool inplace = (grad == student);
+  if (inplace && ld_g != ld_s) return FCT_ERR_INVALID_ARG;
+  if (!inplace && overlap(g, rs)) return FCT_ERR_INVALID_ARG;
+  if (overlap(g, rt) || overlap(g, rtg) || overlap(g, rgc) || overlap(g, rgt))
+    return FCT_ERR_INVALID_ARG;
+  for (int i = 0; i < 5; ++i) {
+    const Range r = vec_range(outs[i], BT, 4);
+    if (overlap(r, rs) || overlap(r, rt) || overlap(r, rtg) || overlap(r, g) ||
+        overlap(r, rgc) || overlap(r, rgt))
+      return FCT_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(r, vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
+  }
+  DeviceInfo d;
+  if ((rc = current_device(&d)) != FCT_OK) return rc;
+  const bool vec = vec_ok(student, ld_s, dtype) && vec_ok(teacher, ld_t, dtype) &&
+                   vec_ok(grad, ld_g, dtype);
+  if (!vec) {
+    // Unaligned rows: the two-launch path gives the same results.
+    rc = forward_impl(student, ld_s, teacher, ld_t, dtype, target, BT, V, ignore_index, ce, tvd,
+                      lse_s, lse_t, sigma, dev_status, stream);
+    if (rc != FCT_OK) return rc;
+    return backward_impl(student, ld_s, teacher, ld_t, dtype, target, BT, V, ignore_index, lse_s,
+                         lse_t, sigma, grad_ce, grad_tvd, grad_stride, grad, ld_g, dev_status,
+                         stream);
+  }
+  fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
+                 ce, tvd, lse_s, lse_t, sigma, dev_status, grad, ld_g, grad_ce, grad_tvd,
+                 grad_stride};
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, true, true);
+  if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student, const void* teacher,
+                                  int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                                  int64_t BT, int64_t V, int64_t ignore_index,
+                                  const float* grad_ce, const float* grad_tvd,
+                                  int64_t grad_stride, float* ce, float* tvd,
+                                  float* student_lse, float* teacher_lse, float* sigma,
+                                  void* grad_student, int64_t ld_grad, int32_t* dev_status,
+                                  void* stream) {
+  return forward_backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                               ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd,
+                               student_lse, teacher_lse, sigma, grad_student, ld_grad,
+                               dev_status, stream);
+}
+
 
 int fused_ce_tvd_forward(const void* student, int64_t ld_student, const void* teacher,
                          int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,

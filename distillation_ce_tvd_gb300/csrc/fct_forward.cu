@@ -25,6 +25,10 @@
 //     over p < q.  Then sum|p - q| = (P+ - Q+) + (Q- - P-) and
 //     sigma = P+ - P-, and ties contribute to neither (zero subgradient).
 //   * The grid is persistent: one cluster per row slot, looping over rows.
+//   * With the upstream gradients known before the launch, a third pass over
+//     the still L2-resident row writes the student gradient of the "Backward
+//     Pass" in the same launch (the single-launch forward + backward), so
+//     HBM sees 2 reads and 1 write per element instead of 4 reads and 1 write.
 //   * Student and teacher go through the very same code, so a row whose
 //     teacher equals its student bit for bit gets p == q everywhere and
 //     tvd = sigma = 0 exactly.
@@ -113,6 +117,25 @@ __device__ __forceinline__ void cluster_sum2(float& x, float& y, float2* part, i
   }
 }
 
+// Every CTA folds the step-2 partials of the C CTAs in rank order (all end
+// with identical sums; used when every CTA needs sigma).
+template <int C>
+__device__ __forceinline__ void cluster_sum2_all(float& x, float& y, float2* part) {
+  if constexpr (C > 1) {
+    if (threadIdx.x == 0) *part = make_float2(x, y);
+    cluster_sync_all();
+    cg::cluster_group cl = cg::this_cluster();
+    x = 0.f;
+    y = 0.f;
+#pragma unroll
+    for (int r = 0; r < C; ++r) {
+      const float2 w = *cl.map_shared_rank(part, r);
+      x += w.x;
+      y += w.y;
+    }
+  }
+}
+
 // One element pair of step 2, scalar form (tails and the unaligned path).
 __device__ __forceinline__ void tvd_accum1(float xs, float xt, float ns2, float nt2,
                                            float2& pos, float2& neg) {
@@ -159,9 +182,9 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 
 constexpr int kPerStep = 2;  // vectors per tensor moved by one step
 
-template <typename T, int VE, bool kTvd, int NT, int kStages>
+template <typename T, int VE, bool kTvd, bool kGrad, int NT, int kStages>
 struct Feed {
-  static constexpr int kPasses = kTvd ? 2 : 1;
+  static constexpr int kPasses = kTvd ? (kGrad ? 3 : 2) : 1;
   static constexpr int kTensors = kTvd ? 2 : 1;
   static constexpr uint32_t kSlotBytes = kTensors * kPerStep * NT * 16;
   static constexpr int64_t kStride = int64_t(NT) * 16;  // bytes between a thread's vectors
@@ -192,7 +215,8 @@ struct Feed {
   // empty group once this thread's sequence is exhausted).
   __device__ __forceinline__ void feed(const FwdArgs& p, int slot, int64_t n_clusters) {
     if (row < p.BT) {
-      const uint64_t pol = pass == 0 ? keep : drop;
+      // keep the row in L2 until its last pass reads it
+      const uint64_t pol = (pass + 1 < kPasses) ? keep : drop;
       const uint32_t dst = ring + slot * kSlotBytes;
       const bool two = (2 * q + 1) < n_my;
       cp_async16(dst, sp, pol);
@@ -217,9 +241,10 @@ struct Feed {
   }
 };
 
-template <typename T, int VE, int C, bool kTvd, int NT, int kStages, bool kPacked>
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, int kStages, bool kPacked>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
-  using F = Feed<T, VE, kTvd, NT, kStages>;
+  static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
+  using F = Feed<T, VE, kTvd, kGrad, NT, kStages>;
   static_assert((kStages & (kStages - 1)) == 0, "power-of-two ring");
   extern __shared__ __align__(16) uint4 ring_mem[];
   __shared__ float4 red_lse[kMaxWarps];
@@ -267,10 +292,19 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     const int64_t tg = p.target[row];
     if (tg == p.ignore_index) {
       if (rank == 0 && tid == 0) write_ignored<kTvd>(p, row);
+      if constexpr (kGrad) {  // this CTA's slice of the gradient row is zero
+        T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
+        const float zero[VE] = {};
+        for (int64_t v = vb + tid; v < ve; v += NT) store_vec<T, VE>(grow + v * VE, zero, f.drop);
+        if (owns_tail && tail0 + tid < p.V) Elem<T>::store1(grow + tail0 + tid, 0.f);
+      }
       continue;  // uniform over the cluster; the feed skips this row too
     }
     const T* srow = S + row * p.ld_s;
     const T* trow = kTvd ? Tt + row * p.ld_t : nullptr;
+    // Read before any gradient of this row can overwrite it (in place).
+    const float s_tg =
+        (rank == 0 && tid == 0 && tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
 
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
@@ -310,10 +344,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     const float lse_s = lse2_finish(fa);
 
     if constexpr (!kTvd) {
-      if (rank == 0 && tid == 0) {
-        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
-        write_row<false>(p, row, tg, lse_s, 0.f, 0.f, 0.f, s_tg);
-      }
+      if (rank == 0 && tid == 0) write_row<false>(p, row, tg, lse_s, 0.f, 0.f, 0.f, s_tg);
       // peers may still read part_lse; warps may still read red_lse
       if constexpr (C > 1) {
         cluster_sync_all();
@@ -361,10 +392,62 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       float abs_sum = (pos.x - pos.y) + (neg.y - neg.x);
       float sig = pos.x - neg.x;
       block_sum2<NT>(abs_sum, sig, red_sum);
-      cluster_sum2<C>(abs_sum, sig, &part_sum, rank);
-      if (rank == 0 && tid == 0) {
-        const float s_tg = (tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
-        write_row<true>(p, row, tg, lse_s, lse_t, abs_sum, sig, s_tg);
+      if constexpr (kGrad) {
+        cluster_sum2_all<C>(abs_sum, sig, &part_sum);
+      } else {
+        cluster_sum2<C>(abs_sum, sig, &part_sum, rank);
+      }
+      if (rank == 0 && tid == 0) write_row<true>(p, row, tg, lse_s, lse_t, abs_sum, sig, s_tg);
+
+      if constexpr (kGrad) {
+        // ---- step 3: the "Backward Pass" gradient, same expressions as the
+        // backward kernel: grad = p * c(sign) - grad_ce * [v == target].
+        const float gce = p.grad_ce[row * p.grad_stride];
+        const float h = 0.5f * p.grad_tvd[row * p.grad_stride];
+        const float c_pos = gce + h * (1.f - sig);
+        const float c_neg = gce + h * (-1.f - sig);
+        const float c_zero = gce - h * sig;
+        const bool bad = (tg < 0 || tg >= p.V);
+        T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
+        auto grad_of = [&](float xs, float xt) {
+          const float pp = ex2(fmaf(xs, kLog2e, ns2));
+          const float qq = ex2(fmaf(xt, kLog2e, nt2));
+          const float c = (pp > qq) ? c_pos : ((pp < qq) ? c_neg : c_zero);
+          return pp * c;
+        };
+        auto step3 = [&](uint4 ws, uint4 wt, int64_t v) {
+          float xs[VE], xt[VE], g[VE];
+          unpack_raw<T, VE>(ws, xs);
+          unpack_raw<T, VE>(wt, xt);
+#pragma unroll
+          for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+          const int64_t off = tg - v * VE;
+          if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+#pragma unroll
+            for (int j = 0; j < VE; ++j)
+              if (j == off) g[j] -= gce;
+          }
+          if (bad) {
+#pragma unroll
+            for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
+          }
+          store_vec<T, VE>(grow + v * VE, g, f.drop);
+        };
+        for (int q = 0; q < n_steps; ++q) {
+          cp_async_wait<kStages - 1>();
+          const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
+          const int64_t v = vb + tid + int64_t(2 * q) * NT;
+          step3(cell[0], cell[2 * NT], v);
+          if ((2 * q + 1) < n_my) step3(cell[NT], cell[3 * NT], v + NT);
+          f.feed(p, slot, n_clusters);
+          slot = (slot + 1) & (kStages - 1);
+        }
+        if (owns_tail && tail0 + tid < p.V) {
+          const int64_t v = tail0 + tid;
+          float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
+          if (v == tg) g -= gce;
+          Elem<T>::store1(grow + v, bad ? __uint_as_float(0x7fc00000u) : g);
+        }
       }
     }
   }
@@ -490,10 +573,10 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per process.
-template <typename T, int VE, int C, bool kTvd, int NT, int kStages, bool kPacked>
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, int kStages, bool kPacked>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16;
-  auto kernel = forward_pipelined<T, VE, C, kTvd, NT, kStages, kPacked>;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, kStages, kPacked>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
@@ -519,21 +602,25 @@ cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
   return launch_cluster(kernel, C, kScalarThreads, 0, n, a, st);
 }
 
-template <typename T, int C, bool kTvd>
+template <typename T, int C, bool kTvd, bool kGrad>
 cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr int VE = Elem<T>::kVec;
-  if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
-  if (plan.packed) return run_pipelined<T, VE, C, kTvd, 512, 4, true>(a, plan.slots, st);
-  return run_pipelined<T, VE, C, kTvd, 512, 4, false>(a, plan.slots, st);
+  if constexpr (kGrad) {
+    if (!plan.vec) return cudaErrorInvalidValue;  // the host routes this case to two launches
+  } else {
+    if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
+  }
+  if (plan.packed) return run_pipelined<T, VE, C, kTvd, kGrad, 512, 4, true>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, kGrad, 512, 4, false>(a, plan.slots, st);
 }
 
-template <typename T, bool kTvd>
+template <typename T, bool kTvd, bool kGrad>
 cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   switch (plan.cluster) {
-    case 1: return run<T, 1, kTvd>(a, plan, st);
-    case 2: return run<T, 2, kTvd>(a, plan, st);
-    case 4: return run<T, 4, kTvd>(a, plan, st);
-    default: return run<T, 8, kTvd>(a, plan, st);
+    case 1: return run<T, 1, kTvd, kGrad>(a, plan, st);
+    case 2: return run<T, 2, kTvd, kGrad>(a, plan, st);
+    case 4: return run<T, 4, kTvd, kGrad>(a, plan, st);
+    default: return run<T, 8, kTvd, kGrad>(a, plan, st);
   }
 }
 
@@ -541,9 +628,11 @@ cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   if (a.dtype == FCT_BF16) {
-    return a.tvd ? run_c<bf16_t, true>(a, plan, st) : run_c<bf16_t, false>(a, plan, st);
+    if (a.grad) return run_c<bf16_t, true, true>(a, plan, st);
+    return a.tvd ? run_c<bf16_t, true, false>(a, plan, st) : run_c<bf16_t, false, false>(a, plan, st);
   }
-  return a.tvd ? run_c<float, true>(a, plan, st) : run_c<float, false>(a, plan, st);
+  if (a.grad) return run_c<float, true, true>(a, plan, st);
+  return a.tvd ? run_c<float, true, false>(a, plan, st) : run_c<float, false, false>(a, plan, st);
 }
 
 }  // namespace fct

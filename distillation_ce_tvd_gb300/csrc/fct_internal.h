@@ -21,6 +21,12 @@ struct FwdArgs {
   float* lse_t;
   float* sigma;
   int32_t* dev_status;
+  // single-launch forward + backward only (nullptr grad: forward alone)
+  void* grad;
+  int64_t ld_g;
+  const float* grad_ce;
+  const float* grad_tvd;
+  int64_t grad_stride;
 };
 
 struct FwdPlan {

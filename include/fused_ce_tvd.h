@@ -111,6 +111,33 @@ int fused_ce_tvd_backward(const void* student, int64_t ld_student,
                           int32_t* dev_status, void* stream);
 
 /*
+ * Forward and backward in ONE launch, for callers that know the upstream
+ * gradients before the forward (for instance a mean over tokens, whose
+ * per-row gradients are constants).  Writes everything
+ * fused_ce_tvd_forward writes and the gradient fused_ce_tvd_backward would
+ * write, bit for bit, but reads each logit from HBM once instead of twice:
+ * the row stays in L2 for a third pass that applies the "Backward Pass"
+ * formula with the row's sigma (PR #1384 analysis; fusing the two kernels is
+ * this library's addition).
+ *
+ *   grad_ce, grad_tvd, grad_stride : as for fused_ce_tvd_backward.
+ *   ce ... sigma : (BT,) fp32 outputs, as for fused_ce_tvd_forward.
+ *   grad_student : (BT, V) output; grad_student == student (same ld) is in
+ *                  place.  Rows that are not 16-byte aligned fall back to the
+ *                  two launches (same results).
+ */
+int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
+                                  const void* teacher, int64_t ld_teacher,
+                                  fct_dtype dtype, const int64_t* target,
+                                  int64_t BT, int64_t V, int64_t ignore_index,
+                                  const float* grad_ce, const float* grad_tvd,
+                                  int64_t grad_stride, float* ce, float* tvd,
+                                  float* student_lse, float* teacher_lse,
+                                  float* sigma, void* grad_student,
+                                  int64_t ld_grad, int32_t* dev_status,
+                                  void* stream);
+
+/*
  * Cross-entropy alone: the CE half of "Forward Pass" (one log-sum-exp pass,
  * ce = lse - logits[target]).  ce, lse: (BT,) fp32 outputs.
  */

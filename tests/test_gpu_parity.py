@@ -156,21 +156,33 @@ def test_small_and_ragged_vocab(V, dtype):
     compare(w, fwd, grad, what=f"V={V} ")
 
 
+def padded(w, ld, off):
+    """The same rows stored with row stride `ld` starting `off` elements into
+    a larger buffer (junk around them), to exercise strides, alignment and
+    the vector path's ragged tail."""
+    BT, V = w.student.shape
+    out = []
+    for x, junk in ((w.student, 77.0), (w.teacher, -55.0)):
+        buf = torch.full((BT * ld + off + 16,), junk, device=DEV, dtype=x.dtype)
+        view = buf[off:off + BT * ld].view(BT, ld)[:, :V]
+        view.copy_(x)
+        out.append(view)
+    return workloads.Workload(w.name, out[0], out[1], w.target, w.grad_ce, w.grad_tvd)
+
+
+# (V, ld, off): aligned rows with a ragged tail use the vector path; the rest
+# the scalar path.
+PADDED = [(3005, 3008, 0), (3005, 3048, 8), (3000, 3001, 0), (3000, 3013, 3), (3001, 3001, 1)]
+
+
+@pytest.mark.parametrize("V,ld,off", PADDED)
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
-def test_padded_and_misaligned_rows(dtype):
-    base = workloads.make("bt1024_v32000_bf16", DEV, rows=21, V=3000, dtype=dtype, seed=2)
-    for pad, off in ((0, 1), (40, 0), (13, 3)):
-        ld = 3000 + pad + off
-        S = torch.full((21, ld + off), 77.0, device=DEV, dtype=dtype)
-        Tt = torch.full((21, ld + off), -55.0, device=DEV, dtype=dtype)
-        s = S.view(-1)[off:off + 21 * ld].view(21, ld)[:, :3000]
-        t = Tt.view(-1)[off:off + 21 * ld].view(21, ld)[:, :3000]
-        s.copy_(base.student)
-        t.copy_(base.teacher)
-        w = workloads.Workload(base.name, s, t, base.target, base.grad_ce, base.grad_tvd)
-        fwd, grad, st = run(w)
-        assert st == 0
-        compare(w, fwd, grad, what=f"pad={pad} off={off} ")
+def test_padded_and_misaligned_rows(V, ld, off, dtype):
+    base = workloads.make("bt1024_v32000_bf16", DEV, rows=21, V=V, dtype=dtype, seed=2)
+    w = padded(base, ld, off)
+    fwd, grad, st = run(w)
+    assert st == 0
+    compare(w, fwd, grad, what=f"V={V} ld={ld} off={off} ")
 
 
 def test_empty_batch_is_a_no_op():
@@ -278,3 +290,62 @@ def test_autograd_wrapper_matches_direct_calls():
     fwd, grad, _ = run(w)
     assert torch.equal(ce.detach(), fwd["ce"]) and torch.equal(tvd.detach(), fwd["tvd"])
     assert torch.equal(s.grad, grad)
+
+
+# ------------------------------------------------------------------ single launch
+
+def run_single(w, cluster=0, inplace=False, grads=None):
+    prev = binding.set_forward_cluster(cluster)
+    try:
+        status = torch.zeros(1, dtype=torch.int32, device=DEV)
+        s_in = w.student.clone() if inplace else w.student
+        gce, gtvd = grads if grads is not None else (w.grad_ce, w.grad_tvd)
+        ce, tvd, ls, lt, sg, grad = binding.fused_ce_tvd_forward_backward(
+            s_in, w.teacher, w.target, gce, gtvd, w.ignore_index, inplace=inplace,
+            dev_status=status)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_forward_cluster(prev)
+    fwd = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
+    return fwd, grad, int(status.item())
+
+
+@pytest.mark.parametrize("name,rows,V,dtype,ld", [
+    ("bt8192_v151936_bf16", 40, 151936, torch.bfloat16, None),
+    ("bt1024_v32000_bf16", 33, 32000, torch.bfloat16, None),
+    ("bt4096_v256000_f32", 12, 256000, torch.float32, None),
+    ("bt4096_v256000_f32", 21, 9001, torch.bfloat16, 9008),   # ragged tail, aligned rows
+    ("bt4096_v256000_f32", 21, 9001, torch.float32, 9004),    # ragged tail, aligned rows
+    ("bt1024_v32000_bf16", 17, 3003, torch.bfloat16, None),   # unaligned stride: two launches
+    ("bt1024_v32000_bf16", 9, 5, torch.float32, None),
+])
+@pytest.mark.parametrize("cluster", [0, 2, 8])
+def test_single_launch_equals_forward_then_backward(name, rows, V, dtype, ld, cluster):
+    w = workloads.make(name, DEV, rows=rows, V=V, dtype=dtype, seed=31)
+    if ld is not None:
+        w = padded(w, ld, 0)
+    if rows > 3:
+        w.target[1] = w.ignore_index
+    f1, g1, st1 = run(w, cluster=cluster)
+    f2, g2, st2 = run_single(w, cluster=cluster)
+    assert st1 == st2 == 0
+    for k in f1:
+        assert torch.equal(f1[k], f2[k]), k
+    assert torch.equal(g1, g2)
+    _, g3, _ = run_single(w, cluster=cluster, inplace=True)
+    assert torch.equal(g1, g3)
+
+
+def test_single_launch_parity_and_status():
+    w = workloads.make("bt8192_v151936_bf16", DEV, rows=24, V=151936, seed=32)
+    w.teacher[5] = w.student[5]
+    w.target[7] = 151936          # out of range
+    fwd, grad, st = run_single(w)
+    assert st == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+    compare(w, fwd, grad, what="single ")
+    assert fwd["tvd"][5].item() == 0.0 and fwd["sigma"][5].item() == 0.0
+    # broadcast upstream scalars
+    _, g_b, _ = run_single(w, grads=(0.125, 0.5))
+    _, g_r, _ = run_single(w, grads=(torch.full((24,), 0.125, device=DEV),
+                                     torch.full((24,), 0.5, device=DEV)))
+    assert torch.equal(g_b[~torch.isnan(g_b.float()).any(1)], g_r[~torch.isnan(g_r.float()).any(1)])
