@@ -46,3 +46,38 @@ def fused_ce_tvd_loss(student, teacher, target, ignore_index=binding.IGNORE_INDE
                       inplace=False):
     """Per-row (ce, tvd) with autograd support; reduce them as the caller wishes."""
     return FusedCETVDFunction.apply(student, teacher, target, ignore_index, inplace)
+
+
+class FusedCETVDMeanLoss(torch.autograd.Function):
+    """alpha * mean(ce) + beta * mean(tvd) over the rows not ignored, as a scalar.
+
+    The upstream gradients of a mean are known before the forward (alpha/n and
+    beta/n, computed on the device from the targets), so the forward runs the
+    single-launch forward + backward and keeps the student gradient; the
+    backward only hands it out (scaled by the incoming gradient when that is
+    not 1).  With ``inplace=True`` the gradient overwrites the student logits.
+    """
+
+    @staticmethod
+    def forward(ctx, student, teacher, target, ignore_index=binding.IGNORE_INDEX, alpha=1.0,
+                beta=1.0, inplace=False):
+        gce, gtvd, _ = binding.fused_ce_tvd_mean_upstream(target, ignore_index, alpha, beta)
+        s = student.detach()
+        ce, tvd, _, _, _, grad = binding.fused_ce_tvd_forward_backward(
+            s, teacher.detach(), target, gce, gtvd, ignore_index, inplace=inplace)
+        loss = binding.fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index, alpha, beta)
+        ctx.save_for_backward(grad)
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        (grad,) = ctx.saved_tensors
+        if not torch.equal(grad_out, torch.ones_like(grad_out)):
+            grad = grad * grad_out.to(grad.dtype)
+        return grad, None, None, None, None, None, None
+
+
+def fused_ce_tvd_mean_loss(student, teacher, target, ignore_index=binding.IGNORE_INDEX,
+                           alpha=1.0, beta=1.0, inplace=False):
+    """Scalar alpha * mean(ce) + beta * mean(tvd) with autograd support."""
+    return FusedCETVDMeanLoss.apply(student, teacher, target, ignore_index, alpha, beta, inplace)

@@ -23,8 +23,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
-           "ce_forward", "ce_backward", "fct_status_string", "fct_set_forward_cluster",
-           "fct_version")
+           "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
+           "fct_status_string", "fct_set_forward_cluster", "fct_version")
 
 
 class FctError(RuntimeError):
@@ -52,8 +52,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                                       vp, vp]
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
+        dbl = ctypes.c_double
+        lib.fused_ce_tvd_mean_upstream.argtypes = [vp, i64, i64, dbl, dbl, vp, vp, vp, vp]
+        lib.fused_ce_tvd_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp]
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
-                  "ce_forward", "ce_backward"):
+                  "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream",
+                  "fused_ce_tvd_mean_loss"):
             getattr(lib, f).restype = i32
         lib.fct_status_string.argtypes = [i32]
         lib.fct_status_string.restype = ctypes.c_char_p
@@ -265,3 +269,34 @@ def ce_backward(logits, target, lse, grad_ce, ignore_index=IGNORE_INDEX, *, grad
                             _ptr(dev_status), _stream(stream))
     _check(rc, "ce_backward")
     return grad_logits
+
+
+def fused_ce_tvd_mean_upstream(target, ignore_index=IGNORE_INDEX, alpha=1.0, beta=1.0, *,
+                               grad_ce=None, grad_tvd=None, count=None, stream=None):
+    """Upstream gradients (alpha/n, beta/n) of the mean over the n kept rows,
+    as 1-element device tensors, and n (1-element int64)."""
+    if not target.is_cuda or target.dtype != torch.int64 or target.dim() != 1:
+        raise ValueError("target must be a CUDA int64 vector")
+    dev = target.device
+    gce = grad_ce if grad_ce is not None else torch.empty(1, device=dev, dtype=torch.float32)
+    gtvd = grad_tvd if grad_tvd is not None else torch.empty(1, device=dev, dtype=torch.float32)
+    cnt = count if count is not None else torch.empty(1, device=dev, dtype=torch.int64)
+    rc = load().fused_ce_tvd_mean_upstream(_ptr(target), target.numel(), int(ignore_index),
+                                           float(alpha), float(beta), _ptr(gce), _ptr(gtvd),
+                                           _ptr(cnt), _stream(stream))
+    _check(rc, "fused_ce_tvd_mean_upstream")
+    return gce, gtvd, cnt
+
+
+def fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index=IGNORE_INDEX, alpha=1.0, beta=1.0, *,
+                           loss=None, stream=None):
+    """(alpha * sum ce + beta * sum tvd) / n over the kept rows, as a 1-element tensor."""
+    BT = target.numel()
+    _rows(ce, BT, "ce")
+    _rows(tvd, BT, "tvd")
+    _rows(target, BT, "target", torch.int64)
+    out = loss if loss is not None else torch.empty(1, device=ce.device, dtype=torch.float32)
+    rc = load().fused_ce_tvd_mean_loss(_ptr(ce), _ptr(tvd), _ptr(target), BT, int(ignore_index),
+                                       float(alpha), float(beta), _ptr(out), _stream(stream))
+    _check(rc, "fused_ce_tvd_mean_loss")
+    return out

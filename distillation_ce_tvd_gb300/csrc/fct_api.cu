@@ -326,6 +326,45 @@ int ce_backward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* 
                        stream);
 }
 
+int fused_ce_tvd_mean_upstream(const int64_t* target, int64_t BT, int64_t ignore_index,
+                               double alpha, double beta, float* grad_ce, float* grad_tvd,
+                               int64_t* count, void* stream) {
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (target == nullptr || grad_ce == nullptr || grad_tvd == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(target, 8) || !aligned(grad_ce, 4) || !aligned(grad_tvd, 4) ||
+      (count && !aligned(count, 8)))
+    return FCT_ERR_ALIGNMENT;
+  if (grad_ce == grad_tvd) return FCT_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  fct::LossArgs a{target, BT, ignore_index, nullptr, nullptr, alpha, beta,
+                  nullptr, grad_ce, grad_tvd, count};
+  return fct::launch_mean(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FCT_OK
+                                                                                : FCT_ERR_CUDA;
+}
+
+int fused_ce_tvd_mean_loss(const float* ce, const float* tvd, const int64_t* target, int64_t BT,
+                           int64_t ignore_index, double alpha, double beta, float* loss,
+                           void* stream) {
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (ce == nullptr || tvd == nullptr || target == nullptr || loss == nullptr)
+    return FCT_ERR_INVALID_ARG;
+  if (!aligned(ce, 4) || !aligned(tvd, 4) || !aligned(target, 8) || !aligned(loss, 4))
+    return FCT_ERR_ALIGNMENT;
+  const Range l = vec_range(loss, 1, 4);
+  if (overlap(l, vec_range(ce, BT, 4)) || overlap(l, vec_range(tvd, BT, 4)) ||
+      overlap(l, vec_range(target, BT, 8)))
+    return FCT_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  fct::LossArgs a{target, BT, ignore_index, ce, tvd, alpha, beta,
+                  loss, nullptr, nullptr, nullptr};
+  return fct::launch_mean(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FCT_OK
+                                                                                : FCT_ERR_CUDA;
+}
+
 const char* fct_status_string(int status) {
   switch (status) {
     case FCT_OK: return "FCT_OK";

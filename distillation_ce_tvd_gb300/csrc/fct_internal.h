@@ -54,7 +54,20 @@ struct BwdArgs {
   int32_t* dev_status;
 };
 
+struct LossArgs {
+  const int64_t* target;
+  int64_t BT, ignore_index;
+  const float* ce;   // nullptr: not summed
+  const float* tvd;  // nullptr: not summed
+  double alpha, beta;
+  float* loss;       // outputs, each optional
+  float* grad_ce;
+  float* grad_tvd;
+  int64_t* count;
+};
+
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
+cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st);
 
 }  // namespace fct

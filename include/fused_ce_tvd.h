@@ -157,6 +157,31 @@ int ce_backward(const void* logits, int64_t ld, fct_dtype dtype,
                 int64_t grad_stride, void* grad_logits, int64_t ld_grad,
                 int32_t* dev_status, void* stream);
 
+/*
+ * Mean over tokens.  The method stores per-row ce and tvd and takes per-row
+ * upstream gradients (PR #1384 analysis, "Forward Pass" stores and "Backward
+ * Pass" combine); the reduction to a scalar is the caller's.  These give the
+ * usual one, loss = (alpha * sum_r ce_r + beta * sum_r tvd_r) / n, with n the
+ * number of rows whose target is not ignore_index (ignored rows have
+ * ce = tvd = 0).  Each is one single-CTA launch with a fixed summation order
+ * (fp64 accumulation), so results are deterministic.
+ *
+ * fused_ce_tvd_mean_upstream: from the targets alone (call it before the
+ *   forward), writes grad_ce[0] = alpha / n and grad_tvd[0] = beta / n (0
+ *   when n = 0), to pass with grad_stride = 0 to fused_ce_tvd_backward or
+ *   fused_ce_tvd_forward_backward; *count = n if count is not NULL.
+ * fused_ce_tvd_mean_loss: loss[0] from the forward's ce and tvd.
+ * All pointers are device pointers; BT == 0 gives n = 0.
+ */
+int fused_ce_tvd_mean_upstream(const int64_t* target, int64_t BT,
+                               int64_t ignore_index, double alpha, double beta,
+                               float* grad_ce, float* grad_tvd, int64_t* count,
+                               void* stream);
+int fused_ce_tvd_mean_loss(const float* ce, const float* tvd,
+                           const int64_t* target, int64_t BT,
+                           int64_t ignore_index, double alpha, double beta,
+                           float* loss, void* stream);
+
 /* Human-readable name of a fct_status value (static storage). */
 const char* fct_status_string(int status);
 

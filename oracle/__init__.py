@@ -71,6 +71,9 @@ def _load():
             lib.oracle_ce_backward.restype = i32
             lib.oracle_row_probs.argtypes = [vp, i64, vp, i64, i32, i64, i64, vp, vp]
             lib.oracle_row_probs.restype = None
+            dbl = ctypes.c_double
+            lib.oracle_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp, vp]
+            lib.oracle_mean_loss.restype = i64
             _lib = lib
     return _lib
 
@@ -206,3 +209,16 @@ def row_probs(student, teacher, row):
     _load().oracle_row_probs(_ptr(s), ld_s, _ptr(t), ld_t, code, int(row), V,
                              _ptr(p), _ptr(q))
     return p, q
+
+
+def mean_loss(ce, tvd, target, ignore_index=-100, alpha=1.0, beta=1.0):
+    """(loss, grad_ce, grad_tvd, n) of the mean over non-ignored rows."""
+    ce = np.ascontiguousarray(np.asarray(ce, np.float64))
+    tvd = np.ascontiguousarray(np.asarray(tvd, np.float64))
+    tg = _i64(target)
+    out = np.zeros(3, np.float64)
+    n = _load().oracle_mean_loss(_ptr(ce), _ptr(tvd), _ptr(tg), tg.size, int(ignore_index),
+                                 float(alpha), float(beta), ctypes.c_void_p(out.ctypes.data),
+                                 ctypes.c_void_p(out.ctypes.data + 8),
+                                 ctypes.c_void_p(out.ctypes.data + 16))
+    return float(out[0]), float(out[1]), float(out[2]), int(n)

@@ -229,3 +229,25 @@ int oracle_ce_backward(const void* logits, int64_t ld, int dtype,
   }
   return status;
 }
+
+/* Mean over tokens (the caller-side reduction the method leaves open):
+ * loss = (alpha * sum_r ce_r + beta * sum_r tvd_r) / n over the n rows whose
+ * target is not ignore_index; *grad_ce = alpha / n and *grad_tvd = beta / n
+ * are its derivatives with respect to each kept row's ce and tvd (all 0 when
+ * n = 0).  Returns n. */
+int64_t oracle_mean_loss(const double* ce, const double* tvd, const int64_t* target,
+                         int64_t BT, int64_t ignore_index, double alpha, double beta,
+                         double* loss, double* grad_ce, double* grad_tvd) {
+  int64_t n = 0;
+  double sce = 0.0, stvd = 0.0;
+  for (int64_t r = 0; r < BT; ++r) {
+    if (target[r] == ignore_index) continue;
+    n += 1;
+    sce += ce[r];
+    stvd += tvd[r];
+  }
+  *loss = n ? (alpha * sce + beta * stvd) / (double)n : 0.0;
+  *grad_ce = n ? alpha / (double)n : 0.0;
+  *grad_tvd = n ? beta / (double)n : 0.0;
+  return n;
+}

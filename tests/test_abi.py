@@ -129,6 +129,39 @@ def test_ce_argument_checks(lib):
                            FAKE + (3 << 30) + 64, 1, FAKE + (4 << 30), 128, None, None) == UNSUPPORTED
 
 
+def test_mean_argument_checks(lib):
+    assert lib.fused_ce_tvd_mean_upstream(None, 4, -100, 1.0, 1.0, FAKE, FAKE + 64, None,
+                                          None) == INVALID
+    assert lib.fused_ce_tvd_mean_upstream(FAKE, -1, -100, 1.0, 1.0, FAKE + 256, FAKE + 512,
+                                          None, None) == INVALID
+    assert lib.fused_ce_tvd_mean_upstream(FAKE, 4, -100, 1.0, 1.0, FAKE + 256, FAKE + 256,
+                                          None, None) == INVALID
+    assert lib.fused_ce_tvd_mean_loss(FAKE, FAKE + 64, FAKE + 128, 4, -100, 1.0, 1.0, FAKE + 4,
+                                      None) == INVALID          # loss inside ce
+    assert lib.fused_ce_tvd_mean_loss(FAKE, FAKE + 64, FAKE + 130, 4, -100, 1.0, 1.0,
+                                      FAKE + 512, None) == ALIGN
+
+
+def test_forward_backward_argument_checks(lib):
+    f = lib.fused_ce_tvd_forward_backward
+    base = FAKE + (6 << 30)
+    args = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 4, 100, -100,
+            base, base + 256, 1, base + 512, base + 768, base + 1024, base + 1280, base + 1536,
+            FAKE + (5 << 30), 128, None, None]
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a6=0) == OK
+    assert call(a11=3) == INVALID                  # grad_stride
+    assert call(a9=None) == INVALID                # grad_ce
+    assert call(a17=FAKE, a18=256) == INVALID      # in place with another ld
+    assert call(a12=FAKE + (5 << 30) + 64) == INVALID   # ce inside grad
+    assert call(a13=base + 512) == INVALID         # tvd aliases ce
+    assert call(a17=FAKE + (5 << 30) + 1) == ALIGN       # bf16 gradient off by one byte
+
+
 def test_binding_refuses_host_tensors(lib):
     import torch
     x = torch.zeros(2, 8)

@@ -349,3 +349,45 @@ def test_single_launch_parity_and_status():
     _, g_r, _ = run_single(w, grads=(torch.full((24,), 0.125, device=DEV),
                                      torch.full((24,), 0.5, device=DEV)))
     assert torch.equal(g_b[~torch.isnan(g_b.float()).any(1)], g_r[~torch.isnan(g_r.float()).any(1)])
+
+
+
+# ------------------------------------------------------------------ mean over tokens
+
+def test_mean_front_end_and_autograd_loss():
+    from distillation_ce_tvd_gb300.autograd import fused_ce_tvd_mean_loss
+    w = workloads.make("bt1024_v151936_bf16", DEV, rows=30, V=20000, seed=41)
+    w.target[[3, 4]] = w.ignore_index
+    alpha, beta = 0.8, 1.7
+    gce, gtvd, n = binding.fused_ce_tvd_mean_upstream(w.target, w.ignore_index, alpha, beta)
+    fwd, grad, st = run_single(w, grads=(gce, gtvd))
+    loss = binding.fused_ce_tvd_mean_loss(fwd["ce"], fwd["tvd"], w.target, w.ignore_index,
+                                          alpha, beta)
+    torch.cuda.synchronize()
+    assert st == 0 and int(n.item()) == 28
+    assert abs(gce.item() - alpha / 28) < 1e-9 and abs(gtvd.item() - beta / 28) < 1e-9
+    ref = oracle.mean_loss(fwd["ce"].cpu().numpy(), fwd["tvd"].cpu().numpy(),
+                           w.target.cpu().numpy(), w.ignore_index, alpha, beta)
+    assert abs(loss.item() - ref[0]) < 1e-6
+    # the gradient of the mean loss against the oracle's, row by row
+    s, t = w.student.cpu(), w.teacher.cpu()
+    tg = w.target.cpu().numpy()
+    ref_grad, _ = oracle.fused_ce_tvd_backward(s, t, tg, ref[1], ref[2], w.ignore_index)
+    masks, mass, probs = tie_info(s, t)
+    check_grad(grad.cpu().double().numpy(), ref_grad, np.full(30, ref[2]), masks, mass, probs,
+               tg, w.ignore_index, "mean ", grad.dtype)
+    # autograd wrapper: same loss and gradient
+    sv = w.student.clone().requires_grad_(True)
+    lv = fused_ce_tvd_mean_loss(sv, w.teacher, w.target, w.ignore_index, alpha, beta)
+    lv.backward()
+    assert torch.equal(lv.detach().reshape(1), loss)
+    assert torch.equal(sv.grad, grad)
+
+
+def test_mean_front_end_all_ignored():
+    tg = torch.full((5,), -100, device=DEV, dtype=torch.int64)
+    gce, gtvd, n = binding.fused_ce_tvd_mean_upstream(tg, -100, 1.0, 1.0)
+    z = torch.zeros(5, device=DEV)
+    loss = binding.fused_ce_tvd_mean_loss(z, z, tg)
+    torch.cuda.synchronize()
+    assert n.item() == 0 and gce.item() == 0 and gtvd.item() == 0 and loss.item() == 0

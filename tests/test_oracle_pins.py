@@ -255,3 +255,31 @@ def test_padded_rows_are_read_through_ld():
     b = oracle.fused_ce_tvd_forward(big_s[:, :30], big_t[:, :30], tg)
     for k in ("ce", "tvd", "sigma", "student_lse", "teacher_lse"):
         np.testing.assert_array_equal(a[k], b[k])
+
+
+# ---------------------------------------------------------------- mean over tokens
+
+def test_mean_loss_matches_torch_reductions_and_autograd():
+    s, t, tg = _rows(12, 20, 37)
+    tg = tg.copy(); tg[[2, 9, 10]] = IGN
+    alpha, beta = 0.7, 1.9
+    f = oracle.fused_ce_tvd_forward(s, t, tg)
+    loss, gce, gtvd, n = oracle.mean_loss(f["ce"], f["tvd"], tg, IGN, alpha, beta)
+    assert n == 17
+    S = torch.tensor(s, requires_grad=True)
+    T = torch.tensor(t)
+    TG = torch.tensor(tg)
+    keep = TG != IGN
+    ce_mean = torch.nn.functional.cross_entropy(S, TG, reduction="mean", ignore_index=IGN)
+    tvd_rows = 0.5 * (torch.softmax(S, -1) - torch.softmax(T, -1)).abs().sum(-1)
+    ref = alpha * ce_mean + beta * tvd_rows[keep].mean()
+    ref.backward()
+    assert abs(loss - ref.item()) < 1e-12
+    # the upstream gradients reproduce autograd's gradient of the mean loss
+    g, _ = oracle.fused_ce_tvd_backward(s, t, tg, gce, gtvd)
+    np.testing.assert_allclose(g, S.grad.numpy(), atol=1e-14)
+
+
+def test_mean_loss_with_no_kept_rows():
+    loss, gce, gtvd, n = oracle.mean_loss([0.0, 0.0], [0.0, 0.0], [IGN, IGN])
+    assert (loss, gce, gtvd, n) == (0.0, 0.0, 0.0, 0)
