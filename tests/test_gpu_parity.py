@@ -26,6 +26,14 @@ def _lib():
     binding.set_forward_cluster(0)
 
 
+def same_layout_clone(x):
+    """A copy with the same strides (a plain clone of a padded view would be
+    contiguous and take another code path)."""
+    y = torch.empty_strided(x.shape, x.stride(), dtype=x.dtype, device=x.device)
+    y.copy_(x)
+    return y
+
+
 def run(w, cluster=0, inplace=False, stream=None):
     """Forward + backward of a workload on the GPU; returns host copies."""
     prev = binding.set_forward_cluster(cluster)
@@ -33,7 +41,7 @@ def run(w, cluster=0, inplace=False, stream=None):
         status = torch.zeros(1, dtype=torch.int32, device=DEV)
         ce, tvd, ls, lt, sg = binding.fused_ce_tvd_forward(
             w.student, w.teacher, w.target, w.ignore_index, dev_status=status, stream=stream)
-        s_in = w.student.clone() if inplace else w.student
+        s_in = same_layout_clone(w.student) if inplace else w.student
         grad = binding.fused_ce_tvd_backward(
             s_in, w.teacher, w.target, ls, lt, sg, w.grad_ce, w.grad_tvd, w.ignore_index,
             inplace=inplace, dev_status=status, stream=stream)
@@ -298,7 +306,7 @@ def run_single(w, cluster=0, inplace=False, grads=None):
     prev = binding.set_forward_cluster(cluster)
     try:
         status = torch.zeros(1, dtype=torch.int32, device=DEV)
-        s_in = w.student.clone() if inplace else w.student
+        s_in = same_layout_clone(w.student) if inplace else w.student
         gce, gtvd = grads if grads is not None else (w.grad_ce, w.grad_tvd)
         ce, tvd, ls, lt, sg, grad = binding.fused_ce_tvd_forward_backward(
             s_in, w.teacher, w.target, gce, gtvd, w.ignore_index, inplace=inplace,
