@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <mutex>
+#include <string>
 
 #include "fct_internal.h"
 
@@ -92,12 +93,13 @@ int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
 // results do not depend on how the rows are batched.
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec) {
   fct::FwdPlan plan{vec, 1, 0, false};
-  // FCT_FWD_PACKED=1 selects packed f32x2 arithmetic (tuning experiments).
-  static const bool packed = [] {
-    const char* e = std::getenv("FCT_FWD_PACKED");
-    return e && std::atoi(e) == 1;
+  // FCT_L2_KEEP=normal tags rows that are read again with evict_normal
+  // instead of evict_last (a tuning experiment).
+  static const bool keep_normal = [] {
+    const char* e = std::getenv("FCT_L2_KEEP");
+    return e && std::string(e) == "normal";
   }();
-  plan.packed = packed;
+  plan.keep_normal = keep_normal;
   if (!tvd) return plan;  // one pass: nothing to keep in L2
   const double row_bytes = 2.0 * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
   const double budget = 0.80 * static_cast<double>(d.l2_bytes);
@@ -151,8 +153,9 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
   if ((rc = current_device(&d)) != FCT_OK) return rc;
   const bool vec = vec_ok(student, ld_s, dtype) && (!fused || vec_ok(teacher, ld_t, dtype));
   fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
-                 ce, tvd, lse_s, lse_t, sigma, dev_status, nullptr, 0, nullptr, nullptr, 0};
+                 ce, tvd, lse_s, lse_t, sigma, dev_status, nullptr, 0, nullptr, nullptr, 0, 0};
   const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec);
+  a.keep_normal = plan.keep_normal ? 1 : 0;
   if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
@@ -260,8 +263,9 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
   }
   fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
                  ce, tvd, lse_s, lse_t, sigma, dev_status, grad, ld_g, grad_ce, grad_tvd,
-                 grad_stride};
+                 grad_stride, 0};
   const fct::FwdPlan plan = plan_forward(d, V, dtype, true, true);
+  a.keep_normal = plan.keep_normal ? 1 : 0;
   if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;

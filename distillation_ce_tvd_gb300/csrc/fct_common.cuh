@@ -64,46 +64,12 @@ __device__ __forceinline__ void lse2_update(Lse2& st, const float (&x)[N]) {
   st.s += acc;
 }
 
-// ---------------------------------------------------------------- packed fp32 pairs
-//
-// sm_100+ executes two fp32 operations per lane in one instruction
-// (fma/add/mul .f32x2), each lane rounded exactly like the scalar form.
+// ---------------------------------------------------------------- step-2 sums
 
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 A, B, C, D;\n\t"
-      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\tmov.b64 C, {%6, %7};\n\t"
-      "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-
-__device__ __forceinline__ float2 add2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 A, B, D;\n\t"
-      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %5};\n\t"
-      "add.rn.f32x2 D, A, B;\n\tmov.b64 {%0, %1}, D;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
-// (pp, qp) += (p, q) when p > q; (pn, qn) += (p, q) when p < q; ties add
-// nothing.  Then sum|p - q| = (pp - qp) + (qn - pn) and
-// sum p*sign(p - q) = pp - pn, with sign(0) = 0 exactly.
+// (pos.x, pos.y) += (p, q) when p > q; (neg.x, neg.y) += (p, q) when p < q;
+// ties add nothing.  Then sum|p - q| = (pos.x - pos.y) + (neg.y - neg.x) and
+// sum p*sign(p - q) = pos.x - neg.x, with sign(0) = 0 exactly.
 __device__ __forceinline__ void tvd_split(float p, float q, float2& pos, float2& neg) {
-  asm("{\n\t.reg .pred gt, lt;\n\t.reg .b64 PQ, A;\n\t"
-      "setp.gt.f32 gt, %4, %5;\n\tsetp.lt.f32 lt, %4, %5;\n\t"
-      "mov.b64 PQ, {%4, %5};\n\t"
-      "mov.b64 A, {%0, %1};\n\t@gt add.rn.f32x2 A, A, PQ;\n\tmov.b64 {%0, %1}, A;\n\t"
-      "mov.b64 A, {%2, %3};\n\t@lt add.rn.f32x2 A, A, PQ;\n\tmov.b64 {%2, %3}, A;\n\t}"
-      : "+f"(pos.x), "+f"(pos.y), "+f"(neg.x), "+f"(neg.y)
-      : "f"(p), "f"(q));
-}
-
-// Scalar form of tvd_split: four predicated adds instead of two packed ones.
-__device__ __forceinline__ void tvd_split_scalar(float p, float q, float2& pos, float2& neg) {
   asm("{\n\t.reg .pred gt, lt;\n\t"
       "setp.gt.f32 gt, %4, %5;\n\tsetp.lt.f32 lt, %4, %5;\n\t"
       "@gt add.f32 %0, %0, %4;\n\t@gt add.f32 %1, %1, %5;\n\t"
@@ -133,7 +99,8 @@ __device__ __forceinline__ float vec_max(const float (&x)[N]) {
   }
 }
 
-// Running base-2 log-sum-exp state with two partial sums (summed by add2).
+// Running base-2 log-sum-exp state with two partial sums (two independent
+// accumulation chains).
 struct Lse2x {
   float m2;
   float2 s;
@@ -144,8 +111,8 @@ __device__ __forceinline__ Lse2x lse2x_empty() { return Lse2x{-INFINITY, make_fl
 __device__ __forceinline__ Lse2 lse2x_fold(Lse2x a) { return Lse2{a.m2, a.s.x + a.s.y}; }
 
 // Fold N (even) values: one rescale if the group raises the maximum, then
-// N/2 packed FMAs for the exponents, N ex2, N/2 packed adds.
-template <bool kPacked, int N>
+// N FMAs for the exponents, N ex2 and N adds into two chains.
+template <int N>
 __device__ __forceinline__ void lse2x_update(Lse2x& st, const float (&x)[N]) {
   static_assert(N % 2 == 0, "pairs");
   const float m2n = vec_max(x) * kLog2e;
@@ -155,21 +122,11 @@ __device__ __forceinline__ void lse2x_update(Lse2x& st, const float (&x)[N]) {
     st.s.y *= sc;
     st.m2 = m2n;
   }
-  if constexpr (kPacked) {
-    const float2 L2 = make_float2(kLog2e, kLog2e);
-    const float2 nm = make_float2(-st.m2, -st.m2);
+  const float nm = -st.m2;
 #pragma unroll
-    for (int j = 0; j < N; j += 2) {
-      const float2 a = fma2(make_float2(x[j], x[j + 1]), L2, nm);
-      st.s = add2(st.s, make_float2(ex2(a.x), ex2(a.y)));
-    }
-  } else {
-    const float nm = -st.m2;
-#pragma unroll
-    for (int j = 0; j < N; j += 2) {
-      st.s.x += ex2(fmaf(x[j], kLog2e, nm));
-      st.s.y += ex2(fmaf(x[j + 1], kLog2e, nm));
-    }
+  for (int j = 0; j < N; j += 2) {
+    st.s.x += ex2(fmaf(x[j], kLog2e, nm));
+    st.s.y += ex2(fmaf(x[j + 1], kLog2e, nm));
   }
 }
 
@@ -179,6 +136,11 @@ __device__ __forceinline__ void lse2x_update(Lse2x& st, const float (&x)[N]) {
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -15,13 +15,13 @@
 //     rows in flight (clusters on the GPU) times the row size is kept under
 //     the L2 capacity.  HBM therefore sees each logit about once, and no
 //     (BT, V) buffer is ever written.
-//   * Every thread streams its own vectors through a private ring of
-//     kStages 16-byte slots per tensor in shared memory, filled by
-//     cp.async D steps ahead.  The feed runs on across the step-1/step-2
+//   * Every thread streams its own vectors through a private ring in shared
+//     memory (kStages steps of kPerStep 16-byte vectors per tensor), filled
+//     by cp.async one step ahead of the step being read.  The feed runs on across the step-1/step-2
 //     boundary and into the next row, so loads stay in flight while the CTA
 //     reduces; no thread ever reads another thread's slot, so the ring needs
 //     no barrier.
-//   * Step 2 keeps four packed sums per thread: (sum p, sum q) over p > q and
+//   * Step 2 keeps four predicated sums per thread: (sum p, sum q) over p > q and
 //     over p < q.  Then sum|p - q| = (P+ - Q+) + (Q- - P-) and
 //     sigma = P+ - P-, and ties contribute to neither (zero subgradient).
 //   * The grid is persistent: one cluster per row slot, looping over rows.
@@ -180,9 +180,13 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 // (NT vectors apart) per step.  Both the feed and the consumer walk this
 // same sequence; the feed runs kStages steps ahead.
 
-constexpr int kPerStep = 2;  // vectors per tensor moved by one step
+constexpr int kPerStep = 4;  // vectors per tensor moved by one step
+constexpr int kStages = 2;   // steps in flight per thread
 
-template <typename T, int VE, bool kTvd, bool kGrad, int NT, int kStages>
+// The feed: this thread's cursor in the sequence, issuing one step of
+// cp.async copies per call.  A pass of a row is n_full full steps of
+// kPerStep vectors and, if rem > 0, one final step of rem vectors.
+template <typename T, int VE, bool kTvd, bool kGrad, int NT>
 struct Feed {
   static constexpr int kPasses = kTvd ? (kGrad ? 3 : 2) : 1;
   static constexpr int kTensors = kTvd ? 2 : 1;
@@ -194,40 +198,51 @@ struct Feed {
   int64_t row;
   int32_t q;       // step within the pass
   int32_t pass;
-  int32_t n_my, n_steps;
+  int32_t n_full, rem;
+  bool active;     // false once this thread's sequence is exhausted
   int64_t first_byte;  // byte offset of this thread's first vector within a row
   uint32_t ring;       // shared address of this thread's 16 bytes in slot 0
-  uint64_t keep, drop;
+  uint64_t keep, drop, pol;
 
   __device__ __forceinline__ void seek_row(const FwdArgs& p) {
     sp = static_cast<const char*>(p.student) + (row * p.ld_s) * int64_t(sizeof(T)) + first_byte;
     if constexpr (kTvd)
       tp = static_cast<const char*>(p.teacher) + (row * p.ld_t) * int64_t(sizeof(T)) + first_byte;
+    // keep the row in L2 until its last pass reads it
+    pol = (pass + 1 < kPasses) ? keep : drop;
   }
 
   __device__ __forceinline__ void next_row(const FwdArgs& p, int64_t n_clusters) {
     row += n_clusters;
     while (row < p.BT && p.target[row] == p.ignore_index) row += n_clusters;
-    if (row < p.BT) seek_row(p);
+    active = row < p.BT;
+    if (active) seek_row(p);
   }
 
-  // Issue the next step's copies into `slot` and commit one group (an
-  // empty group once this thread's sequence is exhausted).
-  __device__ __forceinline__ void feed(const FwdArgs& p, int slot, int64_t n_clusters) {
-    if (row < p.BT) {
-      // keep the row in L2 until its last pass reads it
-      const uint64_t pol = (pass + 1 < kPasses) ? keep : drop;
-      const uint32_t dst = ring + slot * kSlotBytes;
-      const bool two = (2 * q + 1) < n_my;
-      cp_async16(dst, sp, pol);
-      if (two) cp_async16(dst + NT * 16, sp + kStride, pol);
-      if constexpr (kTvd) {
-        cp_async16(dst + 2 * NT * 16, tp, pol);
-        if (two) cp_async16(dst + 3 * NT * 16, tp + kStride, pol);
+  template <int kCount>
+  __device__ __forceinline__ void copy(uint32_t dst, int count) {
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) {
+      if (kCount == kPerStep || u < count) {
+        cp_async16(dst + u * NT * 16, sp + u * kStride, pol);
+        if constexpr (kTvd) cp_async16(dst + (kPerStep + u) * NT * 16, tp + u * kStride, pol);
       }
-      sp += 2 * kStride;
-      if constexpr (kTvd) tp += 2 * kStride;
-      if (++q == n_steps) {
+    }
+  }
+
+  // Issue the next step's copies into `slot` and commit one group (an empty
+  // group once the sequence is exhausted, so group counting stays uniform).
+  __device__ __forceinline__ void feed(const FwdArgs& p, int slot, int64_t n_clusters) {
+    if (active) {
+      const uint32_t dst = ring + slot * kSlotBytes;
+      if (q < n_full) {
+        copy<kPerStep>(dst, kPerStep);
+      } else {
+        copy<0>(dst, rem);
+      }
+      sp += kPerStep * kStride;
+      if constexpr (kTvd) tp += kPerStep * kStride;
+      if (++q == n_full + (rem ? 1 : 0)) {
         q = 0;
         if (++pass == kPasses) {
           pass = 0;
@@ -241,11 +256,36 @@ struct Feed {
   }
 };
 
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, int kStages, bool kPacked>
+// One pass of the consumer over this thread's vectors of the current row:
+// fn(s_cell, t_cell, k) for k = 0 .. n_my-1 in order (t_cell only for the
+// fused loss), refilling each slot with the feed's next step once read.
+template <int NT, int kTensors, class FeedT, class Fn>
+__device__ __forceinline__ void consume_pass(FeedT& f, int& slot, const FwdArgs& p,
+                                             int64_t n_clusters, const uint4* mine, int n_full,
+                                             int rem, Fn&& fn) {
+  constexpr int kSlotVecs = kTensors * kPerStep * NT;
+  for (int q = 0; q < n_full; ++q) {
+    cp_async_wait<kStages - 1>();
+    const uint4* cell = mine + slot * kSlotVecs;
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) fn(cell + u * NT, cell + (kPerStep + u) * NT, q * kPerStep + u);
+    f.feed(p, slot, n_clusters);
+    slot ^= 1;
+  }
+  if (rem) {
+    cp_async_wait<kStages - 1>();
+    const uint4* cell = mine + slot * kSlotVecs;
+    for (int u = 0; u < rem; ++u) fn(cell + u * NT, cell + (kPerStep + u) * NT, n_full * kPerStep + u);
+    f.feed(p, slot, n_clusters);
+    slot ^= 1;
+  }
+}
+
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
-  using F = Feed<T, VE, kTvd, kGrad, NT, kStages>;
-  static_assert((kStages & (kStages - 1)) == 0, "power-of-two ring");
+  static_assert(kStages == 2, "the slot index toggles");
+  using F = Feed<T, VE, kTvd, kGrad, NT>;
   extern __shared__ __align__(16) uint4 ring_mem[];
   __shared__ float4 red_lse[kMaxWarps];
   __shared__ float2 red_sum[kMaxWarps];
@@ -264,21 +304,25 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   const int tid = threadIdx.x;
   const bool owns_tail = (rank == C - 1);
 
+  // this thread's vectors in each pass of a row: vb + tid + k*NT, k < n_my
+  const int n_my = (span > tid) ? static_cast<int>((span - tid + NT - 1) / NT) : 0;
+  const int n_full = n_my / kPerStep, rem = n_my % kPerStep;
+
   F f;
-  f.n_my = (span > tid) ? static_cast<int32_t>((span - tid + NT - 1) / NT) : 0;
-  f.n_steps = (f.n_my + 1) / 2;
+  f.n_full = n_full;
+  f.rem = rem;
   f.first_byte = (vb + tid) * 16;
   f.ring = static_cast<uint32_t>(__cvta_generic_to_shared(ring_mem)) + tid * 16;
-  f.keep = policy_evict_last();
+  f.keep = p.keep_normal ? policy_evict_normal() : policy_evict_last();
   f.drop = policy_evict_first();
   f.q = 0;
   f.pass = 0;
   f.row = cluster_id;
   while (f.row < p.BT && p.target[f.row] == p.ignore_index) f.row += n_clusters;
-  if (f.n_my == 0) f.row = p.BT;  // nothing to stream: only empty groups
-  if (f.row < p.BT) f.seek_row(p);
+  f.active = (n_my > 0) && (f.row < p.BT);
+  if (f.active) f.seek_row(p);
 
-  // this thread's 16-byte cell of (slot, tensor, u): mine[((slot*kTensors + tensor)*2 + u)*NT]
+  // this thread's 16-byte cells: ring_mem[((slot*kTensors + tensor)*kPerStep + u)*NT + tid]
   const uint4* mine = ring_mem + tid;
 #pragma unroll
   for (int s = 0; s < kStages; ++s) f.feed(p, s, n_clusters);
@@ -286,7 +330,6 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 
   const T* S = static_cast<const T*>(p.student);
   const T* Tt = static_cast<const T*>(p.teacher);
-  const int n_steps = f.n_steps, n_my = f.n_my;
 
   for (int64_t row = cluster_id; row < p.BT; row += n_clusters) {
     const int64_t tg = p.target[row];
@@ -308,28 +351,16 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
-    for (int q = 0; q < n_steps; ++q) {
-      cp_async_wait<kStages - 1>();
-      const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
-      const bool two = (2 * q + 1) < n_my;
-      float x[VE];
-      unpack_raw<T, VE>(cell[0], x);
-      lse2x_update<kPacked>(a, x);
-      if (two) {
-        unpack_raw<T, VE>(cell[NT], x);
-        lse2x_update<kPacked>(a, x);
-      }
-      if constexpr (kTvd) {
-        unpack_raw<T, VE>(cell[2 * NT], x);
-        lse2x_update<kPacked>(b, x);
-        if (two) {
-          unpack_raw<T, VE>(cell[3 * NT], x);
-          lse2x_update<kPacked>(b, x);
-        }
-      }
-      f.feed(p, slot, n_clusters);
-      slot = (slot + 1) & (kStages - 1);
-    }
+    consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
+                                  [&](const uint4* cs, const uint4* ct, int) {
+                                    float x[VE];
+                                    unpack_raw<T, VE>(*cs, x);
+                                    lse2x_update(a, x);
+                                    if constexpr (kTvd) {
+                                      unpack_raw<T, VE>(*ct, x);
+                                      lse2x_update(b, x);
+                                    }
+                                  });
     Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
     if (owns_tail && tail0 + tid < p.V) {
       float xs[1] = {Elem<T>::load1(srow + tail0 + tid)};
@@ -361,30 +392,16 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 
       // ---- step 2: split sums of (p, q) by the sign of p - q
       float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
-      auto step2 = [&](uint4 ws, uint4 wt) {
-        float xs[VE], xt[VE];
-        unpack_raw<T, VE>(ws, xs);
-        unpack_raw<T, VE>(wt, xt);
+      consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
+                                    [&](const uint4* cs, const uint4* ct, int) {
+                                      float xs[VE], xt[VE];
+                                      unpack_raw<T, VE>(*cs, xs);
+                                      unpack_raw<T, VE>(*ct, xt);
 #pragma unroll
-        for (int j = 0; j < VE; ++j) {
-          if constexpr (kPacked) {
-            const float2 e = fma2(make_float2(xs[j], xt[j]), make_float2(kLog2e, kLog2e),
-                                  make_float2(ns2, nt2));
-            tvd_split(ex2(e.x), ex2(e.y), pos, neg);
-          } else {
-            tvd_split_scalar(ex2(fmaf(xs[j], kLog2e, ns2)), ex2(fmaf(xt[j], kLog2e, nt2)), pos,
-                             neg);
-          }
-        }
-      };
-      for (int q = 0; q < n_steps; ++q) {
-        cp_async_wait<kStages - 1>();
-        const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
-        step2(cell[0], cell[2 * NT]);
-        if ((2 * q + 1) < n_my) step2(cell[NT], cell[3 * NT]);
-        f.feed(p, slot, n_clusters);
-        slot = (slot + 1) & (kStages - 1);
-      }
+                                      for (int j = 0; j < VE; ++j)
+                                        tvd_split(ex2(fmaf(xs[j], kLog2e, ns2)),
+                                                  ex2(fmaf(xt[j], kLog2e, nt2)), pos, neg);
+                                    });
       if (owns_tail && tail0 + tid < p.V) {
         tvd_accum1(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid), ns2,
                    nt2, pos, neg);
@@ -409,39 +426,35 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         const float c_zero = gce - h * sig;
         const bool bad = (tg < 0 || tg >= p.V);
         T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
+        T* gmine = grow + (vb + tid) * VE;
+        // element offset of the target from this thread's first element
+        const int64_t tg_rel = tg - (vb + tid) * VE;
         auto grad_of = [&](float xs, float xt) {
           const float pp = ex2(fmaf(xs, kLog2e, ns2));
           const float qq = ex2(fmaf(xt, kLog2e, nt2));
           const float c = (pp > qq) ? c_pos : ((pp < qq) ? c_neg : c_zero);
           return pp * c;
         };
-        auto step3 = [&](uint4 ws, uint4 wt, int64_t v) {
-          float xs[VE], xt[VE], g[VE];
-          unpack_raw<T, VE>(ws, xs);
-          unpack_raw<T, VE>(wt, xt);
+        consume_pass<NT, F::kTensors>(
+            f, slot, p, n_clusters, mine, n_full, rem,
+            [&](const uint4* cs, const uint4* ct, int k) {
+              float xs[VE], xt[VE], g[VE];
+              unpack_raw<T, VE>(*cs, xs);
+              unpack_raw<T, VE>(*ct, xt);
 #pragma unroll
-          for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
-          const int64_t off = tg - v * VE;
-          if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+              for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+              const int64_t off = tg_rel - int64_t(k) * NT * VE;
+              if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
 #pragma unroll
-            for (int j = 0; j < VE; ++j)
-              if (j == off) g[j] -= gce;
-          }
-          if (bad) {
+                for (int j = 0; j < VE; ++j)
+                  if (j == off) g[j] -= gce;
+              }
+              if (bad) {
 #pragma unroll
-            for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
-          }
-          store_vec<T, VE>(grow + v * VE, g, f.drop);
-        };
-        for (int q = 0; q < n_steps; ++q) {
-          cp_async_wait<kStages - 1>();
-          const uint4* cell = mine + slot * (F::kTensors * kPerStep * NT);
-          const int64_t v = vb + tid + int64_t(2 * q) * NT;
-          step3(cell[0], cell[2 * NT], v);
-          if ((2 * q + 1) < n_my) step3(cell[NT], cell[3 * NT], v + NT);
-          f.feed(p, slot, n_clusters);
-          slot = (slot + 1) & (kStages - 1);
-        }
+                for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
+              }
+              store_vec<T, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
+            });
         if (owns_tail && tail0 + tid < p.V) {
           const int64_t v = tail0 + tid;
           float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
@@ -573,10 +586,10 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per process.
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, int kStages, bool kPacked>
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16;
-  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, kStages, kPacked>;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
@@ -610,8 +623,7 @@ cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   } else {
     if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
   }
-  if (plan.packed) return run_pipelined<T, VE, C, kTvd, kGrad, 512, 4, true>(a, plan.slots, st);
-  return run_pipelined<T, VE, C, kTvd, kGrad, 512, 4, false>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, kGrad, 512>(a, plan.slots, st);
 }
 
 template <typename T, bool kTvd, bool kGrad>

@@ -27,13 +27,14 @@ struct FwdArgs {
   const float* grad_ce;
   const float* grad_tvd;
   int64_t grad_stride;
+  int keep_normal;  // 1: evict_normal instead of evict_last while a row must stay in L2
 };
 
 struct FwdPlan {
   bool vec;     // 16-byte vector path (pointers and strides aligned)
   int cluster;  // CTAs per row: 1, 2, 4 or 8
   int slots;    // rows in flight across the GPU (clusters launched), 0 = as many as fit
-  bool packed;  // packed f32x2 arithmetic in the pipelined path
+  bool keep_normal;  // L2 policy for rows that are read again (tuning)
 };
 
 struct BwdArgs {
