@@ -346,13 +346,21 @@ def main():
         d2h = 2 * BT * 4
 
         def e2e_step():
-            w.student.copy_(hs, non_blocking=True)
-            w.teacher.copy_(ht, non_blocking=True)
-            w.target.copy_(htg, non_blocking=True)
+            # host logits in, per-row ce and tvd out; the copies of later row
+            # blocks overlap the compute of earlier ones
             w.grad_ce.copy_(hgc, non_blocking=True)
             w.grad_tvd.copy_(hgt, non_blocking=True)
-            for _, fn, _ in paths[args.path]:
-                fn()
+            if args.path == "single":
+                binding.fused_ce_tvd_forward_backward_from_host(
+                    hs, ht, htg, w.grad_ce, w.grad_tvd, w.student, w.teacher, w.target,
+                    w.ignore_index, ce=ce, tvd=tvd, student_lse=ls, teacher_lse=lt, sigma=sg,
+                    grad_student=grad, stream=stream)
+            else:
+                w.student.copy_(hs, non_blocking=True)
+                w.teacher.copy_(ht, non_blocking=True)
+                w.target.copy_(htg, non_blocking=True)
+                for _, fn, _ in paths[args.path]:
+                    fn()
             out_ce.copy_(ce, non_blocking=True)
             out_tvd.copy_(tvd, non_blocking=True)
 

@@ -300,3 +300,57 @@ def fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index=IGNORE_INDEX, alpha=1.0
                                        float(alpha), float(beta), _ptr(out), _stream(stream))
     _check(rc, "fused_ce_tvd_mean_loss")
     return out
+
+
+def fused_ce_tvd_forward_backward_from_host(student_h, teacher_h, target_h, grad_ce, grad_tvd,
+                                            student, teacher, target, ignore_index=IGNORE_INDEX,
+                                            *, ce=None, tvd=None, student_lse=None,
+                                            teacher_lse=None, sigma=None, grad_student=None,
+                                            block_rows=1024, copy_streams=2, stream=None):
+    """Single-launch forward + backward for logits that live in pinned host memory.
+
+    Row blocks are copied into the device tensors ``student``/``teacher``/
+    ``target`` on ``copy_streams`` side streams (several DMA engines at once),
+    and each block is computed on ``stream`` as soon as its copy lands, so the
+    transfer of later blocks overlaps the compute of earlier ones.  Rows are
+    independent, so the results equal one call on the whole batch.  Returns
+    the same tuple as fused_ce_tvd_forward_backward; ordering on ``stream``
+    is as if everything ran there.
+    """
+    if not (student_h.is_pinned() and teacher_h.is_pinned()):
+        raise ValueError("host logits must be in pinned memory")
+    BT = student.shape[0]
+    dev = student.device
+    main = stream if stream is not None else torch.cuda.current_stream(dev)
+    outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                                             (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
+    if grad_student is None:
+        grad_student = torch.empty_like(student)
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    per_row = stride_ce == 1 or stride_tvd == 1
+    copiers = [torch.cuda.Stream(dev) for _ in range(max(1, copy_streams))]
+    start = torch.cuda.Event()
+    start.record(main)  # the copies must not overwrite buffers still in use
+    for i, r0 in enumerate(range(0, BT, block_rows)):
+        r1 = min(BT, r0 + block_rows)
+        cs = copiers[i % len(copiers)]
+        cs.wait_event(start)
+        with torch.cuda.stream(cs):
+            student[r0:r1].copy_(student_h[r0:r1], non_blocking=True)
+            teacher[r0:r1].copy_(teacher_h[r0:r1], non_blocking=True)
+            target[r0:r1].copy_(target_h[r0:r1], non_blocking=True)
+        done = torch.cuda.Event()
+        done.record(cs)
+        main.wait_event(done)
+        g1 = (gce[r0:r1], gtvd[r0:r1]) if per_row else (gce, gtvd)
+        fused_ce_tvd_forward_backward(
+            student[r0:r1], teacher[r0:r1], target[r0:r1], g1[0], g1[1], ignore_index,
+            ce=outs[0][r0:r1], tvd=outs[1][r0:r1], student_lse=outs[2][r0:r1],
+            teacher_lse=outs[3][r0:r1], sigma=outs[4][r0:r1], grad_student=grad_student[r0:r1],
+            stream=main)
+    for cs in copiers:  # the caller's stream owns the buffers again afterwards
+        main.wait_stream(cs)
+    return (*outs, grad_student)

@@ -11,9 +11,10 @@
 //
 // GB300 mapping: a pure stream (2 reads + 1 write per element) cut into
 // units of (row, 1024 vectors); a persistent grid of resident CTAs walks the
-// units.  Per element the coefficient of p takes one of three per-row
-// values picked by the sign, so the inner loop is two ex2, one subtract, two
-// selects and one multiply.  Each element is read and then written by the
+// units.  Per element the coefficient of p is c0 + h*sign with per-row
+// c0 = grad_ce - h*sigma and h = grad_tvd/2, and sign from two compares that
+// yield 0 at ties, so the inner loop is two ex2, two compares, one subtract
+// and two FMAs/multiplies.  Each element is read and then written by the
 // same thread, which makes grad_student == student (in place) safe.
 #include "fct_common.cuh"
 #include "fct_internal.h"
@@ -65,15 +66,12 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
 
     const float gce = a.grad_ce[row * a.grad_stride];
     const float ns2 = -(a.lse_s[row] * kLog2e);
-    float nt2 = 0.f, c_pos = gce, c_neg = gce, c_zero = gce;
+    // coefficient of p: c = gce + h * (sign - sigma) = c0 + h * sign
+    float nt2 = 0.f, h = 0.f, c0 = gce;
     if constexpr (kTvd) {
-      const float gtvd = a.grad_tvd[row * a.grad_stride];
-      const float sg = a.sigma[row];
-      const float h = 0.5f * gtvd;
+      h = 0.5f * a.grad_tvd[row * a.grad_stride];
       nt2 = -(a.lse_t[row] * kLog2e);
-      c_pos = gce + h * (1.f - sg);   // sign = +1
-      c_neg = gce + h * (-1.f - sg);  // sign = -1
-      c_zero = gce - h * sg;          // tie
+      c0 = gce - h * a.sigma[row];
     }
 
     auto grad_of = [&](const float (&xs)[VE], const float (&xt)[VE], int64_t base, float (&g)[VE]) {
@@ -81,11 +79,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
       for (int j = 0; j < VE; ++j) {
         const float p = ex2(fmaf(xs[j], kLog2e, ns2));
         float c = gce;
-        if constexpr (kTvd) {
-          const float q = ex2(fmaf(xt[j], kLog2e, nt2));
-          const float d = p - q;
-          c = (d > 0.f) ? c_pos : ((d < 0.f) ? c_neg : c_zero);
-        }
+        if constexpr (kTvd) c = fmaf(h, sgn_pq(p, ex2(fmaf(xt[j], kLog2e, nt2))), c0);
         g[j] = p * c;
       }
       const int64_t off = tg - base;
@@ -128,11 +122,7 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
       // one element: reuse the vector code with VE = 1 semantics
       const float p = ex2(fmaf(xs[0], kLog2e, ns2));
       float c = gce;
-      if constexpr (kTvd) {
-        const float q = ex2(fmaf(xt[0], kLog2e, nt2));
-        const float d = p - q;
-        c = (d > 0.f) ? c_pos : ((d < 0.f) ? c_neg : c_zero);
-      }
+      if constexpr (kTvd) c = fmaf(h, sgn_pq(p, ex2(fmaf(xt[0], kLog2e, nt2))), c0);
       g[0] = p * c;
       if (v == tg) g[0] -= gce;
       Elem<T>::store1(grow + v, g[0]);

@@ -66,16 +66,13 @@ __device__ __forceinline__ void lse2_update(Lse2& st, const float (&x)[N]) {
 
 // ---------------------------------------------------------------- step-2 sums
 
-// (pos.x, pos.y) += (p, q) when p > q; (neg.x, neg.y) += (p, q) when p < q;
-// ties add nothing.  Then sum|p - q| = (pos.x - pos.y) + (neg.y - neg.x) and
-// sum p*sign(p - q) = pos.x - neg.x, with sign(0) = 0 exactly.
-__device__ __forceinline__ void tvd_split(float p, float q, float2& pos, float2& neg) {
-  asm("{\n\t.reg .pred gt, lt;\n\t"
-      "setp.gt.f32 gt, %4, %5;\n\tsetp.lt.f32 lt, %4, %5;\n\t"
-      "@gt add.f32 %0, %0, %4;\n\t@gt add.f32 %1, %1, %5;\n\t"
-      "@lt add.f32 %2, %2, %4;\n\t@lt add.f32 %3, %3, %5;\n\t}"
-      : "+f"(pos.x), "+f"(pos.y), "+f"(neg.x), "+f"(neg.y)
-      : "f"(p), "f"(q));
+// sign(p - q) as a float: +1, -1, or 0 exactly when p == q (the zero
+// subgradient at ties), from two compares that write 1.0f / 0.0f.
+__device__ __forceinline__ float sgn_pq(float p, float q) {
+  float gt, lt;
+  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(gt) : "f"(p), "f"(q));
+  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(lt) : "f"(p), "f"(q));
+  return gt - lt;
 }
 
 // max(a, b, c) in one instruction (sm_100+).

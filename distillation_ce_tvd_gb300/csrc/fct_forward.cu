@@ -21,9 +21,12 @@
 //     boundary and into the next row, so loads stay in flight while the CTA
 //     reduces; no thread ever reads another thread's slot, so the ring needs
 //     no barrier.
-//   * Step 2 keeps four predicated sums per thread: (sum p, sum q) over p > q and
-//     over p < q.  Then sum|p - q| = (P+ - Q+) + (Q- - P-) and
-//     sigma = P+ - P-, and ties contribute to neither (zero subgradient).
+//   * Step 1 takes exponents against a running reference maximum and redoes a
+//     step against a raised maximum only when its sum reaches 2^64, so the
+//     common step costs one FMA, one ex2 and one add per element.
+//   * Step 2 accumulates sigma = sum p*sign(p - q) and tau = sum q*sign(p - q)
+//     with sign from two compares (0 at ties: zero subgradient); then
+//     sum|p - q| = sigma - tau.
 //   * The grid is persistent: one cluster per row slot, looping over rows.
 //   * With the upstream gradients known before the launch, a third pass over
 //     the still L2-resident row writes the student gradient of the "Backward
@@ -136,12 +139,14 @@ __device__ __forceinline__ void cluster_sum2_all(float& x, float& y, float2* par
   }
 }
 
-// One element pair of step 2, scalar form (tails and the unaligned path).
+// One element pair of step 2: sig_p += p*sign(p - q), sig_q += q*sign(p - q).
 __device__ __forceinline__ void tvd_accum1(float xs, float xt, float ns2, float nt2,
-                                           float2& pos, float2& neg) {
+                                           float& sig_p, float& sig_q) {
   const float p = ex2(fmaf(xs, kLog2e, ns2));
   const float q = ex2(fmaf(xt, kLog2e, nt2));
-  tvd_split(p, q, pos, neg);
+  const float sg = sgn_pq(p, q);
+  sig_p = fmaf(p, sg, sig_p);
+  sig_q = fmaf(q, sg, sig_q);
 }
 
 template <bool kTvd>
@@ -181,6 +186,12 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 // same sequence; the feed runs kStages steps ahead.
 
 constexpr int kPerStep = 4;  // vectors per tensor moved by one step
+
+// A step's vector count known at compile time (full steps).
+template <int N>
+struct Count {
+  __device__ __forceinline__ constexpr operator int() const { return N; }
+};
 constexpr int kStages = 2;   // steps in flight per thread
 
 // The feed: this thread's cursor in the sequence, issuing one step of
@@ -256,9 +267,11 @@ struct Feed {
   }
 };
 
-// One pass of the consumer over this thread's vectors of the current row:
-// fn(s_cell, t_cell, k) for k = 0 .. n_my-1 in order (t_cell only for the
-// fused loss), refilling each slot with the feed's next step once read.
+// One pass of the consumer over this thread's vectors of the current row,
+// one step at a time: fn(cell, n, k0) with the step's n vectors at
+// cell[u*NT] (student) and cell[(kPerStep + u)*NT] (teacher), u < n, being
+// this thread's vectors k0 .. k0+n-1.  n is a compile-time constant for full
+// steps.  Each slot is refilled with the feed's next step once read.
 template <int NT, int kTensors, class FeedT, class Fn>
 __device__ __forceinline__ void consume_pass(FeedT& f, int& slot, const FwdArgs& p,
                                              int64_t n_clusters, const uint4* mine, int n_full,
@@ -266,19 +279,70 @@ __device__ __forceinline__ void consume_pass(FeedT& f, int& slot, const FwdArgs&
   constexpr int kSlotVecs = kTensors * kPerStep * NT;
   for (int q = 0; q < n_full; ++q) {
     cp_async_wait<kStages - 1>();
-    const uint4* cell = mine + slot * kSlotVecs;
-#pragma unroll
-    for (int u = 0; u < kPerStep; ++u) fn(cell + u * NT, cell + (kPerStep + u) * NT, q * kPerStep + u);
+    fn(mine + slot * kSlotVecs, Count<kPerStep>{}, q * kPerStep);
     f.feed(p, slot, n_clusters);
     slot ^= 1;
   }
   if (rem) {
     cp_async_wait<kStages - 1>();
-    const uint4* cell = mine + slot * kSlotVecs;
-    for (int u = 0; u < rem; ++u) fn(cell + u * NT, cell + (kPerStep + u) * NT, n_full * kPerStep + u);
+    fn(mine + slot * kSlotVecs, rem, n_full * kPerStep);
     f.feed(p, slot, n_clusters);
     slot ^= 1;
   }
+}
+
+// Step-1 update with one step's vectors of one tensor.  The exponents are
+// taken against the running reference st.m2 without a per-vector maximum;
+// only when the step's sum reaches 2^64 (or is not finite: the first step of
+// a row, a new maximum far above the old one, non-finite data) is the step
+// redone against its own maximum.  Values up to 2^64 above the reference
+// stay exact in fp32 and the sums cannot overflow (2^64 * 2^31 < 2^128).
+template <typename T, int VE, int NT, class N>
+__device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
+  float a0 = 0.f, a1 = 0.f;
+  auto sum_exp = [&](float nm) {
+    a0 = 0.f;
+    a1 = 0.f;
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) {
+      if (u < int(n)) {
+        float x[VE];
+        unpack_raw<T, VE>(cell[u * NT], x);
+#pragma unroll
+        for (int j = 0; j < VE; j += 2) {
+          a0 += ex2(fmaf(x[j], kLog2e, nm));
+          a1 += ex2(fmaf(x[j + 1], kLog2e, nm));
+        }
+      }
+    }
+  };
+  sum_exp(-st.m2);
+  if (!(a0 + a1 < 0x1p64f)) {
+    float vm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) {
+      if (u < int(n)) {
+        float x[VE];
+        unpack_raw<T, VE>(cell[u * NT], x);
+        vm = fmaxf(vm, vec_max(x));
+      }
+    }
+    const float m2n = vm * kLog2e;
+    if (m2n > st.m2) {
+      const float sc = ex2(st.m2 - m2n);
+      st.s.x *= sc;
+      st.s.y *= sc;
+      st.m2 = m2n;
+    }
+    if (st.m2 == -INFINITY) {  // every value so far is -inf: nothing to add
+      a0 = 0.f;
+      a1 = 0.f;
+    } else {
+      sum_exp(-st.m2);
+    }
+  }
+  st.s.x += a0;
+  st.s.y += a1;
 }
 
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
@@ -352,14 +416,9 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
     consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
-                                  [&](const uint4* cs, const uint4* ct, int) {
-                                    float x[VE];
-                                    unpack_raw<T, VE>(*cs, x);
-                                    lse2x_update(a, x);
-                                    if constexpr (kTvd) {
-                                      unpack_raw<T, VE>(*ct, x);
-                                      lse2x_update(b, x);
-                                    }
+                                  [&](const uint4* cell, auto n, int) {
+                                    lse_step<T, VE, NT>(a, cell, n);
+                                    if constexpr (kTvd) lse_step<T, VE, NT>(b, cell + kPerStep * NT, n);
                                   });
     Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
     if (owns_tail && tail0 + tid < p.V) {
@@ -390,24 +449,33 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       const float ns2 = -(lse_s * kLog2e);
       const float nt2 = -(lse_t * kLog2e);
 
-      // ---- step 2: split sums of (p, q) by the sign of p - q
-      float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
+      // ---- step 2: sigma = sum p*sign(p - q) and tau = sum q*sign(p - q);
+      // sum |p - q| = sigma - tau.  Ties have sign 0 and add nothing.
+      float sig_p = 0.f, sig_q = 0.f;
+      auto tvd_pair = [&](float xs, float xt) {
+        const float pp = ex2(fmaf(xs, kLog2e, ns2));
+        const float qq = ex2(fmaf(xt, kLog2e, nt2));
+        const float sg = sgn_pq(pp, qq);
+        sig_p = fmaf(pp, sg, sig_p);
+        sig_q = fmaf(qq, sg, sig_q);
+      };
       consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
-                                    [&](const uint4* cs, const uint4* ct, int) {
-                                      float xs[VE], xt[VE];
-                                      unpack_raw<T, VE>(*cs, xs);
-                                      unpack_raw<T, VE>(*ct, xt);
+                                    [&](const uint4* cell, auto n, int) {
 #pragma unroll
-                                      for (int j = 0; j < VE; ++j)
-                                        tvd_split(ex2(fmaf(xs[j], kLog2e, ns2)),
-                                                  ex2(fmaf(xt[j], kLog2e, nt2)), pos, neg);
+                                      for (int u = 0; u < kPerStep; ++u) {
+                                        if (u < int(n)) {
+                                          float xs[VE], xt[VE];
+                                          unpack_raw<T, VE>(cell[u * NT], xs);
+                                          unpack_raw<T, VE>(cell[(kPerStep + u) * NT], xt);
+#pragma unroll
+                                          for (int j = 0; j < VE; ++j) tvd_pair(xs[j], xt[j]);
+                                        }
+                                      }
                                     });
-      if (owns_tail && tail0 + tid < p.V) {
-        tvd_accum1(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid), ns2,
-                   nt2, pos, neg);
-      }
-      float abs_sum = (pos.x - pos.y) + (neg.y - neg.x);
-      float sig = pos.x - neg.x;
+      if (owns_tail && tail0 + tid < p.V)
+        tvd_pair(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid));
+      float abs_sum = sig_p - sig_q;
+      float sig = sig_p;
       block_sum2<NT>(abs_sum, sig, red_sum);
       if constexpr (kGrad) {
         cluster_sum2_all<C>(abs_sum, sig, &part_sum);
@@ -421,9 +489,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         // backward kernel: grad = p * c(sign) - grad_ce * [v == target].
         const float gce = p.grad_ce[row * p.grad_stride];
         const float h = 0.5f * p.grad_tvd[row * p.grad_stride];
-        const float c_pos = gce + h * (1.f - sig);
-        const float c_neg = gce + h * (-1.f - sig);
-        const float c_zero = gce - h * sig;
+        const float c0 = gce - h * sig;  // coefficient of p: c0 + h * sign
         const bool bad = (tg < 0 || tg >= p.V);
         T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
         T* gmine = grow + (vb + tid) * VE;
@@ -431,30 +497,34 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         const int64_t tg_rel = tg - (vb + tid) * VE;
         auto grad_of = [&](float xs, float xt) {
           const float pp = ex2(fmaf(xs, kLog2e, ns2));
-          const float qq = ex2(fmaf(xt, kLog2e, nt2));
-          const float c = (pp > qq) ? c_pos : ((pp < qq) ? c_neg : c_zero);
-          return pp * c;
+          return pp * fmaf(h, sgn_pq(pp, ex2(fmaf(xt, kLog2e, nt2))), c0);
         };
-        consume_pass<NT, F::kTensors>(
-            f, slot, p, n_clusters, mine, n_full, rem,
-            [&](const uint4* cs, const uint4* ct, int k) {
-              float xs[VE], xt[VE], g[VE];
-              unpack_raw<T, VE>(*cs, xs);
-              unpack_raw<T, VE>(*ct, xt);
+        auto grad_vec = [&](const uint4 ws, const uint4 wt, int k) {
+          float xs[VE], xt[VE], g[VE];
+          unpack_raw<T, VE>(ws, xs);
+          unpack_raw<T, VE>(wt, xt);
 #pragma unroll
-              for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
-              const int64_t off = tg_rel - int64_t(k) * NT * VE;
-              if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+          for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+          const int64_t off = tg_rel - int64_t(k) * NT * VE;
+          if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
 #pragma unroll
-                for (int j = 0; j < VE; ++j)
-                  if (j == off) g[j] -= gce;
-              }
-              if (bad) {
+            for (int j = 0; j < VE; ++j)
+              if (j == off) g[j] -= gce;
+          }
+          if (bad) {
 #pragma unroll
-                for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
-              }
-              store_vec<T, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
-            });
+            for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
+          }
+          store_vec<T, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
+        };
+        consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
+                                      [&](const uint4* cell, auto n, int k0) {
+#pragma unroll
+                                        for (int u = 0; u < kPerStep; ++u)
+                                          if (u < int(n))
+                                            grad_vec(cell[u * NT], cell[(kPerStep + u) * NT],
+                                                     k0 + u);
+                                      });
         if (owns_tail && tail0 + tid < p.V) {
           const int64_t v = tail0 + tid;
           float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
@@ -527,11 +597,11 @@ __global__ void __launch_bounds__(kScalarThreads, 1) forward_scalar(FwdArgs p) {
       const float lse_t = lse2_finish(b);
       const float ns2 = -(lse_s * kLog2e);
       const float nt2 = -(lse_t * kLog2e);
-      float2 pos = make_float2(0.f, 0.f), neg = make_float2(0.f, 0.f);
+      float sig_p = 0.f, sig_q = 0.f;
       for (int64_t v = vb + threadIdx.x; v < ve; v += NT)
-        tvd_accum1(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v), ns2, nt2, pos, neg);
-      float abs_sum = (pos.x - pos.y) + (neg.y - neg.x);
-      float sig = pos.x - neg.x;
+        tvd_accum1(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v), ns2, nt2, sig_p, sig_q);
+      float abs_sum = sig_p - sig_q;  // sum |p - q| = sum (p - q) * sign(p - q)
+      float sig = sig_p;
       block_sum2<NT>(abs_sum, sig, red_sum);
       cluster_sum2<C>(abs_sum, sig, &part_sum, rank);
       if (rank == 0 && threadIdx.x == 0) {

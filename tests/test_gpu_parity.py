@@ -400,3 +400,18 @@ def test_mean_front_end_all_ignored():
     loss = binding.fused_ce_tvd_mean_loss(z, z, tg)
     torch.cuda.synchronize()
     assert n.item() == 0 and gce.item() == 0 and gtvd.item() == 0 and loss.item() == 0
+
+
+def test_from_host_streaming_equals_device_call():
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=70, V=32000, seed=51)
+    f1, g1, _ = run_single(w)
+    hs, ht = w.student.cpu().pin_memory(), w.teacher.cpu().pin_memory()
+    htg = w.target.cpu().pin_memory()
+    ds, dt = torch.empty_like(w.student), torch.empty_like(w.teacher)
+    dtg = torch.empty_like(w.target)
+    out = binding.fused_ce_tvd_forward_backward_from_host(
+        hs, ht, htg, w.grad_ce, w.grad_tvd, ds, dt, dtg, w.ignore_index, block_rows=16)
+    torch.cuda.synchronize()
+    for k, v in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), out[:5]):
+        assert torch.equal(f1[k], v), k
+    assert torch.equal(g1, out[5])
