@@ -374,7 +374,9 @@ def test_mean_front_end_and_autograd_loss():
     torch.cuda.synchronize()
     n_kept = int((w.target != w.ignore_index).sum().item())
     assert st == 0 and int(n.item()) == n_kept
-    assert abs(gce.item() - alpha / n_kept) < 1e-9 and abs(gtvd.item() - beta / n_kept) < 1e-9
+    # fp32 results of alpha/n and beta/n: exact to one rounding
+    assert abs(gce.item() - alpha / n_kept) <= 1e-7 * alpha / n_kept
+    assert abs(gtvd.item() - beta / n_kept) <= 1e-7 * beta / n_kept
     ref = oracle.mean_loss(fwd["ce"].cpu().numpy(), fwd["tvd"].cpu().numpy(),
                            w.target.cpu().numpy(), w.ignore_index, alpha, beta)
     assert abs(loss.item() - ref[0]) < 1e-6
