@@ -183,7 +183,7 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 // cluster (rows cluster_id, cluster_id + n_clusters, ...), step 1's n_my
 // vectors, then (fused loss only) step 2's n_my vectors, two vectors
 // (NT vectors apart) per step.  Both the feed and the consumer walk this
-// same sequence; the feed runs kStages steps ahead.
+// same sequence; the feed runs kStages - 1 steps ahead of the step being read.
 
 constexpr int kPerStep = 4;  // vectors per tensor moved by one step
 
@@ -192,7 +192,7 @@ template <int N>
 struct Count {
   __device__ __forceinline__ constexpr operator int() const { return N; }
 };
-constexpr int kStages = 2;   // steps in flight per thread
+constexpr int kStages = 3;   // ring slots per thread: two steps in flight while one is read
 
 // The feed: this thread's cursor in the sequence, issuing one step of
 // cp.async copies per call.  A pass of a row is n_full full steps of
@@ -281,13 +281,13 @@ __device__ __forceinline__ void consume_pass(FeedT& f, int& slot, const FwdArgs&
     cp_async_wait<kStages - 1>();
     fn(mine + slot * kSlotVecs, Count<kPerStep>{}, q * kPerStep);
     f.feed(p, slot, n_clusters);
-    slot ^= 1;
+    slot = (slot + 1 == kStages) ? 0 : slot + 1;
   }
   if (rem) {
     cp_async_wait<kStages - 1>();
     fn(mine + slot * kSlotVecs, rem, n_full * kPerStep);
     f.feed(p, slot, n_clusters);
-    slot ^= 1;
+    slot = (slot + 1 == kStages) ? 0 : slot + 1;
   }
 }
 
@@ -348,7 +348,6 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
-  static_assert(kStages == 2, "the slot index toggles");
   using F = Feed<T, VE, kTvd, kGrad, NT>;
   extern __shared__ __align__(16) uint4 ring_mem[];
   __shared__ float4 red_lse[kMaxWarps];
