@@ -299,10 +299,12 @@ __device__ __forceinline__ void consume_pass(FeedT& f, int& slot, const FwdArgs&
 // stay exact in fp32 and the sums cannot overflow (2^64 * 2^31 < 2^128).
 template <typename T, int VE, int NT, class N>
 __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
-  float a0 = 0.f, a1 = 0.f;
+  // two accumulation chains, advanced together by packed (f32x2) adds; the
+  // exponent arguments of neighbouring elements by packed FMAs
+  float2 acc = make_float2(0.f, 0.f);
   auto sum_exp = [&](float nm) {
-    a0 = 0.f;
-    a1 = 0.f;
+    acc = make_float2(0.f, 0.f);
+    const float2 L2 = make_float2(kLog2e, kLog2e), nm2 = make_float2(nm, nm);
 #pragma unroll
     for (int u = 0; u < kPerStep; ++u) {
       if (u < int(n)) {
@@ -310,14 +312,14 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
         unpack_raw<T, VE>(cell[u * NT], x);
 #pragma unroll
         for (int j = 0; j < VE; j += 2) {
-          a0 += ex2(fmaf(x[j], kLog2e, nm));
-          a1 += ex2(fmaf(x[j + 1], kLog2e, nm));
+          const float2 e = __ffma2_rn(make_float2(x[j], x[j + 1]), L2, nm2);
+          acc = __fadd2_rn(acc, make_float2(ex2(e.x), ex2(e.y)));
         }
       }
     }
   };
   sum_exp(-st.m2);
-  if (!(a0 + a1 < 0x1p64f)) {
+  if (!(acc.x + acc.y < 0x1p64f)) {
     float vm = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kPerStep; ++u) {
@@ -335,14 +337,12 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
       st.m2 = m2n;
     }
     if (st.m2 == -INFINITY) {  // every value so far is -inf: nothing to add
-      a0 = 0.f;
-      a1 = 0.f;
+      acc = make_float2(0.f, 0.f);
     } else {
       sum_exp(-st.m2);
     }
   }
-  st.s.x += a0;
-  st.s.y += a1;
+  st.s = __fadd2_rn(st.s, acc);
 }
 
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
@@ -451,9 +451,13 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       // ---- step 2: sigma = sum p*sign(p - q) and tau = sum q*sign(p - q);
       // sum |p - q| = sigma - tau.  Ties have sign 0 and add nothing.
       float sig_p = 0.f, sig_q = 0.f;
+      const float2 L2 = make_float2(kLog2e, kLog2e), nst = make_float2(ns2, nt2);
       auto tvd_pair = [&](float xs, float xt) {
-        const float pp = ex2(fmaf(xs, kLog2e, ns2));
-        const float qq = ex2(fmaf(xt, kLog2e, nt2));
+        // the student and teacher exponents of one element in one packed FMA
+        // (each lane rounds exactly like the scalar fmaf of the backward)
+        const float2 e = __ffma2_rn(make_float2(xs, xt), L2, nst);
+        const float pp = ex2(e.x);
+        const float qq = ex2(e.y);
         const float sg = sgn_pq(pp, qq);
         sig_p = fmaf(pp, sg, sig_p);
         sig_q = fmaf(qq, sg, sig_q);
@@ -495,8 +499,9 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         // element offset of the target from this thread's first element
         const int64_t tg_rel = tg - (vb + tid) * VE;
         auto grad_of = [&](float xs, float xt) {
-          const float pp = ex2(fmaf(xs, kLog2e, ns2));
-          return pp * fmaf(h, sgn_pq(pp, ex2(fmaf(xt, kLog2e, nt2))), c0);
+          const float2 e = __ffma2_rn(make_float2(xs, xt), L2, nst);
+          const float pp = ex2(e.x);
+          return pp * fmaf(h, sgn_pq(pp, ex2(e.y)), c0);
         };
         auto grad_vec = [&](const uint4 ws, const uint4 wt, int k) {
           float xs[VE], xt[VE], g[VE];
