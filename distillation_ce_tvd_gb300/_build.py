@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfused_ce_tvd.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu"]
+SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu", "fct_linear.cu"]
 HEADERS = ["fct_common.cuh", "fct_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -69,7 +69,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas",
            "-Xlinker", f"-rpath,{libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

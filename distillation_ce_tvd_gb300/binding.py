@@ -24,6 +24,7 @@ _lib = None
 
 EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
            "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
+           "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fct_status_string", "fct_set_forward_cluster", "fct_version")
 
 
@@ -53,6 +54,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
         dbl = ctypes.c_double
+        lib.fused_linear_ce_tvd_workspace_size.argtypes = [i64, i64]
+        lib.fused_linear_ce_tvd_workspace_size.restype = ctypes.c_size_t
+        lib.fused_linear_ce_tvd_forward_backward.argtypes = [
+            vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
+            vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, ctypes.c_size_t, i64, vp, vp]
+        lib.fused_linear_ce_tvd_forward_backward.restype = i32
         lib.fused_ce_tvd_mean_upstream.argtypes = [vp, i64, i64, dbl, dbl, vp, vp, vp, vp]
         lib.fused_ce_tvd_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp]
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
@@ -354,3 +361,62 @@ def fused_ce_tvd_forward_backward_from_host(student_h, teacher_h, target_h, grad
     for cs in copiers:  # the caller's stream owns the buffers again afterwards
         main.wait_stream(cs)
     return (*outs, grad_student)
+
+
+def fused_linear_ce_tvd_workspace_size(V: int, chunk_rows: int) -> int:
+    """Bytes of device workspace fused_linear_ce_tvd_forward_backward needs."""
+    return int(load().fused_linear_ce_tvd_workspace_size(int(V), int(chunk_rows)))
+
+
+def _mat(x, name):
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise ValueError(f"{name} must be a 2-D bf16 CUDA tensor with unit stride along columns")
+    return max(int(x.stride(0)) if x.shape[0] > 1 else int(x.shape[1]), int(x.shape[1]))
+
+
+def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teacher, target,
+                                         grad_ce, grad_tvd, ignore_index=IGNORE_INDEX, *,
+                                         chunk_rows=1024, workspace=None, grad_h=None,
+                                         grad_w=None, want_grad_h=True, want_grad_w=True,
+                                         dev_status=None, stream=None):
+    """Loss from hidden states and lm_head weights, in row blocks (no (BT, V) logits).
+
+    Returns (ce, tvd, student_lse, teacher_lse, sigma, grad_h, grad_w): grad_h
+    is d loss / d h_student (bf16), grad_w is d loss / d w_student (fp32,
+    accumulated into when passed in; zero-initialised otherwise).
+    """
+    ld_hs, ld_ws = _mat(h_student, "h_student"), _mat(w_student, "w_student")
+    ld_ht, ld_wt = _mat(h_teacher, "h_teacher"), _mat(w_teacher, "w_teacher")
+    BT, ds = h_student.shape
+    V = w_student.shape[0]
+    dt = h_teacher.shape[1]
+    if w_student.shape[1] != ds or w_teacher.shape != (V, dt) or h_teacher.shape[0] != BT:
+        raise ValueError("inconsistent hidden / weight shapes")
+    dev = h_student.device
+    _rows(target, BT, "target", torch.int64)
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    stride = max(stride_ce, stride_tvd)
+    outs = [torch.empty(BT, device=dev, dtype=torch.float32) for _ in range(5)]
+    rows = max(1, min(int(chunk_rows), BT))
+    need = fused_linear_ce_tvd_workspace_size(V, rows)
+    if workspace is None:
+        workspace = torch.empty(need, device=dev, dtype=torch.uint8)
+    if want_grad_h and grad_h is None:
+        grad_h = torch.empty_like(h_student)
+    if want_grad_w and grad_w is None:
+        grad_w = torch.zeros(V, ds, device=dev, dtype=torch.float32)
+    ld_gh = _mat(grad_h, "grad_h") if grad_h is not None else ds
+    if grad_w is not None and (grad_w.dtype != torch.float32 or grad_w.shape != (V, ds)):
+        raise ValueError("grad_w must be (V, d_student) float32")
+    ld_gw = int(grad_w.stride(0)) if grad_w is not None else ds
+    rc = load().fused_linear_ce_tvd_forward_backward(
+        _ptr(h_student), ld_hs, _ptr(w_student), ld_ws, ds, _ptr(h_teacher), ld_ht,
+        _ptr(w_teacher), ld_wt, dt, _ptr(target), BT, V, int(ignore_index), _ptr(gce),
+        _ptr(gtvd), stride, *map(_ptr, outs), _ptr(grad_h), ld_gh, _ptr(grad_w), ld_gw,
+        _ptr(workspace), workspace.numel() * workspace.element_size(), rows,
+        _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_linear_ce_tvd_forward_backward")
+    return (*outs, grad_h, grad_w)

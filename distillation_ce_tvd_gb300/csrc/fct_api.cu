@@ -271,9 +271,93 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
   return FCT_OK;
 }
 
+int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, int64_t d_s,
+                const void* h_t, int64_t ld_ht, const void* w_t, int64_t ld_wt, int64_t d_t,
+                const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
+                const float* grad_ce, const float* grad_tvd, int64_t grad_stride, float* ce,
+                float* tvd, float* lse_s, float* lse_t, float* sigma, void* grad_h_s,
+                int64_t ld_ghs, float* grad_w_s, int64_t ld_gws, void* workspace,
+                size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status, void* stream) {
+  if (BT < 0 || V <= 0 || d_s <= 0 || d_t <= 0 || chunk_rows <= 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  const int64_t kInt = 2147483647;  // cuBLAS takes int sizes and strides
+  if (V > kInt || d_s > kInt || d_t > kInt || ld_hs > kInt || ld_ws > kInt || ld_ht > kInt ||
+      ld_wt > kInt || ld_ghs > kInt || ld_gws > kInt || chunk_rows > kInt)
+    return FCT_ERR_UNSUPPORTED;
+  if (!h_s || !w_s || !h_t || !w_t || !target || !grad_ce || !grad_tvd || !workspace)
+    return FCT_ERR_INVALID_ARG;
+  if (ld_hs < d_s || ld_ws < d_s || ld_ht < d_t || ld_wt < d_t) return FCT_ERR_INVALID_ARG;
+  if (grad_h_s && ld_ghs < d_s) return FCT_ERR_INVALID_ARG;
+  if (grad_w_s && ld_gws < d_s) return FCT_ERR_INVALID_ARG;
+  if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
+  const void* bf[6] = {h_s, w_s, h_t, w_t, grad_h_s, nullptr};
+  for (const void* q : bf)
+    if (q && !aligned(q, 2)) return FCT_ERR_ALIGNMENT;
+  if (!aligned(target, 8) || !aligned(grad_ce, 4) || !aligned(grad_tvd, 4) ||
+      (grad_w_s && !aligned(grad_w_s, 4)) || !aligned(workspace, 256) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return FCT_ERR_ALIGNMENT;
+  float* outs[5] = {ce, tvd, lse_s, lse_t, sigma};
+  for (int i = 0; i < 5; ++i) {
+    if (outs[i] == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(outs[i], 4)) return FCT_ERR_ALIGNMENT;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(vec_range(outs[i], BT, 4), vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
+  }
+  const int64_t rows = chunk_rows < BT ? chunk_rows : BT;
+  if (workspace_bytes < fct::linear_workspace_bytes(V, rows)) return FCT_ERR_INVALID_ARG;
+  // outputs must not overlap the inputs or the workspace
+  const Range ins[5] = {mat_range(h_s, BT, ld_hs, d_s, 2), mat_range(w_s, V, ld_ws, d_s, 2),
+                        mat_range(h_t, BT, ld_ht, d_t, 2), mat_range(w_t, V, ld_wt, d_t, 2),
+                        vec_range(workspace, static_cast<int64_t>(workspace_bytes), 1)};
+  Range outr[7];
+  int n_out = 0;
+  for (int i = 0; i < 5; ++i) outr[n_out++] = vec_range(outs[i], BT, 4);
+  if (grad_h_s) outr[n_out++] = mat_range(grad_h_s, BT, ld_ghs, d_s, 2);
+  if (grad_w_s) outr[n_out++] = mat_range(grad_w_s, V, ld_gws, d_s, 4);
+  for (int i = 0; i < n_out; ++i)
+    for (int j = 0; j < 5; ++j)
+      if (overlap(outr[i], ins[j])) return FCT_ERR_INVALID_ARG;
+  if (grad_h_s && grad_w_s && overlap(outr[5], outr[6])) return FCT_ERR_INVALID_ARG;
+
+  DeviceInfo d;
+  int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  fct::LinArgs a{h_s, ld_hs, w_s, ld_ws, d_s, h_t, ld_ht, w_t, ld_wt, d_t, target, BT, V,
+                 ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd, lse_s, lse_t, sigma,
+                 grad_h_s, ld_ghs, grad_w_s, ld_gws, workspace, chunk_rows, dev_status};
+  const fct::FwdPlan plan = plan_forward(d, V, FCT_F32, true, true);
+  if (fct::launch_linear(a, plan, dev, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows) {
+  if (V <= 0 || chunk_rows <= 0) return 0;
+  return fct::linear_workspace_bytes(V, chunk_rows);
+}
+
+int fused_linear_ce_tvd_forward_backward(
+    const void* h_student, int64_t ld_h_student, const void* w_student, int64_t ld_w_student,
+    int64_t d_student, const void* h_teacher, int64_t ld_h_teacher, const void* w_teacher,
+    int64_t ld_w_teacher, int64_t d_teacher, const int64_t* target, int64_t BT, int64_t V,
+    int64_t ignore_index, const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
+    float* ce, float* tvd, float* student_lse, float* teacher_lse, float* sigma,
+    void* grad_h_student, int64_t ld_grad_h, float* grad_w_student, int64_t ld_grad_w,
+    void* workspace, size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status,
+    void* stream) {
+  return linear_impl(h_student, ld_h_student, w_student, ld_w_student, d_student, h_teacher,
+                     ld_h_teacher, w_teacher, ld_w_teacher, d_teacher, target, BT, V,
+                     ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd, student_lse,
+                     teacher_lse, sigma, grad_h_student, ld_grad_h, grad_w_student, ld_grad_w,
+                     workspace, workspace_bytes, chunk_rows, dev_status, stream);
+}
 
 int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student, const void* teacher,
                                   int64_t ld_teacher, fct_dtype dtype, const int64_t* target,

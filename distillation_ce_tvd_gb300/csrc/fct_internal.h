@@ -67,6 +67,40 @@ struct LossArgs {
   int64_t* count;
 };
 
+// Fused-linear (hidden states and lm_head weights in, bf16) chunked loss.
+struct LinArgs {
+  const void* h_s;  // (BT, d_s) bf16
+  int64_t ld_hs;
+  const void* w_s;  // (V, d_s) bf16
+  int64_t ld_ws, d_s;
+  const void* h_t;  // (BT, d_t) bf16
+  int64_t ld_ht;
+  const void* w_t;  // (V, d_t) bf16
+  int64_t ld_wt, d_t;
+  const int64_t* target;
+  int64_t BT, V, ignore_index;
+  const float* grad_ce;
+  const float* grad_tvd;
+  int64_t grad_stride;
+  float* ce;
+  float* tvd;
+  float* lse_s;
+  float* lse_t;
+  float* sigma;
+  void* grad_h_s;   // (BT, d_s) bf16, or nullptr
+  int64_t ld_ghs;
+  float* grad_w_s;  // (V, d_s) fp32, accumulated, or nullptr
+  int64_t ld_gws;
+  void* workspace;  // linear_workspace_bytes(V, chunk_rows), 256-byte aligned
+  int64_t chunk_rows;
+  int32_t* dev_status;
+};
+
+int64_t linear_logits_ld(int64_t V);
+size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows);
+cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,
+                          cudaStream_t st);
+
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st);

@@ -18,7 +18,8 @@
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - All array arguments are DEVICE pointers, owned by the caller.  The
- *    library allocates nothing and keeps no state between calls.
+ *    library allocates no device memory and keeps no state between calls
+ *    (the fused-linear entry point below keeps one cuBLAS handle per device).
  *  - Logit matrices are row-major (BT, V) with a row stride `ld` (in
  *    elements, ld >= V).  Student and teacher share one element type.
  *  - `target` is int64 (BT,).  A row whose target equals `ignore_index`
@@ -44,6 +45,7 @@
 #ifndef FUSED_CE_TVD_H_
 #define FUSED_CE_TVD_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -136,6 +138,46 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
                                   float* sigma, void* grad_student,
                                   int64_t ld_grad, int32_t* dev_status,
                                   void* stream);
+
+/*
+ * Fused-linear CE + TVD: the loss from hidden states and lm_head weights,
+ * without ever holding the (BT, V) logits.  Rows go through in blocks of
+ * chunk_rows: per block, cuBLAS GEMMs (bf16 in, fp32 accumulate) write the
+ * block's student and teacher logits (fp32) into `workspace`, the
+ * single-launch forward + backward of the PR #1384 analysis's loss runs on
+ * them, its logit gradient is rounded to bf16, and two more GEMMs give
+ * d loss / d h_student for the block and accumulate d loss / d w_student.
+ * (Computing logits in row blocks is the chunking that the Liger-Kernel
+ * overview page describes for its fused linear cross-entropy; applying it to
+ * CE + TVD is this library's addition.)  The teacher is frozen.
+ *
+ *   h_student (BT, d_student), w_student (V, d_student),
+ *   h_teacher (BT, d_teacher), w_teacher (V, d_teacher): bf16, row strides ld_*.
+ *   target, grad_ce, grad_tvd, grad_stride, ce ... sigma: as for
+ *                    fused_ce_tvd_forward_backward.
+ *   grad_h_student : (BT, d_student) bf16 output, or NULL.
+ *   grad_w_student : (V, d_student) fp32, ACCUMULATED into (+=), or NULL.
+ *   workspace      : device memory of fused_linear_ce_tvd_workspace_size(V,
+ *                    chunk_rows) bytes, 256-byte aligned; clobbered.
+ *
+ * The logits the loss sees are fp32 (bf16 products, fp32 sums); the logit
+ * gradient is rounded to bf16 before the two gradient GEMMs.  The library
+ * keeps one cuBLAS handle per device (created on first use); calls on one
+ * device are serialised by a lock.
+ */
+size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows);
+
+int fused_linear_ce_tvd_forward_backward(
+    const void* h_student, int64_t ld_h_student, const void* w_student,
+    int64_t ld_w_student, int64_t d_student, const void* h_teacher,
+    int64_t ld_h_teacher, const void* w_teacher, int64_t ld_w_teacher,
+    int64_t d_teacher, const int64_t* target, int64_t BT, int64_t V,
+    int64_t ignore_index, const float* grad_ce, const float* grad_tvd,
+    int64_t grad_stride, float* ce, float* tvd, float* student_lse,
+    float* teacher_lse, float* sigma, void* grad_h_student, int64_t ld_grad_h,
+    float* grad_w_student, int64_t ld_grad_w, void* workspace,
+    size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status,
+    void* stream);
 
 /*
  * Cross-entropy alone: the CE half of "Forward Pass" (one log-sum-exp pass,

@@ -417,3 +417,73 @@ def test_from_host_streaming_equals_device_call():
     for k, v in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), out[:5]):
         assert torch.equal(f1[k], v), k
     assert torch.equal(g1, out[5])
+
+
+
+# ------------------------------------------------------------------ fused linear (chunked)
+
+def _linear_case(BT, ds, dt, V, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    hs = torch.randn(BT, ds, generator=g, device=DEV).bfloat16()
+    ht = torch.randn(BT, dt, generator=g, device=DEV).bfloat16()
+    ws = (torch.randn(V, ds, generator=g, device=DEV) * (2.0 / ds ** 0.5)).bfloat16()
+    wt = (torch.randn(V, dt, generator=g, device=DEV) * (2.0 / dt ** 0.5)).bfloat16()
+    tg = torch.randint(0, V, (BT,), generator=g, device=DEV)
+    tg[::7] = -100
+    return hs, ws, ht, wt, tg
+
+
+@pytest.mark.parametrize("BT,ds,dt,V,chunk", [(50, 128, 96, 1003, 16), (64, 256, 256, 4096, 64),
+                                              (33, 64, 128, 2048, 100)])
+def test_fused_linear_against_fp64(BT, ds, dt, V, chunk):
+    hs, ws, ht, wt, tg = _linear_case(BT, ds, dt, V, seed=BT + V)
+    gce = torch.full((BT,), 1.0 / BT, device=DEV)
+    gtvd = torch.full((BT,), 0.7 / BT, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ce, tvd, ls, lt, sg, gh, gw = binding.fused_linear_ce_tvd_forward_backward(
+        hs, ws, ht, wt, tg, gce, gtvd, chunk_rows=chunk, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    # fp64 reference: library matmuls for the logits, the oracle for the loss
+    Hs, Ws, Ht, Wt = (x.cpu().double() for x in (hs, ws, ht, wt))
+    Ls, Lt = Hs @ Ws.T, Ht @ Wt.T
+    tgc = tg.cpu().numpy()
+    ref = oracle.fused_ce_tvd_forward(Ls, Lt, tgc)
+    G, _ = oracle.fused_ce_tvd_backward(Ls, Lt, tgc, gce.cpu().numpy(), gtvd.cpu().numpy())
+    masks, mass, probs = tie_info(Ls, Lt)
+    got = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
+    # The GPU's logits are fp32 sums of D exact bf16 products: each is off by
+    # at most D * 2^-24 * sum_k |h_k w_vk|; every per-row output moves by at
+    # most twice the largest logit error on top of the fp32 tolerance.
+    bound = np.maximum((np.abs(Hs.numpy()) @ np.abs(Ws.numpy()).T).max(1) * ds,
+                       (np.abs(Ht.numpy()) @ np.abs(Wt.numpy()).T).max(1) * dt) * 2.0 ** -24
+    check_forward(torch.float32, tgc, {k: v.cpu().numpy() for k, v in got.items()}, ref, mass,
+                  what="linear ", atol=1e-5 + 2.0 * bound)
+    # gradient bounds: the logit gradient is rounded to bf16 (2^-8 relative) on
+    # top of its own tolerance (2e-3 relative, 1e-6 absolute), the GEMM sums in
+    # fp32, and grad_h is itself rounded to bf16
+    G_abs = np.abs(G)
+    e_rel = 2.0 ** -8 + 2e-3 + V * 2.0 ** -24
+    ref_gh = G @ Ws.numpy()
+    tol_gh = e_rel * (G_abs @ np.abs(Ws.numpy())) + 1e-6 * np.abs(Ws.numpy()).sum(0) \
+        + 2.0 ** -8 * np.abs(ref_gh) + 1e-9
+    err_gh = np.abs(gh.cpu().double().numpy() - ref_gh)
+    assert np.all(err_gh <= tol_gh), float((err_gh / tol_gh).max())
+    ref_gw = G.T @ Hs.numpy()
+    e_rel_w = 2.0 ** -8 + 2e-3 + BT * 2.0 ** -24
+    tol_gw = e_rel_w * (G_abs.T @ np.abs(Hs.numpy())) + 1e-6 * np.abs(Hs.numpy()).sum(0) + 1e-9
+    err_gw = np.abs(gw.cpu().double().numpy() - ref_gw)
+    assert np.all(err_gw <= tol_gw), float((err_gw / tol_gw).max())
+
+
+def test_fused_linear_chunking_is_invisible():
+    hs, ws, ht, wt, tg = _linear_case(70, 128, 128, 3000, seed=5)
+    a = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, 0.01, 0.02, chunk_rows=70)
+    b = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, 0.01, 0.02, chunk_rows=9)
+    torch.cuda.synchronize()
+    # The GEMMs may pick other algorithms (summation orders) for other block
+    # sizes, so results agree to fp32 rounding rather than bit for bit.
+    for x, y in zip(a[:5], b[:5]):
+        assert torch.allclose(x, y, rtol=0, atol=2e-5)
+    assert torch.allclose(a[5].float(), b[5].float(), rtol=2 ** -7, atol=1e-7)
+    assert torch.allclose(a[6], b[6], rtol=1e-3, atol=1e-7)
