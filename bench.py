@@ -206,6 +206,69 @@ def run_reference(args, world, rank):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------- fused linear
+
+def run_linear(args, world, rank, local):
+    """Fused-linear CE + TVD: hidden states and lm_head weights in, the loss and
+    the student's hidden and weight gradients out, logits only in row blocks.
+    Dominated by four GEMMs per block (tensor cores, cuBLAS)."""
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    binding.load()
+    w = workloads.make_linear(args.workload, dev, rows=args.rows)
+    BT, ds = w.h_student.shape
+    V, dt = w.w_teacher.shape
+    rows = min(args.chunk_rows, BT)
+    ws_bytes = binding.fused_linear_ce_tvd_workspace_size(V, rows)
+    workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
+    grad_h = torch.empty_like(w.h_student)
+    grad_w = torch.zeros(V, ds, device=dev, dtype=torch.float32)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        binding.fused_linear_ce_tvd_forward_backward(
+            w.h_student, w.w_student, w.h_teacher, w.w_teacher, w.target, w.grad_ce, w.grad_tvd,
+            w.ignore_index, chunk_rows=rows, workspace=workspace, grad_h=grad_h, grad_w=grad_w,
+            stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    clocks = ClockSampler(local) if not args.no_clocks else None
+    if clocks:
+        clocks.__enter__()
+    barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    if clocks:
+        clocks.__exit__(None, None, None)
+    ms = sharding.max_over_ranks(a.elapsed_time(b) / K, world, dev)
+    flops = 2.0 * BT * V * (ds + dt) + 2.0 * 2.0 * BT * V * ds  # logits of both; d hidden, d weight
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = json.load(open(peaks_path))["bf16_tflops_sustained"] if os.path.exists(peaks_path) else 1700.0
+    tflops = flops / (ms * 1e-3) / 1e12
+    if rank == 0:
+        print(json.dumps({
+            "metric": "fused-linear CE+TVD fwd+bwd tokens/s (GEMM-bound), 1 GB300",
+            "value": world * BT / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": args.workload, "BT": BT, "V": V, "d_student": ds,
+                       "d_teacher": dt, "chunk_rows": rows, "workspace_bytes": ws_bytes},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
+                         "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
+                         "peak_source": "measured cuBLAS bf16, sustained"},
+            "gpu_launches": None,
+            "clocks": clocks.summary() if clocks else None,
+        }))
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -214,7 +277,9 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(workloads.WORKLOADS) + sorted(workloads.LINEAR_WORKLOADS))
+    ap.add_argument("--chunk-rows", type=int, default=1024, help="row block of the fused-linear path")
     ap.add_argument("--rows", type=int, default=None, help="override BT (profiling)")
     ap.add_argument("--path", default="single", choices=["single", "two"],
                     help="headline step: one fused forward+backward launch, or the forward "
@@ -235,6 +300,9 @@ def main():
     world, rank, local = dist_setup()
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.workload in workloads.LINEAR_WORKLOADS:
+        run_linear(args, world, rank, local)
+        return
 
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)

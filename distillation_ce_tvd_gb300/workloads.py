@@ -195,3 +195,39 @@ def make(name: str, device="cpu", rows: int | None = None, V: int | None = None,
         s, t, target, gce, gtvd = _RECIPES[name](BT, V, dtype, _gen(dev, seed), dev)
     return Workload(name, s.contiguous(), t.contiguous(), target.contiguous(),
                     gce.float().contiguous(), gtvd.float().contiguous())
+
+
+LINEAR_WORKLOADS = {
+    "linear_bt8192_d4096_v151936_bf16": dict(BT=8192, ds=4096, dt=4096, V=151936, seed=5),
+}
+
+
+@dataclasses.dataclass
+class LinearWorkload:
+    name: str
+    h_student: torch.Tensor  # (BT, ds) bf16
+    w_student: torch.Tensor  # (V, ds) bf16
+    h_teacher: torch.Tensor  # (BT, dt) bf16
+    w_teacher: torch.Tensor  # (V, dt) bf16
+    target: torch.Tensor
+    grad_ce: torch.Tensor
+    grad_tvd: torch.Tensor
+    ignore_index: int = IGNORE_INDEX
+
+
+def make_linear(name: str, device="cpu", rows: int | None = None) -> LinearWorkload:
+    """Hidden states ~ N(0, 1) and lm_head weights ~ N(0, (2/sqrt(d))^2), so the
+    logits are ~ N(0, 2^2) like the logit workloads; targets uniform with 3%
+    ignored; upstream gradients 1/BT."""
+    cfg = LINEAR_WORKLOADS[name]
+    BT = cfg["BT"] if rows is None else int(rows)
+    dev = torch.device(device)
+    g = _gen(dev, cfg["seed"])
+    with torch.no_grad():
+        hs = _randn((BT, cfg["ds"]), g, dev).bfloat16()
+        ws = (_randn((cfg["V"], cfg["ds"]), g, dev) * (2.0 / cfg["ds"] ** 0.5)).bfloat16()
+        ht = _randn((BT, cfg["dt"]), g, dev).bfloat16()
+        wt = (_randn((cfg["V"], cfg["dt"]), g, dev) * (2.0 / cfg["dt"] ** 0.5)).bfloat16()
+        target = _ignore(torch.randint(0, cfg["V"], (BT,), generator=g, device=dev), 0.03, g, dev)
+        gce = torch.full((BT,), 1.0 / BT, device=dev)
+    return LinearWorkload(name, hs, ws, ht, wt, target, gce, gce.clone())
