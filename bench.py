@@ -279,7 +279,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.LINEAR_WORKLOADS))
-    ap.add_argument("--chunk-rows", type=int, default=1024, help="row block of the fused-linear path")
+    ap.add_argument("--chunk-rows", type=int, default=2048, help="row block of the fused-linear path")
     ap.add_argument("--rows", type=int, default=None, help="override BT (profiling)")
     ap.add_argument("--path", default="single", choices=["single", "two"],
                     help="headline step: one fused forward+backward launch, or the forward "
