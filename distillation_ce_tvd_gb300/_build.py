@@ -19,7 +19,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfused_ce_tvd.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
-SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu", "fct_linear.cu"]
+SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu", "fct_linear.cu",
+           "fct_noalloc.cu"]
 HEADERS = ["fct_common.cuh", "fct_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -25,6 +25,7 @@ _lib = None
 EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
            "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
+           "fused_linear_ce_tvd_forward_backward_noalloc",
            "fct_status_string", "fct_set_forward_cluster", "fct_version")
 
 
@@ -60,6 +61,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
             vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, ctypes.c_size_t, i64, vp, vp]
         lib.fused_linear_ce_tvd_forward_backward.restype = i32
+        lib.fused_linear_ce_tvd_forward_backward_noalloc.argtypes = [
+            vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
+            vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
+        lib.fused_linear_ce_tvd_forward_backward_noalloc.restype = i32
         lib.fused_ce_tvd_mean_upstream.argtypes = [vp, i64, i64, dbl, dbl, vp, vp, vp, vp]
         lib.fused_ce_tvd_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp]
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
@@ -419,4 +424,51 @@ def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teac
         _ptr(workspace), workspace.numel() * workspace.element_size(), rows,
         _ptr(dev_status), _stream(stream))
     _check(rc, "fused_linear_ce_tvd_forward_backward")
+    return (*outs, grad_h, grad_w)
+
+
+def fused_linear_ce_tvd_forward_backward_noalloc(h_student, w_student, h_teacher, w_teacher,
+                                                 target, grad_ce, grad_tvd, ce, tvd, student_lse,
+                                                 teacher_lse, sigma, grad_h=None, grad_w=None,
+                                                 ignore_index=IGNORE_INDEX, *, dev_status=None,
+                                                 stream=None):
+    """fused_linear_ce_tvd_forward_backward with every buffer supplied by the
+    caller, for callers that cannot let a library allocate device memory.
+
+    grad_ce and grad_tvd are fp32 CUDA tensors of BT values or of one value
+    (broadcast); ce ... sigma are (BT,) fp32 outputs; grad_h (BT, d_student)
+    bf16 and grad_w (V, d_student) fp32 (accumulated into) are optional.
+    Nothing is allocated here or in the library call.
+    """
+    ld_hs, ld_ws = _mat(h_student, "h_student"), _mat(w_student, "w_student")
+    ld_ht, ld_wt = _mat(h_teacher, "h_teacher"), _mat(w_teacher, "w_teacher")
+    BT, ds = h_student.shape
+    V = w_student.shape[0]
+    dt = h_teacher.shape[1]
+    if w_student.shape[1] != ds or w_teacher.shape != (V, dt) or h_teacher.shape[0] != BT:
+        raise ValueError("inconsistent hidden / weight shapes")
+    _rows(target, BT, "target", torch.int64)
+    strides = []
+    for g, name in ((grad_ce, "grad_ce"), (grad_tvd, "grad_tvd")):
+        if not torch.is_tensor(g) or g.numel() not in (1, BT):
+            raise ValueError(f"{name} must be a CUDA tensor of {BT} values or of one value")
+        strides.append(0 if g.numel() == 1 and BT != 1 else 1)
+        _rows(g.reshape(-1), g.numel(), name)
+    if strides[0] != strides[1]:
+        raise ValueError("grad_ce and grad_tvd must both be per-row or both be one value")
+    outs = [_rows(x, BT, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                                          (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
+    ld_gh = _mat(grad_h, "grad_h") if grad_h is not None else ds
+    if grad_h is not None and grad_h.shape != (BT, ds):
+        raise ValueError("grad_h must be (BT, d_student) bf16")
+    if grad_w is not None and (grad_w.dtype != torch.float32 or grad_w.shape != (V, ds)
+                               or (ds > 1 and grad_w.stride(1) != 1)):
+        raise ValueError("grad_w must be (V, d_student) float32 with unit column stride")
+    ld_gw = max(int(grad_w.stride(0)), ds) if grad_w is not None else ds
+    rc = load().fused_linear_ce_tvd_forward_backward_noalloc(
+        _ptr(h_student), ld_hs, _ptr(w_student), ld_ws, ds, _ptr(h_teacher), ld_ht,
+        _ptr(w_teacher), ld_wt, dt, _ptr(target), BT, V, int(ignore_index), _ptr(grad_ce),
+        _ptr(grad_tvd), strides[0], *map(_ptr, outs), _ptr(grad_h), ld_gh, _ptr(grad_w), ld_gw,
+        _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_linear_ce_tvd_forward_backward_noalloc")
     return (*outs, grad_h, grad_w)

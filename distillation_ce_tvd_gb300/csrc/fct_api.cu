@@ -336,6 +336,23 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
 
 }  // namespace
 
+namespace fct {
+
+int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms) {
+  DeviceInfo d;
+  const int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  if (cudaGetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return FCT_ERR_CUDA;
+  }
+  *plan = plan_forward(d, V, FCT_F32, true, true);
+  *sms = d.sms;
+  return FCT_OK;
+}
+
+}  // namespace fct
+
 extern "C" {
 
 size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows) {

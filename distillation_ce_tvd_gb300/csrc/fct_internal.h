@@ -101,6 +101,11 @@ size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows);
 cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,
                           cudaStream_t st);
 
+// The forward plan the fused-linear path uses (fp32 logit rows of width V)
+// on the calling thread's current device, with that device's index and SM
+// count.  Returns an fct_status.
+int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms);
+
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st);

@@ -19,7 +19,8 @@
  * ---------------------------------------
  *  - All array arguments are DEVICE pointers, owned by the caller.  The
  *    library allocates no device memory and keeps no state between calls
- *    (the fused-linear entry point below keeps one cuBLAS handle per device).
+ *    (the fused-linear entry point below keeps one cuBLAS handle per device;
+ *    its no-allocation variant uses a fixed device array of the library).
  *  - Logit matrices are row-major (BT, V) with a row stride `ld` (in
  *    elements, ld >= V).  Student and teacher share one element type.
  *  - `target` is int64 (BT,).  A row whose target equals `ignore_index`
@@ -177,6 +178,54 @@ int fused_linear_ce_tvd_forward_backward(
     float* teacher_lse, float* sigma, void* grad_h_student, int64_t ld_grad_h,
     float* grad_w_student, int64_t ld_grad_w, void* workspace,
     size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status,
+    void* stream);
+
+/*
+ * Fused-linear CE + TVD that allocates nothing (no counterpart in the PR
+ * #1384 analysis or the Liger-Kernel pages: it only changes where the
+ * temporary logit blocks live).
+ *
+ * Some callers cannot let a library allocate device memory while they run:
+ * processes whose memory is fixed up front (a caching allocator or a KV
+ * cache that owns all free HBM, where a cudaMalloc outside it fails or
+ * fragments it) and code that must not synchronise the device, which
+ * cudaMalloc and cudaFree may do.  The entry point above needs a caller
+ * workspace and a cuBLAS handle, whose creation allocates.  This one takes
+ * the same arguments minus workspace, workspace_bytes and chunk_rows, and
+ * computes the same outputs with:
+ *   - its logit blocks in a fixed array of FCT_NOALLOC_SCRATCH_BYTES
+ *     (64 MiB) of device memory that belongs to the library (a file-scope
+ *     __device__ array): the driver reserves it on each device when the
+ *     library's module holding it is loaded there and keeps it until the
+ *     process exits;
+ *   - its GEMMs on a tiled CUDA-core kernel of the library (fp32
+ *     accumulation) instead of cuBLAS, so it is much slower than the entry
+ *     point above at large sizes;
+ *   - the same loss kernel and the same bf16 rounding of the logit gradient.
+ * Rows go through in blocks of FCT_NOALLOC_SCRATCH_BYTES /
+ * (8 * round_up(V, 8)) rows.  V up to 8,388,608 is supported; a larger V
+ * (one student + teacher fp32 row would not fit) returns
+ * FCT_ERR_UNSUPPORTED before any launch.
+ *
+ * Set-up: the first call on each device (with that device current) looks up
+ * the array's device address with cudaGetSymbolAddress and queries the
+ * device; make that first call before any stream capture.  Every call
+ * shares the one array and leaves its last contents there; nothing in it
+ * needs to start at zero (each block writes its logits before reading
+ * them).  Calls whose work can overlap on the GPU (other streams, other host
+ * threads) race on the array and give wrong results; order them.
+ */
+#define FCT_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+int fused_linear_ce_tvd_forward_backward_noalloc(
+    const void* h_student, int64_t ld_h_student, const void* w_student,
+    int64_t ld_w_student, int64_t d_student, const void* h_teacher,
+    int64_t ld_h_teacher, const void* w_teacher, int64_t ld_w_teacher,
+    int64_t d_teacher, const int64_t* target, int64_t BT, int64_t V,
+    int64_t ignore_index, const float* grad_ce, const float* grad_tvd,
+    int64_t grad_stride, float* ce, float* tvd, float* student_lse,
+    float* teacher_lse, float* sigma, void* grad_h_student, int64_t ld_grad_h,
+    float* grad_w_student, int64_t ld_grad_w, int32_t* dev_status,
     void* stream);
 
 /*

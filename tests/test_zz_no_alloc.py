@@ -1,0 +1,141 @@
+"""The no-allocation fused-linear entry point against the regular one.
+
+The file name sorts last, so in a full run this also exercises the entry point
+after every other GPU test in the same process; it passes alone as well.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from distillation_ce_tvd_gb300 import binding
+from parity_util import tie_info
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+FCT_ERR_UNSUPPORTED = 2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    binding.load()
+
+
+def _case(BT, ds, dt, V, seed):
+    g = torch.Generator(device=DEV).manual_seed(seed)
+    hs = torch.randn(BT, ds, generator=g, device=DEV).bfloat16()
+    ht = torch.randn(BT, dt, generator=g, device=DEV).bfloat16()
+    ws = (torch.randn(V, ds, generator=g, device=DEV) * (2.0 / ds ** 0.5)).bfloat16()
+    wt = (torch.randn(V, dt, generator=g, device=DEV) * (2.0 / dt ** 0.5)).bfloat16()
+    tg = torch.randint(0, V, (BT,), generator=g, device=DEV)
+    tg[::7] = -100
+    gce = torch.full((BT,), 1.0 / BT, device=DEV)
+    gtvd = torch.full((BT,), 0.7 / BT, device=DEV)
+    return hs, ws, ht, wt, tg, gce, gtvd
+
+
+def _outputs(BT, V, ds):
+    """Caller-owned outputs, pre-filled with NaN so that an unwritten value shows."""
+    outs = [torch.full((BT,), float("nan"), device=DEV) for _ in range(5)]
+    grad_h = torch.full((BT, ds), float("nan"), device=DEV, dtype=torch.bfloat16)
+    grad_w = torch.zeros(V, ds, device=DEV)
+    return outs, grad_h, grad_w
+
+
+def _tolerances(case):
+    """The fused-linear tests' tolerances, doubled: each entry point is within
+    them of the fp64 result, so the two are within twice them of each other."""
+    hs, ws, ht, wt, tg, gce, gtvd = case
+    ds, dt = hs.shape[1], ht.shape[1]
+    BT, V = hs.shape[0], ws.shape[0]
+    Hs, Ws, Ht, Wt = (x.cpu().double().numpy() for x in (hs, ws, ht, wt))
+    Ls, Lt = Hs @ Ws.T, Ht @ Wt.T
+    tgc = tg.cpu().numpy()
+    G, _ = oracle.fused_ce_tvd_backward(Ls, Lt, tgc, gce.cpu().numpy(), gtvd.cpu().numpy())
+    _, mass, _ = tie_info(Ls, Lt)
+    # logits are fp32 sums of D exact bf16 products (error <= D 2^-24 sum |h w|);
+    # a per-row output moves by at most twice the largest logit error
+    bound = np.maximum((np.abs(Hs) @ np.abs(Ws).T).max(1) * ds,
+                       (np.abs(Ht) @ np.abs(Wt).T).max(1) * dt) * 2.0 ** -24
+    row = 2.0 * (1e-5 + 2.0 * bound)
+    sigma = row + 2.0 * 2.0 * mass
+    G_abs = np.abs(G)
+    e_rel = 2.0 ** -8 + 2e-3 + V * 2.0 ** -24
+    ref_gh = G @ Ws
+    tol_gh = 2.0 * (e_rel * (G_abs @ np.abs(Ws)) + 1e-6 * np.abs(Ws).sum(0)
+                    + 2.0 ** -8 * np.abs(ref_gh) + 1e-9)
+    e_rel_w = 2.0 ** -8 + 2e-3 + BT * 2.0 ** -24
+    tol_gw = 2.0 * (e_rel_w * (G_abs.T @ np.abs(Hs)) + 1e-6 * np.abs(Hs).sum(0) + 1e-9)
+    return tgc, row, sigma, tol_gh, tol_gw
+
+
+def _compare(got, ref, tols, what):
+    tgc, row, sigma, tol_gh, tol_gw = tols
+    ign = tgc == -100
+    names = ("ce", "tvd", "student_lse", "teacher_lse", "sigma")
+    for k, name in enumerate(names):
+        a = got[k].cpu().double().numpy()
+        b = ref[k].cpu().double().numpy()
+        assert np.all(a[ign] == 0.0) and np.all(b[ign] == 0.0), f"{what}{name}: ignored rows"
+        tol = sigma if name == "sigma" else row
+        err = np.abs(a - b)
+        assert np.all(err <= tol), f"{what}{name}: worst err/tol {(err / tol).max():.3g}"
+    gh_a, gh_b = (x.cpu().double().numpy() for x in (got[5], ref[5]))
+    assert np.all(gh_a[ign] == 0.0), f"{what}grad_h: ignored rows must be 0"
+    err = np.abs(gh_a - gh_b)
+    assert np.all(err <= tol_gh), f"{what}grad_h: worst err/tol {(err / tol_gh).max():.3g}"
+    err = np.abs(got[6].cpu().double().numpy() - ref[6].cpu().double().numpy())
+    assert np.all(err <= tol_gw), f"{what}grad_w: worst err/tol {(err / tol_gw).max():.3g}"
+
+
+# (50, 128, 96, 1003): the rows fit in one block of the fixed scratch.
+# (120, 64, 64, 151936): 64 MiB holds 55 rows of 2 x 151936 fp32 logits, so
+# three blocks, the last one ragged (10 rows).
+@pytest.mark.parametrize("BT,ds,dt,V", [(50, 128, 96, 1003), (120, 64, 64, 151936)])
+def test_noalloc_matches_regular_entry_point(BT, ds, dt, V):
+    cases = [_case(BT, ds, dt, V, seed=BT + V + k) for k in range(2)]
+    bufs = [_outputs(BT, V, ds) for _ in cases]
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    # two calls in a row; the second finds the first one's data in the scratch
+    def call(case, buf):
+        hs, ws, ht, wt, tg, gce, gtvd = case
+        outs, grad_h, grad_w = buf
+        return binding.fused_linear_ce_tvd_forward_backward_noalloc(
+            hs, ws, ht, wt, tg, gce, gtvd, *outs, grad_h=grad_h, grad_w=grad_w,
+            dev_status=status)
+
+    got = [call(cases[0], bufs[0])]
+    torch.cuda.synchronize()
+    free_before = torch.cuda.mem_get_info()[0]
+    got.append(call(cases[1], bufs[1]))
+    torch.cuda.synchronize()
+    # set-up happened in the first call; the second allocates nothing
+    assert torch.cuda.mem_get_info()[0] == free_before
+    assert status.item() == 0
+
+    for k, (case, g) in enumerate(zip(cases, got)):
+        hs, ws, ht, wt, tg, gce, gtvd = case
+        ref = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, gce, gtvd)
+        torch.cuda.synchronize()
+        _compare(g, ref, _tolerances(case), what=f"call {k}: ")
+
+
+def test_noalloc_rejects_vocab_beyond_scratch():
+    # 8 * round8(V) bytes (one student + one teacher fp32 row) must fit in
+    # 64 MiB: V = 8,388,609 does not.  The buffers are real and sized for V,
+    # and the refusal comes before any launch, leaving the outputs untouched.
+    BT, d, V = 2, 8, 8 * 1024 * 1024 + 1
+    hs = torch.zeros(BT, d, device=DEV, dtype=torch.bfloat16)
+    w = torch.zeros(V, d, device=DEV, dtype=torch.bfloat16)
+    tg = torch.zeros(BT, dtype=torch.int64, device=DEV)
+    g = torch.ones(BT, device=DEV)
+    outs = [torch.full((BT,), 7.0, device=DEV) for _ in range(5)]
+    with pytest.raises(binding.FctError) as e:
+        binding.fused_linear_ce_tvd_forward_backward_noalloc(hs, w, hs, w, tg, g, g, *outs)
+    assert e.value.status == FCT_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert all(bool((o == 7.0).all()) for o in outs)
