@@ -75,6 +75,20 @@ __device__ __forceinline__ float sgn_pq(float p, float q) {
   return gt - lt;
 }
 
+// Per lane of two (p, q) pairs: 1.0 where p > q (resp. p < q), else 0.0.
+__device__ __forceinline__ float2 gt_pq2(float2 p, float2 q) {
+  float2 r;
+  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(r.x) : "f"(p.x), "f"(q.x));
+  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(r.y) : "f"(p.y), "f"(q.y));
+  return r;
+}
+__device__ __forceinline__ float2 lt_pq2(float2 p, float2 q) {
+  float2 r;
+  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r.x) : "f"(p.x), "f"(q.x));
+  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r.y) : "f"(p.y), "f"(q.y));
+  return r;
+}
+
 // max(a, b, c) in one instruction (sm_100+).
 __device__ __forceinline__ float max3(float a, float b, float c) {
   float d;

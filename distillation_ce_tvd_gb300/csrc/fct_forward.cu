@@ -29,9 +29,13 @@
 //     sum|p - q| = sigma - tau.
 //   * The grid is persistent: one cluster per row slot, looping over rows.
 //   * With the upstream gradients known before the launch, a third pass over
-//     the still L2-resident row writes the student gradient of the "Backward
-//     Pass" in the same launch (the single-launch forward + backward), so
-//     HBM sees 2 reads and 1 write per element instead of 4 reads and 1 write.
+//     the still L2-resident student row writes the student gradient of the
+//     "Backward Pass" in the same launch (the single-launch forward +
+//     backward), so HBM sees 2 reads and 1 write per element instead of 4
+//     reads and 1 write.  Step 2 leaves each element's sign bit in shared
+//     memory, so step 3 reads only the student (p from the student logit, the
+//     coefficient of p picked by the bit); a thread that met an exact tie
+//     recomputes the sign from the teacher instead.
 //   * Student and teacher go through the very same code, so a row whose
 //     teacher equals its student bit for bit gets p == q everywhere and
 //     tvd = sigma = 0 exactly.
@@ -193,6 +197,12 @@ struct Count {
   __device__ __forceinline__ constexpr operator int() const { return N; }
 };
 constexpr int kStages = 3;   // ring slots per thread: two steps in flight while one is read
+// Single launch: step 2 leaves one sign bit per element in shared memory, one
+// 32-bit word per step of a row, so step 3 needs the student row only (and
+// the teacher row may leave L2 after step 2).  Up to kMaxSignWords steps per
+// row per thread (V <= 262,144 bf16 with one CTA of 512 threads per row);
+// beyond that step 3 re-reads the teacher as well.
+constexpr int kMaxSignWords = 16;
 
 // The feed: this thread's cursor in the sequence, issuing one step of
 // cp.async copies per call.  A pass of a row is n_full full steps of
@@ -210,17 +220,19 @@ struct Feed {
   int32_t q;       // step within the pass
   int32_t pass;
   int32_t n_full, rem;
+  int32_t passes_t;  // passes that read the teacher (2 when step 3 uses sign bits)
   bool active;     // false once this thread's sequence is exhausted
   int64_t first_byte;  // byte offset of this thread's first vector within a row
   uint32_t ring;       // shared address of this thread's 16 bytes in slot 0
-  uint64_t keep, drop, pol;
+  uint64_t keep, drop, pol_s, pol_t;
 
   __device__ __forceinline__ void seek_row(const FwdArgs& p) {
     sp = static_cast<const char*>(p.student) + (row * p.ld_s) * int64_t(sizeof(T)) + first_byte;
     if constexpr (kTvd)
       tp = static_cast<const char*>(p.teacher) + (row * p.ld_t) * int64_t(sizeof(T)) + first_byte;
-    // keep the row in L2 until its last pass reads it
-    pol = (pass + 1 < kPasses) ? keep : drop;
+    // keep each row in L2 until its last pass reads it
+    pol_s = (pass + 1 < kPasses) ? keep : drop;
+    pol_t = (pass + 1 < passes_t) ? keep : drop;
   }
 
   __device__ __forceinline__ void next_row(const FwdArgs& p, int64_t n_clusters) {
@@ -235,8 +247,11 @@ struct Feed {
 #pragma unroll
     for (int u = 0; u < kPerStep; ++u) {
       if (kCount == kPerStep || u < count) {
-        cp_async16(dst + u * NT * 16, sp + u * kStride, pol);
-        if constexpr (kTvd) cp_async16(dst + (kPerStep + u) * NT * 16, tp + u * kStride, pol);
+        cp_async16(dst + u * NT * 16, sp + u * kStride, pol_s);
+        if constexpr (kTvd) {
+          if (!kGrad || pass < passes_t)
+            cp_async16(dst + (kPerStep + u) * NT * 16, tp + u * kStride, pol_t);
+        }
       }
     }
   }
@@ -380,6 +395,10 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   f.drop = policy_evict_first();
   f.q = 0;
   f.pass = 0;
+  // steps per row of the thread with the most vectors (thread 0)
+  const int64_t max_steps = ((span + NT - 1) / NT + kPerStep - 1) / kPerStep;
+  const bool use_bits = kGrad && max_steps <= kMaxSignWords;
+  f.passes_t = use_bits ? 2 : F::kPasses;
   f.row = cluster_id;
   while (f.row < p.BT && p.target[f.row] == p.ignore_index) f.row += n_clusters;
   f.active = (n_my > 0) && (f.row < p.BT);
@@ -387,6 +406,8 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 
   // this thread's 16-byte cells: ring_mem[((slot*kTensors + tensor)*kPerStep + u)*NT + tid]
   const uint4* mine = ring_mem + tid;
+  // sign words of step 2 after the ring: word w of this thread at sbits[w*NT + tid]
+  uint32_t* sbits = reinterpret_cast<uint32_t*>(ring_mem + kStages * F::kTensors * kPerStep * NT);
 #pragma unroll
   for (int s = 0; s < kStages; ++s) f.feed(p, s, n_clusters);
   int slot = 0;
@@ -411,7 +432,6 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     // Read before any gradient of this row can overwrite it (in place).
     const float s_tg =
         (rank == 0 && tid == 0 && tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
-
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
     consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
@@ -452,7 +472,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       // sum |p - q| = sigma - tau.  Ties have sign 0 and add nothing.
       float sig_p = 0.f, sig_q = 0.f;
       const float2 L2 = make_float2(kLog2e, kLog2e), nst = make_float2(ns2, nt2);
-      auto tvd_pair = [&](float xs, float xt) {
+      auto tvd_pair = [&](float xs, float xt) {  // one element (the row's ragged tail)
         // the student and teacher exponents of one element in one packed FMA
         // (each lane rounds exactly like the scalar fmaf of the backward)
         const float2 e = __ffma2_rn(make_float2(xs, xt), L2, nst);
@@ -462,8 +482,29 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         sig_p = fmaf(pp, sg, sig_p);
         sig_q = fmaf(qq, sg, sig_q);
       };
+      // Two neighbouring elements at a time, each tensor's pair in one packed
+      // op (neighbours of one tensor come out of the unpack side by side);
+      // sigma and tau run as two packed partial sums.
+      const float2 ns22 = make_float2(ns2, ns2), nt22 = make_float2(nt2, nt2);
+      const float2 minus1 = make_float2(-1.f, -1.f);
+      float2 sp2 = make_float2(0.f, 0.f), sq2 = make_float2(0.f, 0.f);
+      auto tvd_two = [&](float s0, float s1, float t0, float t1) {
+        const float2 es = __ffma2_rn(make_float2(s0, s1), L2, ns22);
+        const float2 et = __ffma2_rn(make_float2(t0, t1), L2, nt22);
+        const float2 pp = make_float2(ex2(es.x), ex2(es.y));
+        const float2 qq = make_float2(ex2(et.x), ex2(et.y));
+        const float2 sg = __ffma2_rn(lt_pq2(pp, qq), minus1, gt_pq2(pp, qq));  // gt - lt, exact
+        sp2 = __ffma2_rn(pp, sg, sp2);
+        sq2 = __ffma2_rn(qq, sg, sq2);
+        return sg;
+      };
+      // Single launch: the sign bit of each element (1 for p < q), shifted in
+      // element order into one word per step, and the AND of all signs' bit
+      // patterns, whose exponent bits clear at a tie (sign +0; NaN gives 0 too).
+      uint32_t tie_and = 0xffffffffu;
       consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
-                                    [&](const uint4* cell, auto n, int) {
+                                    [&](const uint4* cell, auto n, int k0) {
+                                      [[maybe_unused]] uint32_t word = 0;
 #pragma unroll
                                       for (int u = 0; u < kPerStep; ++u) {
                                         if (u < int(n)) {
@@ -471,10 +512,27 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
                                           unpack_raw<T, VE>(cell[u * NT], xs);
                                           unpack_raw<T, VE>(cell[(kPerStep + u) * NT], xt);
 #pragma unroll
-                                          for (int j = 0; j < VE; ++j) tvd_pair(xs[j], xt[j]);
+                                          for (int j = 0; j < VE; j += 2) {
+                                            const float2 sg = tvd_two(xs[j], xs[j + 1], xt[j], xt[j + 1]);
+                                            if constexpr (kGrad) {
+                                              const uint32_t b0 = __float_as_uint(sg.x);
+                                              const uint32_t b1 = __float_as_uint(sg.y);
+                                              word = __funnelshift_l(b1, __funnelshift_l(b0, word, 1), 1);
+                                              tie_and &= b0 & b1;
+                                            }
+                                          }
+                                        }
+                                      }
+                                      if constexpr (kGrad) {
+                                        if (use_bits) {
+                                          // a short step's bits move up to the full step's positions
+                                          if (int(n) < kPerStep) word <<= (kPerStep - int(n)) * VE;
+                                          sbits[(k0 / kPerStep) * NT + tid] = word;
                                         }
                                       }
                                     });
+      sig_p = sp2.x + sp2.y;
+      sig_q = sq2.x + sq2.y;
       if (owns_tail && tail0 + tid < p.V)
         tvd_pair(Elem<T>::load1(srow + tail0 + tid), Elem<T>::load1(trow + tail0 + tid));
       float abs_sum = sig_p - sig_q;
@@ -503,12 +561,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
           const float pp = ex2(e.x);
           return pp * fmaf(h, sgn_pq(pp, ex2(e.y)), c0);
         };
-        auto grad_vec = [&](const uint4 ws, const uint4 wt, int k) {
-          float xs[VE], xt[VE], g[VE];
-          unpack_raw<T, VE>(ws, xs);
-          unpack_raw<T, VE>(wt, xt);
-#pragma unroll
-          for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+        auto finish_vec = [&](float (&g)[VE], int k) {
           const int64_t off = tg_rel - int64_t(k) * NT * VE;
           if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
 #pragma unroll
@@ -521,14 +574,59 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
           }
           store_vec<T, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
         };
-        consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
-                                      [&](const uint4* cell, auto n, int k0) {
+        auto grad_vec = [&](const uint4 ws, const uint4 wt, int k) {
+          float xs[VE], xt[VE], g[VE];
+          unpack_raw<T, VE>(ws, xs);
+          unpack_raw<T, VE>(wt, xt);
 #pragma unroll
-                                        for (int u = 0; u < kPerStep; ++u)
-                                          if (u < int(n))
-                                            grad_vec(cell[u * NT], cell[(kPerStep + u) * NT],
-                                                     k0 + u);
-                                      });
+          for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+          finish_vec(g, k);
+        };
+        // With step 2's sign bits and no tie in this thread's elements, the
+        // coefficient of p is one of fmaf(h, +-1, c0), the values the backward
+        // kernel's expression takes at sign +-1, so the gradient is bit-identical.
+        const bool from_bits = use_bits && (tie_and & 0x3f800000u) == 0x3f800000u;
+        const float c_plus = fmaf(h, 1.f, c0), c_minus = fmaf(h, -1.f, c0);
+        const float2 ns22 = make_float2(ns2, ns2);
+        const T* tmine = trow + (vb + tid) * VE;
+        consume_pass<NT, F::kTensors>(
+            f, slot, p, n_clusters, mine, n_full, rem, [&](const uint4* cell, auto n, int k0) {
+              if (from_bits) {
+                const uint32_t word = sbits[(k0 / kPerStep) * NT + tid];
+#pragma unroll
+                for (int u = 0; u < kPerStep; ++u) {
+                  if (u < int(n)) {
+                    float xs[VE], g[VE];
+                    unpack_raw<T, VE>(cell[u * NT], xs);
+#pragma unroll
+                    for (int j = 0; j < VE; j += 2) {
+                      const float2 e = __ffma2_rn(make_float2(xs[j], xs[j + 1]), L2, ns22);
+                      constexpr int kBits = kPerStep * VE;
+                      const int b0 = kBits - 1 - (u * VE + j);
+                      const float ca = ((word >> b0) & 1u) ? c_minus : c_plus;
+                      const float cb = ((word >> (b0 - 1)) & 1u) ? c_minus : c_plus;
+                      const float2 gg = __fmul2_rn(make_float2(ex2(e.x), ex2(e.y)),
+                                                   make_float2(ca, cb));
+                      g[j] = gg.x;
+                      g[j + 1] = gg.y;
+                    }
+                    finish_vec(g, k0 + u);
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int u = 0; u < kPerStep; ++u) {
+                  if (u < int(n)) {
+                    // the teacher comes from the ring unless step 3 was planned
+                    // on sign bits (then it was not copied: read it from L2/HBM)
+                    const uint4 wt =
+                        use_bits ? load_raw<T, VE>(tmine + int64_t(k0 + u) * NT * VE, f.drop)
+                                 : cell[(kPerStep + u) * NT];
+                    grad_vec(cell[u * NT], wt, k0 + u);
+                  }
+                }
+              }
+            });
         if (owns_tail && tail0 + tid < p.V) {
           const int64_t v = tail0 + tid;
           float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
@@ -662,7 +760,8 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 // occupancy query are done once per process.
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
-  constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16;
+  constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
+                           (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
   auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -344,6 +344,28 @@ def test_single_launch_equals_forward_then_backward(name, rows, V, dtype, ld, cl
     assert torch.equal(g1, g3)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("cluster", [0, 2])
+def test_single_launch_ties_equal_forward_then_backward(dtype, cluster):
+    # Rows with exact ties (teacher == student), near ties (teacher shifted by
+    # a constant, so p and q agree to rounding and some elements tie exactly)
+    # and a row tied on a block of columns only: the single launch must still
+    # match forward + backward bit for bit, tie threads included.
+    w = workloads.make("bt8192_v151936_bf16", DEV, rows=10, V=151936, dtype=dtype, seed=33)
+    w.teacher[2] = w.student[2]
+    w.teacher[3] = (w.student[3].float() + 1.0).to(dtype)
+    w.teacher[4] = (w.student[4].float() - 0.5).to(dtype)
+    w.teacher[6, 1000:70000] = w.student[6, 1000:70000]
+    w.target[8] = w.ignore_index
+    f1, g1, st1 = run(w, cluster=cluster)
+    f2, g2, st2 = run_single(w, cluster=cluster)
+    assert st1 == st2 == 0
+    for k in f1:
+        assert torch.equal(f1[k], f2[k]), k
+    assert torch.equal(g1, g2)
+    assert f2["tvd"][2].item() == 0.0 and f2["sigma"][2].item() == 0.0
+
+
 def test_single_launch_parity_and_status():
     w = workloads.make("bt8192_v151936_bf16", DEV, rows=24, V=151936, seed=32)
     w.teacher[5] = w.student[5]
