@@ -4,6 +4,8 @@
 // x * log2(e), so every exponential is one ex2 (MUFU) after one FFMA.
 #pragma once
 
+#include <type_traits>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -303,6 +305,27 @@ __device__ __forceinline__ void store_vec(T* p, const float (&x)[VE], uint64_t p
     Elem<T>::store1(p, x[0]);
   } else {
     st16(p, Elem<T>::pack(x), pol);
+  }
+}
+
+// A gradient vector of VE values in the gradient's element type TG, from a
+// logits vector of type T: the same 16-byte store when TG == T, an 8-byte
+// store of 4 bf16 values for fp32 logits with a bf16 gradient.
+__device__ __forceinline__ void st8(void* ptr, uint32_t a, uint32_t b, uint64_t pol) {
+  asm volatile("st.global.L1::no_allocate.L2::cache_hint.v2.u32 [%0], {%1,%2}, %3;"
+               :
+               : "l"(ptr), "r"(a), "r"(b), "l"(pol)
+               : "memory");
+}
+
+template <typename T, typename TG, int VE>
+__device__ __forceinline__ void store_grad(TG* p, const float (&x)[VE], uint64_t pol) {
+  if constexpr (std::is_same<T, TG>::value || VE == 1) {
+    store_vec<TG, VE>(p, x, pol);
+  } else {
+    static_assert(std::is_same<T, float>::value && std::is_same<TG, bf16_t>::value && VE == 4,
+                  "a bf16 gradient of fp32 logits");
+    st8(p, pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pol);
   }
 }
 

@@ -360,7 +360,9 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
   st.s = __fadd2_rn(st.s, acc);
 }
 
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
+// TG: element type of the gradient written by the single launch (the logits'
+// type, or bf16 for fp32 logits).
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG = T>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
   using F = Feed<T, VE, kTvd, kGrad, NT>;
@@ -420,10 +422,11 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     if (tg == p.ignore_index) {
       if (rank == 0 && tid == 0) write_ignored<kTvd>(p, row);
       if constexpr (kGrad) {  // this CTA's slice of the gradient row is zero
-        T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
+        TG* grow = static_cast<TG*>(p.grad) + row * p.ld_g;
         const float zero[VE] = {};
-        for (int64_t v = vb + tid; v < ve; v += NT) store_vec<T, VE>(grow + v * VE, zero, f.drop);
-        if (owns_tail && tail0 + tid < p.V) Elem<T>::store1(grow + tail0 + tid, 0.f);
+        for (int64_t v = vb + tid; v < ve; v += NT)
+          store_grad<T, TG, VE>(grow + v * VE, zero, f.drop);
+        if (owns_tail && tail0 + tid < p.V) Elem<TG>::store1(grow + tail0 + tid, 0.f);
       }
       continue;  // uniform over the cluster; the feed skips this row too
     }
@@ -552,8 +555,8 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         const float h = 0.5f * p.grad_tvd[row * p.grad_stride];
         const float c0 = gce - h * sig;  // coefficient of p: c0 + h * sign
         const bool bad = (tg < 0 || tg >= p.V);
-        T* grow = static_cast<T*>(p.grad) + row * p.ld_g;
-        T* gmine = grow + (vb + tid) * VE;
+        TG* grow = static_cast<TG*>(p.grad) + row * p.ld_g;
+        TG* gmine = grow + (vb + tid) * VE;
         // element offset of the target from this thread's first element
         const int64_t tg_rel = tg - (vb + tid) * VE;
         auto grad_of = [&](float xs, float xt) {
@@ -572,7 +575,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 #pragma unroll
             for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
           }
-          store_vec<T, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
+          store_grad<T, TG, VE>(gmine + int64_t(k) * NT * VE, g, f.drop);
         };
         auto grad_vec = [&](const uint4 ws, const uint4 wt, int k) {
           float xs[VE], xt[VE], g[VE];
@@ -631,7 +634,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
           const int64_t v = tail0 + tid;
           float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
           if (v == tg) g -= gce;
-          Elem<T>::store1(grow + v, bad ? __uint_as_float(0x7fc00000u) : g);
+          Elem<TG>::store1(grow + v, bad ? __uint_as_float(0x7fc00000u) : g);
         }
       }
     }
@@ -758,11 +761,11 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per process.
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT>
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
                            (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
-  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT>;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
@@ -788,7 +791,7 @@ cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
   return launch_cluster(kernel, C, kScalarThreads, 0, n, a, st);
 }
 
-template <typename T, int C, bool kTvd, bool kGrad>
+template <typename T, int C, bool kTvd, bool kGrad, typename TG>
 cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr int VE = Elem<T>::kVec;
   if constexpr (kGrad) {
@@ -796,16 +799,16 @@ cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   } else {
     if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
   }
-  return run_pipelined<T, VE, C, kTvd, kGrad, 512>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, kGrad, 512, TG>(a, plan.slots, st);
 }
 
-template <typename T, bool kTvd, bool kGrad>
+template <typename T, bool kTvd, bool kGrad, typename TG = T>
 cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   switch (plan.cluster) {
-    case 1: return run<T, 1, kTvd, kGrad>(a, plan, st);
-    case 2: return run<T, 2, kTvd, kGrad>(a, plan, st);
-    case 4: return run<T, 4, kTvd, kGrad>(a, plan, st);
-    default: return run<T, 8, kTvd, kGrad>(a, plan, st);
+    case 1: return run<T, 1, kTvd, kGrad, TG>(a, plan, st);
+    case 2: return run<T, 2, kTvd, kGrad, TG>(a, plan, st);
+    case 4: return run<T, 4, kTvd, kGrad, TG>(a, plan, st);
+    default: return run<T, 8, kTvd, kGrad, TG>(a, plan, st);
   }
 }
 
@@ -816,7 +819,10 @@ cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t s
     if (a.grad) return run_c<bf16_t, true, true>(a, plan, st);
     return a.tvd ? run_c<bf16_t, true, false>(a, plan, st) : run_c<bf16_t, false, false>(a, plan, st);
   }
-  if (a.grad) return run_c<float, true, true>(a, plan, st);
+  if (a.grad) {
+    return a.grad_bf16 ? run_c<float, true, true, bf16_t>(a, plan, st)
+                       : run_c<float, true, true>(a, plan, st);
+  }
   return a.tvd ? run_c<float, true, false>(a, plan, st) : run_c<float, false, false>(a, plan, st);
 }
 

@@ -28,6 +28,7 @@ struct FwdArgs {
   const float* grad_tvd;
   int64_t grad_stride;
   int keep_normal;  // 1: evict_normal instead of evict_last while a row must stay in L2
+  int grad_bf16 = 0;  // single launch on fp32 logits: write the gradient as bf16
 };
 
 struct FwdPlan {

@@ -292,7 +292,7 @@ extern "C" int fused_linear_ce_tvd_forward_backward_noalloc(
   int rc = check(a);
   if (rc != FCT_OK) return rc;
   // One student + one teacher fp32 row must fit in the scratch array.
-  const size_t row_bytes = fct::linear_workspace_bytes(V, 1);
+  const size_t row_bytes = size_t(2) * sizeof(float) * size_t(fct::linear_logits_ld(V));
   if (row_bytes == 0 || row_bytes > kScratchBytes) return FCT_ERR_UNSUPPORTED;
   const int64_t per_block = static_cast<int64_t>(kScratchBytes / row_bytes);
   a.chunk_rows = per_block < BT ? per_block : BT;

@@ -146,8 +146,9 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
  * chunk_rows: per block, cuBLAS GEMMs (bf16 in, fp32 accumulate) write the
  * block's student and teacher logits (fp32) into `workspace`, the
  * single-launch forward + backward of the PR #1384 analysis's loss runs on
- * them, its logit gradient is rounded to bf16, and two more GEMMs give
- * d loss / d h_student for the block and accumulate d loss / d w_student.
+ * them and writes their logit gradient rounded to bf16 (also in
+ * `workspace`), and two more GEMMs give d loss / d h_student for the block
+ * and accumulate d loss / d w_student.
  * (Computing logits in row blocks is the chunking that the Liger-Kernel
  * overview page describes for its fused linear cross-entropy; applying it to
  * CE + TVD is this library's addition.)  The teacher is frozen.
