@@ -335,10 +335,20 @@ def main():
                                               student_lse=ls, teacher_lse=lt, sigma=sg,
                                               grad_student=grad, stream=stream)
 
+    ce_lse = torch.empty_like(ce)
+
+    def ce_fwd():  # the cross-entropy subset: student only
+        binding.ce_forward(w.student, w.target, w.ignore_index, ce=ce, lse=ce_lse, stream=stream)
+
+    def ce_bwd():
+        binding.ce_backward(w.student, w.target, ce_lse, w.grad_ce, w.ignore_index,
+                            grad_logits=grad, stream=stream)
+
     # the launches of one step of each path, with the algorithmic bytes of each launch
     paths = {
         "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
         "single": [("forward_backward", single, 3 * BT * V * elem)],
+        "ce": [("ce_forward", ce_fwd, BT * V * elem), ("ce_backward", ce_bwd, 2 * BT * V * elem)],
     }
 
     def time_path(name, K, sampler=None):
@@ -380,10 +390,15 @@ def main():
     value = world * BT / (ms * 1e-3)
     other_name = "two" if args.path == "single" else "single"
     other = None
+    ce_path = None
     if not args.no_other:
         oms, okern = time_path(other_name, K)
         other = {"path": other_name, "ms_per_step": oms, "value": world * BT / (oms * 1e-3),
                  "kernels": okern}
+        # cross-entropy alone (student logits only): forward + backward, 3 V e per row
+        cms, ckern = time_path("ce", K)
+        ce_path = {"path": "ce", "ms_per_step": cms, "value": world * BT / (cms * 1e-3),
+                   "unit": "tokens/s", "kernels": ckern}
 
     peaks = measured_peaks()
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -478,6 +493,7 @@ def main():
                          "traffic": traffic},
             "gpu_launches": len(paths[args.path]) * K,
             "other_path": other,
+            "ce_path": ce_path,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary() if clocks else None,
