@@ -366,6 +366,26 @@ def test_single_launch_ties_equal_forward_then_backward(dtype, cluster):
     assert f2["tvd"][2].item() == 0.0 and f2["sigma"][2].item() == 0.0
 
 
+@pytest.mark.parametrize("dtype,V,ld", [(torch.bfloat16, 300003, 300008),
+                                        (torch.float32, 140001, 140004)])
+def test_single_launch_without_sign_words(dtype, V, ld):
+    # One CTA per row over a long row: more steps per thread than the shared
+    # memory keeps sign words for, so the third pass re-reads the teacher.
+    # (Rows padded to 16-byte strides: the vector path, which the single
+    # launch needs.)
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=6, V=V, dtype=dtype, seed=34)
+    w = padded(w, ld, 0)
+    w.teacher[1] = w.student[1]
+    w.target[4] = w.ignore_index
+    f1, g1, st1 = run(w, cluster=1)
+    f2, g2, st2 = run_single(w, cluster=1)
+    assert st1 == st2 == 0
+    for k in f1:
+        assert torch.equal(f1[k], f2[k]), k
+    assert torch.equal(g1, g2)
+    compare(w, f2, g2, what="long rows ")
+
+
 def test_single_launch_parity_and_status():
     w = workloads.make("bt8192_v151936_bf16", DEV, rows=24, V=151936, seed=32)
     w.teacher[5] = w.student[5]
