@@ -10,8 +10,8 @@
 // with zero rows for ignore_index and a zero subgradient at ties.
 //
 // GB300 mapping: a pure stream (2 reads + 1 write per element) cut into
-// units of (row, 1024 vectors); a persistent grid of resident CTAs walks the
-// units.  Per element the coefficient of p is c0 + h*sign with per-row
+// units of (row, 1024 vectors) (2048 for cross-entropy alone, which reads one
+// tensor); a persistent grid of resident CTAs walks the units.  Per element the coefficient of p is c0 + h*sign with per-row
 // c0 = grad_ce - h*sigma and h = grad_tvd/2, and sign from two compares that
 // yield 0 at ties, so the inner loop is two ex2, two compares, one subtract
 // and two FMAs/multiplies.  Each element is read and then written by the
@@ -24,11 +24,18 @@ namespace fct {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
-constexpr int64_t kSeg = int64_t(kThreads) * kUnroll;  // vectors per unit
+// Vectors per thread per unit, all loaded before any is used: 4 per tensor for
+// the fused loss (student + teacher), 8 for cross-entropy alone, so both keep
+// about the same bytes in flight.
+template <bool kTvd>
+constexpr int kUnrollOf = kTvd ? 4 : 8;
+template <bool kTvd>
+constexpr int64_t kSegOf = int64_t(kThreads) * kUnrollOf<kTvd>;  // vectors per unit
 
 template <typename T, int VE, bool kTvd>
 __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
+  constexpr int kUnroll = kUnrollOf<kTvd>;
+  constexpr int64_t kSeg = kSegOf<kTvd>;
   const T* S = static_cast<const T*>(a.student);
   const T* Tt = static_cast<const T*>(a.teacher);
   T* G = static_cast<T*>(a.grad);
@@ -146,6 +153,7 @@ int blocks_per_sm() {
 
 template <typename T, int VE, bool kTvd>
 cudaError_t go(const BwdArgs& a, int sms, cudaStream_t st) {
+  constexpr int64_t kSeg = kSegOf<kTvd>;
   const int64_t nvec = a.V / VE;
   const int64_t nseg = nvec > 0 ? (nvec + kSeg - 1) / kSeg : 1;
   const int64_t units = a.BT * nseg;

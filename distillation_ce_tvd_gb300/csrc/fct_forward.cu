@@ -143,6 +143,23 @@ __device__ __forceinline__ void cluster_sum2_all(float& x, float& y, float2* par
   }
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 with a cache policy (one TMA
+// request; p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes, uint64_t pol) {
+  asm volatile(
+      "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %0;\n\t"
+      "cp.async.bulk.prefetch.L2.global.L2::cache_hint [g], %1, %2;\n\t}" ::"l"(p),
+      "r"(bytes), "l"(pol)
+      : "memory");
+}
+
+// Cross-entropy alone streams each row once: thread 0 requests the CTA's
+// slice kPrefetchSteps steps ahead of the ring into L2, so HBM sees more
+// bytes in flight than the ring holds.  (The fused passes keep rows in L2
+// for later passes; there, extra prefetched bytes evict rows still needed,
+// measured slower.)
+constexpr int kPrefetchSteps = 6;
+
 // One element pair of step 2: sig_p += p*sign(p - q), sig_q += q*sign(p - q).
 __device__ __forceinline__ void tvd_accum1(float xs, float xt, float ns2, float nt2,
                                            float& sig_p, float& sig_q) {
@@ -438,7 +455,15 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     // ---- step 1: log-sum-exp of both rows
     Lse2x a = lse2x_empty(), b = lse2x_empty();
     consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
-                                  [&](const uint4* cell, auto n, int) {
+                                  [&](const uint4* cell, auto n, int k0) {
+                                    if constexpr (!kTvd) {
+                                      constexpr int64_t kChunk = int64_t(kPerStep) * NT * 16;
+                                      const int64_t off = (k0 / kPerStep + kPrefetchSteps) * kChunk;
+                                      if (tid == 0 && off < span * 16)
+                                        prefetch_l2(reinterpret_cast<const char*>(srow) + vb * 16 + off,
+                                                    static_cast<uint32_t>(min(kChunk, span * 16 - off)),
+                                                    f.pol_s);
+                                    }
                                     lse_step<T, VE, NT>(a, cell, n);
                                     if constexpr (kTvd) lse_step<T, VE, NT>(b, cell + kPerStep * NT, n);
                                   });
