@@ -281,7 +281,7 @@ def main():
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.LINEAR_WORKLOADS))
     ap.add_argument("--chunk-rows", type=int, default=2048, help="row block of the fused-linear path")
     ap.add_argument("--rows", type=int, default=None, help="override BT (profiling)")
-    ap.add_argument("--path", default="single", choices=["single", "two"],
+    ap.add_argument("--path", default="single", choices=["single", "two", "two_signs"],
                     help="headline step: one fused forward+backward launch, or the forward "
                          "and backward launches")
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -336,6 +336,19 @@ def main():
                                               grad_student=grad, stream=stream)
 
     ce_lse = torch.empty_like(ce)
+    signs = torch.empty(BT, binding.fused_ce_tvd_signs_row_bytes(V, w.student.dtype), device=dev,
+                        dtype=torch.uint8)
+    sign_bytes = BT * signs.shape[1]
+
+    def fwd_signs():  # the forward that keeps sign words for its backward
+        binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, w.ignore_index, ce=ce,
+                                           tvd=tvd, student_lse=ls, teacher_lse=lt, sigma=sg,
+                                           signs=signs, stream=stream)
+
+    def bwd_signs():
+        binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, ls, lt, sg, signs,
+                                            w.grad_ce, w.grad_tvd, w.ignore_index,
+                                            grad_student=grad, stream=stream)
 
     def ce_fwd():  # the cross-entropy subset: student only
         binding.ce_forward(w.student, w.target, w.ignore_index, ce=ce, lse=ce_lse, stream=stream)
@@ -349,6 +362,10 @@ def main():
         "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
         "single": [("forward_backward", single, 3 * BT * V * elem)],
         "ce": [("ce_forward", ce_fwd, BT * V * elem), ("ce_backward", ce_bwd, 2 * BT * V * elem)],
+        # two launches with sign words: the backward reads the student and the
+        # bits (V/8 bytes per bf16 row) instead of the teacher
+        "two_signs": [("forward_signs", fwd_signs, 2 * BT * V * elem + sign_bytes),
+                      ("backward_signs", bwd_signs, 2 * BT * V * elem + sign_bytes)],
     }
 
     def time_path(name, K, sampler=None):
@@ -391,6 +408,7 @@ def main():
     other_name = "two" if args.path == "single" else "single"
     other = None
     ce_path = None
+    signs_path = None
     if not args.no_other:
         oms, okern = time_path(other_name, K)
         other = {"path": other_name, "ms_per_step": oms, "value": world * BT / (oms * 1e-3),
@@ -399,6 +417,9 @@ def main():
         cms, ckern = time_path("ce", K)
         ce_path = {"path": "ce", "ms_per_step": cms, "value": world * BT / (cms * 1e-3),
                    "unit": "tokens/s", "kernels": ckern}
+        sms_, skern = time_path("two_signs", K)
+        signs_path = {"path": "two_signs", "ms_per_step": sms_,
+                      "value": world * BT / (sms_ * 1e-3), "unit": "tokens/s", "kernels": skern}
 
     peaks = measured_peaks()
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -494,6 +515,7 @@ def main():
             "gpu_launches": len(paths[args.path]) * K,
             "other_path": other,
             "ce_path": ce_path,
+            "signs_path": signs_path,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary() if clocks else None,

@@ -2,8 +2,10 @@
 
 The shape of the PR #1384 analysis's LigerFusedCETVDFunction: the forward
 keeps only the O(BT) state (student_lse, teacher_lse, sigma) besides the
-inputs, and the backward recomputes p and q from it.  No (BT, V)
-intermediate is saved.
+inputs, and the backward recomputes p from it.  No (BT, V) intermediate of
+the logits' size is saved: the per-row wrapper keeps the sign of p - q as one
+bit per element (sign words), so its backward reads the student and those
+bits instead of the teacher, with the same gradient bit for bit.
 """
 from __future__ import annotations
 
@@ -22,22 +24,22 @@ class FusedCETVDFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, student, teacher, target, ignore_index=binding.IGNORE_INDEX, inplace=False):
-        ce, tvd, lse_s, lse_t, sigma = binding.fused_ce_tvd_forward(
+        ce, tvd, lse_s, lse_t, sigma, signs = binding.fused_ce_tvd_forward_signs(
             student.detach(), teacher.detach(), target, ignore_index)
-        ctx.save_for_backward(student, teacher, target, lse_s, lse_t, sigma)
+        ctx.save_for_backward(student, teacher, target, lse_s, lse_t, sigma, signs)
         ctx.ignore_index = ignore_index
         ctx.inplace = inplace
         return ce, tvd
 
     @staticmethod
     def backward(ctx, grad_ce, grad_tvd):
-        student, teacher, target, lse_s, lse_t, sigma = ctx.saved_tensors
+        student, teacher, target, lse_s, lse_t, sigma, signs = ctx.saved_tensors
         BT = student.shape[0]
         dev = student.device
         gce = torch.zeros(BT, device=dev) if grad_ce is None else grad_ce.float().contiguous()
         gtvd = torch.zeros(BT, device=dev) if grad_tvd is None else grad_tvd.float().contiguous()
-        grad = binding.fused_ce_tvd_backward(
-            student.detach(), teacher.detach(), target, lse_s, lse_t, sigma, gce, gtvd,
+        grad = binding.fused_ce_tvd_backward_signs(
+            student.detach(), teacher.detach(), target, lse_s, lse_t, sigma, signs, gce, gtvd,
             ctx.ignore_index, inplace=ctx.inplace)
         return grad, None, None, None, None
 

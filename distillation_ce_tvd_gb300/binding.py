@@ -23,6 +23,8 @@ _lock = threading.Lock()
 _lib = None
 
 EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
+           "fused_ce_tvd_signs_row_bytes", "fused_ce_tvd_forward_signs",
+           "fused_ce_tvd_backward_signs",
            "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fused_linear_ce_tvd_forward_backward_noalloc",
@@ -52,6 +54,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fused_ce_tvd_forward_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                                       vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
                                                       vp, vp]
+        lib.fused_ce_tvd_signs_row_bytes.argtypes = [i64, i32]
+        lib.fused_ce_tvd_signs_row_bytes.restype = i64
+        lib.fused_ce_tvd_forward_signs.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                                   vp, vp, vp, vp, vp, vp, i64, vp, vp]
+        lib.fused_ce_tvd_forward_signs.restype = i32
+        lib.fused_ce_tvd_backward_signs.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                                    vp, vp, vp, vp, i64, vp, vp, i64, vp, i64,
+                                                    vp, vp]
+        lib.fused_ce_tvd_backward_signs.restype = i32
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
         dbl = ctypes.c_double
@@ -245,6 +256,84 @@ def fused_ce_tvd_forward_backward(student, teacher, target, grad_ce, grad_tvd,
         _ptr(dev_status), _stream(stream))
     _check(rc, "fused_ce_tvd_forward_backward")
     return (*outs, grad_student)
+
+
+def fused_ce_tvd_signs_row_bytes(V: int, dtype) -> int:
+    """Minimum row stride, in bytes, of the sign words for V logits of ``dtype``."""
+    code = {torch.float32: FCT_F32, torch.bfloat16: FCT_BF16}[dtype]
+    return int(load().fused_ce_tvd_signs_row_bytes(int(V), code))
+
+
+def _signs(x, BT, V, dtype, device):
+    if x is None:
+        return torch.empty(BT, fused_ce_tvd_signs_row_bytes(V, dtype), device=device,
+                           dtype=torch.uint8)
+    if not x.is_cuda or x.dtype != torch.uint8 or x.dim() != 2 or x.shape[0] != BT or \
+            (BT > 1 and x.stride(1) != 1):
+        raise ValueError(f"signs must be a (BT, >= row bytes) uint8 CUDA tensor with unit "
+                         f"column stride")
+    return x
+
+
+def fused_ce_tvd_forward_signs(student, teacher, target, ignore_index=IGNORE_INDEX, *, ce=None,
+                               tvd=None, student_lse=None, teacher_lse=None, sigma=None,
+                               signs=None, dev_status=None, stream=None):
+    """fused_ce_tvd_forward that also stores the sign words its backward reads
+    instead of the teacher.  Returns (ce, tvd, student_lse, teacher_lse, sigma,
+    signs), signs a (BT, row bytes) uint8 tensor."""
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    BT, V = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                                             (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
+    signs = _signs(signs, BT, V, student.dtype, dev)
+    ld_b = int(signs.stride(0)) if BT > 1 else int(signs.shape[1])
+    rc = load().fused_ce_tvd_forward_signs(_ptr(student), ld_s, _ptr(teacher), ld_t, code,
+                                           _ptr(target), BT, V, int(ignore_index),
+                                           *map(_ptr, outs), _ptr(signs), ld_b,
+                                           _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_ce_tvd_forward_signs")
+    return (*outs, signs)
+
+
+def fused_ce_tvd_backward_signs(student, teacher, target, student_lse, teacher_lse, sigma, signs,
+                                grad_ce, grad_tvd, ignore_index=IGNORE_INDEX, *,
+                                grad_student=None, inplace=False, dev_status=None, stream=None):
+    """fused_ce_tvd_backward reading the forward's sign words instead of the
+    teacher (which rows with a tie still need); bit-identical gradient."""
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    BT, V = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    for x, n in ((student_lse, "student_lse"), (teacher_lse, "teacher_lse"), (sigma, "sigma")):
+        _rows(x, BT, n)
+    signs = _signs(signs, BT, V, student.dtype, dev)
+    ld_b = int(signs.stride(0)) if BT > 1 else int(signs.shape[1])
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    stride = max(stride_ce, stride_tvd)
+    if inplace:
+        grad_student = student
+    elif grad_student is None:
+        grad_student = torch.empty_like(student)
+    code_g, ld_g = _logits(grad_student, "grad_student")
+    if code_g != code or grad_student.shape != student.shape:
+        raise ValueError("grad_student must match the student's shape and dtype")
+    rc = load().fused_ce_tvd_backward_signs(
+        _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V, int(ignore_index),
+        _ptr(student_lse), _ptr(teacher_lse), _ptr(sigma), _ptr(signs), ld_b, _ptr(gce),
+        _ptr(gtvd), stride, _ptr(grad_student), ld_g, _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_ce_tvd_backward_signs")
+    return grad_student
 
 
 def ce_forward(logits, target, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,

@@ -71,6 +71,13 @@ int check_logits(const void* x, int64_t ld, int dtype, int64_t V) {
   return FCT_OK;
 }
 
+// Sign words of one row: a uint32 tie flag, then one byte per 16-byte vector
+// (the row's ragged tail has none), padded to a multiple of 4 bytes.
+int64_t signs_row_bytes(int64_t V, int dtype) {
+  const int64_t nvec = V / (16 / static_cast<int64_t>(elem_size(dtype)));
+  return 4 + (nvec + 3) / 4 * 4;
+}
+
 bool vec_ok(const void* x, int64_t ld, int dtype) {
   return aligned(x, 16) && ((ld * static_cast<int64_t>(elem_size(dtype))) % 16) == 0;
 }
@@ -122,8 +129,10 @@ fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, b
 int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t ld_t,
                  int dtype, const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
                  float* ce, float* tvd, float* lse_s, float* lse_t, float* sigma,
-                 int32_t* dev_status, void* stream) {
+                 int32_t* dev_status, void* stream, uint8_t* signs = nullptr,
+                 int64_t ld_signs = 0) {
   const bool fused = (tvd != nullptr);
+  if (signs != nullptr && !fused) return FCT_ERR_INVALID_ARG;
   if (BT < 0) return FCT_ERR_INVALID_ARG;
   if (BT == 0) return FCT_OK;
   int rc = check_common(dtype, target, BT, V);
@@ -148,6 +157,16 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
     for (int j = i + 1; j < n_out; ++j)
       if (overlap(r, vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
   }
+  const int64_t sb = signs_row_bytes(V, dtype);
+  if (signs != nullptr) {
+    if (!aligned(signs, 4) || ld_signs % 4 != 0) return FCT_ERR_ALIGNMENT;
+    if (ld_signs < sb) return FCT_ERR_INVALID_ARG;
+    const Range r = mat_range(signs, BT, ld_signs, sb, 1);
+    for (int j = 0; j < 3; ++j)
+      if (overlap(r, ins[j])) return FCT_ERR_INVALID_ARG;
+    for (int i = 0; i < n_out; ++i)
+      if (overlap(r, vec_range(outs[i], BT, 4))) return FCT_ERR_INVALID_ARG;
+  }
 
   DeviceInfo d;
   if ((rc = current_device(&d)) != FCT_OK) return rc;
@@ -156,8 +175,20 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
                  ce, tvd, lse_s, lse_t, sigma, dev_status, nullptr, 0, nullptr, nullptr, 0, 0};
   const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec);
   a.keep_normal = plan.keep_normal ? 1 : 0;
-  if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return FCT_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (signs != nullptr) {
+    if (vec) {
+      a.signs = signs;
+      a.ld_signs = ld_signs;
+    } else if (cudaMemset2DAsync(signs, static_cast<size_t>(ld_signs), 0x01, 4,
+                                 static_cast<size_t>(BT), st) != cudaSuccess) {
+      // unaligned rows have no sign words: every row's tie flag is set, so
+      // the backward recomputes the signs from the teacher
+      cudaGetLastError();
+      return FCT_ERR_CUDA;
+    }
+  }
+  if (fct::launch_forward(a, plan, st) != cudaSuccess) return FCT_ERR_CUDA;
   return FCT_OK;
 }
 
@@ -165,8 +196,10 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
                   int dtype, const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
                   const float* lse_s, const float* lse_t, const float* sigma,
                   const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
-                  void* grad, int64_t ld_g, int32_t* dev_status, void* stream) {
+                  void* grad, int64_t ld_g, int32_t* dev_status, void* stream,
+                  const uint8_t* signs = nullptr, int64_t ld_signs = 0) {
   const bool fused = (teacher != nullptr) || (lse_t != nullptr);
+  if (signs != nullptr && !fused) return FCT_ERR_INVALID_ARG;
   if (BT < 0) return FCT_ERR_INVALID_ARG;
   if (BT == 0) return FCT_OK;
   int rc = check_common(dtype, target, BT, V);
@@ -193,6 +226,12 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
     const int64_t n = (i == 1 || i == 4) ? (grad_stride ? BT : 1) : BT;
     if (overlap(g, vec_range(rows[i], n, 4))) return FCT_ERR_INVALID_ARG;
   }
+  if (signs != nullptr) {
+    if (!aligned(signs, 4) || ld_signs % 4 != 0) return FCT_ERR_ALIGNMENT;
+    if (ld_signs < signs_row_bytes(V, dtype)) return FCT_ERR_INVALID_ARG;
+    if (overlap(g, mat_range(signs, BT, ld_signs, signs_row_bytes(V, dtype), 1)))
+      return FCT_ERR_INVALID_ARG;
+  }
 
   DeviceInfo d;
   if ((rc = current_device(&d)) != FCT_OK) return rc;
@@ -201,6 +240,10 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
   fct::BwdArgs a{student, fused ? teacher : nullptr, ld_s, ld_t, dtype, target, BT, V,
                  ignore_index, lse_s, lse_t, sigma, grad_ce, grad_tvd, grad_stride,
                  grad, ld_g, dev_status};
+  if (signs != nullptr && vec) {  // without the vector path the signs are recomputed
+    a.signs = signs;
+    a.ld_signs = ld_signs;
+  }
   if (fct::launch_backward(a, vec, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
@@ -413,6 +456,41 @@ int fused_ce_tvd_backward(const void* student, int64_t ld_student, const void* t
   return backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
                        ignore_index, student_lse, teacher_lse, sigma, grad_ce, grad_tvd,
                        grad_stride, grad_student, ld_grad, dev_status, stream);
+}
+
+int64_t fused_ce_tvd_signs_row_bytes(int64_t V, fct_dtype dtype) {
+  if (V <= 0 || (dtype != FCT_F32 && dtype != FCT_BF16)) return 0;
+  return signs_row_bytes(V, dtype);
+}
+
+int fused_ce_tvd_forward_signs(const void* student, int64_t ld_student, const void* teacher,
+                               int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                               int64_t BT, int64_t V, int64_t ignore_index, float* ce, float* tvd,
+                               float* student_lse, float* teacher_lse, float* sigma,
+                               uint8_t* signs, int64_t ld_signs, int32_t* dev_status,
+                               void* stream) {
+  if (teacher == nullptr || tvd == nullptr || teacher_lse == nullptr || sigma == nullptr ||
+      signs == nullptr)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  return forward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                      ignore_index, ce, tvd, student_lse, teacher_lse, sigma, dev_status, stream,
+                      signs, ld_signs);
+}
+
+int fused_ce_tvd_backward_signs(const void* student, int64_t ld_student, const void* teacher,
+                                int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                                int64_t BT, int64_t V, int64_t ignore_index,
+                                const float* student_lse, const float* teacher_lse,
+                                const float* sigma, const uint8_t* signs, int64_t ld_signs,
+                                const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
+                                void* grad_student, int64_t ld_grad, int32_t* dev_status,
+                                void* stream) {
+  if (teacher == nullptr || teacher_lse == nullptr || sigma == nullptr || grad_tvd == nullptr ||
+      signs == nullptr)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  return backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                       ignore_index, student_lse, teacher_lse, sigma, grad_ce, grad_tvd,
+                       grad_stride, grad_student, ld_grad, dev_status, stream, signs, ld_signs);
 }
 
 int ce_forward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target, int64_t BT,

@@ -27,15 +27,23 @@ constexpr int kThreads = 256;
 // Vectors per thread per unit, all loaded before any is used: 4 per tensor for
 // the fused loss (student + teacher), 8 for cross-entropy alone, so both keep
 // about the same bytes in flight.
-template <bool kTvd>
-constexpr int kUnrollOf = kTvd ? 4 : 8;
-template <bool kTvd>
-constexpr int64_t kSegOf = int64_t(kThreads) * kUnrollOf<kTvd>;  // vectors per unit
+// (Also 8 when the signs come from the forward's sign words: the teacher is
+// then read only for rows with a tie.)
+template <bool kTwo>
+constexpr int kUnrollOf = kTwo ? 4 : 8;
+template <bool kTwo>
+constexpr int64_t kSegOf = int64_t(kThreads) * kUnrollOf<kTwo>;  // vectors per unit
 
-template <typename T, int VE, bool kTvd>
+// kSigns: the sign of p - q comes from the forward's sign words (a byte of
+// bits per vector) for rows whose tie flag is clear; the coefficient of p is
+// then fmaf(h, +-1, c0), the very values the sign expression gives, so the
+// gradient is bit-identical.  Rows with a tie, and the ragged tail, recompute
+// the sign from the teacher.
+template <typename T, int VE, bool kTvd, bool kSigns = false>
 __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
-  constexpr int kUnroll = kUnrollOf<kTvd>;
-  constexpr int64_t kSeg = kSegOf<kTvd>;
+  static_assert(!kSigns || (kTvd && VE > 1), "sign words cover the fused loss's vectors");
+  constexpr int kUnroll = kUnrollOf<kTvd && !kSigns>;
+  constexpr int64_t kSeg = kSegOf<kTvd && !kSigns>;
   const T* S = static_cast<const T*>(a.student);
   const T* Tt = static_cast<const T*>(a.teacher);
   T* G = static_cast<T*>(a.grad);
@@ -98,7 +106,54 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
     };
 
     int64_t i = v0 + threadIdx.x;
-    if (i + (kUnroll - 1) * kThreads < v1) {  // full unit: all loads first
+    bool from_bits = false;
+    const uint8_t* brow = nullptr;
+    if constexpr (kSigns) {
+      brow = a.signs + row * a.ld_signs;
+      from_bits = (*reinterpret_cast<const uint32_t*>(brow) == 0u);
+    }
+    if (kSigns && from_bits) {
+      const float c_plus = fmaf(h, 1.f, c0), c_minus = fmaf(h, -1.f, c0);
+      auto grad_bits = [&](const float (&xs)[VE], uint32_t bits, int64_t base, float (&g)[VE]) {
+#pragma unroll
+        for (int j = 0; j < VE; ++j) {
+          const float p = ex2(fmaf(xs[j], kLog2e, ns2));
+          g[j] = p * (((bits >> (VE - 1 - j)) & 1u) ? c_minus : c_plus);
+        }
+        const int64_t off = tg - base;
+        if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+#pragma unroll
+          for (int j = 0; j < VE; ++j)
+            if (j == off) g[j] -= gce;
+        }
+      };
+      const uint8_t* bits = brow + 4;
+      if (i + (kUnroll - 1) * kThreads < v1) {
+        uint4 rs[kUnroll];
+        uint32_t sb[kUnroll];
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          rs[k] = load_raw<T, VE>(srow + (i + k * kThreads) * VE, drop);
+          sb[k] = bits[i + k * kThreads];
+        }
+#pragma unroll
+        for (int k = 0; k < kUnroll; ++k) {
+          float xs[VE], g[VE];
+          unpack_raw<T, VE>(rs[k], xs);
+          grad_bits(xs, sb[k], (i + k * kThreads) * VE, g);
+          store_vec<T, VE>(grow + (i + k * kThreads) * VE, g, drop);
+        }
+      } else {
+        for (; i < v1; i += kThreads) {
+          float xs[VE], g[VE];
+          unpack_raw<T, VE>(load_raw<T, VE>(srow + i * VE, drop), xs);
+          grad_bits(xs, bits[i], i * VE, g);
+          store_vec<T, VE>(grow + i * VE, g, drop);
+        }
+      }
+    } else if (!kSigns && i + (kUnroll - 1) * kThreads < v1) {  // full unit: all loads first
+      // (with sign words only rows with a tie come here: the plain loop below
+      // serves them and keeps the register count of the common case down)
       uint4 rs[kUnroll], rt[kUnroll];
 #pragma unroll
       for (int k = 0; k < kUnroll; ++k) {
@@ -137,11 +192,12 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
   }
 }
 
-template <typename T, int VE, bool kTvd>
+template <typename T, int VE, bool kTvd, bool kSigns>
 int blocks_per_sm() {
   static int cached = [] {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, backward_kernel<T, VE, kTvd>, kThreads, 0) !=
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, backward_kernel<T, VE, kTvd, kSigns>,
+                                                      kThreads, 0) !=
         cudaSuccess) {
       cudaGetLastError();
       n = 1;
@@ -151,15 +207,15 @@ int blocks_per_sm() {
   return cached;
 }
 
-template <typename T, int VE, bool kTvd>
+template <typename T, int VE, bool kTvd, bool kSigns = false>
 cudaError_t go(const BwdArgs& a, int sms, cudaStream_t st) {
-  constexpr int64_t kSeg = kSegOf<kTvd>;
+  constexpr int64_t kSeg = kSegOf<kTvd && !kSigns>;
   const int64_t nvec = a.V / VE;
   const int64_t nseg = nvec > 0 ? (nvec + kSeg - 1) / kSeg : 1;
   const int64_t units = a.BT * nseg;
-  int64_t grid = int64_t(sms) * blocks_per_sm<T, VE, kTvd>();
+  int64_t grid = int64_t(sms) * blocks_per_sm<T, VE, kTvd, kSigns>();
   if (grid > units) grid = units;
-  backward_kernel<T, VE, kTvd><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
+  backward_kernel<T, VE, kTvd, kSigns><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -167,6 +223,11 @@ cudaError_t go(const BwdArgs& a, int sms, cudaStream_t st) {
 
 cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st) {
   const bool tvd = a.teacher != nullptr;
+  if (a.signs) {  // sign words: vector path of the fused loss only
+    if (!vec || !tvd) return cudaErrorInvalidValue;
+    return a.dtype == FCT_BF16 ? go<bf16_t, 8, true, true>(a, sms, st)
+                               : go<float, 4, true, true>(a, sms, st);
+  }
   if (a.dtype == FCT_BF16) {
     if (tvd) return vec ? go<bf16_t, 8, true>(a, sms, st) : go<bf16_t, 1, true>(a, sms, st);
     return vec ? go<bf16_t, 8, false>(a, sms, st) : go<bf16_t, 1, false>(a, sms, st);

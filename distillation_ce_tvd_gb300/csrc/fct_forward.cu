@@ -378,10 +378,14 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
 }
 
 // TG: element type of the gradient written by the single launch (the logits'
-// type, or bf16 for fp32 logits).
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG = T>
+// type, or bf16 for fp32 logits).  kSigns: the forward alone also stores each
+// element's sign bit and a per-row tie flag for the backward (sign words).
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG = T,
+          bool kSigns = false>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
+  static_assert(!kSigns || (kTvd && !kGrad), "sign words come from the forward alone");
+  constexpr bool kBits = kGrad || kSigns;  // step 2 builds sign words
   using F = Feed<T, VE, kTvd, kGrad, NT>;
   extern __shared__ __align__(16) uint4 ring_mem[];
   __shared__ float4 red_lse[kMaxWarps];
@@ -449,6 +453,13 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
     }
     const T* srow = S + row * p.ld_s;
     const T* trow = kTvd ? Tt + row * p.ld_t : nullptr;
+    // The row's tie flag starts clear; threads that meet a tie set it after
+    // step 2 (past the CTA / cluster barriers that follow this store).
+    uint32_t* tie_flag = nullptr;
+    if constexpr (kSigns) {
+      tie_flag = reinterpret_cast<uint32_t*>(p.signs + row * p.ld_signs);
+      if (rank == 0 && tid == 0) *tie_flag = 0u;
+    }
     // Read before any gradient of this row can overwrite it (in place).
     const float s_tg =
         (rank == 0 && tid == 0 && tg >= 0 && tg < p.V) ? Elem<T>::load1(srow + tg) : 0.f;
@@ -542,7 +553,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
 #pragma unroll
                                           for (int j = 0; j < VE; j += 2) {
                                             const float2 sg = tvd_two(xs[j], xs[j + 1], xt[j], xt[j + 1]);
-                                            if constexpr (kGrad) {
+                                            if constexpr (kBits) {
                                               const uint32_t b0 = __float_as_uint(sg.x);
                                               const uint32_t b1 = __float_as_uint(sg.y);
                                               word = __funnelshift_l(b1, __funnelshift_l(b0, word, 1), 1);
@@ -551,14 +562,28 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
                                           }
                                         }
                                       }
+                                      if constexpr (kBits) {
+                                        // a short step's bits move up to the full step's positions
+                                        if (int(n) < kPerStep) word <<= (kPerStep - int(n)) * VE;
+                                      }
                                       if constexpr (kGrad) {
-                                        if (use_bits) {
-                                          // a short step's bits move up to the full step's positions
-                                          if (int(n) < kPerStep) word <<= (kPerStep - int(n)) * VE;
-                                          sbits[(k0 / kPerStep) * NT + tid] = word;
-                                        }
+                                        if (use_bits) sbits[(k0 / kPerStep) * NT + tid] = word;
+                                      }
+                                      if constexpr (kSigns) {
+                                        // one byte per vector: its VE bits, element j at bit VE-1-j
+                                        uint8_t* dst = p.signs + row * p.ld_signs + 4 + vb + tid +
+                                                       int64_t(k0) * NT;
+#pragma unroll
+                                        for (int u = 0; u < kPerStep; ++u)
+                                          if (u < int(n))
+                                            dst[u * NT] = static_cast<uint8_t>(
+                                                (word >> (kPerStep * VE - VE * (u + 1))) &
+                                                ((1u << VE) - 1u));
                                       }
                                     });
+      if constexpr (kSigns) {
+        if ((tie_and & 0x3f800000u) != 0x3f800000u) atomicOr(tie_flag, 1u);
+      }
       sig_p = sp2.x + sp2.y;
       sig_q = sq2.x + sq2.y;
       if (owns_tail && tail0 + tid < p.V)
@@ -786,11 +811,11 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per process.
-template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG>
+template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG, bool kSigns>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
                            (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
-  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG>;
+  auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG, kSigns>;
   static int n_max = [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
@@ -816,7 +841,7 @@ cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
   return launch_cluster(kernel, C, kScalarThreads, 0, n, a, st);
 }
 
-template <typename T, int C, bool kTvd, bool kGrad, typename TG>
+template <typename T, int C, bool kTvd, bool kGrad, typename TG, bool kSigns>
 cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr int VE = Elem<T>::kVec;
   if constexpr (kGrad) {
@@ -824,22 +849,27 @@ cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   } else {
     if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
   }
-  return run_pipelined<T, VE, C, kTvd, kGrad, 512, TG>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, kGrad, 512, TG, kSigns>(a, plan.slots, st);
 }
 
-template <typename T, bool kTvd, bool kGrad, typename TG = T>
+template <typename T, bool kTvd, bool kGrad, typename TG = T, bool kSigns = false>
 cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   switch (plan.cluster) {
-    case 1: return run<T, 1, kTvd, kGrad, TG>(a, plan, st);
-    case 2: return run<T, 2, kTvd, kGrad, TG>(a, plan, st);
-    case 4: return run<T, 4, kTvd, kGrad, TG>(a, plan, st);
-    default: return run<T, 8, kTvd, kGrad, TG>(a, plan, st);
+    case 1: return run<T, 1, kTvd, kGrad, TG, kSigns>(a, plan, st);
+    case 2: return run<T, 2, kTvd, kGrad, TG, kSigns>(a, plan, st);
+    case 4: return run<T, 4, kTvd, kGrad, TG, kSigns>(a, plan, st);
+    default: return run<T, 8, kTvd, kGrad, TG, kSigns>(a, plan, st);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  if (a.signs) {  // the forward alone with sign words (vector path only)
+    if (!plan.vec || !a.tvd || a.grad) return cudaErrorInvalidValue;
+    return a.dtype == FCT_BF16 ? run_c<bf16_t, true, false, bf16_t, true>(a, plan, st)
+                               : run_c<float, true, false, float, true>(a, plan, st);
+  }
   if (a.dtype == FCT_BF16) {
     if (a.grad) return run_c<bf16_t, true, true>(a, plan, st);
     return a.tvd ? run_c<bf16_t, true, false>(a, plan, st) : run_c<bf16_t, false, false>(a, plan, st);

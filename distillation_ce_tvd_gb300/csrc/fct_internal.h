@@ -29,6 +29,10 @@ struct FwdArgs {
   int64_t grad_stride;
   int keep_normal;  // 1: evict_normal instead of evict_last while a row must stay in L2
   int grad_bf16 = 0;  // single launch on fp32 logits: write the gradient as bf16
+  // forward alone: per row, a uint32 tie flag then one byte of sign bits per
+  // 16-byte vector (nullptr: none)
+  uint8_t* signs = nullptr;
+  int64_t ld_signs = 0;
 };
 
 struct FwdPlan {
@@ -54,6 +58,9 @@ struct BwdArgs {
   void* grad;
   int64_t ld_g;
   int32_t* dev_status;
+  // the forward's sign words (see FwdArgs::signs), or nullptr
+  const uint8_t* signs = nullptr;
+  int64_t ld_signs = 0;
 };
 
 struct LossArgs {

@@ -114,6 +114,51 @@ int fused_ce_tvd_backward(const void* student, int64_t ld_student,
                           int32_t* dev_status, void* stream);
 
 /*
+ * Forward and backward with sign words.  The "Backward Pass" reloads student
+ * and teacher to recompute p, q and sign(p - q).  These two calls let the
+ * forward keep the one piece of the teacher the backward needs, the sign of
+ * p_v - q_v, as one bit per element, so the backward reads the student and
+ * the bits (about V/8 bytes per row) instead of the teacher.  At 8192 x
+ * 151936 bf16 that is 5.1 GB of backward traffic instead of 7.5 GB.  The
+ * outputs are bit-identical to fused_ce_tvd_forward / fused_ce_tvd_backward.
+ *
+ *   signs    : (BT, ld_signs) bytes, written by the forward and read by the
+ *              backward.  Per row: a uint32 tie flag, then one byte of sign
+ *              bits per 16-byte vector of the row (element j of the vector at
+ *              bit VEC-1-j, 1 where p < q).  ld_signs >=
+ *              fused_ce_tvd_signs_row_bytes(V, dtype) and a multiple of 4;
+ *              4-byte aligned.
+ *   teacher  : still required by the backward.  A row with an exact tie
+ *              (sign 0 somewhere), and the ragged tail of every row (V not a
+ *              multiple of the vector), recompute their signs from it, and
+ *              so does a whole call whose rows are not 16-byte aligned (the
+ *              forward then sets every row's tie flag).
+ * All other arguments are as for fused_ce_tvd_forward / fused_ce_tvd_backward.
+ */
+int64_t fused_ce_tvd_signs_row_bytes(int64_t V, fct_dtype dtype);
+
+int fused_ce_tvd_forward_signs(const void* student, int64_t ld_student,
+                               const void* teacher, int64_t ld_teacher,
+                               fct_dtype dtype, const int64_t* target,
+                               int64_t BT, int64_t V, int64_t ignore_index,
+                               float* ce, float* tvd, float* student_lse,
+                               float* teacher_lse, float* sigma,
+                               uint8_t* signs, int64_t ld_signs,
+                               int32_t* dev_status, void* stream);
+
+int fused_ce_tvd_backward_signs(const void* student, int64_t ld_student,
+                                const void* teacher, int64_t ld_teacher,
+                                fct_dtype dtype, const int64_t* target,
+                                int64_t BT, int64_t V, int64_t ignore_index,
+                                const float* student_lse,
+                                const float* teacher_lse, const float* sigma,
+                                const uint8_t* signs, int64_t ld_signs,
+                                const float* grad_ce, const float* grad_tvd,
+                                int64_t grad_stride, void* grad_student,
+                                int64_t ld_grad, int32_t* dev_status,
+                                void* stream);
+
+/*
  * Forward and backward in ONE launch, for callers that know the upstream
  * gradients before the forward (for instance a mean over tokens, whose
  * per-row gradients are constants).  Writes everything

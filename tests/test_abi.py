@@ -121,6 +121,45 @@ def test_backward_argument_checks(lib):
     assert bwd(lib, lt=None) == INVALID
 
 
+def test_sign_words_row_bytes_and_argument_checks(lib):
+    # a uint32 tie flag, then one byte per 16-byte vector, padded to 4 bytes
+    assert lib.fused_ce_tvd_signs_row_bytes(151936, 1) == 4 + 18992
+    assert lib.fused_ce_tvd_signs_row_bytes(151937, 1) == 4 + 18992
+    assert lib.fused_ce_tvd_signs_row_bytes(10, 0) == 4 + 4     # 2 fp32 vectors, padded
+    assert lib.fused_ce_tvd_signs_row_bytes(7, 1) == 4          # no full bf16 vector
+    assert lib.fused_ce_tvd_signs_row_bytes(0, 1) == 0
+    assert lib.fused_ce_tvd_signs_row_bytes(100, 5) == 0
+    sb = FAKE + (6 << 30)
+
+    def fs(**kw):
+        a = dict(signs=sb, ld=112, BT=4)
+        a.update(kw)
+        base = FAKE + (3 << 30)
+        return lib.fused_ce_tvd_forward_signs(FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30),
+                                              a["BT"], 100, -100, base, base + 4096, base + 8192,
+                                              base + 12288, base + 16384, a["signs"], a["ld"],
+                                              None, None)
+
+    def bs(**kw):
+        a = dict(signs=sb, ld=112, BT=4)
+        a.update(kw)
+        base = FAKE + (4 << 30)
+        return lib.fused_ce_tvd_backward_signs(FAKE, 128, FAKE + (1 << 30), 128, 1,
+                                               FAKE + (2 << 30), a["BT"], 100, -100, base,
+                                               base + 4096, base + 8192, a["signs"], a["ld"],
+                                               base + 12288, base + 16384, 1, FAKE + (5 << 30),
+                                               128, None, None)
+
+    for f in (fs, bs):
+        assert f(BT=0) == OK
+        assert f(signs=None) == INVALID
+        assert f(ld=4 + 8) == INVALID              # V = 100 bf16 needs 4 + 12 -> 16 bytes
+        assert f(ld=18) == ALIGN                    # a multiple of 4
+        assert f(signs=sb + 2) == ALIGN
+    assert fs(signs=FAKE + 64) == INVALID          # sign words over the student
+    assert bs(signs=FAKE + (5 << 30) + 8) == INVALID  # sign words under the gradient
+
+
 def test_ce_argument_checks(lib):
     assert lib.ce_forward(FAKE, 128, 1, FAKE + (2 << 30), 0, 100, -100, None, None, None, None) == OK
     assert lib.ce_forward(FAKE, 128, 1, FAKE + (2 << 30), 4, 100, -100, None,

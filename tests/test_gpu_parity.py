@@ -300,6 +300,54 @@ def test_autograd_wrapper_matches_direct_calls():
     assert torch.equal(s.grad, grad)
 
 
+# ------------------------------------------------------------------ sign words
+
+@pytest.mark.parametrize("dtype,V,ld,cluster", [
+    (torch.bfloat16, 151936, None, 0),
+    (torch.bfloat16, 20003, 20008, 2),     # ragged tail, aligned rows, 2-CTA clusters
+    (torch.float32, 9001, 9004, 8),        # ragged tail, 8-CTA clusters
+    (torch.float32, 32000, None, 0),
+    (torch.bfloat16, 3003, None, 0),       # unaligned rows: flags set, signs recomputed
+])
+def test_sign_words_match_plain_forward_and_backward(dtype, V, ld, cluster):
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=12, V=V, dtype=dtype, seed=35)
+    if ld is not None:
+        w = padded(w, ld, 0)
+    w.teacher[2] = w.student[2]                                   # every element ties
+    w.teacher[3] = (w.student[3].float() + 1.0).to(dtype)         # near ties
+    w.target[5] = w.ignore_index
+    w.target[7] = V + 3                                           # out of range
+    prev = binding.set_forward_cluster(cluster)
+    try:
+        st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+        st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+        f1 = binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, dev_status=st1)
+        g1 = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, *f1[2:], w.grad_ce,
+                                           w.grad_tvd, dev_status=st1)
+        f2 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, dev_status=st2)
+        signs = f2[5]
+        g2 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f2[2:5], signs,
+                                                 w.grad_ce, w.grad_tvd, dev_status=st2)
+        s_in = same_layout_clone(w.student)
+        g3 = binding.fused_ce_tvd_backward_signs(s_in, w.teacher, w.target, *f2[2:5], signs,
+                                                 w.grad_ce, w.grad_tvd, inplace=True)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_forward_cluster(prev)
+    assert st1.item() == st2.item() == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+
+    def bits(x):  # compare bit patterns: the out-of-range row holds NaN
+        x = x.contiguous()
+        return x.view(torch.int32 if x.element_size() == 4 else torch.int16)
+
+    for a, b in zip(f1, f2[:5]):
+        assert torch.equal(bits(a), bits(b))
+    assert torch.equal(bits(g1), bits(g2))
+    assert torch.equal(bits(g1), bits(g3))
+    flags = signs[:, :4].contiguous().view(torch.int32)[:, 0]
+    assert flags[2].item() != 0               # the tied row falls back to the teacher
+
+
 # ------------------------------------------------------------------ single launch
 
 def run_single(w, cluster=0, inplace=False, grads=None):
