@@ -16,6 +16,8 @@
 // yield 0 at ties, so the inner loop is two ex2, two compares, one subtract
 // and two FMAs/multiplies.  Each element is read and then written by the
 // same thread, which makes grad_student == student (in place) safe.
+#include <mutex>
+
 #include "fct_common.cuh"
 #include "fct_internal.h"
 
@@ -192,19 +194,27 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
   }
 }
 
+// Resident CTAs per SM of one backward configuration, queried once per device.
 template <typename T, int VE, bool kTvd, bool kSigns>
 int blocks_per_sm() {
-  static int cached = [] {
+  static std::mutex mu;
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (cached[dev] == 0) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, backward_kernel<T, VE, kTvd, kSigns>,
-                                                      kThreads, 0) !=
-        cudaSuccess) {
+                                                      kThreads, 0) != cudaSuccess) {
       cudaGetLastError();
       n = 1;
     }
-    return n > 0 ? n : 1;
-  }();
-  return cached;
+    cached[dev] = n > 0 ? n : 1;
+  }
+  return cached[dev];
 }
 
 template <typename T, int VE, bool kTvd, bool kSigns = false>

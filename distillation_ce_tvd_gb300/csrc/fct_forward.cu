@@ -41,6 +41,8 @@
 //     tvd = sigma = 0 exactly.
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "fct_common.cuh"
 #include "fct_internal.h"
 
@@ -809,21 +811,46 @@ int max_clusters(K kernel, int C, int nt, size_t smem) {
   return n > 0 ? n : 1;
 }
 
+// One-time set-up of a kernel configuration on each device: the shared-memory
+// opt-in is a per-device property of the function, and the occupancy query
+// is answered for the current device.
+struct PerDevice {
+  std::mutex mu;
+  int value[64];
+  bool done[64] = {};
+};
+
+template <class Init>
+int per_device(PerDevice& c, Init&& init) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> lk(c.mu);
+  if (!c.done[dev]) {
+    c.value[dev] = init();
+    c.done[dev] = true;
+  }
+  return c.value[dev];
+}
+
 // One (kernel, configuration) instance: shared-memory opt-in and the
-// occupancy query are done once per process.
+// occupancy query are done once per device.
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG, bool kSigns>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
                            (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
   auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG, kSigns>;
-  static int n_max = [&] {
+  static PerDevice cache;
+  const int n_max = per_device(cache, [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kSmem)) != cudaSuccess) {
       cudaGetLastError();
       return -1;
     }
     return max_clusters(kernel, C, NT, kSmem);
-  }();
+  });
   if (n_max < 0) return cudaErrorInvalidConfiguration;
   int n = n_max;
   if (n_slots > 0 && n > n_slots) n = n_slots;
@@ -834,7 +861,9 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
 template <typename T, int C, bool kTvd>
 cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
   auto kernel = forward_scalar<T, C, kTvd>;
-  static int n_max = max_clusters(kernel, C, kScalarThreads, 0);
+  static PerDevice cache;
+  const int n_max = per_device(cache, [&] { return max_clusters(kernel, C, kScalarThreads, 0); });
+  if (n_max < 0) return cudaErrorInvalidDevice;
   int n = n_max;
   if (n_slots > 0 && n > n_slots) n = n_slots;
   if (n > a.BT) n = static_cast<int>(a.BT);
