@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -51,10 +52,16 @@ KERNEL_SOURCES = ["fct_common.cuh", "fct_forward.cu", "fct_backward.cu"]
 # ---------------------------------------------------------------- helpers
 
 def kernel_source_hash() -> str:
+    """Hash of the kernels' code: comments and blank lines are left out, so a
+    measured traffic figure stays attached to the code it was measured on."""
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "distillation_ce_tvd_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "distillation_ce_tvd_gb300", "csrc", f)) as fh:
+            text = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        for line in text.splitlines():
+            code = re.sub(r"//.*$", "", line).strip()
+            if code:
+                h.update(code.encode() + b"\n")
     return h.hexdigest()[:16]
 
 

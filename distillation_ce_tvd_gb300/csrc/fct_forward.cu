@@ -7,9 +7,11 @@
 // 0.5*sum|p - q| and sigma = sum p*sign(p - q), then five per-row stores.
 //
 // GB300 mapping
-//   * A row is owned by a thread-block cluster of C CTAs (C in {1,2,4,8});
-//     each CTA streams a contiguous 1/C of the row's 16-byte vectors.  The
-//     CTAs exchange only scalar partials, through distributed shared memory.
+//   * A row is owned by one CTA of 512 threads or, when the rows in flight
+//     would not fit L2 that way, by a thread-block cluster of C CTAs
+//     (C in {2,4,8}); each CTA streams a contiguous 1/C of the row's 16-byte
+//     vectors.  The CTAs exchange only scalar partials, through distributed
+//     shared memory.
 //   * Step 1 reads the row from HBM with an L2 evict_last hint; step 2
 //     re-reads the same bytes, which are still in L2 because the number of
 //     rows in flight (clusters on the GPU) times the row size is kept under
@@ -17,10 +19,10 @@
 //     (BT, V) buffer is ever written.
 //   * Every thread streams its own vectors through a private ring in shared
 //     memory (kStages steps of kPerStep 16-byte vectors per tensor), filled
-//     by cp.async one step ahead of the step being read.  The feed runs on across the step-1/step-2
-//     boundary and into the next row, so loads stay in flight while the CTA
-//     reduces; no thread ever reads another thread's slot, so the ring needs
-//     no barrier.
+//     by cp.async kStages - 1 steps ahead of the step being read.  The feed
+//     runs on across the pass boundaries and into the next row, so loads
+//     stay in flight while the CTA reduces; no thread ever reads another
+//     thread's slot, so the ring needs no barrier.
 //   * Step 1 takes exponents against a running reference maximum and redoes a
 //     step against a raised maximum only when its sum reaches 2^64, so the
 //     common step costs one FMA, one ex2 and one add per element.
@@ -36,6 +38,9 @@
 //     memory, so step 3 reads only the student (p from the student logit, the
 //     coefficient of p picked by the bit); a thread that met an exact tie
 //     recomputes the sign from the teacher instead.
+//   * The forward alone can also store those sign bits in global memory (one
+//     byte per vector after a per-row tie flag), so that the backward reads
+//     the student and the bits instead of the teacher.
 //   * Student and teacher go through the very same code, so a row whose
 //     teacher equals its student bit for bit gets p == q everywhere and
 //     tvd = sigma = 0 exactly.
@@ -204,9 +209,10 @@ __device__ __forceinline__ void write_ignored(const FwdArgs& p, int64_t row) {
 //
 // Per thread, the sequence of steps is: for each non-ignored row of this
 // cluster (rows cluster_id, cluster_id + n_clusters, ...), step 1's n_my
-// vectors, then (fused loss only) step 2's n_my vectors, two vectors
-// (NT vectors apart) per step.  Both the feed and the consumer walk this
-// same sequence; the feed runs kStages - 1 steps ahead of the step being read.
+// vectors, then (fused loss only) step 2's n_my vectors, then (single launch)
+// step 3's, kPerStep vectors per tensor (NT vectors apart) per step.  Both
+// the feed and the consumer walk this same sequence; the feed runs
+// kStages - 1 steps ahead of the step being read.
 
 constexpr int kPerStep = 4;  // vectors per tensor moved by one step
 
