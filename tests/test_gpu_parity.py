@@ -348,6 +348,50 @@ def test_sign_words_match_plain_forward_and_backward(dtype, V, ld, cluster):
     assert flags[2].item() != 0               # the tied row falls back to the teacher
 
 
+# ------------------------------------------------------------------ randomized layouts
+
+def _random_case(k):
+    """Seeded random shape, dtype, layout, cluster size and row structure."""
+    g = np.random.default_rng(1000 + k)
+    dtype = [torch.bfloat16, torch.float32][int(g.integers(2))]
+    V = int(g.choice([1, 2, 7, 8, 33, 257, 1000, 4099, 20000, 70001]))
+    rows = int(g.integers(1, 20))
+    vec = 8 if dtype == torch.bfloat16 else 4
+    layout = int(g.integers(3))          # 0 contiguous, 1 padded to a vector, 2 odd stride
+    ld = {0: None, 1: (V + vec - 1) // vec * vec + vec, 2: V + 1}[layout]
+    cluster = int(g.choice([0, 1, 2, 4, 8]))
+    return dtype, V, rows, ld, cluster, int(g.integers(1 << 30))
+
+
+@pytest.mark.parametrize("k", range(24))
+def test_randomized_layouts_all_paths(k):
+    dtype, V, rows, ld, cluster, seed = _random_case(k)
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=rows, V=V, dtype=dtype, seed=seed)
+    if ld is not None:
+        w = padded(w, ld, 0)
+    if rows > 2:
+        w.teacher[1] = w.student[1]
+        w.target[2] = w.ignore_index
+    f1, g1, st1 = run(w, cluster=cluster)
+    f2, g2, st2 = run_single(w, cluster=cluster)
+    assert st1 == st2 == 0
+    for key in f1:
+        assert torch.equal(f1[key], f2[key]), key
+    assert torch.equal(g1, g2)
+    prev = binding.set_forward_cluster(cluster)
+    try:
+        f3 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target)
+        g3 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f3[2:5], f3[5],
+                                                 w.grad_ce, w.grad_tvd)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_forward_cluster(prev)
+    for key, x in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), f3[:5]):
+        assert torch.equal(f1[key], x), key
+    assert torch.equal(g1, g3)
+    compare(w, f1, g1, what=f"case {k} ")
+
+
 # ------------------------------------------------------------------ single launch
 
 def run_single(w, cluster=0, inplace=False, grads=None):
