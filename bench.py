@@ -364,11 +364,16 @@ def main():
         binding.ce_backward(w.student, w.target, ce_lse, w.grad_ce, w.ignore_index,
                             grad_logits=grad, stream=stream)
 
+    def ce_single():  # cross-entropy forward + backward in one launch
+        binding.ce_forward_backward(w.student, w.target, w.grad_ce, w.ignore_index, ce=ce,
+                                    lse=ce_lse, grad_logits=grad, stream=stream)
+
     # the launches of one step of each path, with the algorithmic bytes of each launch
     paths = {
         "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
         "single": [("forward_backward", single, 3 * BT * V * elem)],
         "ce": [("ce_forward", ce_fwd, BT * V * elem), ("ce_backward", ce_bwd, 2 * BT * V * elem)],
+        "ce_single": [("ce_forward_backward", ce_single, 2 * BT * V * elem)],
         # two launches with sign words: the backward reads the student and the
         # bits (V/8 bytes per bf16 row) instead of the teacher
         "two_signs": [("forward_signs", fwd_signs, 2 * BT * V * elem + sign_bytes),
@@ -422,8 +427,11 @@ def main():
                  "kernels": okern}
         # cross-entropy alone (student logits only): forward + backward, 3 V e per row
         cms, ckern = time_path("ce", K)
+        c1ms, c1kern = time_path("ce_single", K)
         ce_path = {"path": "ce", "ms_per_step": cms, "value": world * BT / (cms * 1e-3),
-                   "unit": "tokens/s", "kernels": ckern}
+                   "unit": "tokens/s", "kernels": ckern,
+                   "single_launch": {"ms_per_step": c1ms, "value": world * BT / (c1ms * 1e-3),
+                                     "kernels": c1kern}}
         sms_, skern = time_path("two_signs", K)
         signs_path = {"path": "two_signs", "ms_per_step": sms_,
                       "value": world * BT / (sms_ * 1e-3), "unit": "tokens/s", "kernels": skern}

@@ -25,7 +25,8 @@ _lib = None
 EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
            "fused_ce_tvd_signs_row_bytes", "fused_ce_tvd_forward_signs",
            "fused_ce_tvd_backward_signs",
-           "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
+           "ce_forward", "ce_backward", "ce_forward_backward", "fused_ce_tvd_mean_upstream",
+           "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fused_linear_ce_tvd_forward_backward_noalloc",
            "fct_status_string", "fct_set_forward_cluster", "fct_version")
@@ -65,6 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fused_ce_tvd_backward_signs.restype = i32
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
+        lib.ce_forward_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, i64, vp, vp, vp,
+                                            i64, vp, vp]
+        lib.ce_forward_backward.restype = i32
         dbl = ctypes.c_double
         lib.fused_linear_ce_tvd_workspace_size.argtypes = [i64, i64]
         lib.fused_linear_ce_tvd_workspace_size.restype = ctypes.c_size_t
@@ -370,6 +374,31 @@ def ce_backward(logits, target, lse, grad_ce, ignore_index=IGNORE_INDEX, *, grad
                             _ptr(dev_status), _stream(stream))
     _check(rc, "ce_backward")
     return grad_logits
+
+
+def ce_forward_backward(logits, target, grad_ce, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,
+                        grad_logits=None, inplace=False, dev_status=None, stream=None):
+    """Cross-entropy forward and backward in one launch: (ce, lse, grad_logits),
+    bit-identical to ce_forward followed by ce_backward."""
+    code, ld = _logits(logits, "logits")
+    BT, V = logits.shape
+    dev = logits.device
+    _rows(target, BT, "target", torch.int64)
+    gce, stride = _upstream(grad_ce, BT, dev, "grad_ce")
+    ce = _out(ce, BT, dev, "ce")
+    lse = _out(lse, BT, dev, "lse")
+    if inplace:
+        grad_logits = logits
+    elif grad_logits is None:
+        grad_logits = torch.empty_like(logits)
+    code_g, ld_g = _logits(grad_logits, "grad_logits")
+    if code_g != code or grad_logits.shape != logits.shape:
+        raise ValueError("grad_logits must match the logits' shape and dtype")
+    rc = load().ce_forward_backward(_ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index),
+                                    _ptr(gce), stride, _ptr(ce), _ptr(lse), _ptr(grad_logits), ld_g,
+                                    _ptr(dev_status), _stream(stream))
+    _check(rc, "ce_forward_backward")
+    return ce, lse, grad_logits
 
 
 def fused_ce_tvd_mean_upstream(target, ignore_index=IGNORE_INDEX, alpha=1.0, beta=1.0, *,

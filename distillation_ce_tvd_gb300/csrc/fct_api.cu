@@ -98,7 +98,10 @@ int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
 // over a cluster of C CTAs until every SM still gets at least one CTA.
 // Depends on V, the element type and the device only (never on BT), so
 // results do not depend on how the rows are batched.
-fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec) {
+// kept: the row re-read from L2 in a later pass is student + teacher (tvd),
+// or the student alone (cross-entropy in one launch, ce_grad).
+fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec,
+                          bool ce_grad = false) {
   fct::FwdPlan plan{vec, 1, 0, false};
   // FCT_L2_KEEP=normal tags rows that are read again with evict_normal
   // instead of evict_last (a tuning experiment).
@@ -107,8 +110,9 @@ fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, b
     return e && std::string(e) == "normal";
   }();
   plan.keep_normal = keep_normal;
-  if (!tvd) return plan;  // one pass: nothing to keep in L2
-  const double row_bytes = 2.0 * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
+  if (!tvd && !ce_grad) return plan;  // one pass: nothing to keep in L2
+  const double row_bytes =
+      (tvd ? 2.0 : 1.0) * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
   const double budget = 0.80 * static_cast<double>(d.l2_bytes);
   int64_t fit = static_cast<int64_t>(budget / row_bytes);
   if (fit < 1) fit = 1;
@@ -314,6 +318,55 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
   return FCT_OK;
 }
 
+// Cross-entropy forward + backward in one launch: ce_forward's and
+// ce_backward's checks, no overlap between the gradient and the per-row
+// outputs; unaligned rows take the two launches (same results).
+int ce_forward_backward_impl(const void* logits, int64_t ld, int dtype, const int64_t* target,
+                             int64_t BT, int64_t V, int64_t ignore_index, const float* grad_ce,
+                             int64_t grad_stride, float* ce, float* lse, void* grad, int64_t ld_g,
+                             int32_t* dev_status, void* stream) {
+  if (BT < 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  int rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(logits, ld, dtype, V)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
+  if (grad_ce == nullptr || ce == nullptr || lse == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(grad_ce, 4) || !aligned(ce, 4) || !aligned(lse, 4)) return FCT_ERR_ALIGNMENT;
+  if (dev_status && !aligned(dev_status, 4)) return FCT_ERR_ALIGNMENT;
+  const size_t e = elem_size(dtype);
+  const Range rs = mat_range(logits, BT, ld, V, e), g = mat_range(grad, BT, ld_g, V, e);
+  const Range rtg = vec_range(target, BT, 8), rgc = vec_range(grad_ce, grad_stride ? BT : 1, 4);
+  const bool inplace = (grad == logits);
+  if (inplace && ld_g != ld) return FCT_ERR_INVALID_ARG;
+  if (!inplace && overlap(g, rs)) return FCT_ERR_INVALID_ARG;
+  if (overlap(g, rtg) || overlap(g, rgc)) return FCT_ERR_INVALID_ARG;
+  const Range rce = vec_range(ce, BT, 4), rl = vec_range(lse, BT, 4);
+  if (overlap(rce, rl)) return FCT_ERR_INVALID_ARG;
+  for (const Range& r : {rce, rl})
+    if (overlap(r, rs) || overlap(r, rtg) || overlap(r, g) || overlap(r, rgc))
+      return FCT_ERR_INVALID_ARG;
+  DeviceInfo d;
+  if ((rc = current_device(&d)) != FCT_OK) return rc;
+  if (!(vec_ok(logits, ld, dtype) && vec_ok(grad, ld_g, dtype))) {
+    rc = forward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, ce, nullptr,
+                      lse, nullptr, nullptr, dev_status, stream);
+    if (rc != FCT_OK) return rc;
+    return backward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, lse,
+                         nullptr, nullptr, grad_ce, nullptr, grad_stride, grad, ld_g, dev_status,
+                         stream);
+  }
+  fct::FwdArgs a{logits, nullptr, ld, ld, dtype, target, BT, V, ignore_index,
+                 ce, nullptr, lse, nullptr, nullptr, dev_status, grad, ld_g, grad_ce, nullptr,
+                 grad_stride, 0};
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, false, true, /*ce_grad=*/true);
+  a.keep_normal = plan.keep_normal ? 1 : 0;
+  if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
 int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, int64_t d_s,
                 const void* h_t, int64_t ld_ht, const void* w_t, int64_t ld_wt, int64_t d_t,
                 const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
@@ -491,6 +544,14 @@ int fused_ce_tvd_backward_signs(const void* student, int64_t ld_student, const v
   return backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
                        ignore_index, student_lse, teacher_lse, sigma, grad_ce, grad_tvd,
                        grad_stride, grad_student, ld_grad, dev_status, stream, signs, ld_signs);
+}
+
+int ce_forward_backward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target,
+                        int64_t BT, int64_t V, int64_t ignore_index, const float* grad_ce,
+                        int64_t grad_stride, float* ce, float* lse, void* grad_logits,
+                        int64_t ld_grad, int32_t* dev_status, void* stream) {
+  return ce_forward_backward_impl(logits, ld, dtype, target, BT, V, ignore_index, grad_ce,
+                                  grad_stride, ce, lse, grad_logits, ld_grad, dev_status, stream);
 }
 
 int ce_forward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target, int64_t BT,

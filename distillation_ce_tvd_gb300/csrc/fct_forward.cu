@@ -234,7 +234,7 @@ constexpr int kMaxSignWords = 16;
 // kPerStep vectors and, if rem > 0, one final step of rem vectors.
 template <typename T, int VE, bool kTvd, bool kGrad, int NT>
 struct Feed {
-  static constexpr int kPasses = kTvd ? (kGrad ? 3 : 2) : 1;
+  static constexpr int kPasses = kTvd ? (kGrad ? 3 : 2) : (kGrad ? 2 : 1);
   static constexpr int kTensors = kTvd ? 2 : 1;
   static constexpr uint32_t kSlotBytes = kTensors * kPerStep * NT * 16;
   static constexpr int64_t kStride = int64_t(NT) * 16;  // bytes between a thread's vectors
@@ -391,7 +391,6 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG = T,
           bool kSigns = false>
 __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
-  static_assert(kTvd || !kGrad, "the single-launch path is the fused loss");
   static_assert(!kSigns || (kTvd && !kGrad), "sign words come from the forward alone");
   constexpr bool kBits = kGrad || kSigns;  // step 2 builds sign words
   using F = Feed<T, VE, kTvd, kGrad, NT>;
@@ -428,7 +427,7 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   f.pass = 0;
   // steps per row of the thread with the most vectors (thread 0)
   const int64_t max_steps = ((span + NT - 1) / NT + kPerStep - 1) / kPerStep;
-  const bool use_bits = kGrad && max_steps <= kMaxSignWords;
+  const bool use_bits = kGrad && kTvd && max_steps <= kMaxSignWords;
   f.passes_t = use_bits ? 2 : F::kPasses;
   f.row = cluster_id;
   while (f.row < p.BT && p.target[f.row] == p.ignore_index) f.row += n_clusters;
@@ -506,6 +505,51 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
         cluster_sync_all();
       } else {
         __syncthreads();
+      }
+      if constexpr (kGrad) {
+        // ---- cross-entropy alone in one launch: a second pass over the
+        // L2-resident row writes grad_ce * (p - [v == target]) with the
+        // backward kernel's expressions, so the result is bit-identical.
+        const float gce = p.grad_ce[row * p.grad_stride];
+        const float ns2 = -(lse_s * kLog2e);
+        const bool bad = (tg < 0 || tg >= p.V);
+        TG* grow = static_cast<TG*>(p.grad) + row * p.ld_g;
+        TG* gmine = grow + (vb + tid) * VE;
+        const int64_t tg_rel = tg - (vb + tid) * VE;
+        const float2 L2 = make_float2(kLog2e, kLog2e), ns22 = make_float2(ns2, ns2);
+        consume_pass<NT, F::kTensors>(
+            f, slot, p, n_clusters, mine, n_full, rem, [&](const uint4* cell, auto n, int k0) {
+#pragma unroll
+              for (int u = 0; u < kPerStep; ++u) {
+                if (u < int(n)) {
+                  float xs[VE], g[VE];
+                  unpack_raw<T, VE>(cell[u * NT], xs);
+#pragma unroll
+                  for (int j = 0; j < VE; j += 2) {
+                    const float2 e = __ffma2_rn(make_float2(xs[j], xs[j + 1]), L2, ns22);
+                    g[j] = ex2(e.x) * gce;
+                    g[j + 1] = ex2(e.y) * gce;
+                  }
+                  const int64_t off = tg_rel - int64_t(k0 + u) * NT * VE;
+                  if (static_cast<uint64_t>(off) < static_cast<uint64_t>(VE)) {
+#pragma unroll
+                    for (int j = 0; j < VE; ++j)
+                      if (j == off) g[j] -= gce;
+                  }
+                  if (bad) {
+#pragma unroll
+                    for (int j = 0; j < VE; ++j) g[j] = __uint_as_float(0x7fc00000u);
+                  }
+                  store_grad<T, TG, VE>(gmine + int64_t(k0 + u) * NT * VE, g, f.drop);
+                }
+              }
+            });
+        if (owns_tail && tail0 + tid < p.V) {
+          const int64_t v = tail0 + tid;
+          float g = ex2(fmaf(Elem<T>::load1(srow + v), kLog2e, ns2)) * gce;
+          if (v == tg) g -= gce;
+          Elem<TG>::store1(grow + v, bad ? __uint_as_float(0x7fc00000u) : g);
+        }
       }
     } else {
       const float lse_t = lse2_finish(fb);
@@ -846,7 +890,7 @@ int per_device(PerDevice& c, Init&& init) {
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG, bool kSigns>
 cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
-                           (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
+                           ((kGrad && kTvd) ? size_t(kMaxSignWords) * NT * 4 : 0);
   auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG, kSigns>;
   static PerDevice cache;
   const int n_max = per_device(cache, [&] {
@@ -904,6 +948,10 @@ cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t s
     if (!plan.vec || !a.tvd || a.grad) return cudaErrorInvalidValue;
     return a.dtype == FCT_BF16 ? run_c<bf16_t, true, false, bf16_t, true>(a, plan, st)
                                : run_c<float, true, false, float, true>(a, plan, st);
+  }
+  if (a.grad && !a.tvd) {  // cross-entropy alone in one launch
+    return a.dtype == FCT_BF16 ? run_c<bf16_t, false, true>(a, plan, st)
+                               : run_c<float, false, true>(a, plan, st);
   }
   if (a.dtype == FCT_BF16) {
     if (a.grad) return run_c<bf16_t, true, true>(a, plan, st);

@@ -295,6 +295,23 @@ int ce_backward(const void* logits, int64_t ld, fct_dtype dtype,
                 int32_t* dev_status, void* stream);
 
 /*
+ * Cross-entropy forward and backward in one launch, given grad_ce: the
+ * single-launch idea applied to the CE subset.  The row is read from HBM once
+ * for its log-sum-exp and again from L2 for grad_ce*(p_v - 1[v==target]), so
+ * HBM sees 1 read and 1 write per element instead of 2 reads and 1 write.
+ * Outputs (ce, lse, grad_logits) are bit-identical to ce_forward followed by
+ * ce_backward; grad_logits may equal logits (with ld_grad == ld) for an
+ * in-place gradient.  Rows that are not 16-byte aligned take those two
+ * launches.
+ */
+int ce_forward_backward(const void* logits, int64_t ld, fct_dtype dtype,
+                        const int64_t* target, int64_t BT, int64_t V,
+                        int64_t ignore_index, const float* grad_ce,
+                        int64_t grad_stride, float* ce, float* lse,
+                        void* grad_logits, int64_t ld_grad,
+                        int32_t* dev_status, void* stream);
+
+/*
  * Mean over tokens.  The method stores per-row ce and tvd and takes per-row
  * upstream gradients (PR #1384 analysis, "Forward Pass" stores and "Backward
  * Pass" combine); the reduction to a scalar is the caller's.  These give the

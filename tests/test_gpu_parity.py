@@ -269,6 +269,40 @@ def test_repeat_runs_are_deterministic():
 
 # ------------------------------------------------------------------ CE subset, autograd
 
+@pytest.mark.parametrize("dtype,V,ld,cluster", [
+    (torch.bfloat16, 151936, None, 0), (torch.float32, 256000, None, 0),   # fp32: 2-CTA rows
+    (torch.bfloat16, 20003, 20008, 0), (torch.float32, 9001, 9004, 4),
+    (torch.bfloat16, 3003, None, 0),                                        # unaligned: two launches
+    (torch.bfloat16, 5, None, 0)])
+def test_ce_single_launch_equals_two(dtype, V, ld, cluster):
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=10, V=V, dtype=dtype, seed=36)
+    if ld is not None:
+        w = padded(w, ld, 0)
+    w.target[3] = w.ignore_index
+    w.target[6] = -7                                   # out of range
+    prev = binding.set_forward_cluster(cluster)
+    try:
+        st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+        st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+        ce1, lse1 = binding.ce_forward(w.student, w.target, dev_status=st1)
+        g1 = binding.ce_backward(w.student, w.target, lse1, w.grad_ce, dev_status=st1)
+        ce2, lse2, g2 = binding.ce_forward_backward(w.student, w.target, w.grad_ce, dev_status=st2)
+        s_in = same_layout_clone(w.student)
+        ce3, lse3, g3 = binding.ce_forward_backward(s_in, w.target, 0.25, inplace=True)
+        g4 = binding.ce_backward(w.student, w.target, lse1, 0.25)
+        torch.cuda.synchronize()
+    finally:
+        binding.set_forward_cluster(prev)
+    assert st1.item() == st2.item() == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+
+    def bits(x):
+        x = x.contiguous()
+        return x.view(torch.int32 if x.element_size() == 4 else torch.int16)
+
+    for a, b in ((ce1, ce2), (lse1, lse2), (g1, g2), (ce1, ce3), (lse1, lse3), (g4, g3)):
+        assert torch.equal(bits(a), bits(b))
+
+
 @pytest.mark.parametrize("dtype,V", [(torch.bfloat16, 151936), (torch.float32, 32003), (torch.bfloat16, 5)])
 def test_ce_subset(dtype, V):
     w = workloads.make("bt1024_v32000_bf16", DEV, rows=24, V=V, dtype=dtype, seed=12)
