@@ -627,6 +627,6 @@ int fct_set_forward_cluster(int ctas_per_row) {
   return g_cluster_override.exchange(ctas_per_row);
 }
 
-int fct_version(void) { return 100; }
+int fct_version(void) { return 200; }  // 0.2.0: sign words, cross-entropy in one launch, no-allocation fused linear
 
 }  // extern "C"
