@@ -206,3 +206,20 @@ def test_binding_refuses_host_tensors(lib):
     x = torch.zeros(2, 8)
     with pytest.raises(ValueError):
         binding.fused_ce_tvd_forward(x, x, torch.zeros(2, dtype=torch.int64))
+
+
+def test_no_library_means_an_error_not_a_fallback(monkeypatch):
+    # Without a buildable library every entry point raises: there is no CPU
+    # or PyTorch path behind the binding.
+    from distillation_ce_tvd_gb300 import _build
+
+    def no_nvcc():
+        raise RuntimeError("nvcc not found")
+
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(_build, "_stale", lambda: True)
+    monkeypatch.setattr(_build, "_nvcc", no_nvcc)
+    with pytest.raises(RuntimeError):
+        binding.load()
+    with pytest.raises(RuntimeError):
+        binding.version()
