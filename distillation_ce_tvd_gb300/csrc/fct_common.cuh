@@ -190,6 +190,21 @@ __device__ __forceinline__ void cp_async16(uint32_t smem_dst, const void* src, u
                : "r"(smem_dst), "l"(src), "l"(pol)
                : "memory");
 }
+// Four 16-byte copies, shared dst + kBase + i*kDst <- global src + i*kSrc
+// (i = 0..3), with the constant offsets folded into the instructions'
+// addresses instead of computed into registers per copy.
+template <int kBase, int kDst, int kSrc>
+__device__ __forceinline__ void cp_async16x4(uint32_t smem_dst, const void* src, uint64_t pol) {
+  asm volatile(
+      "cp.async.cg.shared.global.L2::cache_hint [%0+%3], [%1], 16, %2;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+%4], [%1+%5], 16, %2;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+%6], [%1+%7], 16, %2;\n\t"
+      "cp.async.cg.shared.global.L2::cache_hint [%0+%8], [%1+%9], 16, %2;"
+      :
+      : "r"(smem_dst), "l"(src), "l"(pol), "n"(kBase), "n"(kBase + kDst), "n"(kSrc),
+        "n"(kBase + 2 * kDst), "n"(2 * kSrc), "n"(kBase + 3 * kDst), "n"(3 * kSrc)
+      : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");
 }

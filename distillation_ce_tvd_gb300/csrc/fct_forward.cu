@@ -269,13 +269,21 @@ struct Feed {
 
   template <int kCount>
   __device__ __forceinline__ void copy(uint32_t dst, int count) {
+    if constexpr (kCount == 4 && kPerStep == 4) {  // a full step: offsets folded
+      cp_async16x4<0, NT * 16, static_cast<int>(kStride)>(dst, sp, pol_s);
+      if constexpr (kTvd) {
+        if (!kGrad || pass < passes_t)
+          cp_async16x4<kPerStep * NT * 16, NT * 16, static_cast<int>(kStride)>(dst, tp, pol_t);
+      }
+    } else {
 #pragma unroll
-    for (int u = 0; u < kPerStep; ++u) {
-      if (kCount == kPerStep || u < count) {
-        cp_async16(dst + u * NT * 16, sp + u * kStride, pol_s);
-        if constexpr (kTvd) {
-          if (!kGrad || pass < passes_t)
-            cp_async16(dst + (kPerStep + u) * NT * 16, tp + u * kStride, pol_t);
+      for (int u = 0; u < kPerStep; ++u) {
+        if (kCount == kPerStep || u < count) {
+          cp_async16(dst + u * NT * 16, sp + u * kStride, pol_s);
+          if constexpr (kTvd) {
+            if (!kGrad || pass < passes_t)
+              cp_async16(dst + (kPerStep + u) * NT * 16, tp + u * kStride, pol_t);
+          }
         }
       }
     }
