@@ -167,6 +167,28 @@ def host_rows(name: str, rows: int, BT: int | None = None):
     return workloads.make(name, "cpu", rows=rows)
 
 
+def cpu_model() -> str:
+    """The host CPU's model name as the OS reports it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def single_core_rate(name: str = "bt1024_v32000_bf16", seconds: float = 2.0) -> dict:
+    """The oracle on one thread, on rows of a small workload, for scale."""
+    probe = host_rows(name, 2)
+    rate, _, _ = cpu_oracle_rate(probe, threads=1)
+    rows = int(max(2, min(workloads.WORKLOADS[name]["BT"], rate * seconds)))
+    rate, dt, _ = cpu_oracle_rate(host_rows(name, rows), threads=1)
+    return {"workload": name, "rows": rows, "value": rate, "unit": "tokens/s", "seconds": dt}
+
+
 def cpu_baseline(name: str, target_seconds: float = 12.0) -> dict:
     probe = host_rows(name, 8)
     rate, dt, n = cpu_oracle_rate(probe)
@@ -174,7 +196,8 @@ def cpu_baseline(name: str, target_seconds: float = 12.0) -> dict:
     sample = host_rows(name, rows)
     rate, dt, n = cpu_oracle_rate(sample)
     return {"value": rate, "unit": "tokens/s", "cores": n, "kind": "oracle",
-            "sample": f"{rows} rows of {name} (fwd+bwd, fp64, OpenMP over rows), {dt:.1f} s"}
+            "sample": f"{rows} rows of {name} (fwd+bwd, fp64, OpenMP over rows), {dt:.1f} s",
+            "cpu_model": cpu_model(), "single_core": single_core_rate()}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -206,7 +229,8 @@ def run_reference(args, world, rank):
                    "logit_dtype": "bf16" if cfg["dtype"] == torch.bfloat16 else "f32",
                    "rows_per_step": rows},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": n, "kind": "oracle",
-                         "sample": f"{rows} rows of {name} per step (fwd+bwd, fp64)"},
+                         "sample": f"{rows} rows of {name} per step (fwd+bwd, fp64)",
+                         "cpu_model": cpu_model()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
