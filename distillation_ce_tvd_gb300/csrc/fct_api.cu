@@ -177,7 +177,10 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
   const bool vec = vec_ok(student, ld_s, dtype) && (!fused || vec_ok(teacher, ld_t, dtype));
   fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
                  ce, tvd, lse_s, lse_t, sigma, dev_status, nullptr, 0, nullptr, nullptr, 0, 0};
-  const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec);
+  // Cross-entropy alone takes the row split of its single launch
+  // (ce_forward_backward), so both reduce each row in the same order and give
+  // the same bits.
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec, /*ce_grad=*/!fused);
   a.keep_normal = plan.keep_normal ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (signs != nullptr) {

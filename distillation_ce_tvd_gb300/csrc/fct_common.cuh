@@ -346,14 +346,18 @@ __device__ __forceinline__ void store_grad(TG* p, const float (&x)[VE], uint64_t
 
 // ---------------------------------------------------------------- warp
 
-__device__ __forceinline__ Lse2 shfl_xor(Lse2 a, int m) {
-  return Lse2{__shfl_xor_sync(0xffffffffu, a.m2, m), __shfl_xor_sync(0xffffffffu, a.s, m)};
-}
-
+// Warp-wide merge of Lse2 states: the maximum first, then each lane's sum
+// rescaled once to it, then a plain sum.  Every butterfly step combines the
+// same two values in both lanes with a commutative operation (max, add), so
+// all lanes end with identical results.
 __device__ __forceinline__ Lse2 warp_merge(Lse2 a) {
+  float m = a.m2;
 #pragma unroll
-  for (int m = 16; m >= 1; m >>= 1) a = lse2_merge(a, shfl_xor(a, m));
-  return a;
+  for (int k = 16; k >= 1; k >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, k));
+  float s = (a.m2 == -INFINITY) ? 0.f : a.s * ex2(a.m2 - m);
+#pragma unroll
+  for (int k = 16; k >= 1; k >>= 1) s += __shfl_xor_sync(0xffffffffu, s, k);
+  return Lse2{m, s};
 }
 
 __device__ __forceinline__ float warp_sum(float a) {
