@@ -223,3 +223,23 @@ def test_no_library_means_an_error_not_a_fallback(monkeypatch):
         binding.load()
     with pytest.raises(RuntimeError):
         binding.version()
+
+
+def test_plain_c_client_links_and_runs(tmp_path, lib):
+    # The header and the library from C alone: compile, link, run (no GPU
+    # calls; the client checks version, sizes and argument errors).
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    so = os.path.join(root, "distillation_ce_tvd_gb300", "libfused_ce_tvd.so")
+    exe = str(tmp_path / "client")
+    r = subprocess.run(["gcc", "-std=c11", "-O1", "-I", os.path.join(root, "include"),
+                        os.path.join(root, "tests", "c_abi_client.c"), so,
+                        "-Wl,-rpath," + os.path.dirname(so), "-o", exe],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.startswith("ok ")
