@@ -83,3 +83,46 @@ def fused_ce_tvd_mean_loss(student, teacher, target, ignore_index=binding.IGNORE
                            alpha=1.0, beta=1.0, inplace=False):
     """Scalar alpha * mean(ce) + beta * mean(tvd) with autograd support."""
     return FusedCETVDMeanLoss.apply(student, teacher, target, ignore_index, alpha, beta, inplace)
+
+
+class FusedLinearCETVDMeanLoss(torch.autograd.Function):
+    """alpha * mean(ce) + beta * mean(tvd) from hidden states and lm_head weights.
+
+    The student's logits are h_student @ w_student.T and the teacher's
+    h_teacher @ w_teacher.T, computed in row blocks and never held whole.
+    As for FusedCETVDMeanLoss, the upstream gradients of the mean are known
+    before the forward, so the forward runs the whole fused-linear forward +
+    backward and keeps d loss / d h_student and d loss / d w_student; the
+    backward hands them out.  The teacher is frozen.  The weight gradient is
+    accumulated in fp32; autograd casts it to the weight's dtype.
+    """
+
+    @staticmethod
+    def forward(ctx, h_student, w_student, h_teacher, w_teacher, target,
+                ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0, chunk_rows=1024):
+        gce, gtvd, _ = binding.fused_ce_tvd_mean_upstream(target, ignore_index, alpha, beta)
+        ce, tvd, _, _, _, grad_h, grad_w = binding.fused_linear_ce_tvd_forward_backward(
+            h_student.detach(), w_student.detach(), h_teacher.detach(), w_teacher.detach(),
+            target, gce, gtvd, ignore_index, chunk_rows=chunk_rows,
+            want_grad_h=ctx.needs_input_grad[0], want_grad_w=ctx.needs_input_grad[1])
+        loss = binding.fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index, alpha, beta)
+        ctx.grads = (grad_h, grad_w)
+        return loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        grad_h, grad_w = ctx.grads
+        ctx.grads = None
+        if not torch.equal(grad_out, torch.ones_like(grad_out)):
+            grad_h = None if grad_h is None else grad_h * grad_out.to(grad_h.dtype)
+            grad_w = None if grad_w is None else grad_w * grad_out.to(grad_w.dtype)
+        return grad_h, grad_w, None, None, None, None, None, None, None
+
+
+def fused_linear_ce_tvd_mean_loss(h_student, w_student, h_teacher, w_teacher, target,
+                                  ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0,
+                                  chunk_rows=1024):
+    """Scalar alpha * mean(ce) + beta * mean(tvd) of the lm_head logits, with
+    autograd support for h_student and w_student (2-D bf16 tensors)."""
+    return FusedLinearCETVDMeanLoss.apply(h_student, w_student, h_teacher, w_teacher, target,
+                                          ignore_index, alpha, beta, chunk_rows)

@@ -655,3 +655,29 @@ def test_fused_linear_chunking_is_invisible():
         assert torch.allclose(x, y, rtol=0, atol=2e-5)
     assert torch.allclose(a[5].float(), b[5].float(), rtol=2 ** -7, atol=1e-7)
     assert torch.allclose(a[6], b[6], rtol=1e-3, atol=1e-7)
+
+
+def test_fused_linear_autograd_wrapper_matches_direct_calls():
+    from distillation_ce_tvd_gb300.autograd import fused_linear_ce_tvd_mean_loss
+    hs, ws, ht, wt, tg = _linear_case(90, 128, 96, 3001, seed=11)
+    alpha, beta = 0.6, 1.3
+    gce, gtvd, _ = binding.fused_ce_tvd_mean_upstream(tg, -100, alpha, beta)
+    direct = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, gce, gtvd,
+                                                          chunk_rows=32)
+    ref_loss = binding.fused_ce_tvd_mean_loss(direct[0], direct[1], tg, -100, alpha, beta)
+
+    h = hs.clone().requires_grad_(True)
+    w = ws.clone().requires_grad_(True)
+    loss = fused_linear_ce_tvd_mean_loss(h, w, ht, wt, tg, -100, alpha, beta, chunk_rows=32)
+    (2.0 * loss).backward()
+    torch.cuda.synchronize()
+    assert loss.shape == () and torch.equal(loss.detach(), ref_loss.reshape(()))
+    assert torch.equal(h.grad, direct[5] * 2.0)
+    assert w.grad.dtype == torch.bfloat16
+    assert torch.equal(w.grad, (direct[6] * 2.0).to(torch.bfloat16))
+
+    # only the hidden states need a gradient: the weight-gradient GEMM is skipped
+    h2 = hs.clone().requires_grad_(True)
+    fused_linear_ce_tvd_mean_loss(h2, ws, ht, wt, tg, -100, alpha, beta, chunk_rows=32).backward()
+    torch.cuda.synchronize()
+    assert torch.equal(h2.grad, direct[5])
