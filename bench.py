@@ -250,7 +250,8 @@ def run_linear(args, world, rank, local):
     BT, ds = w.h_student.shape
     V, dt = w.w_teacher.shape
     rows = min(args.chunk_rows, BT)
-    ws_bytes = binding.fused_linear_ce_tvd_workspace_size(V, rows)
+    ldt = torch.bfloat16 if args.logits_dtype == "bf16" else torch.float32
+    ws_bytes = binding.fused_linear_ce_tvd_workspace_size(V, rows, ldt)
     workspace = torch.empty(ws_bytes, device=dev, dtype=torch.uint8)
     grad_h = torch.empty_like(w.h_student)
     grad_w = torch.zeros(V, ds, device=dev, dtype=torch.float32)
@@ -259,7 +260,8 @@ def run_linear(args, world, rank, local):
     def step():
         binding.fused_linear_ce_tvd_forward_backward(
             w.h_student, w.w_student, w.h_teacher, w.w_teacher, w.target, w.grad_ce, w.grad_tvd,
-            w.ignore_index, chunk_rows=rows, workspace=workspace, grad_h=grad_h, grad_w=grad_w,
+            w.ignore_index, chunk_rows=rows, logits_dtype=ldt, workspace=workspace,
+            grad_h=grad_h, grad_w=grad_w,
             stream=stream)
 
     for _ in range(args.warmup):
@@ -291,7 +293,8 @@ def run_linear(args, world, rank, local):
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": args.workload, "BT": BT, "V": V, "d_student": ds,
-                       "d_teacher": dt, "chunk_rows": rows, "workspace_bytes": ws_bytes},
+                       "d_teacher": dt, "chunk_rows": rows, "logits_dtype": args.logits_dtype,
+                       "workspace_bytes": ws_bytes},
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
                          "peak_source": "measured cuBLAS bf16, sustained"},
@@ -311,6 +314,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=sorted(workloads.WORKLOADS) + sorted(workloads.LINEAR_WORKLOADS))
     ap.add_argument("--chunk-rows", type=int, default=2048, help="row block of the fused-linear path")
+    ap.add_argument("--logits-dtype", default="f32", choices=["f32", "bf16"],
+                    help="element type of the fused-linear path's logit blocks")
     ap.add_argument("--rows", type=int, default=None, help="override BT (profiling)")
     ap.add_argument("--path", default="single", choices=["single", "two", "two_signs"],
                     help="headline step: one fused forward+backward launch, or the forward "

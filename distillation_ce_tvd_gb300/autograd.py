@@ -99,11 +99,12 @@ class FusedLinearCETVDMeanLoss(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, h_student, w_student, h_teacher, w_teacher, target,
-                ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0, chunk_rows=1024):
+                ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0, chunk_rows=1024,
+                logits_dtype=torch.float32):
         gce, gtvd, _ = binding.fused_ce_tvd_mean_upstream(target, ignore_index, alpha, beta)
         ce, tvd, _, _, _, grad_h, grad_w = binding.fused_linear_ce_tvd_forward_backward(
             h_student.detach(), w_student.detach(), h_teacher.detach(), w_teacher.detach(),
-            target, gce, gtvd, ignore_index, chunk_rows=chunk_rows,
+            target, gce, gtvd, ignore_index, chunk_rows=chunk_rows, logits_dtype=logits_dtype,
             want_grad_h=ctx.needs_input_grad[0], want_grad_w=ctx.needs_input_grad[1])
         loss = binding.fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index, alpha, beta)
         ctx.grads = (grad_h, grad_w)
@@ -116,13 +117,15 @@ class FusedLinearCETVDMeanLoss(torch.autograd.Function):
         if not torch.equal(grad_out, torch.ones_like(grad_out)):
             grad_h = None if grad_h is None else grad_h * grad_out.to(grad_h.dtype)
             grad_w = None if grad_w is None else grad_w * grad_out.to(grad_w.dtype)
-        return grad_h, grad_w, None, None, None, None, None, None, None
+        return grad_h, grad_w, None, None, None, None, None, None, None, None
 
 
 def fused_linear_ce_tvd_mean_loss(h_student, w_student, h_teacher, w_teacher, target,
                                   ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0,
-                                  chunk_rows=1024):
+                                  chunk_rows=1024, logits_dtype=torch.float32):
     """Scalar alpha * mean(ce) + beta * mean(tvd) of the lm_head logits, with
-    autograd support for h_student and w_student (2-D bf16 tensors)."""
+    autograd support for h_student and w_student (2-D bf16 tensors).
+    ``logits_dtype`` is the element type of the logit blocks (float32 or
+    bfloat16)."""
     return FusedLinearCETVDMeanLoss.apply(h_student, w_student, h_teacher, w_teacher, target,
-                                          ignore_index, alpha, beta, chunk_rows)
+                                          ignore_index, alpha, beta, chunk_rows, logits_dtype)

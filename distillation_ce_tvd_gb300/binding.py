@@ -70,11 +70,11 @@ def load(path: str | None = None) -> ctypes.CDLL:
                                             i64, vp, vp]
         lib.ce_forward_backward.restype = i32
         dbl = ctypes.c_double
-        lib.fused_linear_ce_tvd_workspace_size.argtypes = [i64, i64]
+        lib.fused_linear_ce_tvd_workspace_size.argtypes = [i64, i64, i32]
         lib.fused_linear_ce_tvd_workspace_size.restype = ctypes.c_size_t
         lib.fused_linear_ce_tvd_forward_backward.argtypes = [
             vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
-            vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, ctypes.c_size_t, i64, vp, vp]
+            vp, vp, vp, vp, vp, vp, i64, vp, i64, i32, vp, ctypes.c_size_t, i64, vp, vp]
         lib.fused_linear_ce_tvd_forward_backward.restype = i32
         lib.fused_linear_ce_tvd_forward_backward_noalloc.argtypes = [
             vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
@@ -486,9 +486,19 @@ def fused_ce_tvd_forward_backward_from_host(student_h, teacher_h, target_h, grad
     return (*outs, grad_student)
 
 
-def fused_linear_ce_tvd_workspace_size(V: int, chunk_rows: int) -> int:
+def _logits_dtype(dtype) -> int:
+    if dtype == torch.float32:
+        return FCT_F32
+    if dtype == torch.bfloat16:
+        return FCT_BF16
+    raise ValueError("logits_dtype must be torch.float32 or torch.bfloat16")
+
+
+def fused_linear_ce_tvd_workspace_size(V: int, chunk_rows: int,
+                                       logits_dtype=torch.float32) -> int:
     """Bytes of device workspace fused_linear_ce_tvd_forward_backward needs."""
-    return int(load().fused_linear_ce_tvd_workspace_size(int(V), int(chunk_rows)))
+    return int(load().fused_linear_ce_tvd_workspace_size(int(V), int(chunk_rows),
+                                                         _logits_dtype(logits_dtype)))
 
 
 def _mat(x, name):
@@ -499,14 +509,17 @@ def _mat(x, name):
 
 def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teacher, target,
                                          grad_ce, grad_tvd, ignore_index=IGNORE_INDEX, *,
-                                         chunk_rows=1024, workspace=None, grad_h=None,
-                                         grad_w=None, want_grad_h=True, want_grad_w=True,
-                                         dev_status=None, stream=None):
+                                         chunk_rows=1024, logits_dtype=torch.float32,
+                                         workspace=None, grad_h=None, grad_w=None,
+                                         want_grad_h=True, want_grad_w=True, dev_status=None,
+                                         stream=None):
     """Loss from hidden states and lm_head weights, in row blocks (no (BT, V) logits).
 
     Returns (ce, tvd, student_lse, teacher_lse, sigma, grad_h, grad_w): grad_h
     is d loss / d h_student (bf16), grad_w is d loss / d w_student (fp32,
     accumulated into when passed in; zero-initialised otherwise).
+    ``logits_dtype`` (torch.float32 or torch.bfloat16) is the element type of
+    the logit blocks the loss kernel reads.
     """
     ld_hs, ld_ws = _mat(h_student, "h_student"), _mat(w_student, "w_student")
     ld_ht, ld_wt = _mat(h_teacher, "h_teacher"), _mat(w_teacher, "w_teacher")
@@ -524,7 +537,8 @@ def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teac
     stride = max(stride_ce, stride_tvd)
     outs = [torch.empty(BT, device=dev, dtype=torch.float32) for _ in range(5)]
     rows = max(1, min(int(chunk_rows), BT))
-    need = fused_linear_ce_tvd_workspace_size(V, rows)
+    code = _logits_dtype(logits_dtype)
+    need = fused_linear_ce_tvd_workspace_size(V, rows, logits_dtype)
     if workspace is None:
         workspace = torch.empty(need, device=dev, dtype=torch.uint8)
     if want_grad_h and grad_h is None:
@@ -538,7 +552,7 @@ def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teac
     rc = load().fused_linear_ce_tvd_forward_backward(
         _ptr(h_student), ld_hs, _ptr(w_student), ld_ws, ds, _ptr(h_teacher), ld_ht,
         _ptr(w_teacher), ld_wt, dt, _ptr(target), BT, V, int(ignore_index), _ptr(gce),
-        _ptr(gtvd), stride, *map(_ptr, outs), _ptr(grad_h), ld_gh, _ptr(grad_w), ld_gw,
+        _ptr(gtvd), stride, *map(_ptr, outs), _ptr(grad_h), ld_gh, _ptr(grad_w), ld_gw, code,
         _ptr(workspace), workspace.numel() * workspace.element_size(), rows,
         _ptr(dev_status), _stream(stream))
     _check(rc, "fused_linear_ce_tvd_forward_backward")

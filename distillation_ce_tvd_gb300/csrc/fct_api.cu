@@ -375,9 +375,11 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
                 const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
                 const float* grad_ce, const float* grad_tvd, int64_t grad_stride, float* ce,
                 float* tvd, float* lse_s, float* lse_t, float* sigma, void* grad_h_s,
-                int64_t ld_ghs, float* grad_w_s, int64_t ld_gws, void* workspace,
-                size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status, void* stream) {
+                int64_t ld_ghs, float* grad_w_s, int64_t ld_gws, int logits_dtype,
+                void* workspace, size_t workspace_bytes, int64_t chunk_rows,
+                int32_t* dev_status, void* stream) {
   if (BT < 0 || V <= 0 || d_s <= 0 || d_t <= 0 || chunk_rows <= 0) return FCT_ERR_INVALID_ARG;
+  if (logits_dtype != FCT_F32 && logits_dtype != FCT_BF16) return FCT_ERR_UNSUPPORTED;
   if (BT == 0) return FCT_OK;
   const int64_t kInt = 2147483647;  // cuBLAS takes int sizes and strides
   if (V > kInt || d_s > kInt || d_t > kInt || ld_hs > kInt || ld_ws > kInt || ld_ht > kInt ||
@@ -404,7 +406,8 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
       if (overlap(vec_range(outs[i], BT, 4), vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
   }
   const int64_t rows = chunk_rows < BT ? chunk_rows : BT;
-  if (workspace_bytes < fct::linear_workspace_bytes(V, rows)) return FCT_ERR_INVALID_ARG;
+  if (workspace_bytes < fct::linear_workspace_bytes(V, rows, logits_dtype))
+    return FCT_ERR_INVALID_ARG;
   // outputs must not overlap the inputs or the workspace
   const Range ins[5] = {mat_range(h_s, BT, ld_hs, d_s, 2), mat_range(w_s, V, ld_ws, d_s, 2),
                         mat_range(h_t, BT, ld_ht, d_t, 2), mat_range(w_t, V, ld_wt, d_t, 2),
@@ -426,8 +429,9 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
   cudaGetDevice(&dev);
   fct::LinArgs a{h_s, ld_hs, w_s, ld_ws, d_s, h_t, ld_ht, w_t, ld_wt, d_t, target, BT, V,
                  ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd, lse_s, lse_t, sigma,
-                 grad_h_s, ld_ghs, grad_w_s, ld_gws, workspace, chunk_rows, dev_status};
-  const fct::FwdPlan plan = plan_forward(d, V, FCT_F32, true, true);
+                 grad_h_s, ld_ghs, grad_w_s, ld_gws, workspace, chunk_rows, dev_status,
+                 logits_dtype};
+  const fct::FwdPlan plan = plan_forward(d, V, logits_dtype, true, true);
   if (fct::launch_linear(a, plan, dev, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
@@ -437,7 +441,7 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
 
 namespace fct {
 
-int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms) {
+int plan_linear_forward(int64_t V, int logits_dtype, FwdPlan* plan, int* device, int* sms) {
   DeviceInfo d;
   const int rc = current_device(&d);
   if (rc != FCT_OK) return rc;
@@ -445,7 +449,7 @@ int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms) {
     cudaGetLastError();
     return FCT_ERR_CUDA;
   }
-  *plan = plan_forward(d, V, FCT_F32, true, true);
+  *plan = plan_forward(d, V, logits_dtype, true, true);
   *sms = d.sms;
   return FCT_OK;
 }
@@ -454,9 +458,11 @@ int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms) {
 
 extern "C" {
 
-size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows) {
+size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows,
+                                          fct_dtype logits_dtype) {
   if (V <= 0 || chunk_rows <= 0) return 0;
-  return fct::linear_workspace_bytes(V, chunk_rows);
+  if (logits_dtype != FCT_F32 && logits_dtype != FCT_BF16) return 0;
+  return fct::linear_workspace_bytes(V, chunk_rows, logits_dtype);
 }
 
 int fused_linear_ce_tvd_forward_backward(
@@ -466,13 +472,13 @@ int fused_linear_ce_tvd_forward_backward(
     int64_t ignore_index, const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
     float* ce, float* tvd, float* student_lse, float* teacher_lse, float* sigma,
     void* grad_h_student, int64_t ld_grad_h, float* grad_w_student, int64_t ld_grad_w,
-    void* workspace, size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status,
-    void* stream) {
+    fct_dtype logits_dtype, void* workspace, size_t workspace_bytes, int64_t chunk_rows,
+    int32_t* dev_status, void* stream) {
   return linear_impl(h_student, ld_h_student, w_student, ld_w_student, d_student, h_teacher,
                      ld_h_teacher, w_teacher, ld_w_teacher, d_teacher, target, BT, V,
                      ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd, student_lse,
                      teacher_lse, sigma, grad_h_student, ld_grad_h, grad_w_student, ld_grad_w,
-                     workspace, workspace_bytes, chunk_rows, dev_status, stream);
+                     logits_dtype, workspace, workspace_bytes, chunk_rows, dev_status, stream);
 }
 
 int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student, const void* teacher,

@@ -99,20 +99,21 @@ struct LinArgs {
   int64_t ld_ghs;
   float* grad_w_s;  // (V, d_s) fp32, accumulated, or nullptr
   int64_t ld_gws;
-  void* workspace;  // linear_workspace_bytes(V, chunk_rows), 256-byte aligned
+  void* workspace;  // linear_workspace_bytes(V, chunk_rows, logits_dtype), 256-byte aligned
   int64_t chunk_rows;
   int32_t* dev_status;
+  int logits_dtype = FCT_F32;  // element type of the logit blocks
 };
 
 int64_t linear_logits_ld(int64_t V);
-size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows);
+size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows, int logits_dtype);
 cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,
                           cudaStream_t st);
 
-// The forward plan the fused-linear path uses (fp32 logit rows of width V)
-// on the calling thread's current device, with that device's index and SM
-// count.  Returns an fct_status.
-int plan_linear_forward(int64_t V, FwdPlan* plan, int* device, int* sms);
+// The forward plan the fused-linear path uses (logit rows of width V and
+// element type logits_dtype) on the calling thread's current device, with
+// that device's index and SM count.  Returns an fct_status.
+int plan_linear_forward(int64_t V, int logits_dtype, FwdPlan* plan, int* device, int* sms);
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);

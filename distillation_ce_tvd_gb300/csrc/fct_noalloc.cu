@@ -299,7 +299,7 @@ extern "C" int fused_linear_ce_tvd_forward_backward_noalloc(
 
   fct::FwdPlan plan;
   int device = 0, sms = 0;
-  if ((rc = fct::plan_linear_forward(V, &plan, &device, &sms)) != FCT_OK) return rc;
+  if ((rc = fct::plan_linear_forward(V, FCT_F32, &plan, &device, &sms)) != FCT_OK) return rc;
   if ((rc = scratch_on(device, &a.workspace)) != FCT_OK) return rc;
   if (run_blocks(a, plan, sms, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
     cudaGetLastError();

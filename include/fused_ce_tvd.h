@@ -189,11 +189,11 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
  * Fused-linear CE + TVD: the loss from hidden states and lm_head weights,
  * without ever holding the (BT, V) logits.  Rows go through in blocks of
  * chunk_rows: per block, cuBLAS GEMMs (bf16 in, fp32 accumulate) write the
- * block's student and teacher logits (fp32) into `workspace`, the
- * single-launch forward + backward of the PR #1384 analysis's loss runs on
- * them and writes their logit gradient rounded to bf16 (also in
- * `workspace`), and two more GEMMs give d loss / d h_student for the block
- * and accumulate d loss / d w_student.
+ * block's student and teacher logits into `workspace`, the single-launch
+ * forward + backward of the PR #1384 analysis's loss runs on them and writes
+ * their logit gradient as bf16 (also in `workspace`), and two more GEMMs
+ * give d loss / d h_student for the block and accumulate d loss / d
+ * w_student.
  * (Computing logits in row blocks is the chunking that the Liger-Kernel
  * overview page describes for its fused linear cross-entropy; applying it to
  * CE + TVD is this library's addition.)  The teacher is frozen.
@@ -204,15 +204,24 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
  *                    fused_ce_tvd_forward_backward.
  *   grad_h_student : (BT, d_student) bf16 output, or NULL.
  *   grad_w_student : (V, d_student) fp32, ACCUMULATED into (+=), or NULL.
+ *   logits_dtype   : element type of the logit blocks the loss sees.
+ *                    FCT_F32: the GEMMs' fp32 sums of bf16 products, the
+ *                    logit gradient rounded to bf16 into its own region.
+ *                    FCT_BF16: those sums rounded once to bf16 (what a bf16
+ *                    model's lm_head outputs, and the element type of the
+ *                    analysis's V = 151936 workload); half the block bytes,
+ *                    and the bf16 gradient overwrites the student block.
+ *                    Anything else: FCT_ERR_UNSUPPORTED.
  *   workspace      : device memory of fused_linear_ce_tvd_workspace_size(V,
- *                    chunk_rows) bytes, 256-byte aligned; clobbered.
+ *                    chunk_rows, logits_dtype) bytes, 256-byte aligned;
+ *                    clobbered.  fused_linear_ce_tvd_workspace_size returns
+ *                    0 for V <= 0, chunk_rows <= 0 or an unknown dtype.
  *
- * The logits the loss sees are fp32 (bf16 products, fp32 sums); the logit
- * gradient is rounded to bf16 before the two gradient GEMMs.  The library
- * keeps one cuBLAS handle per device (created on first use); calls on one
- * device are serialised by a lock.
+ * The library keeps one cuBLAS handle per device (created on first use);
+ * calls on one device are serialised by a lock.
  */
-size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows);
+size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows,
+                                          fct_dtype logits_dtype);
 
 int fused_linear_ce_tvd_forward_backward(
     const void* h_student, int64_t ld_h_student, const void* w_student,
@@ -222,9 +231,9 @@ int fused_linear_ce_tvd_forward_backward(
     int64_t ignore_index, const float* grad_ce, const float* grad_tvd,
     int64_t grad_stride, float* ce, float* tvd, float* student_lse,
     float* teacher_lse, float* sigma, void* grad_h_student, int64_t ld_grad_h,
-    float* grad_w_student, int64_t ld_grad_w, void* workspace,
-    size_t workspace_bytes, int64_t chunk_rows, int32_t* dev_status,
-    void* stream);
+    float* grad_w_student, int64_t ld_grad_w, fct_dtype logits_dtype,
+    void* workspace, size_t workspace_bytes, int64_t chunk_rows,
+    int32_t* dev_status, void* stream);
 
 /*
  * Fused-linear CE + TVD that allocates nothing (no counterpart in the PR
@@ -237,8 +246,9 @@ int fused_linear_ce_tvd_forward_backward(
  * fragments it) and code that must not synchronise the device, which
  * cudaMalloc and cudaFree may do.  The entry point above needs a caller
  * workspace and a cuBLAS handle, whose creation allocates.  This one takes
- * the same arguments minus workspace, workspace_bytes and chunk_rows, and
- * computes the same outputs with:
+ * the same arguments minus logits_dtype, workspace, workspace_bytes and
+ * chunk_rows, and computes the outputs of the entry point above with
+ * logits_dtype = FCT_F32, with:
  *   - its logit blocks in a fixed array of FCT_NOALLOC_SCRATCH_BYTES
  *     (64 MiB) of device memory that belongs to the library (a file-scope
  *     __device__ array): the driver reserves it on each device when the

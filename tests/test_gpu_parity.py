@@ -193,6 +193,60 @@ def test_padded_and_misaligned_rows(V, ld, off, dtype):
     compare(w, fwd, grad, what=f"V={V} ld={ld} off={off} ")
 
 
+def test_row_offsets_beyond_4_gib():
+    """Rows that start more than 2^32 bytes (2^31 elements) past the base
+    pointer: every entry point gives bitwise the results of a compact layout
+    with the same 16-byte alignment, which itself matches the oracle."""
+    V, ld = 4099, (1 << 30) + 64  # bf16: row r starts r * (2 GiB + 128 B) in
+    base = workloads.make("bt1024_v32000_bf16", DEV, rows=3, V=V, dtype=torch.bfloat16, seed=9)
+    small = padded(base, 4104, 0)
+    fwd, grad, st = run(small)
+    assert st == 0
+    compare(small, fwd, grad, what="compact ")
+
+    bufs = [torch.empty(2 * ld + V, dtype=torch.bfloat16, device=DEV) for _ in range(3)]
+
+    def far(k, x=None):
+        view = bufs[k].as_strided((3, V), (ld, 1))
+        if x is not None:
+            view.copy_(x)
+        return view
+
+    s_b, t_b = far(0, base.student), far(1, base.teacher)
+    s_s, t_s = small.student, small.teacher
+    tg, gce, gtvd = base.target, base.grad_ce, base.grad_tvd
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+
+    def same(xs, ys, what):
+        torch.cuda.synchronize()
+        assert status.item() == 0, what
+        for k, (x, y) in enumerate(zip(xs, ys)):
+            assert torch.equal(x, y), f"{what} output {k}"
+
+    f_s = binding.fused_ce_tvd_forward(s_s, t_s, tg)
+    f_b = binding.fused_ce_tvd_forward(s_b, t_b, tg, dev_status=status)
+    same(f_s, f_b, "forward")
+    g_s = binding.fused_ce_tvd_backward(s_s, t_s, tg, *f_s[2:], gce, gtvd,
+                                        grad_student=same_layout_clone(s_s))
+    g_b = binding.fused_ce_tvd_backward(s_b, t_b, tg, *f_b[2:], gce, gtvd, grad_student=far(2),
+                                        dev_status=status)
+    same([g_s], [g_b], "backward")
+    o_s = binding.fused_ce_tvd_forward_backward(s_s, t_s, tg, gce, gtvd,
+                                                grad_student=same_layout_clone(s_s))
+    o_b = binding.fused_ce_tvd_forward_backward(s_b, t_b, tg, gce, gtvd, grad_student=far(2),
+                                                dev_status=status)
+    same(o_s, o_b, "single launch")
+    w_s = binding.fused_ce_tvd_forward_signs(s_s, t_s, tg)
+    w_b = binding.fused_ce_tvd_forward_signs(s_b, t_b, tg, dev_status=status)
+    same(w_s, w_b, "forward with sign words")
+    b_b = binding.fused_ce_tvd_backward_signs(s_b, t_b, tg, *w_b[2:], gce, gtvd,
+                                              grad_student=far(2), dev_status=status)
+    same([g_s], [b_b], "backward from sign words")
+    c_s = binding.ce_forward_backward(s_s, tg, gce, grad_logits=same_layout_clone(s_s))
+    c_b = binding.ce_forward_backward(s_b, tg, gce, grad_logits=far(2), dev_status=status)
+    same(c_s, c_b, "cross-entropy single launch")
+
+
 def test_empty_batch_is_a_no_op():
     s = torch.empty(0, 100, device=DEV, dtype=torch.bfloat16)
     tg = torch.empty(0, device=DEV, dtype=torch.int64)
@@ -627,21 +681,81 @@ def test_fused_linear_against_fp64(BT, ds, dt, V, chunk):
                        (np.abs(Ht.numpy()) @ np.abs(Wt.numpy()).T).max(1) * dt) * 2.0 ** -24
     check_forward(torch.float32, tgc, {k: v.cpu().numpy() for k, v in got.items()}, ref, mass,
                   what="linear ", atol=1e-5 + 2.0 * bound)
-    # gradient bounds: the logit gradient is rounded to bf16 (2^-8 relative) on
-    # top of its own tolerance (2e-3 relative, 1e-6 absolute), the GEMM sums in
-    # fp32, and grad_h is itself rounded to bf16
+    check_linear_grads(gh, gw, G, Hs.numpy(), Ws.numpy())
+
+
+def check_linear_grads(gh, gw, G, Hs, Ws, what=""):
+    """d hidden and d weight against G @ Ws and G.T @ Hs in fp64 (G: the
+    oracle's logit gradient).  Bounds: the logit gradient is rounded to bf16
+    (2^-8 relative) on top of its own tolerance (2e-3 relative, 1e-6
+    absolute), the GEMMs sum in fp32, and d hidden is itself rounded to bf16."""
+    BT, V = G.shape
     G_abs = np.abs(G)
     e_rel = 2.0 ** -8 + 2e-3 + V * 2.0 ** -24
-    ref_gh = G @ Ws.numpy()
-    tol_gh = e_rel * (G_abs @ np.abs(Ws.numpy())) + 1e-6 * np.abs(Ws.numpy()).sum(0) \
+    ref_gh = G @ Ws
+    tol_gh = e_rel * (G_abs @ np.abs(Ws)) + 1e-6 * np.abs(Ws).sum(0) \
         + 2.0 ** -8 * np.abs(ref_gh) + 1e-9
     err_gh = np.abs(gh.cpu().double().numpy() - ref_gh)
-    assert np.all(err_gh <= tol_gh), float((err_gh / tol_gh).max())
-    ref_gw = G.T @ Hs.numpy()
+    assert np.all(err_gh <= tol_gh), f"{what}grad_h {float((err_gh / tol_gh).max())}"
+    ref_gw = G.T @ Hs
     e_rel_w = 2.0 ** -8 + 2e-3 + BT * 2.0 ** -24
-    tol_gw = e_rel_w * (G_abs.T @ np.abs(Hs.numpy())) + 1e-6 * np.abs(Hs.numpy()).sum(0) + 1e-9
+    tol_gw = e_rel_w * (G_abs.T @ np.abs(Hs)) + 1e-6 * np.abs(Hs).sum(0) + 1e-9
     err_gw = np.abs(gw.cpu().double().numpy() - ref_gw)
-    assert np.all(err_gw <= tol_gw), float((err_gw / tol_gw).max())
+    assert np.all(err_gw <= tol_gw), f"{what}grad_w {float((err_gw / tol_gw).max())}"
+
+
+def _dyadic_linear_case(BT, ds, dt, V, seed):
+    """Hidden states in quarters up to 3/4 and weights in sixteenths up to
+    7/16: every product is a multiple of 1/64 and every partial sum stays far
+    below 2^24 / 64 in magnitude (hidden sizes up to 256), so the GEMMs' fp32
+    sums are exact in any order and the logits the loss kernel reads are known
+    exactly on the host."""
+    g = torch.Generator(device=DEV).manual_seed(seed)
+
+    def q(shape, k, den):
+        x = torch.randint(-k, k + 1, shape, generator=g, device=DEV).float() / den
+        return x.bfloat16()
+    hs, ht = q((BT, ds), 3, 4.0), q((BT, dt), 3, 4.0)
+    ws, wt = q((V, ds), 7, 16.0), q((V, dt), 7, 16.0)
+    tg = torch.randint(0, V, (BT,), generator=g, device=DEV)
+    tg[::7] = -100
+    return hs, ws, ht, wt, tg
+
+
+@pytest.mark.parametrize("logits_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("BT,ds,dt,V,chunk", [(50, 128, 96, 1003, 16), (33, 64, 256, 2048, 100),
+                                              (20, 256, 128, 151936, 8)])
+def test_fused_linear_exact_logits(logits_dtype, BT, ds, dt, V, chunk):
+    # With exact GEMMs the loss sees known logits (rounded once to bf16 for
+    # bf16 blocks), so the per-row outputs meet the logit-level tolerances of
+    # that element type, and they do not depend on the block size.
+    hs, ws, ht, wt, tg = _dyadic_linear_case(BT, ds, dt, V, seed=3 * BT + V)
+    gce = torch.full((BT,), 1.0 / BT, device=DEV)
+    gtvd = torch.full((BT,), 0.7 / BT, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = binding.fused_linear_ce_tvd_forward_backward(
+        hs, ws, ht, wt, tg, gce, gtvd, chunk_rows=chunk, logits_dtype=logits_dtype,
+        dev_status=status)
+    other = binding.fused_linear_ce_tvd_forward_backward(
+        hs, ws, ht, wt, tg, gce, gtvd, chunk_rows=BT, logits_dtype=logits_dtype)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    for k in range(5):
+        assert torch.equal(out[k], other[k]), k
+    Hs, Ws, Ht, Wt = (x.cpu().double() for x in (hs, ws, ht, wt))
+    Ls, Lt = (Hs @ Ws.T), (Ht @ Wt.T)
+    assert torch.equal(Ls, Ls.float().double()) and torch.equal(Lt, Lt.float().double())
+    if logits_dtype == torch.bfloat16:
+        Ls, Lt = Ls.float().bfloat16().double(), Lt.float().bfloat16().double()
+    Ls, Lt = Ls.numpy(), Lt.numpy()
+    tgc = tg.cpu().numpy()
+    ref = oracle.fused_ce_tvd_forward(Ls, Lt, tgc)
+    G, _ = oracle.fused_ce_tvd_backward(Ls, Lt, tgc, gce.cpu().numpy(), gtvd.cpu().numpy())
+    masks, mass, probs = tie_info(Ls, Lt)
+    got = dict(zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"),
+                   (x.cpu().numpy() for x in out[:5])))
+    check_forward(logits_dtype, tgc, got, ref, mass, what="linear exact ")
+    check_linear_grads(out[5], out[6], G, Hs.numpy(), Ws.numpy(), what="linear exact ")
 
 
 def test_fused_linear_chunking_is_invisible():
@@ -681,3 +795,16 @@ def test_fused_linear_autograd_wrapper_matches_direct_calls():
     fused_linear_ce_tvd_mean_loss(h2, ws, ht, wt, tg, -100, alpha, beta, chunk_rows=32).backward()
     torch.cuda.synchronize()
     assert torch.equal(h2.grad, direct[5])
+
+    # bf16 logit blocks through the wrapper
+    direct = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, gce, gtvd,
+                                                          chunk_rows=32,
+                                                          logits_dtype=torch.bfloat16)
+    h3 = hs.clone().requires_grad_(True)
+    loss = fused_linear_ce_tvd_mean_loss(h3, ws, ht, wt, tg, -100, alpha, beta, chunk_rows=32,
+                                         logits_dtype=torch.bfloat16)
+    loss.backward()
+    torch.cuda.synchronize()
+    assert torch.equal(h3.grad, direct[5])
+    assert torch.equal(loss.detach(), binding.fused_ce_tvd_mean_loss(
+        direct[0], direct[1], tg, -100, alpha, beta).reshape(()))
