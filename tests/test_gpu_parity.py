@@ -704,19 +704,20 @@ def check_linear_grads(gh, gw, G, Hs, Ws, what=""):
     assert np.all(err_gw <= tol_gw), f"{what}grad_w {float((err_gw / tol_gw).max())}"
 
 
-def _dyadic_linear_case(BT, ds, dt, V, seed):
-    """Hidden states in quarters up to 3/4 and weights in sixteenths up to
-    7/16: every product is a multiple of 1/64 and every partial sum stays far
-    below 2^24 / 64 in magnitude (hidden sizes up to 256), so the GEMMs' fp32
-    sums are exact in any order and the logits the loss kernel reads are known
-    exactly on the host."""
+def _dyadic_linear_case(BT, ds, dt, V, seed, wden=16.0):
+    """Hidden states in quarters up to 3/4 and weights in multiples of 1/wden
+    up to 7/wden: every product is a multiple of 1/(4 wden) and every partial
+    sum stays below 2^24 / (4 wden) in magnitude (d * 3/4 * 7/wden * 4 wden =
+    21 d < 2^24), so the GEMMs' fp32 sums are exact in any order and the
+    logits the loss kernel reads are known exactly on the host."""
+    assert 21 * max(ds, dt) < 2 ** 24
     g = torch.Generator(device=DEV).manual_seed(seed)
 
     def q(shape, k, den):
-        x = torch.randint(-k, k + 1, shape, generator=g, device=DEV).float() / den
-        return x.bfloat16()
+        x = torch.randint(-k, k + 1, shape, generator=g, device=DEV, dtype=torch.int16)
+        return x.to(torch.bfloat16).div_(den)
     hs, ht = q((BT, ds), 3, 4.0), q((BT, dt), 3, 4.0)
-    ws, wt = q((V, ds), 7, 16.0), q((V, dt), 7, 16.0)
+    ws, wt = q((V, ds), 7, wden), q((V, dt), 7, wden)
     tg = torch.randint(0, V, (BT,), generator=g, device=DEV)
     tg[::7] = -100
     return hs, ws, ht, wt, tg
@@ -808,3 +809,80 @@ def test_fused_linear_autograd_wrapper_matches_direct_calls():
     assert torch.equal(h3.grad, direct[5])
     assert torch.equal(loss.detach(), binding.fused_ce_tvd_mean_loss(
         direct[0], direct[1], tg, -100, alpha, beta).reshape(()))
+
+
+@pytest.mark.parametrize("logits_dtype", [torch.float32, torch.bfloat16])
+def test_fused_linear_full_size_sampled_rows(logits_dtype):
+    # The fused-linear bench workload's shapes and block size (8192 rows,
+    # hidden 4096, V = 151936, 2048-row blocks) with exact GEMMs.  The
+    # upstream gradients are nonzero on sampled rows only (block edges, an
+    # ignored row, the last row), so every other logit-gradient row is
+    # exactly 0 and the whole (V, d) weight gradient is a sum over the sampled
+    # rows, which the oracle gives.
+    BT, d, V, chunk = 8192, 4096, 151936, 2048
+    hs, ws, ht, wt, tg = _dyadic_linear_case(BT, d, d, V, seed=41, wden=64.0)
+    rows = torch.tensor([0, 7, 2047, 2048, 4095, 6001, 8191])
+    assert int(tg[7]) == -100
+    rows_d = rows.to(DEV)
+    gce = torch.zeros(BT, device=DEV)
+    gtvd = torch.zeros(BT, device=DEV)
+    gce[rows_d], gtvd[rows_d] = 1.0 / 8, 0.5 / 8
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ce, tvd, ls, lt, sg, gh, gw = binding.fused_linear_ce_tvd_forward_backward(
+        hs, ws, ht, wt, tg, gce, gtvd, chunk_rows=chunk, logits_dtype=logits_dtype,
+        dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+
+    Ws_h, Wt_h = ws.cpu(), wt.cpu()
+    Hs_r, Ht_r = hs[rows_d].cpu().double(), ht[rows_d].cpu().double()
+    n = rows.numel()
+    Ls, Lt = torch.empty(n, V, dtype=torch.float64), torch.empty(n, V, dtype=torch.float64)
+    step = 16384
+    for v0 in range(0, V, step):
+        Ls[:, v0:v0 + step] = Hs_r @ Ws_h[v0:v0 + step].double().T
+        Lt[:, v0:v0 + step] = Ht_r @ Wt_h[v0:v0 + step].double().T
+    assert torch.equal(Ls, Ls.float().double()) and torch.equal(Lt, Lt.float().double())
+    if logits_dtype == torch.bfloat16:
+        Ls, Lt = Ls.float().bfloat16().double(), Lt.float().bfloat16().double()
+    Ls, Lt = Ls.numpy(), Lt.numpy()
+    tgc = tg[rows_d].cpu().numpy()
+    ref = oracle.fused_ce_tvd_forward(Ls, Lt, tgc)
+    G, _ = oracle.fused_ce_tvd_backward(Ls, Lt, tgc, np.full(n, 1.0 / 8), np.full(n, 0.5 / 8))
+    masks, mass, probs = tie_info(Ls, Lt)
+    got = {k: v[rows_d].cpu().numpy()
+           for k, v in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"),
+                           (ce, tvd, ls, lt, sg))}
+    check_forward(logits_dtype, tgc, got, ref, mass, what="linear full size ")
+
+    # d hidden: zero outside the sampled rows; on them, the bounds of
+    # check_linear_grads with the fp64 products summed over vocabulary slices
+    others = torch.ones(BT, dtype=torch.bool, device=DEV)
+    others[rows_d] = False
+    assert torch.all(gh[others] == 0)
+    Hs_abs = np.abs(Hs_r.numpy())
+    ref_gh = np.zeros((n, d))
+    abs_gh = np.zeros((n, d))
+    w_abs_sum = np.zeros(d)
+    for v0 in range(0, V, step):
+        Wc = Ws_h[v0:v0 + step].double().numpy()
+        ref_gh += G[:, v0:v0 + step] @ Wc
+        abs_gh += np.abs(G[:, v0:v0 + step]) @ np.abs(Wc)
+        w_abs_sum += np.abs(Wc).sum(0)
+    e_rel = 2.0 ** -8 + 2e-3 + V * 2.0 ** -24
+    tol_gh = e_rel * abs_gh + 1e-6 * w_abs_sum + 2.0 ** -8 * np.abs(ref_gh) + 1e-9
+    err_gh = np.abs(gh[rows_d].cpu().double().numpy() - ref_gh)
+    assert np.all(err_gh <= tol_gh), float((err_gh / tol_gh).max())
+
+    # d weight, all V x d entries, against G.T @ H of the sampled rows
+    gw_h = gw.cpu()
+    e_rel_w = 2.0 ** -8 + 2e-3 + BT * 2.0 ** -24
+    h_abs_sum = Hs_abs.sum(0)
+    worst = 0.0
+    for v0 in range(0, V, step):
+        Gc = G[:, v0:v0 + step]
+        ref_gw = Gc.T @ Hs_r.numpy()
+        tol_gw = e_rel_w * (np.abs(Gc).T @ Hs_abs) + 1e-6 * h_abs_sum + 1e-9
+        err_gw = np.abs(gw_h[v0:v0 + step].double().numpy() - ref_gw)
+        worst = max(worst, float((err_gw / tol_gw).max()))
+    assert worst <= 1.0, worst
