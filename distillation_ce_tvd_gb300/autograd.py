@@ -113,7 +113,6 @@ class FusedLinearCETVDMeanLoss(torch.autograd.Function):
     @staticmethod
     def backward(ctx, grad_out):
         grad_h, grad_w = ctx.grads
-        ctx.grads = None
         if not torch.equal(grad_out, torch.ones_like(grad_out)):
             grad_h = None if grad_h is None else grad_h * grad_out.to(grad_h.dtype)
             grad_w = None if grad_w is None else grad_w * grad_out.to(grad_w.dtype)
