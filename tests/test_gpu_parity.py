@@ -269,6 +269,36 @@ def test_all_rows_ignored_and_out_of_range_target():
     assert torch.isnan(grad[1].float()).all() and torch.isnan(grad[3].float()).all()
 
 
+@pytest.mark.parametrize("ignore_index", [-1, 5])
+def test_other_ignore_index_values(ignore_index):
+    # ignore_index is an argument, not a constant: -1, or even a vocabulary
+    # index (rows whose target is 5 are then ignored).  A target of -100 is
+    # out of range for both.
+    import dataclasses
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=40, V=4104, seed=71)
+    w = dataclasses.replace(w, ignore_index=ignore_index)
+    w.target[[2, 9, 30]] = ignore_index
+    w.target[11] = -100
+    fwd, grad, st = run(w)
+    assert st == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+    compare(w, fwd, grad, what=f"ignore_index={ignore_index} ")
+    assert torch.all(grad[[2, 9, 30]] == 0) and torch.isnan(fwd["ce"][11])
+    f2, g2, st2 = run_single(w)
+    assert st2 == st
+    nan_safe = ~torch.isnan(fwd["ce"])
+    for k in fwd:
+        assert torch.equal(fwd[k][nan_safe], f2[k][nan_safe]), k
+    assert torch.equal(grad[nan_safe], g2[nan_safe])
+    # cross-entropy alone and the mean front end take the same argument
+    ce, lse, gl = binding.ce_forward_backward(w.student, w.target, w.grad_ce, ignore_index)
+    torch.cuda.synchronize()
+    assert torch.all(ce[[2, 9, 30]] == 0) and torch.all(gl[[2, 9, 30]] == 0)
+    assert torch.equal(ce[nan_safe], fwd["ce"][nan_safe])
+    _, _, n = binding.fused_ce_tvd_mean_upstream(w.target, ignore_index, 1.0, 1.0)
+    torch.cuda.synchronize()
+    assert int(n.item()) == int((w.target != ignore_index).sum().item())
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_inplace_matches_out_of_place(dtype):
     w = workloads.make("bt1024_v151936_bf16", DEV, rows=17, V=12345, dtype=dtype, seed=8)
@@ -861,6 +891,32 @@ def test_fused_linear_autograd_wrapper_matches_direct_calls():
     assert torch.equal(h3.grad, direct[5])
     assert torch.equal(loss.detach(), binding.fused_ce_tvd_mean_loss(
         direct[0], direct[1], tg, -100, alpha, beta).reshape(()))
+
+
+def test_fused_linear_other_ignore_index():
+    BT, d, V = 40, 64, 1003
+    hs, ws, ht, wt, tg = _dyadic_linear_case(BT, d, d, V, seed=13)
+    tg[tg == -100] = 3
+    tg[::5] = -1
+    gce = torch.full((BT,), 1.0 / BT, device=DEV)
+    gtvd = torch.full((BT,), 0.5 / BT, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, gce, gtvd, -1,
+                                                       chunk_rows=16, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    Ls = (hs.cpu().double() @ ws.cpu().double().T).numpy()
+    Lt = (ht.cpu().double() @ wt.cpu().double().T).numpy()
+    tgc = tg.cpu().numpy()
+    ref = oracle.fused_ce_tvd_forward(Ls, Lt, tgc, -1)
+    G, _ = oracle.fused_ce_tvd_backward(Ls, Lt, tgc, gce.cpu().numpy(), gtvd.cpu().numpy(), -1)
+    _, mass, _ = tie_info(Ls, Lt)
+    got = dict(zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"),
+                   (x.cpu().numpy() for x in out[:5])))
+    check_forward(torch.float32, tgc, got, ref, mass, -1, what="linear ignore -1 ")
+    assert torch.all(out[5][::5] == 0)
+    check_linear_grads(out[5], out[6], G, hs.cpu().double().numpy(), ws.cpu().double().numpy(),
+                       what="linear ignore -1 ")
 
 
 @pytest.mark.parametrize("logits_dtype", [torch.float32, torch.bfloat16])
