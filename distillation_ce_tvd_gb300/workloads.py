@@ -6,7 +6,7 @@ output without sharing any of the method's code.  Random draws come from
 ``torch.Generator`` on the requested device (the CPU and CUDA streams differ,
 so a test generates once and hands the same bytes to both sides).
 
-Named workloads follow the problem statement's configurations:
+Named workloads (the sizes the loss is tested and measured on):
 
 ================================  ======  =======  =====  ==================================
 name                              BT      V        dtype  recipe

@@ -21,7 +21,7 @@
  * two-pass (exact max, then sum of exponentials, then log) in fp64, one row
  * at a time, no blocking or fusion.
  *
- * Readings where the pages are silent (each is listed in the design notes):
+ * Readings where the pages are silent:
  *   - ignore rows: ce = tvd = lse_s = lse_t = sigma = 0 and a zero gradient row;
  *   - target outside [0, V) and not ignore_index: the row's ce is NaN, its
  *     gradient row is NaN, other outputs are computed, and bit 0x1 is set

@@ -1,7 +1,6 @@
 """Element-by-element comparison of the CUDA path against the CPU oracle.
 
-Tolerances (from the problem statement; their derivation is in the design
-notes):
+Tolerances:
   * per-row ce, tvd, student_lse, teacher_lse: abs 2e-4 for bf16 logits,
     abs 1e-5 for fp32 logits;
   * sigma: the same, widened by 2 * (oracle probability mass of the row's
