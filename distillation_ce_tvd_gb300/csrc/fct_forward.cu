@@ -46,6 +46,7 @@
 //     tvd = sigma = 0 exactly.
 #include <cooperative_groups.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "fct_common.cuh"
@@ -228,6 +229,9 @@ constexpr int kStages = 3;   // ring slots per thread: two steps in flight while
 // row per thread (V <= 262,144 bf16 with one CTA of 512 threads per row);
 // beyond that step 3 re-reads the teacher as well.
 constexpr int kMaxSignWords = 16;
+
+// Interleaved start groups of the clusters of a multi-pass launch.
+constexpr int kStaggerGroups = 8;
 
 // The feed: this thread's cursor in the sequence, issuing one step of
 // cp.async copies per call.  A pass of a row is n_full full steps of
@@ -446,6 +450,19 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   const uint4* mine = ring_mem + tid;
   // sign words of step 2 after the ring: word w of this thread at sbits[w*NT + tid]
   uint32_t* sbits = reinterpret_cast<uint32_t*>(ring_mem + kStages * F::kTensors * kPerStep * NT);
+  // Clusters start staggered in kStaggerGroups interleaved groups: started
+  // together, every SM runs its HBM-bound first pass at the same moment and
+  // its L2-bound later passes at the same moment, and they stay roughly in
+  // step.  Consecutive clusters go to different groups, so each group is
+  // spread over the whole chip.  The wait is bounded by the clock and by an
+  // iteration count.
+  if (p.stagger > 0) {
+    const long long wait =
+        static_cast<long long>(p.stagger * (cluster_id % kStaggerGroups) / kStaggerGroups);
+    const long long t0 = clock64();
+    for (int it = 0; it < (1 << 22) && clock64() - t0 < wait; ++it) {
+    }
+  }
 #pragma unroll
   for (int s = 0; s < kStages; ++s) f.feed(p, s, n_clusters);
   int slot = 0;
@@ -893,6 +910,31 @@ int per_device(PerDevice& c, Init&& init) {
   return c.value[dev];
 }
 
+// Start stagger of the multi-pass kernels: the clusters' start times are
+// spread, in kStaggerGroups interleaved groups, over stagger_fraction() times
+// an estimate of one row's time (about 0.1 clock cycles per byte a CTA reads
+// in one pass of a row, measured on GB300 for the single launch at V = 151936
+// bf16), when every cluster has at least kStaggerMinRows rows (with fewer,
+// the last group's wait costs more than the spread saves).  Measured at 8192
+// x 151936 bf16, against starting together: a spread of half a row's time in
+// 8 interleaved groups, one launch 1.619 -> 1.582 ms and the forward alone
+// 2.130 -> 2.084 ms with its backward; a whole row's time, 1.579 and 2.100;
+// the same spreads over contiguous ranges of clusters gained about half as
+// much.  FCT_STAGGER=<fraction> overrides the fraction (0 turns it off; a
+// tuning knob for measurements).
+constexpr double kStaggerCyclesPerByte = 0.1;
+constexpr int kStaggerMinRows = 32;
+
+double stagger_fraction() {
+  static const double f = [] {
+    const char* e = std::getenv("FCT_STAGGER");
+    if (e == nullptr) return 0.5;
+    const double v = std::atof(e);
+    return (v >= 0.0 && v <= 4.0) ? v : 0.5;
+  }();
+  return f;
+}
+
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per device.
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG, bool kSigns>
@@ -913,7 +955,14 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   int n = n_max;
   if (n_slots > 0 && n > n_slots) n = n_slots;
   if (n > a.BT) n = static_cast<int>(a.BT);
-  return launch_cluster(kernel, C, NT, kSmem, n, a, st);
+  FwdArgs b = a;
+  if constexpr (kTvd || kGrad) {  // several passes per row: stagger the clusters' start
+    if (a.BT >= int64_t(kStaggerMinRows) * n) {
+      const double row_bytes = (kTvd ? 2.0 : 1.0) * double(a.V) * double(sizeof(T)) / C;
+      b.stagger = static_cast<int64_t>(stagger_fraction() * kStaggerCyclesPerByte * row_bytes);
+    }
+  }
+  return launch_cluster(kernel, C, NT, kSmem, n, b, st);
 }
 
 template <typename T, int C, bool kTvd>

@@ -33,6 +33,9 @@ struct FwdArgs {
   // 16-byte vector (nullptr: none)
   uint8_t* signs = nullptr;
   int64_t ld_signs = 0;
+  // start stagger (set by the launcher): cluster i of n waits stagger * i / n
+  // clock cycles before its first load
+  int64_t stagger = 0;
 };
 
 struct FwdPlan {
