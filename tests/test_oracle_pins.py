@@ -157,6 +157,30 @@ def test_ignore_rows_and_out_of_range_target():
     assert np.all(np.isfinite(g[[0, 3]]))
 
 
+@pytest.mark.parametrize("ignore_index", [-1, 5])
+def test_ignore_index_is_the_argument(ignore_index):
+    # "Backward Pass" ignore_index handling: which rows are ignored depends
+    # only on the argument.  Rows whose target equals it give exactly what
+    # the same rows give with target -100 and the default ignore_index; a
+    # target of -100 is then an ordinary out-of-range target.
+    s, t, tg = _rows(9, 6, 12)
+    tg = tg.copy()
+    tg[[1, 4]] = ignore_index
+    ref_tg = tg.copy()
+    ref_tg[[1, 4]] = IGN
+    a = oracle.fused_ce_tvd_forward(s, t, tg, ignore_index)
+    b = oracle.fused_ce_tvd_forward(s, t, ref_tg)
+    for k in ("ce", "tvd", "student_lse", "teacher_lse", "sigma"):
+        np.testing.assert_array_equal(a[k], b[k])
+    ga, _ = oracle.fused_ce_tvd_backward(s, t, tg, 0.5, 0.25, ignore_index)
+    gb, _ = oracle.fused_ce_tvd_backward(s, t, ref_tg, 0.5, 0.25)
+    np.testing.assert_array_equal(ga, gb)
+    assert np.all(ga[[1, 4]] == 0.0)
+    tg[2] = IGN
+    out = oracle.fused_ce_tvd_forward(s, t, tg, ignore_index)
+    assert out["status"] == oracle.TARGET_OUT_OF_RANGE and math.isnan(out["ce"][2])
+
+
 # ---------------------------------------------------------------- derivatives
 
 def test_central_finite_differences():
