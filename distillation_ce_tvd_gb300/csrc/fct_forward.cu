@@ -30,6 +30,10 @@
 //     with sign from two compares (0 at ties: zero subgradient); then
 //     sum|p - q| = sigma - tau.
 //   * The grid is persistent: one cluster per row slot, looping over rows.
+//     When every cluster has many rows, the clusters start in interleaved
+//     groups spread over about half a row's time (a one-off wait on the SM
+//     clock before the first loads), so that their HBM-bound first passes do
+//     not all fall at the same moments.
 //   * With the upstream gradients known before the launch, a third pass over
 //     the still L2-resident student row writes the student gradient of the
 //     "Backward Pass" in the same launch (the single-launch forward +
