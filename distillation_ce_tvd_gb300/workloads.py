@@ -215,11 +215,17 @@ class LinearWorkload:
     ignore_index: int = IGNORE_INDEX
 
 
-def make_linear(name: str, device="cpu", rows: int | None = None) -> LinearWorkload:
+def make_linear(name: str, device="cpu", rows: int | None = None, V: int | None = None,
+                d: int | None = None) -> LinearWorkload:
     """Hidden states ~ N(0, 1) and lm_head weights ~ N(0, (2/sqrt(d))^2), so the
     logits are ~ N(0, 2^2) like the logit workloads; targets uniform with 3%
-    ignored; upstream gradients 1/BT."""
-    cfg = LINEAR_WORKLOADS[name]
+    ignored; upstream gradients 1/BT.  ``rows``, ``V`` and ``d`` (both hidden
+    sizes) override the named sizes, keeping the recipe."""
+    cfg = dict(LINEAR_WORKLOADS[name])
+    if V is not None:
+        cfg["V"] = int(V)
+    if d is not None:
+        cfg["ds"] = cfg["dt"] = int(d)
     BT = cfg["BT"] if rows is None else int(rows)
     dev = torch.device(device)
     g = _gen(dev, cfg["seed"])
