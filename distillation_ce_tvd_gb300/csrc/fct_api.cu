@@ -636,6 +636,6 @@ int fct_set_forward_cluster(int ctas_per_row) {
   return g_cluster_override.exchange(ctas_per_row);
 }
 
-int fct_version(void) { return 200; }  // 0.2.0: sign words, cross-entropy in one launch, no-allocation fused linear
+int fct_version(void) { return 300; }  // 0.3.0: the fused-linear entry point takes logits_dtype
 
 }  // extern "C"

@@ -358,7 +358,8 @@ const char* fct_status_string(int status);
  */
 int fct_set_forward_cluster(int ctas_per_row);
 
-/* Library version as 10000*major + 100*minor + patch. */
+/* Library version as 10000*major + 100*minor + patch.  300 and later: the
+ * fused-linear entry point and its workspace query take logits_dtype. */
 int fct_version(void);
 
 #ifdef __cplusplus
