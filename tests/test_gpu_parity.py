@@ -155,6 +155,55 @@ def test_full_size_sampled_rows_and_properties(name):
 
 # ------------------------------------------------------------------ edge cases
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_extreme_rows(dtype):
+    # A maximum far above everything before it (at the end of a row) and at
+    # its start, rows far from zero, -inf entries in the student, in the
+    # teacher and in both identically, a constant row and an ignored row:
+    # the first pass's rescaling paths and -inf handling.
+    V, BT = 4104, 8
+    big = 100.0 if dtype == torch.bfloat16 else 50.0  # > 64 / log2(e): forces a rescale
+    g = torch.Generator(device=DEV).manual_seed(81)
+    s = torch.randn(BT, V, generator=g, device=DEV)
+    t = s + 0.5 * torch.randn(BT, V, generator=g, device=DEV)
+    tg = torch.randint(V // 2, V - 1, (BT,), generator=g, device=DEV)
+    s[0, V - 1] = big
+    s[1, 0] = big
+    s[2] -= 200.0
+    t[2] -= 200.0
+    s[3, : V // 2] = float("-inf")
+    t[4, ::2] = float("-inf")
+    s[5, ::3] = float("-inf")
+    t[5] = s[5]
+    s[6] = 0.0
+    tg[5] = V - 2  # a finite student entry of row 5 (every third one is -inf)
+    tg[7] = -100
+    w = workloads.Workload("extreme", s.to(dtype).contiguous(), t.to(dtype).contiguous(), tg,
+                           torch.full((BT,), 1.0 / BT, device=DEV),
+                           torch.full((BT,), 0.5 / BT, device=DEV))
+    fwd, grad, st = run(w)
+    f2, g2, st2 = run_single(w)
+    assert st == st2 == 0
+    for k in fwd:
+        assert torch.equal(fwd[k], f2[k]), k
+    assert torch.equal(grad, g2)
+    sh, th = w.student.cpu(), w.teacher.cpu()
+    tgc = tg.cpu().numpy()
+    ref, ref_grad = oracle_rows(sh, th, tgc, w.grad_ce.cpu().numpy(), w.grad_tvd.cpu().numpy())
+    masks, mass, probs = tie_info(sh, th)
+    got = {k: v.cpu().numpy() for k, v in fwd.items()}
+    # the outputs are fp32: allow a few of their own ulps at large magnitudes
+    mag = np.maximum.reduce([np.abs(ref["student_lse"]), np.abs(ref["teacher_lse"]),
+                             np.abs(np.nan_to_num(ref["ce"]))])
+    atol = row_atol(dtype) + 8.0 * 2.0 ** -23 * mag
+    check_forward(dtype, tgc, got, ref, mass, what="extreme ", atol=atol)
+    check_grad(grad.cpu().double().numpy(), ref_grad, w.grad_tvd.cpu().numpy(), masks, mass,
+               probs, tgc, what="extreme ", out_dtype=dtype)
+    assert fwd["tvd"][5].item() == 0.0 and fwd["sigma"][5].item() == 0.0
+    assert abs(fwd["ce"][6].item() - np.log(V)) <= row_atol(dtype)
+    assert torch.isfinite(grad).all()
+
+
 @pytest.mark.parametrize("V", [1, 2, 3, 7, 8, 9, 17, 1023])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_small_and_ragged_vocab(V, dtype):
