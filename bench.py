@@ -321,6 +321,8 @@ def main():
                     help="headline step: one fused forward+backward launch, or the forward "
                          "and backward launches")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-block-rows", type=int, default=512,
+                    help="row block of the host-buffer entry point")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
@@ -343,7 +345,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
-    binding.set_forward_cluster(args.cluster)
+    opts = binding.options(ctas_per_row=args.cluster)
     # each rank holds its own batch of the workload (weak scaling, no exchange)
     seed = workloads.WORKLOADS[args.workload]["seed"] + 1000 * rank
     w = workloads.make(args.workload, dev, rows=args.rows, seed=seed)
@@ -359,7 +361,8 @@ def main():
 
     def fwd():
         binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, w.ignore_index, ce=ce, tvd=tvd,
-                                     student_lse=ls, teacher_lse=lt, sigma=sg, stream=stream)
+                                     student_lse=ls, teacher_lse=lt, sigma=sg, stream=stream,
+                                     options=opts)
 
     def bwd():
         binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, ls, lt, sg, w.grad_ce,
@@ -369,7 +372,7 @@ def main():
         binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
                                               w.grad_tvd, w.ignore_index, ce=ce, tvd=tvd,
                                               student_lse=ls, teacher_lse=lt, sigma=sg,
-                                              grad_student=grad, stream=stream)
+                                              grad_student=grad, stream=stream, options=opts)
 
     ce_lse = torch.empty_like(ce)
     signs = torch.empty(BT, binding.fused_ce_tvd_signs_row_bytes(V, w.student.dtype), device=dev,
@@ -379,7 +382,7 @@ def main():
     def fwd_signs():  # the forward that keeps sign words for its backward
         binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, w.ignore_index, ce=ce,
                                            tvd=tvd, student_lse=ls, teacher_lse=lt, sigma=sg,
-                                           signs=signs, stream=stream)
+                                           signs=signs, stream=stream, options=opts)
 
     def bwd_signs():
         binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, ls, lt, sg, signs,
@@ -387,7 +390,8 @@ def main():
                                             grad_student=grad, stream=stream)
 
     def ce_fwd():  # the cross-entropy subset: student only
-        binding.ce_forward(w.student, w.target, w.ignore_index, ce=ce, lse=ce_lse, stream=stream)
+        binding.ce_forward(w.student, w.target, w.ignore_index, ce=ce, lse=ce_lse, stream=stream,
+                           options=opts)
 
     def ce_bwd():
         binding.ce_backward(w.student, w.target, ce_lse, w.grad_ce, w.ignore_index,
@@ -395,7 +399,7 @@ def main():
 
     def ce_single():  # cross-entropy forward + backward in one launch
         binding.ce_forward_backward(w.student, w.target, w.grad_ce, w.ignore_index, ce=ce,
-                                    lse=ce_lse, grad_logits=grad, stream=stream)
+                                    lse=ce_lse, grad_logits=grad, stream=stream, options=opts)
 
     # the launches of one step of each path, with the algorithmic bytes of each launch
     paths = {
@@ -480,7 +484,9 @@ def main():
     step_gbs = step_bytes / (ms * 1e-3) / 1e9
     two_bytes = sum(b for _, _, b in paths["two"])
 
-    # ---- end to end through the public API: pinned host inputs in, per-row loss out
+    # ---- end to end through the C ABI's host-buffer entry point: pinned host
+    # logits, targets and upstream gradients in; the student gradient and the
+    # five per-row outputs out, every step
     e2e = None
     if not args.no_e2e:
         hs = w.student.cpu().pin_memory()
@@ -488,29 +494,20 @@ def main():
         htg = w.target.cpu().pin_memory()
         hgc = w.grad_ce.cpu().pin_memory()
         hgt = w.grad_tvd.cpu().pin_memory()
-        out_ce = torch.empty(BT, pin_memory=True)
-        out_tvd = torch.empty(BT, pin_memory=True)
+        houts = [torch.empty(BT, pin_memory=True) for _ in range(5)]
+        hgrad = torch.empty(BT, V, dtype=w.student.dtype, pin_memory=True)
+        hstatus = torch.zeros(1, dtype=torch.int32, pin_memory=True)
+        rows_e2e = min(args.e2e_block_rows, BT)
+        wsp = torch.empty(binding.fused_ce_tvd_host_workspace_size(V, w.student.dtype, rows_e2e),
+                          device=dev, dtype=torch.uint8)
         h2d = sum(x.numel() * x.element_size() for x in (hs, ht, htg, hgc, hgt))
-        d2h = 2 * BT * 4
+        d2h = hgrad.numel() * hgrad.element_size() + 5 * BT * 4 + 4
 
         def e2e_step():
-            # host logits in, per-row ce and tvd out; the copies of later row
-            # blocks overlap the compute of earlier ones
-            w.grad_ce.copy_(hgc, non_blocking=True)
-            w.grad_tvd.copy_(hgt, non_blocking=True)
-            if args.path == "single":
-                binding.fused_ce_tvd_forward_backward_from_host(
-                    hs, ht, htg, w.grad_ce, w.grad_tvd, w.student, w.teacher, w.target,
-                    w.ignore_index, ce=ce, tvd=tvd, student_lse=ls, teacher_lse=lt, sigma=sg,
-                    grad_student=grad, stream=stream)
-            else:
-                w.student.copy_(hs, non_blocking=True)
-                w.teacher.copy_(ht, non_blocking=True)
-                w.target.copy_(htg, non_blocking=True)
-                for _, fn, _ in paths[args.path]:
-                    fn()
-            out_ce.copy_(ce, non_blocking=True)
-            out_tvd.copy_(tvd, non_blocking=True)
+            binding.fused_ce_tvd_forward_backward_host(
+                hs, ht, htg, hgc, hgt, w.ignore_index, ce=houts[0], tvd=houts[1],
+                student_lse=houts[2], teacher_lse=houts[3], sigma=houts[4], grad_student=hgrad,
+                block_rows=rows_e2e, workspace=wsp, status=hstatus, stream=stream)
 
         for _ in range(2):
             e2e_step()
@@ -524,10 +521,14 @@ def main():
         b.record(stream)
         torch.cuda.synchronize(dev)
         e2e_ms = sharding.max_over_ranks(a.elapsed_time(b) / E, world, dev)
+        if int(hstatus.item()) != 0:
+            raise RuntimeError(f"device status {int(hstatus.item())} in the end-to-end run")
         e2e = {"value": world * BT / (e2e_ms * 1e-3), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "steps": E}
-        del hs, ht
+               "steps": E, "api": "fused_ce_tvd_forward_backward_host (C ABI, host buffers)",
+               "block_rows": rows_e2e,
+               "link_gbs": (h2d + d2h) / (e2e_ms * 1e-3) / 1e9}
+        del hs, ht, hgrad, wsp
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:

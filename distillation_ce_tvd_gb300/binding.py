@@ -22,14 +22,29 @@ IGNORE_INDEX = -100
 _lock = threading.Lock()
 _lib = None
 
-EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
+EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_forward_ex", "fused_ce_tvd_backward",
+           "fused_ce_tvd_forward_backward", "fused_ce_tvd_forward_backward_ex",
+           "fused_ce_tvd_host_workspace_size", "fused_ce_tvd_forward_backward_host",
            "fused_ce_tvd_signs_row_bytes", "fused_ce_tvd_forward_signs",
-           "fused_ce_tvd_backward_signs",
-           "ce_forward", "ce_backward", "ce_forward_backward", "fused_ce_tvd_mean_upstream",
-           "fused_ce_tvd_mean_loss",
+           "fused_ce_tvd_forward_signs_ex", "fused_ce_tvd_backward_signs",
+           "ce_forward", "ce_forward_ex", "ce_backward", "ce_forward_backward",
+           "ce_forward_backward_ex", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fused_linear_ce_tvd_forward_backward_noalloc",
-           "fct_status_string", "fct_set_forward_cluster", "fct_version")
+           "fct_status_string", "fct_version")
+
+
+class Options(ctypes.Structure):
+    """fct_options: launch options of one call (see include/fused_ce_tvd.h)."""
+    _fields_ = [("ctas_per_row", ctypes.c_int32), ("l2_keep", ctypes.c_int32),
+                ("stagger", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+def options(ctas_per_row: int = 0, l2_keep: int = 0, stagger: float = 0.0) -> Options | None:
+    """An fct_options value, or None when every field is automatic."""
+    if ctas_per_row == 0 and l2_keep == 0 and stagger == 0.0:
+        return None
+    return Options(int(ctas_per_row), int(l2_keep), float(stagger), 0)
 
 
 class FctError(RuntimeError):
@@ -48,27 +63,49 @@ def load(path: str | None = None) -> ctypes.CDLL:
             return _lib
         lib = ctypes.CDLL(path or _build.build())
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        op = ctypes.POINTER(Options)
         lib.fused_ce_tvd_forward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                              vp, vp, vp, vp, vp, vp, vp]
+        lib.fused_ce_tvd_forward_ex.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                                vp, vp, vp, vp, vp, op, vp, vp]
+        lib.fused_ce_tvd_forward_ex.restype = i32
         lib.fused_ce_tvd_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                               vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
         lib.fused_ce_tvd_forward_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                                       vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
                                                       vp, vp]
+        lib.fused_ce_tvd_forward_backward_ex.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64,
+                                                         i64, vp, vp, i64, vp, vp, vp, vp, vp,
+                                                         vp, i64, op, vp, vp]
+        lib.fused_ce_tvd_forward_backward_ex.restype = i32
+        lib.fused_ce_tvd_host_workspace_size.argtypes = [i64, i32, i64]
+        lib.fused_ce_tvd_host_workspace_size.restype = ctypes.c_size_t
+        lib.fused_ce_tvd_forward_backward_host.argtypes = [
+            vp, i64, vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
+            vp, ctypes.c_size_t, i64, vp, vp]
+        lib.fused_ce_tvd_forward_backward_host.restype = i32
         lib.fused_ce_tvd_signs_row_bytes.argtypes = [i64, i32]
         lib.fused_ce_tvd_signs_row_bytes.restype = i64
         lib.fused_ce_tvd_forward_signs.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                                    vp, vp, vp, vp, vp, vp, i64, vp, vp]
         lib.fused_ce_tvd_forward_signs.restype = i32
+        lib.fused_ce_tvd_forward_signs_ex.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
+                                                      vp, vp, vp, vp, vp, vp, i64, op, vp, vp]
+        lib.fused_ce_tvd_forward_signs_ex.restype = i32
         lib.fused_ce_tvd_backward_signs.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64,
                                                     vp, vp, vp, vp, i64, vp, vp, i64, vp, i64,
                                                     vp, vp]
         lib.fused_ce_tvd_backward_signs.restype = i32
         lib.ce_forward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
+        lib.ce_forward_ex.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, op, vp, vp]
+        lib.ce_forward_ex.restype = i32
         lib.ce_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, vp, i64, vp, i64, vp, vp]
         lib.ce_forward_backward.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, i64, vp, vp, vp,
                                             i64, vp, vp]
         lib.ce_forward_backward.restype = i32
+        lib.ce_forward_backward_ex.argtypes = [vp, i64, i32, vp, i64, i64, i64, vp, i64, vp, vp,
+                                               vp, i64, op, vp, vp]
+        lib.ce_forward_backward_ex.restype = i32
         dbl = ctypes.c_double
         lib.fused_linear_ce_tvd_workspace_size.argtypes = [i64, i64, i32]
         lib.fused_linear_ce_tvd_workspace_size.restype = ctypes.c_size_t
@@ -88,8 +125,6 @@ def load(path: str | None = None) -> ctypes.CDLL:
             getattr(lib, f).restype = i32
         lib.fct_status_string.argtypes = [i32]
         lib.fct_status_string.restype = ctypes.c_char_p
-        lib.fct_set_forward_cluster.argtypes = [i32]
-        lib.fct_set_forward_cluster.restype = i32
         lib.fct_version.argtypes = []
         lib.fct_version.restype = i32
         if path is None:
@@ -99,14 +134,6 @@ def load(path: str | None = None) -> ctypes.CDLL:
 
 def status_string(status: int) -> str:
     return load().fct_status_string(int(status)).decode()
-
-
-def set_forward_cluster(ctas_per_row: int) -> int:
-    """CTAs per row of the fused forward (1, 2, 4, 8; 0 = automatic)."""
-    prev = load().fct_set_forward_cluster(int(ctas_per_row))
-    if prev < 0:
-        raise ValueError("ctas_per_row must be 0, 1, 2, 4 or 8")
-    return prev
 
 
 def version() -> int:
@@ -147,6 +174,15 @@ def _upstream(g, BT: int, device, name: str):
     return _rows(g, BT, name), 1
 
 
+def _opts(opts):
+    """(suffix, extra ctypes args): the plain entry point for None, else its _ex form."""
+    if opts is None:
+        return "", ()
+    if not isinstance(opts, Options):
+        raise TypeError("options must be a binding.Options (see binding.options())")
+    return "_ex", (ctypes.byref(opts),)
+
+
 def _stream(stream):
     if stream is None:
         stream = torch.cuda.current_stream()
@@ -168,7 +204,7 @@ def _out(x, n, device, name):
 
 def fused_ce_tvd_forward(student, teacher, target, ignore_index=IGNORE_INDEX, *, ce=None,
                          tvd=None, student_lse=None, teacher_lse=None, sigma=None,
-                         dev_status=None, stream=None):
+                         dev_status=None, stream=None, options=None):
     """Per-row (ce, tvd, student_lse, teacher_lse, sigma), all fp32 (BT,)."""
     code, ld_s = _logits(student, "student")
     code_t, ld_t = _logits(teacher, "teacher")
@@ -179,9 +215,10 @@ def fused_ce_tvd_forward(student, teacher, target, ignore_index=IGNORE_INDEX, *,
     _rows(target, BT, "target", torch.int64)
     outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
                                              (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
-    rc = load().fused_ce_tvd_forward(_ptr(student), ld_s, _ptr(teacher), ld_t, code,
-                                     _ptr(target), BT, V, int(ignore_index), *map(_ptr, outs),
-                                     _ptr(dev_status), _stream(stream))
+    sfx, extra = _opts(options)
+    rc = getattr(load(), "fused_ce_tvd_forward" + sfx)(
+        _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V, int(ignore_index),
+        *map(_ptr, outs), *extra, _ptr(dev_status), _stream(stream))
     _check(rc, "fused_ce_tvd_forward")
     return tuple(outs)
 
@@ -227,7 +264,7 @@ def fused_ce_tvd_forward_backward(student, teacher, target, grad_ce, grad_tvd,
                                   ignore_index=IGNORE_INDEX, *, ce=None, tvd=None,
                                   student_lse=None, teacher_lse=None, sigma=None,
                                   grad_student=None, inplace=False, dev_status=None,
-                                  stream=None):
+                                  stream=None, options=None):
     """Forward and backward in one launch, given the upstream gradients.
 
     Returns (ce, tvd, student_lse, teacher_lse, sigma, grad_student); the
@@ -254,10 +291,11 @@ def fused_ce_tvd_forward_backward(student, teacher, target, grad_ce, grad_tvd,
     code_g, ld_g = _logits(grad_student, "grad_student")
     if code_g != code or grad_student.shape != student.shape:
         raise ValueError("grad_student must match the student's shape and dtype")
-    rc = load().fused_ce_tvd_forward_backward(
+    sfx, extra = _opts(options)
+    rc = getattr(load(), "fused_ce_tvd_forward_backward" + sfx)(
         _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V, int(ignore_index),
         _ptr(gce), _ptr(gtvd), stride, *map(_ptr, outs), _ptr(grad_student), ld_g,
-        _ptr(dev_status), _stream(stream))
+        *extra, _ptr(dev_status), _stream(stream))
     _check(rc, "fused_ce_tvd_forward_backward")
     return (*outs, grad_student)
 
@@ -281,7 +319,7 @@ def _signs(x, BT, V, dtype, device):
 
 def fused_ce_tvd_forward_signs(student, teacher, target, ignore_index=IGNORE_INDEX, *, ce=None,
                                tvd=None, student_lse=None, teacher_lse=None, sigma=None,
-                               signs=None, dev_status=None, stream=None):
+                               signs=None, dev_status=None, stream=None, options=None):
     """fused_ce_tvd_forward that also stores the sign words its backward reads
     instead of the teacher.  Returns (ce, tvd, student_lse, teacher_lse, sigma,
     signs), signs a (BT, row bytes) uint8 tensor."""
@@ -296,10 +334,10 @@ def fused_ce_tvd_forward_signs(student, teacher, target, ignore_index=IGNORE_IND
                                              (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
     signs = _signs(signs, BT, V, student.dtype, dev)
     ld_b = int(signs.stride(0)) if BT > 1 else int(signs.shape[1])
-    rc = load().fused_ce_tvd_forward_signs(_ptr(student), ld_s, _ptr(teacher), ld_t, code,
-                                           _ptr(target), BT, V, int(ignore_index),
-                                           *map(_ptr, outs), _ptr(signs), ld_b,
-                                           _ptr(dev_status), _stream(stream))
+    sfx, extra = _opts(options)
+    rc = getattr(load(), "fused_ce_tvd_forward_signs" + sfx)(
+        _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V, int(ignore_index),
+        *map(_ptr, outs), _ptr(signs), ld_b, *extra, _ptr(dev_status), _stream(stream))
     _check(rc, "fused_ce_tvd_forward_signs")
     return (*outs, signs)
 
@@ -341,15 +379,17 @@ def fused_ce_tvd_backward_signs(student, teacher, target, student_lse, teacher_l
 
 
 def ce_forward(logits, target, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,
-               dev_status=None, stream=None):
+               dev_status=None, stream=None, options=None):
     """Per-row (ce, lse) of plain cross-entropy, fp32 (BT,)."""
     code, ld = _logits(logits, "logits")
     BT, V = logits.shape
     _rows(target, BT, "target", torch.int64)
     ce = _out(ce, BT, logits.device, "ce")
     lse = _out(lse, BT, logits.device, "lse")
-    rc = load().ce_forward(_ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index),
-                           _ptr(ce), _ptr(lse), _ptr(dev_status), _stream(stream))
+    sfx, extra = _opts(options)
+    rc = getattr(load(), "ce_forward" + sfx)(_ptr(logits), ld, code, _ptr(target), BT, V,
+                                             int(ignore_index), _ptr(ce), _ptr(lse), *extra,
+                                             _ptr(dev_status), _stream(stream))
     _check(rc, "ce_forward")
     return ce, lse
 
@@ -377,7 +417,8 @@ def ce_backward(logits, target, lse, grad_ce, ignore_index=IGNORE_INDEX, *, grad
 
 
 def ce_forward_backward(logits, target, grad_ce, ignore_index=IGNORE_INDEX, *, ce=None, lse=None,
-                        grad_logits=None, inplace=False, dev_status=None, stream=None):
+                        grad_logits=None, inplace=False, dev_status=None, stream=None,
+                        options=None):
     """Cross-entropy forward and backward in one launch: (ce, lse, grad_logits),
     bit-identical to ce_forward followed by ce_backward."""
     code, ld = _logits(logits, "logits")
@@ -394,9 +435,10 @@ def ce_forward_backward(logits, target, grad_ce, ignore_index=IGNORE_INDEX, *, c
     code_g, ld_g = _logits(grad_logits, "grad_logits")
     if code_g != code or grad_logits.shape != logits.shape:
         raise ValueError("grad_logits must match the logits' shape and dtype")
-    rc = load().ce_forward_backward(_ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index),
-                                    _ptr(gce), stride, _ptr(ce), _ptr(lse), _ptr(grad_logits), ld_g,
-                                    _ptr(dev_status), _stream(stream))
+    sfx, extra = _opts(options)
+    rc = getattr(load(), "ce_forward_backward" + sfx)(
+        _ptr(logits), ld, code, _ptr(target), BT, V, int(ignore_index), _ptr(gce), stride,
+        _ptr(ce), _ptr(lse), _ptr(grad_logits), ld_g, *extra, _ptr(dev_status), _stream(stream))
     _check(rc, "ce_forward_backward")
     return ce, lse, grad_logits
 
@@ -432,57 +474,103 @@ def fused_ce_tvd_mean_loss(ce, tvd, target, ignore_index=IGNORE_INDEX, alpha=1.0
     return out
 
 
-def fused_ce_tvd_forward_backward_from_host(student_h, teacher_h, target_h, grad_ce, grad_tvd,
-                                            student, teacher, target, ignore_index=IGNORE_INDEX,
-                                            *, ce=None, tvd=None, student_lse=None,
-                                            teacher_lse=None, sigma=None, grad_student=None,
-                                            block_rows=1024, copy_streams=2, stream=None):
-    """Single-launch forward + backward for logits that live in pinned host memory.
+def fused_ce_tvd_host_workspace_size(V: int, dtype, block_rows: int) -> int:
+    """Bytes of device workspace fused_ce_tvd_forward_backward_host needs."""
+    code = {torch.float32: FCT_F32, torch.bfloat16: FCT_BF16}[dtype]
+    return int(load().fused_ce_tvd_host_workspace_size(int(V), code, int(block_rows)))
 
-    Row blocks are copied into the device tensors ``student``/``teacher``/
-    ``target`` on ``copy_streams`` side streams (several DMA engines at once),
-    and each block is computed on ``stream`` as soon as its copy lands, so the
-    transfer of later blocks overlaps the compute of earlier ones.  Rows are
-    independent, so the results equal one call on the whole batch.  Returns
-    the same tuple as fused_ce_tvd_forward_backward; ordering on ``stream``
-    is as if everything ran there.
+
+def _host(x, name, dtype=None, dims=None):
+    if x.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if dtype is not None and x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}")
+    if dims is not None and x.dim() != dims:
+        raise ValueError(f"{name} must have {dims} dimension(s)")
+    if x.dim() == 1 and x.numel() > 1 and x.stride(0) != 1:
+        raise ValueError(f"{name} must be contiguous")
+    if x.dim() == 2 and x.shape[1] > 1 and x.stride(1) != 1:
+        raise ValueError(f"{name} must have unit stride along V")
+    return x
+
+
+def fused_ce_tvd_forward_backward_host(student, teacher, target, grad_ce, grad_tvd,
+                                       ignore_index=IGNORE_INDEX, *, ce=None, tvd=None,
+                                       student_lse=None, teacher_lse=None, sigma=None,
+                                       grad_student=None, want_grad=True, block_rows=512,
+                                       workspace=None, status=None, device=None, stream=None):
+    """Single-launch forward + backward with every input and output in host memory.
+
+    ``student``/``teacher`` (BT, V), ``target`` (BT,) int64 and the upstream
+    gradients (BT values or one) are CPU tensors, page-locked for the copies
+    to overlap the compute (``tensor.pin_memory()``).  The library copies row
+    blocks of ``block_rows`` rows through a device ``workspace`` (allocated
+    here when not given), computes them, and copies the gradient and the five
+    per-row outputs back into CPU tensors (allocated pinned when not given).
+    Returns (ce, tvd, student_lse, teacher_lse, sigma, grad_student); read them
+    after synchronising ``stream``.  ``status`` (a 1-element int32 CPU tensor)
+    receives the device status bits.
     """
-    if not (student_h.is_pinned() and teacher_h.is_pinned()):
-        raise ValueError("host logits must be in pinned memory")
-    BT = student.shape[0]
-    dev = student.device
-    main = stream if stream is not None else torch.cuda.current_stream(dev)
-    outs = [_out(x, BT, dev, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
-                                             (teacher_lse, "teacher_lse"), (sigma, "sigma"))]
-    if grad_student is None:
-        grad_student = torch.empty_like(student)
-    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
-    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    _host(student, "student", dims=2)
+    _host(teacher, "teacher", dims=2)
+    if student.dtype != teacher.dtype or student.shape != teacher.shape:
+        raise ValueError("student and teacher must share shape and dtype")
+    code = {torch.float32: FCT_F32, torch.bfloat16: FCT_BF16}.get(student.dtype)
+    if code is None:
+        raise TypeError(f"dtype {student.dtype} is not float32 or bfloat16")
+    BT, V = student.shape
+    ld_s = max(int(student.stride(0)) if BT > 1 else V, V)
+    ld_t = max(int(teacher.stride(0)) if BT > 1 else V, V)
+    _host(target, "target", torch.int64, 1)
+    if target.numel() != BT:
+        raise ValueError("target must hold BT values")
+    ups = []
+    for g, name in ((grad_ce, "grad_ce"), (grad_tvd, "grad_tvd")):
+        if not torch.is_tensor(g):
+            g = torch.tensor([float(g)], dtype=torch.float32)
+        _host(g, name, torch.float32)
+        g = g.reshape(-1) if g.dim() != 1 else g
+        if g.numel() not in (1, BT) or (g.numel() > 1 and g.stride(0) != 1):
+            raise ValueError(f"{name} must be a contiguous float32 vector of {BT} values or one")
+        ups.append(g)
+    stride_ce, stride_tvd = int(ups[0].numel() != 1 or BT == 1), int(ups[1].numel() != 1 or BT == 1)
     if stride_ce != stride_tvd:
-        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
-    per_row = stride_ce == 1 or stride_tvd == 1
-    copiers = [torch.cuda.Stream(dev) for _ in range(max(1, copy_streams))]
-    start = torch.cuda.Event()
-    start.record(main)  # the copies must not overwrite buffers still in use
-    for i, r0 in enumerate(range(0, BT, block_rows)):
-        r1 = min(BT, r0 + block_rows)
-        cs = copiers[i % len(copiers)]
-        cs.wait_event(start)
-        with torch.cuda.stream(cs):
-            student[r0:r1].copy_(student_h[r0:r1], non_blocking=True)
-            teacher[r0:r1].copy_(teacher_h[r0:r1], non_blocking=True)
-            target[r0:r1].copy_(target_h[r0:r1], non_blocking=True)
-        done = torch.cuda.Event()
-        done.record(cs)
-        main.wait_event(done)
-        g1 = (gce[r0:r1], gtvd[r0:r1]) if per_row else (gce, gtvd)
-        fused_ce_tvd_forward_backward(
-            student[r0:r1], teacher[r0:r1], target[r0:r1], g1[0], g1[1], ignore_index,
-            ce=outs[0][r0:r1], tvd=outs[1][r0:r1], student_lse=outs[2][r0:r1],
-            teacher_lse=outs[3][r0:r1], sigma=outs[4][r0:r1], grad_student=grad_student[r0:r1],
-            stream=main)
-    for cs in copiers:  # the caller's stream owns the buffers again afterwards
-        main.wait_stream(cs)
+        ups = [u.expand(BT).contiguous() if u.numel() == 1 else u for u in ups]
+    stride = max(stride_ce, stride_tvd)
+    pin = student.is_pinned()
+    outs = []
+    for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),
+                 (teacher_lse, "teacher_lse"), (sigma, "sigma")):
+        if x is None:
+            x = torch.empty(BT, dtype=torch.float32, pin_memory=pin)
+        _host(x, n, torch.float32, 1)
+        if x.numel() != BT:
+            raise ValueError(f"{n} must hold BT values")
+        outs.append(x)
+    if grad_student is None and want_grad:
+        grad_student = torch.empty(BT, V, dtype=student.dtype, pin_memory=pin)
+    ld_g = V
+    if grad_student is not None:
+        _host(grad_student, "grad_student", student.dtype, 2)
+        if grad_student.shape != student.shape:
+            raise ValueError("grad_student must match the student's shape")
+        ld_g = max(int(grad_student.stride(0)) if BT > 1 else V, V)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    rows = max(1, min(int(block_rows), max(BT, 1)))
+    need = fused_ce_tvd_host_workspace_size(V, student.dtype, rows)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    if not workspace.is_cuda:
+        raise ValueError("workspace must be device memory")
+    if status is not None:
+        _host(status, "status", torch.int32, 1)
+    with torch.cuda.device(dev):
+        rc = load().fused_ce_tvd_forward_backward_host(
+            _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, V,
+            int(ignore_index), _ptr(ups[0]), _ptr(ups[1]), stride, *map(_ptr, outs),
+            _ptr(grad_student), ld_g, _ptr(workspace),
+            workspace.numel() * workspace.element_size(), rows, _ptr(status), _stream(stream))
+    _check(rc, "fused_ce_tvd_forward_backward_host")
     return (*outs, grad_student)
 
 
@@ -582,10 +670,12 @@ def fused_linear_ce_tvd_forward_backward_noalloc(h_student, w_student, h_teacher
     _rows(target, BT, "target", torch.int64)
     strides = []
     for g, name in ((grad_ce, "grad_ce"), (grad_tvd, "grad_tvd")):
-        if not torch.is_tensor(g) or g.numel() not in (1, BT):
-            raise ValueError(f"{name} must be a CUDA tensor of {BT} values or of one value")
+        # exactly the tensor handed to the library: a 1-D vector (no reshape,
+        # which could silently copy a non-contiguous view)
+        if not torch.is_tensor(g) or g.dim() != 1 or g.numel() not in (1, BT):
+            raise ValueError(f"{name} must be a 1-D CUDA tensor of {BT} values or of one value")
         strides.append(0 if g.numel() == 1 and BT != 1 else 1)
-        _rows(g.reshape(-1), g.numel(), name)
+        _rows(g, g.numel(), name)
     if strides[0] != strides[1]:
         raise ValueError("grad_ce and grad_tvd must both be per-row or both be one value")
     outs = [_rows(x, BT, n) for x, n in ((ce, "ce"), (tvd, "tvd"), (student_lse, "student_lse"),

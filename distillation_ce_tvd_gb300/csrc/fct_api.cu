@@ -1,9 +1,6 @@
 // C ABI of libfused_ce_tvd.so: argument checks, launch planning, dispatch.
 // The operations themselves are described in include/fused_ce_tvd.h.
-#include <atomic>
-#include <cstdlib>
 #include <mutex>
-#include <string>
 
 #include "fct_internal.h"
 
@@ -18,7 +15,6 @@ struct DeviceInfo {
 
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
-std::atomic<int> g_cluster_override{0};
 
 // Properties of the calling thread's current device, queried once.
 int current_device(DeviceInfo* out) {
@@ -64,9 +60,19 @@ Range vec_range(const void* p, int64_t n, size_t e) {
 }
 bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
 
-int check_logits(const void* x, int64_t ld, int dtype, int64_t V) {
+// Whether a (rows, cols) matrix of e-byte elements with row stride ld spans
+// at most 2^62 bytes, checked without overflowing, so that every byte range
+// and element offset computed from the sizes is exact.
+bool span_fits(int64_t rows, int64_t ld, int64_t cols, int64_t e) {
+  const int64_t lim = (int64_t(1) << 62) / e;
+  if (rows <= 0 || cols <= 0 || ld < cols || cols > lim) return false;
+  return rows - 1 <= (lim - cols) / ld;
+}
+
+int check_logits(const void* x, int64_t ld, int dtype, int64_t V, int64_t BT) {
   if (x == nullptr) return FCT_ERR_INVALID_ARG;
   if (ld < V) return FCT_ERR_INVALID_ARG;
+  if (!span_fits(BT, ld, V, static_cast<int64_t>(elem_size(dtype)))) return FCT_ERR_UNSUPPORTED;
   if (!aligned(x, elem_size(dtype))) return FCT_ERR_ALIGNMENT;
   return FCT_OK;
 }
@@ -91,32 +97,45 @@ int check_common(int dtype, const int64_t* target, int64_t BT, int64_t V) {
   return FCT_OK;
 }
 
+// Launch options of one call: NULL means automatic.  Returns an fct_status.
+int check_options(const fct_options* o) {
+  if (o == nullptr) return FCT_OK;
+  const int c = o->ctas_per_row;
+  if (c != 0 && c != 1 && c != 2 && c != 4 && c != 8) return FCT_ERR_INVALID_ARG;
+  if (o->l2_keep != 0 && o->l2_keep != 1) return FCT_ERR_INVALID_ARG;
+  if (!(o->stagger <= 4.0f) || o->reserved != 0) return FCT_ERR_INVALID_ARG;  // rejects NaN too
+  return FCT_OK;
+}
+
+// Default start stagger of the multi-pass forward kernels: half of an
+// estimated row time (measured best for the forward alone, inside the flat
+// optimum for the single launch at 8192 x 151936 bf16).
+constexpr double kDefaultStagger = 0.5;
+
 // Rows in flight and CTAs per row for the two-pass fused forward.  The
 // second pass re-reads each row from L2, so the rows in flight times the
 // bytes of a student+teacher row must stay inside L2 (80%: measured on
 // GB300, one CTA per row at V = 151936 bf16 beats splitting rows); rows are split
 // over a cluster of C CTAs until every SM still gets at least one CTA.
-// Depends on V, the element type and the device only (never on BT), so
-// results do not depend on how the rows are batched.
+// Depends on V, the element type, the device and the call's options only
+// (never on BT), so results do not depend on how the rows are batched.
 // kept: the row re-read from L2 in a later pass is student + teacher (tvd),
 // or the student alone (cross-entropy in one launch, ce_grad).
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec,
-                          bool ce_grad = false) {
-  fct::FwdPlan plan{vec, 1, 0, false};
-  // FCT_L2_KEEP=normal tags rows that are read again with evict_normal
-  // instead of evict_last (a tuning experiment).
-  static const bool keep_normal = [] {
-    const char* e = std::getenv("FCT_L2_KEEP");
-    return e && std::string(e) == "normal";
-  }();
-  plan.keep_normal = keep_normal;
+                          bool ce_grad = false, const fct_options* opts = nullptr) {
+  fct::FwdPlan plan{vec, 1, 0, false, kDefaultStagger};
+  if (opts != nullptr) {
+    plan.keep_normal = opts->l2_keep == 1;
+    if (opts->stagger > 0.f) plan.stagger = opts->stagger;
+    if (opts->stagger < 0.f) plan.stagger = 0.0;
+  }
   if (!tvd && !ce_grad) return plan;  // one pass: nothing to keep in L2
   const double row_bytes =
       (tvd ? 2.0 : 1.0) * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
   const double budget = 0.80 * static_cast<double>(d.l2_bytes);
   int64_t fit = static_cast<int64_t>(budget / row_bytes);
   if (fit < 1) fit = 1;
-  int C = g_cluster_override.load();
+  int C = opts ? opts->ctas_per_row : 0;
   if (C == 0) {
     C = 1;
     while (C < 8 && fit * C < d.sms) C *= 2;
@@ -134,15 +153,17 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
                  int dtype, const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
                  float* ce, float* tvd, float* lse_s, float* lse_t, float* sigma,
                  int32_t* dev_status, void* stream, uint8_t* signs = nullptr,
-                 int64_t ld_signs = 0) {
+                 int64_t ld_signs = 0, const fct_options* opts = nullptr) {
   const bool fused = (tvd != nullptr);
   if (signs != nullptr && !fused) return FCT_ERR_INVALID_ARG;
   if (BT < 0) return FCT_ERR_INVALID_ARG;
-  if (BT == 0) return FCT_OK;
-  int rc = check_common(dtype, target, BT, V);
+  int rc = check_options(opts);
   if (rc != FCT_OK) return rc;
-  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
-  if (fused && (rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
+  if (BT == 0) return FCT_OK;
+  rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V, BT)) != FCT_OK) return rc;
+  if (fused && (rc = check_logits(teacher, ld_t, dtype, V, BT)) != FCT_OK) return rc;
   float* outs[5] = {ce, lse_s, tvd, lse_t, sigma};
   const int n_out = fused ? 5 : 2;
   for (int i = 0; i < n_out; ++i) {
@@ -180,7 +201,7 @@ int forward_impl(const void* student, int64_t ld_s, const void* teacher, int64_t
   // Cross-entropy alone takes the row split of its single launch
   // (ce_forward_backward), so both reduce each row in the same order and give
   // the same bits.
-  const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec, /*ce_grad=*/!fused);
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, fused, vec, /*ce_grad=*/!fused, opts);
   a.keep_normal = plan.keep_normal ? 1 : 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (signs != nullptr) {
@@ -211,9 +232,9 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
   if (BT == 0) return FCT_OK;
   int rc = check_common(dtype, target, BT, V);
   if (rc != FCT_OK) return rc;
-  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
-  if (fused && (rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
-  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V, BT)) != FCT_OK) return rc;
+  if (fused && (rc = check_logits(teacher, ld_t, dtype, V, BT)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V, BT)) != FCT_OK) return rc;
   if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
   const float* rows[5] = {lse_s, grad_ce, lse_t, sigma, grad_tvd};
   const int n_rows = fused ? 5 : 2;
@@ -263,14 +284,16 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
                           int64_t ignore_index, const float* grad_ce, const float* grad_tvd,
                           int64_t grad_stride, float* ce, float* tvd, float* lse_s, float* lse_t,
                           float* sigma, void* grad, int64_t ld_g, int32_t* dev_status,
-                          void* stream) {
+                          void* stream, const fct_options* opts = nullptr) {
   if (BT < 0) return FCT_ERR_INVALID_ARG;
-  if (BT == 0) return FCT_OK;
-  int rc = check_common(dtype, target, BT, V);
+  int rc = check_options(opts);
   if (rc != FCT_OK) return rc;
-  if ((rc = check_logits(student, ld_s, dtype, V)) != FCT_OK) return rc;
-  if ((rc = check_logits(teacher, ld_t, dtype, V)) != FCT_OK) return rc;
-  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if (BT == 0) return FCT_OK;
+  rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V, BT)) != FCT_OK) return rc;
+  if ((rc = check_logits(teacher, ld_t, dtype, V, BT)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V, BT)) != FCT_OK) return rc;
   if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
   if (grad_ce == nullptr || grad_tvd == nullptr) return FCT_ERR_INVALID_ARG;
   if (!aligned(grad_ce, 4) || !aligned(grad_tvd, 4)) return FCT_ERR_ALIGNMENT;
@@ -305,7 +328,7 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
   if (!vec) {
     // Unaligned rows: the two-launch path gives the same results.
     rc = forward_impl(student, ld_s, teacher, ld_t, dtype, target, BT, V, ignore_index, ce, tvd,
-                      lse_s, lse_t, sigma, dev_status, stream);
+                      lse_s, lse_t, sigma, dev_status, stream, nullptr, 0, opts);
     if (rc != FCT_OK) return rc;
     return backward_impl(student, ld_s, teacher, ld_t, dtype, target, BT, V, ignore_index, lse_s,
                          lse_t, sigma, grad_ce, grad_tvd, grad_stride, grad, ld_g, dev_status,
@@ -314,7 +337,7 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
   fct::FwdArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V, ignore_index,
                  ce, tvd, lse_s, lse_t, sigma, dev_status, grad, ld_g, grad_ce, grad_tvd,
                  grad_stride, 0};
-  const fct::FwdPlan plan = plan_forward(d, V, dtype, true, true);
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, true, true, false, opts);
   a.keep_normal = plan.keep_normal ? 1 : 0;
   if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
@@ -327,13 +350,15 @@ int forward_backward_impl(const void* student, int64_t ld_s, const void* teacher
 int ce_forward_backward_impl(const void* logits, int64_t ld, int dtype, const int64_t* target,
                              int64_t BT, int64_t V, int64_t ignore_index, const float* grad_ce,
                              int64_t grad_stride, float* ce, float* lse, void* grad, int64_t ld_g,
-                             int32_t* dev_status, void* stream) {
+                             int32_t* dev_status, void* stream, const fct_options* opts = nullptr) {
   if (BT < 0) return FCT_ERR_INVALID_ARG;
-  if (BT == 0) return FCT_OK;
-  int rc = check_common(dtype, target, BT, V);
+  int rc = check_options(opts);
   if (rc != FCT_OK) return rc;
-  if ((rc = check_logits(logits, ld, dtype, V)) != FCT_OK) return rc;
-  if ((rc = check_logits(grad, ld_g, dtype, V)) != FCT_OK) return rc;
+  if (BT == 0) return FCT_OK;
+  rc = check_common(dtype, target, BT, V);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(logits, ld, dtype, V, BT)) != FCT_OK) return rc;
+  if ((rc = check_logits(grad, ld_g, dtype, V, BT)) != FCT_OK) return rc;
   if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
   if (grad_ce == nullptr || ce == nullptr || lse == nullptr) return FCT_ERR_INVALID_ARG;
   if (!aligned(grad_ce, 4) || !aligned(ce, 4) || !aligned(lse, 4)) return FCT_ERR_ALIGNMENT;
@@ -354,7 +379,7 @@ int ce_forward_backward_impl(const void* logits, int64_t ld, int dtype, const in
   if ((rc = current_device(&d)) != FCT_OK) return rc;
   if (!(vec_ok(logits, ld, dtype) && vec_ok(grad, ld_g, dtype))) {
     rc = forward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, ce, nullptr,
-                      lse, nullptr, nullptr, dev_status, stream);
+                      lse, nullptr, nullptr, dev_status, stream, nullptr, 0, opts);
     if (rc != FCT_OK) return rc;
     return backward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, lse,
                          nullptr, nullptr, grad_ce, nullptr, grad_stride, grad, ld_g, dev_status,
@@ -363,7 +388,7 @@ int ce_forward_backward_impl(const void* logits, int64_t ld, int dtype, const in
   fct::FwdArgs a{logits, nullptr, ld, ld, dtype, target, BT, V, ignore_index,
                  ce, nullptr, lse, nullptr, nullptr, dev_status, grad, ld_g, grad_ce, nullptr,
                  grad_stride, 0};
-  const fct::FwdPlan plan = plan_forward(d, V, dtype, false, true, /*ce_grad=*/true);
+  const fct::FwdPlan plan = plan_forward(d, V, dtype, false, true, /*ce_grad=*/true, opts);
   a.keep_normal = plan.keep_normal ? 1 : 0;
   if (fct::launch_forward(a, plan, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
@@ -381,6 +406,13 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
   if (BT < 0 || V <= 0 || d_s <= 0 || d_t <= 0 || chunk_rows <= 0) return FCT_ERR_INVALID_ARG;
   if (logits_dtype != FCT_F32 && logits_dtype != FCT_BF16) return FCT_ERR_UNSUPPORTED;
   if (BT == 0) return FCT_OK;
+  if (ld_hs < d_s || ld_ws < d_s || ld_ht < d_t || ld_wt < d_t) return FCT_ERR_INVALID_ARG;
+  if ((grad_h_s && ld_ghs < d_s) || (grad_w_s && ld_gws < d_s)) return FCT_ERR_INVALID_ARG;
+  if (!span_fits(BT, ld_hs, d_s, 2) || !span_fits(V, ld_ws, d_s, 2) ||
+      !span_fits(BT, ld_ht, d_t, 2) || !span_fits(V, ld_wt, d_t, 2) ||
+      (grad_h_s && !span_fits(BT, ld_ghs, d_s, 2)) ||
+      (grad_w_s && !span_fits(V, ld_gws, d_s, 4)) || !span_fits(1, BT, BT, 8))
+    return FCT_ERR_UNSUPPORTED;
   const int64_t kInt = 2147483647;  // cuBLAS takes int sizes and strides
   if (V > kInt || d_s > kInt || d_t > kInt || ld_hs > kInt || ld_ws > kInt || ld_ht > kInt ||
       ld_wt > kInt || ld_ghs > kInt || ld_gws > kInt || chunk_rows > kInt)
@@ -495,6 +527,21 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student, const
                                dev_status, stream);
 }
 
+int fused_ce_tvd_forward_backward_ex(const void* student, int64_t ld_student,
+                                     const void* teacher, int64_t ld_teacher, fct_dtype dtype,
+                                     const int64_t* target, int64_t BT, int64_t V,
+                                     int64_t ignore_index, const float* grad_ce,
+                                     const float* grad_tvd, int64_t grad_stride, float* ce,
+                                     float* tvd, float* student_lse, float* teacher_lse,
+                                     float* sigma, void* grad_student, int64_t ld_grad,
+                                     const fct_options* options, int32_t* dev_status,
+                                     void* stream) {
+  return forward_backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                               ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd,
+                               student_lse, teacher_lse, sigma, grad_student, ld_grad,
+                               dev_status, stream, options);
+}
+
 
 int fused_ce_tvd_forward(const void* student, int64_t ld_student, const void* teacher,
                          int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
@@ -505,6 +552,18 @@ int fused_ce_tvd_forward(const void* student, int64_t ld_student, const void* te
     return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
   return forward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
                       ignore_index, ce, tvd, student_lse, teacher_lse, sigma, dev_status, stream);
+}
+
+int fused_ce_tvd_forward_ex(const void* student, int64_t ld_student, const void* teacher,
+                            int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                            int64_t BT, int64_t V, int64_t ignore_index, float* ce, float* tvd,
+                            float* student_lse, float* teacher_lse, float* sigma,
+                            const fct_options* options, int32_t* dev_status, void* stream) {
+  if (teacher == nullptr || tvd == nullptr || teacher_lse == nullptr || sigma == nullptr)
+    return BT == 0 ? check_options(options) : FCT_ERR_INVALID_ARG;
+  return forward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                      ignore_index, ce, tvd, student_lse, teacher_lse, sigma, dev_status, stream,
+                      nullptr, 0, options);
 }
 
 int fused_ce_tvd_backward(const void* student, int64_t ld_student, const void* teacher,
@@ -539,6 +598,21 @@ int fused_ce_tvd_forward_signs(const void* student, int64_t ld_student, const vo
                       signs, ld_signs);
 }
 
+int fused_ce_tvd_forward_signs_ex(const void* student, int64_t ld_student, const void* teacher,
+                                  int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                                  int64_t BT, int64_t V, int64_t ignore_index, float* ce,
+                                  float* tvd, float* student_lse, float* teacher_lse,
+                                  float* sigma, uint8_t* signs, int64_t ld_signs,
+                                  const fct_options* options, int32_t* dev_status,
+                                  void* stream) {
+  if (teacher == nullptr || tvd == nullptr || teacher_lse == nullptr || sigma == nullptr ||
+      signs == nullptr)
+    return BT == 0 ? check_options(options) : FCT_ERR_INVALID_ARG;
+  return forward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V,
+                      ignore_index, ce, tvd, student_lse, teacher_lse, sigma, dev_status, stream,
+                      signs, ld_signs, options);
+}
+
 int fused_ce_tvd_backward_signs(const void* student, int64_t ld_student, const void* teacher,
                                 int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
                                 int64_t BT, int64_t V, int64_t ignore_index,
@@ -563,11 +637,28 @@ int ce_forward_backward(const void* logits, int64_t ld, fct_dtype dtype, const i
                                   grad_stride, ce, lse, grad_logits, ld_grad, dev_status, stream);
 }
 
+int ce_forward_backward_ex(const void* logits, int64_t ld, fct_dtype dtype,
+                           const int64_t* target, int64_t BT, int64_t V, int64_t ignore_index,
+                           const float* grad_ce, int64_t grad_stride, float* ce, float* lse,
+                           void* grad_logits, int64_t ld_grad, const fct_options* options,
+                           int32_t* dev_status, void* stream) {
+  return ce_forward_backward_impl(logits, ld, dtype, target, BT, V, ignore_index, grad_ce,
+                                  grad_stride, ce, lse, grad_logits, ld_grad, dev_status, stream,
+                                  options);
+}
+
 int ce_forward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target, int64_t BT,
                int64_t V, int64_t ignore_index, float* ce, float* lse, int32_t* dev_status,
                void* stream) {
   return forward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, ce, nullptr,
                       lse, nullptr, nullptr, dev_status, stream);
+}
+
+int ce_forward_ex(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target,
+                  int64_t BT, int64_t V, int64_t ignore_index, float* ce, float* lse,
+                  const fct_options* options, int32_t* dev_status, void* stream) {
+  return forward_impl(logits, ld, nullptr, ld, dtype, target, BT, V, ignore_index, ce, nullptr,
+                      lse, nullptr, nullptr, dev_status, stream, nullptr, 0, options);
 }
 
 int ce_backward(const void* logits, int64_t ld, fct_dtype dtype, const int64_t* target,
@@ -629,13 +720,6 @@ const char* fct_status_string(int status) {
   }
 }
 
-int fct_set_forward_cluster(int ctas_per_row) {
-  if (ctas_per_row != 0 && ctas_per_row != 1 && ctas_per_row != 2 && ctas_per_row != 4 &&
-      ctas_per_row != 8)
-    return -1;
-  return g_cluster_override.exchange(ctas_per_row);
-}
-
-int fct_version(void) { return 300; }  // 0.3.0: the fused-linear entry point takes logits_dtype
+int fct_version(void) { return 400; }  // 0.4.0: per-call fct_options, no process-wide knob
 
 }  // extern "C"

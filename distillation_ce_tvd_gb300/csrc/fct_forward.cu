@@ -50,7 +50,6 @@
 //     tvd = sigma = 0 exactly.
 #include <cooperative_groups.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "fct_common.cuh"
@@ -915,34 +914,23 @@ int per_device(PerDevice& c, Init&& init) {
 }
 
 // Start stagger of the multi-pass kernels: the clusters' start times are
-// spread, in kStaggerGroups interleaved groups, over stagger_fraction() times
-// an estimate of one row's time (about 0.1 clock cycles per byte a CTA reads
-// in one pass of a row, measured on GB300 for the single launch at V = 151936
+// spread, in kStaggerGroups interleaved groups, over plan.stagger times an
+// estimate of one row's time (about 0.1 clock cycles per byte a CTA reads in
+// one pass of a row, measured on GB300 for the single launch at V = 151936
 // bf16), when every cluster has at least kStaggerMinRows rows (with fewer,
 // the last group's wait costs more than the spread saves).  Measured at 8192
 // x 151936 bf16, against starting together: a spread of half a row's time in
 // 8 interleaved groups, one launch 1.619 -> 1.582 ms and the forward alone
 // 2.130 -> 2.084 ms with its backward; a whole row's time, 1.579 and 2.100;
 // the same spreads over contiguous ranges of clusters gained about half as
-// much.  FCT_STAGGER=<fraction> overrides the fraction (0 turns it off; a
-// tuning knob for measurements).
+// much.
 constexpr double kStaggerCyclesPerByte = 0.1;
 constexpr int kStaggerMinRows = 32;
-
-double stagger_fraction() {
-  static const double f = [] {
-    const char* e = std::getenv("FCT_STAGGER");
-    if (e == nullptr) return 0.5;
-    const double v = std::atof(e);
-    return (v >= 0.0 && v <= 4.0) ? v : 0.5;
-  }();
-  return f;
-}
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per device.
 template <typename T, int VE, int C, bool kTvd, bool kGrad, int NT, typename TG, bool kSigns>
-cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
+cudaError_t run_pipelined(const FwdArgs& a, int n_slots, double stagger, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kStages) * (kTvd ? 2 : 1) * kPerStep * NT * 16 +
                            ((kGrad && kTvd) ? size_t(kMaxSignWords) * NT * 4 : 0);
   auto kernel = forward_pipelined<T, VE, C, kTvd, kGrad, NT, TG, kSigns>;
@@ -963,7 +951,7 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, cudaStream_t st) {
   if constexpr (kTvd || kGrad) {  // several passes per row: stagger the clusters' start
     if (a.BT >= int64_t(kStaggerMinRows) * n) {
       const double row_bytes = (kTvd ? 2.0 : 1.0) * double(a.V) * double(sizeof(T)) / C;
-      b.stagger = static_cast<int64_t>(stagger_fraction() * kStaggerCyclesPerByte * row_bytes);
+      b.stagger = static_cast<int64_t>(stagger * kStaggerCyclesPerByte * row_bytes);
     }
   }
   return launch_cluster(kernel, C, NT, kSmem, n, b, st);
@@ -989,7 +977,7 @@ cudaError_t run(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   } else {
     if (!plan.vec) return run_scalar<T, C, kTvd>(a, plan.slots, st);
   }
-  return run_pipelined<T, VE, C, kTvd, kGrad, 512, TG, kSigns>(a, plan.slots, st);
+  return run_pipelined<T, VE, C, kTvd, kGrad, 512, TG, kSigns>(a, plan.slots, plan.stagger, st);
 }
 
 template <typename T, bool kTvd, bool kGrad, typename TG = T, bool kSigns = false>

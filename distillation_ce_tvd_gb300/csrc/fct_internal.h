@@ -43,6 +43,7 @@ struct FwdPlan {
   int cluster;  // CTAs per row: 1, 2, 4 or 8
   int slots;    // rows in flight across the GPU (clusters launched), 0 = as many as fit
   bool keep_normal;  // L2 policy for rows that are read again (tuning)
+  double stagger;    // start stagger, fraction of an estimated row time (0: none)
 };
 
 struct BwdArgs {

@@ -234,14 +234,31 @@ Span mat_span(const void* p, int64_t rows, int64_t ld, int64_t cols, int64_t e) 
 }
 bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi; }
 
+// Whether a (rows, cols) matrix of e-byte elements with row stride ld spans
+// at most 2^62 bytes, checked without overflowing, so that every byte range
+// computed from the sizes is exact.
+bool span_fits(int64_t rows, int64_t ld, int64_t cols, int64_t e) {
+  const int64_t lim = (int64_t(1) << 62) / e;
+  if (rows <= 0 || cols <= 0 || ld < cols || cols > lim) return false;
+  return rows - 1 <= (lim - cols) / ld;
+}
+
 int check(const fct::LinArgs& a) {
   if (a.V <= 0 || a.d_s <= 0 || a.d_t <= 0) return FCT_ERR_INVALID_ARG;
-  if (!a.h_s || !a.w_s || !a.h_t || !a.w_t || !a.target || !a.grad_ce || !a.grad_tvd)
-    return FCT_ERR_INVALID_ARG;
+  // One student + one teacher fp32 row must fit in the scratch array; test
+  // V before any size arithmetic.
+  if (a.V > int64_t(kScratchBytes / (2 * sizeof(float)))) return FCT_ERR_UNSUPPORTED;
   if (a.ld_hs < a.d_s || a.ld_ws < a.d_s || a.ld_ht < a.d_t || a.ld_wt < a.d_t)
     return FCT_ERR_INVALID_ARG;
-  if (a.grad_h_s && a.ld_ghs < a.d_s) return FCT_ERR_INVALID_ARG;
-  if (a.grad_w_s && a.ld_gws < a.d_s) return FCT_ERR_INVALID_ARG;
+  if ((a.grad_h_s && a.ld_ghs < a.d_s) || (a.grad_w_s && a.ld_gws < a.d_s))
+    return FCT_ERR_INVALID_ARG;
+  if (!span_fits(a.BT, a.ld_hs, a.d_s, 2) || !span_fits(a.V, a.ld_ws, a.d_s, 2) ||
+      !span_fits(a.BT, a.ld_ht, a.d_t, 2) || !span_fits(a.V, a.ld_wt, a.d_t, 2) ||
+      (a.grad_h_s && !span_fits(a.BT, a.ld_ghs, a.d_s, 2)) ||
+      (a.grad_w_s && !span_fits(a.V, a.ld_gws, a.d_s, 4)) || !span_fits(1, a.BT, a.BT, 8))
+    return FCT_ERR_UNSUPPORTED;
+  if (!a.h_s || !a.w_s || !a.h_t || !a.w_t || !a.target || !a.grad_ce || !a.grad_tvd)
+    return FCT_ERR_INVALID_ARG;
   if (a.grad_stride != 0 && a.grad_stride != 1) return FCT_ERR_INVALID_ARG;
   const void* bf[5] = {a.h_s, a.w_s, a.h_t, a.w_t, a.grad_h_s};
   for (const void* q : bf)

@@ -17,10 +17,13 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- *  - All array arguments are DEVICE pointers, owned by the caller.  The
- *    library allocates no device memory and keeps no state between calls
- *    (the fused-linear entry point below keeps one cuBLAS handle per device;
- *    its no-allocation variant uses a fixed device array of the library).
+ *  - All array arguments are DEVICE pointers, owned by the caller (except
+ *    in the host-buffer entry point, which says which of its pointers are
+ *    host memory).  The library allocates no device memory and keeps no
+ *    state between calls that changes results or launches (it caches device
+ *    properties and per-kernel occupancy; the fused-linear entry point below
+ *    keeps one cuBLAS handle per device; its no-allocation variant uses a
+ *    fixed device array of the library).
  *  - Logit matrices are row-major (BT, V) with a row stride `ld` (in
  *    elements, ld >= V).  Student and teacher share one element type.
  *  - `target` is int64 (BT,).  A row whose target equals `ignore_index`
@@ -67,6 +70,36 @@ typedef enum {
 #define FCT_DEV_TARGET_OUT_OF_RANGE 0x1
 
 /*
+ * Launch options of the multi-pass forward kernels (a tuning and measurement
+ * aid with no counterpart in the method's description).  Every entry point
+ * without the _ex suffix behaves as its _ex form with options == NULL; a
+ * NULL pointer and a zero-initialised struct both mean "automatic".  The
+ * options belong to the one call they are passed to: the library keeps no
+ * tuning state between calls.
+ *
+ *   ctas_per_row : 0 = automatic (depends on V, the element type and the
+ *                  device only, never on BT); 1, 2, 4 or 8 = the CTAs of one
+ *                  thread-block cluster that share a row.  The per-row
+ *                  reduction order follows it, so results can differ in the
+ *                  last bits between settings; a forward and the backward or
+ *                  single launch it is compared with should use the same.
+ *                  Anything else: FCT_ERR_INVALID_ARG.
+ *   l2_keep      : 0 = rows that a later pass reads again are tagged
+ *                  evict_last in L2; 1 = evict_normal.  Anything else:
+ *                  FCT_ERR_INVALID_ARG.
+ *   stagger      : start stagger of the multi-pass kernels, as a fraction of
+ *                  an estimated row time: 0 = automatic (0.5), > 0 = that
+ *                  fraction (at most 4), < 0 = none.  Results do not depend
+ *                  on it.
+ */
+typedef struct {
+  int32_t ctas_per_row;
+  int32_t l2_keep;
+  float stagger;
+  int32_t reserved; /* must be 0 */
+} fct_options;
+
+/*
  * Forward of the fused loss (PR #1384 analysis, "Forward Pass": step 1 is the
  * per-row log-sum-exp of student and teacher, step 2 the TVD and sigma
  * reductions, closed by the five per-row stores).
@@ -85,6 +118,13 @@ int fused_ce_tvd_forward(const void* student, int64_t ld_student,
                          int64_t V, int64_t ignore_index, float* ce,
                          float* tvd, float* student_lse, float* teacher_lse,
                          float* sigma, int32_t* dev_status, void* stream);
+int fused_ce_tvd_forward_ex(const void* student, int64_t ld_student,
+                            const void* teacher, int64_t ld_teacher,
+                            fct_dtype dtype, const int64_t* target, int64_t BT,
+                            int64_t V, int64_t ignore_index, float* ce,
+                            float* tvd, float* student_lse, float* teacher_lse,
+                            float* sigma, const fct_options* options,
+                            int32_t* dev_status, void* stream);
 
 /*
  * Backward of the fused loss (PR #1384 analysis, "Backward Pass": reload the
@@ -145,6 +185,15 @@ int fused_ce_tvd_forward_signs(const void* student, int64_t ld_student,
                                float* teacher_lse, float* sigma,
                                uint8_t* signs, int64_t ld_signs,
                                int32_t* dev_status, void* stream);
+int fused_ce_tvd_forward_signs_ex(const void* student, int64_t ld_student,
+                                  const void* teacher, int64_t ld_teacher,
+                                  fct_dtype dtype, const int64_t* target,
+                                  int64_t BT, int64_t V, int64_t ignore_index,
+                                  float* ce, float* tvd, float* student_lse,
+                                  float* teacher_lse, float* sigma,
+                                  uint8_t* signs, int64_t ld_signs,
+                                  const fct_options* options,
+                                  int32_t* dev_status, void* stream);
 
 int fused_ce_tvd_backward_signs(const void* student, int64_t ld_student,
                                 const void* teacher, int64_t ld_teacher,
@@ -184,6 +233,64 @@ int fused_ce_tvd_forward_backward(const void* student, int64_t ld_student,
                                   float* sigma, void* grad_student,
                                   int64_t ld_grad, int32_t* dev_status,
                                   void* stream);
+int fused_ce_tvd_forward_backward_ex(
+    const void* student, int64_t ld_student, const void* teacher,
+    int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
+    int64_t V, int64_t ignore_index, const float* grad_ce,
+    const float* grad_tvd, int64_t grad_stride, float* ce, float* tvd,
+    float* student_lse, float* teacher_lse, float* sigma, void* grad_student,
+    int64_t ld_grad, const fct_options* options, int32_t* dev_status,
+    void* stream);
+
+/*
+ * The single launch above with its inputs and outputs in HOST memory, end to
+ * end: row blocks of block_rows rows are copied to the device, computed, and
+ * their gradient and per-row outputs copied back, with the copies of later
+ * blocks overlapping the compute of earlier ones (PR #1384 analysis: the
+ * "Forward Pass" and "Backward Pass" of the loss; streaming it from and to
+ * host memory is this library's addition).  The results equal
+ * fused_ce_tvd_forward_backward on the same rows, bit for bit.
+ *
+ *   student, teacher, target, grad_ce, grad_tvd : HOST inputs, laid out as
+ *                  for fused_ce_tvd_forward_backward.
+ *   ce, tvd, student_lse, teacher_lse, sigma : HOST outputs of BT floats, or
+ *                  NULL (not returned).
+ *   grad_student : HOST output (BT, V) with row stride ld_grad, or NULL.
+ *                  Host outputs must not overlap the host inputs.
+ *   workspace    : DEVICE memory of fused_ce_tvd_host_workspace_size(V,
+ *                  dtype, min(block_rows, BT)) bytes, 256-byte aligned,
+ *                  clobbered: a ring of three slots, each holding a block of
+ *                  student and teacher logits (the gradient is computed in
+ *                  place over the student block) and its per-row vectors.
+ *   status       : HOST int32 or NULL; receives the OR of the device status
+ *                  bits (FCT_DEV_*) of all blocks once `stream` reaches the
+ *                  end of this call's work.
+ *   stream       : the caller's stream; the kernels run on it, and the copies
+ *                  on two streams of this call that are ordered after the
+ *                  caller's earlier work on `stream` and joined back into it
+ *                  before the call returns (later work on `stream` sees every
+ *                  output).  The streams and events are created and released
+ *                  by each call.
+ *
+ * The host buffers must be page-locked (cudaHostAlloc or cudaHostRegister)
+ * for the copies to run asynchronously and overlap the compute; with
+ * pageable memory the results are the same but the copies serialise.  Read
+ * the host outputs only after synchronising `stream`.  BT == 0 returns
+ * FCT_OK and writes nothing.  A block_rows or V beyond the supported range
+ * (V > 2^40, block_rows > 2^20) returns FCT_ERR_UNSUPPORTED, as does the
+ * workspace query (0).
+ */
+size_t fused_ce_tvd_host_workspace_size(int64_t V, fct_dtype dtype,
+                                        int64_t block_rows);
+
+int fused_ce_tvd_forward_backward_host(
+    const void* student, int64_t ld_student, const void* teacher,
+    int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
+    int64_t V, int64_t ignore_index, const float* grad_ce,
+    const float* grad_tvd, int64_t grad_stride, float* ce, float* tvd,
+    float* student_lse, float* teacher_lse, float* sigma, void* grad_student,
+    int64_t ld_grad, void* workspace, size_t workspace_bytes,
+    int64_t block_rows, int32_t* status, void* stream);
 
 /*
  * Fused-linear CE + TVD: the loss from hidden states and lm_head weights,
@@ -292,6 +399,11 @@ int ce_forward(const void* logits, int64_t ld, fct_dtype dtype,
                const int64_t* target, int64_t BT, int64_t V,
                int64_t ignore_index, float* ce, float* lse,
                int32_t* dev_status, void* stream);
+int ce_forward_ex(const void* logits, int64_t ld, fct_dtype dtype,
+                  const int64_t* target, int64_t BT, int64_t V,
+                  int64_t ignore_index, float* ce, float* lse,
+                  const fct_options* options, int32_t* dev_status,
+                  void* stream);
 
 /*
  * Cross-entropy gradient alone: grad_ce*(p_v - 1[v==target]), the first of
@@ -320,6 +432,13 @@ int ce_forward_backward(const void* logits, int64_t ld, fct_dtype dtype,
                         int64_t grad_stride, float* ce, float* lse,
                         void* grad_logits, int64_t ld_grad,
                         int32_t* dev_status, void* stream);
+int ce_forward_backward_ex(const void* logits, int64_t ld, fct_dtype dtype,
+                           const int64_t* target, int64_t BT, int64_t V,
+                           int64_t ignore_index, const float* grad_ce,
+                           int64_t grad_stride, float* ce, float* lse,
+                           void* grad_logits, int64_t ld_grad,
+                           const fct_options* options, int32_t* dev_status,
+                           void* stream);
 
 /*
  * Mean over tokens.  The method stores per-row ce and tvd and takes per-row
@@ -349,17 +468,10 @@ int fused_ce_tvd_mean_loss(const float* ce, const float* tvd,
 /* Human-readable name of a fct_status value (static storage). */
 const char* fct_status_string(int status);
 
-/*
- * Tuning knob (no counterpart in the method's description): number of CTAs
- * (1, 2, 4 or 8, one thread-block cluster) that share one row in the fused
- * forward.  0 restores the automatic choice, which depends only on V, the
- * element type and the device, never on BT.  Process-wide; returns the
- * previous value, or -1 for an invalid argument.
- */
-int fct_set_forward_cluster(int ctas_per_row);
-
 /* Library version as 10000*major + 100*minor + patch.  300 and later: the
- * fused-linear entry point and its workspace query take logits_dtype. */
+ * fused-linear entry point and its workspace query take logits_dtype.  400
+ * and later: tuning goes through fct_options on the _ex entry points (no
+ * process-wide knob). */
 int fct_version(void);
 
 #ifdef __cplusplus

@@ -58,10 +58,94 @@ def test_status_strings_and_version(lib):
     assert binding.version() >= 100
 
 
-def test_cluster_knob(lib):
-    assert lib.fct_set_forward_cluster(3) == -1
-    prev = lib.fct_set_forward_cluster(4)
-    assert lib.fct_set_forward_cluster(prev) == 4
+def test_no_process_wide_tuning_state(lib):
+    # Tuning is a per-call argument (fct_options); nothing process-wide is
+    # exported and the library reads no environment variable.
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    assert "fct_set_forward_cluster" not in out
+    undefined = subprocess.run(["nm", "-D", "--undefined-only", _build.LIB_PATH],
+                               capture_output=True, text=True, check=True).stdout
+    assert "getenv" not in undefined
+    assert binding.version() >= 400
+
+
+def test_options_are_checked_per_call(lib):
+    import ctypes
+    base = FAKE + (3 << 30)
+    args = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 0, 100, -100, base,
+            base + 4096, base + 8192, base + 12288, base + 16384]
+
+    def call(opts):
+        return lib.fused_ce_tvd_forward_ex(*args, ctypes.byref(opts), None, None)
+    assert call(binding.Options(0, 0, 0.0, 0)) == OK          # BT = 0, valid options
+    assert call(binding.Options(3, 0, 0.0, 0)) == INVALID     # ctas_per_row
+    assert call(binding.Options(16, 0, 0.0, 0)) == INVALID
+    assert call(binding.Options(2, 2, 0.0, 0)) == INVALID     # l2_keep
+    assert call(binding.Options(2, 0, 5.0, 0)) == INVALID     # stagger above 4
+    assert call(binding.Options(2, 0, float("nan"), 0)) == INVALID
+    assert call(binding.Options(2, 0, 0.0, 1)) == INVALID     # reserved
+    assert call(binding.Options(8, 1, -1.0, 0)) == OK
+    assert lib.fused_ce_tvd_forward_ex(*args, None, None, None) == OK   # NULL = automatic
+    fb = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 0, 100, -100,
+          base, base + 256, 1, base + 512, base + 768, base + 1024, base + 1280, base + 1536,
+          FAKE + (5 << 30), 128]
+    assert lib.fused_ce_tvd_forward_backward_ex(*fb, ctypes.byref(binding.Options(3, 0, 0, 0)),
+                                                None, None) == INVALID
+    assert lib.ce_forward_backward_ex(FAKE, 128, 1, FAKE + (2 << 30), 0, 100, -100, base, 1,
+                                      base + 256, base + 512, FAKE + (5 << 30), 128,
+                                      ctypes.byref(binding.Options(0, 7, 0, 0)), None,
+                                      None) == INVALID
+    assert binding.options() is None
+    assert binding.options(ctas_per_row=2).ctas_per_row == 2
+
+
+def test_host_entry_point_sizes_and_argument_checks(lib):
+    import ctypes
+    import torch
+    # three slots of: two (rows, round16B(V)) logit blocks, an int64 target
+    # vector, and seven fp32 vectors, each rounded up to 256 bytes; plus 256
+    rup = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    slot = 2 * rup(4 * 104 * 2) + rup(4 * 8) + 7 * rup(4 * 4)
+    assert lib.fused_ce_tvd_host_workspace_size(100, 1, 4) == 256 + 3 * slot
+    slot32 = 2 * rup(5 * 12 * 4) + rup(5 * 8) + 7 * rup(5 * 4)
+    assert lib.fused_ce_tvd_host_workspace_size(10, 0, 5) == 256 + 3 * slot32
+    assert lib.fused_ce_tvd_host_workspace_size(0, 1, 4) == 0
+    assert lib.fused_ce_tvd_host_workspace_size(100, 3, 4) == 0
+    assert lib.fused_ce_tvd_host_workspace_size(100, 1, 0) == 0
+    assert lib.fused_ce_tvd_host_workspace_size(100, 1, 1 << 21) == 0
+    need = lib.fused_ce_tvd_host_workspace_size(100, 1, 4)
+    # host buffers: real, so nothing is read unless a copy is enqueued (none is)
+    s = torch.zeros(4, 100, dtype=torch.bfloat16)
+    tg = torch.zeros(4, dtype=torch.int64)
+    g = torch.ones(4)
+    out = torch.zeros(5, 4)
+    P = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    args = [P(s), 100, P(s), 100, 1, P(tg), 4, 100, -100, P(g), P(g), 1,
+            P(out[0]), P(out[1]), P(out[2]), P(out[3]), P(out[4]), None, 100,
+            FAKE, need, 4, None, None]
+    f = lib.fused_ce_tvd_forward_backward_host
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a6=0) == OK                         # empty batch: nothing happens
+    assert call(a6=-1) == INVALID
+    assert call(a21=0) == INVALID                   # block_rows
+    assert call(a4=9) == UNSUPPORTED
+    assert call(a7=0) == INVALID                    # V
+    assert call(a0=None) == INVALID
+    assert call(a5=None) == INVALID
+    assert call(a19=None) == INVALID                # workspace
+    assert call(a1=99) == INVALID                   # ld < V
+    assert call(a17=P(s), a18=50) == INVALID        # gradient ld < V
+    assert call(a11=2) == INVALID                   # grad_stride
+    assert call(a20=need - 1) == INVALID            # workspace one byte short
+    assert call(a19=FAKE + 16) == ALIGN             # workspace not 256-byte aligned
+    assert call(a5=ctypes.c_void_p(tg.data_ptr() + 4)) == ALIGN
+    assert call(a21=1 << 21) == UNSUPPORTED
 
 
 def fwd(lib, **kw):

@@ -23,7 +23,6 @@ def _lib():
         pytest.skip("no CUDA device")
     binding.load()
     yield
-    binding.set_forward_cluster(0)
 
 
 def same_layout_clone(x):
@@ -35,19 +34,18 @@ def same_layout_clone(x):
 
 
 def run(w, cluster=0, inplace=False, stream=None):
-    """Forward + backward of a workload on the GPU; returns host copies."""
-    prev = binding.set_forward_cluster(cluster)
-    try:
-        status = torch.zeros(1, dtype=torch.int32, device=DEV)
-        ce, tvd, ls, lt, sg = binding.fused_ce_tvd_forward(
-            w.student, w.teacher, w.target, w.ignore_index, dev_status=status, stream=stream)
-        s_in = same_layout_clone(w.student) if inplace else w.student
-        grad = binding.fused_ce_tvd_backward(
-            s_in, w.teacher, w.target, ls, lt, sg, w.grad_ce, w.grad_tvd, w.ignore_index,
-            inplace=inplace, dev_status=status, stream=stream)
-        torch.cuda.synchronize()
-    finally:
-        binding.set_forward_cluster(prev)
+    """Forward + backward of a workload on the GPU (cluster: CTAs per row of
+    the forward, 0 = automatic)."""
+    opts = binding.options(ctas_per_row=cluster)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ce, tvd, ls, lt, sg = binding.fused_ce_tvd_forward(
+        w.student, w.teacher, w.target, w.ignore_index, dev_status=status, stream=stream,
+        options=opts)
+    s_in = same_layout_clone(w.student) if inplace else w.student
+    grad = binding.fused_ce_tvd_backward(
+        s_in, w.teacher, w.target, ls, lt, sg, w.grad_ce, w.grad_tvd, w.ignore_index,
+        inplace=inplace, dev_status=status, stream=stream)
+    torch.cuda.synchronize()
     fwd = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
     return fwd, grad, int(status.item())
 
@@ -413,19 +411,17 @@ def test_ce_single_launch_equals_two(dtype, V, ld, cluster):
         w = padded(w, ld, 0)
     w.target[3] = w.ignore_index
     w.target[6] = -7                                   # out of range
-    prev = binding.set_forward_cluster(cluster)
-    try:
-        st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
-        st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
-        ce1, lse1 = binding.ce_forward(w.student, w.target, dev_status=st1)
-        g1 = binding.ce_backward(w.student, w.target, lse1, w.grad_ce, dev_status=st1)
-        ce2, lse2, g2 = binding.ce_forward_backward(w.student, w.target, w.grad_ce, dev_status=st2)
-        s_in = same_layout_clone(w.student)
-        ce3, lse3, g3 = binding.ce_forward_backward(s_in, w.target, 0.25, inplace=True)
-        g4 = binding.ce_backward(w.student, w.target, lse1, 0.25)
-        torch.cuda.synchronize()
-    finally:
-        binding.set_forward_cluster(prev)
+    opts = binding.options(ctas_per_row=cluster)
+    st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    ce1, lse1 = binding.ce_forward(w.student, w.target, dev_status=st1, options=opts)
+    g1 = binding.ce_backward(w.student, w.target, lse1, w.grad_ce, dev_status=st1)
+    ce2, lse2, g2 = binding.ce_forward_backward(w.student, w.target, w.grad_ce, dev_status=st2,
+                                                options=opts)
+    s_in = same_layout_clone(w.student)
+    ce3, lse3, g3 = binding.ce_forward_backward(s_in, w.target, 0.25, inplace=True, options=opts)
+    g4 = binding.ce_backward(w.student, w.target, lse1, 0.25)
+    torch.cuda.synchronize()
     assert st1.item() == st2.item() == binding.FCT_DEV_TARGET_OUT_OF_RANGE
 
     def bits(x):
@@ -484,23 +480,21 @@ def test_sign_words_match_plain_forward_and_backward(dtype, V, ld, cluster):
     w.teacher[3] = (w.student[3].float() + 1.0).to(dtype)         # near ties
     w.target[5] = w.ignore_index
     w.target[7] = V + 3                                           # out of range
-    prev = binding.set_forward_cluster(cluster)
-    try:
-        st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
-        st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
-        f1 = binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, dev_status=st1)
-        g1 = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, *f1[2:], w.grad_ce,
-                                           w.grad_tvd, dev_status=st1)
-        f2 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, dev_status=st2)
-        signs = f2[5]
-        g2 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f2[2:5], signs,
-                                                 w.grad_ce, w.grad_tvd, dev_status=st2)
-        s_in = same_layout_clone(w.student)
-        g3 = binding.fused_ce_tvd_backward_signs(s_in, w.teacher, w.target, *f2[2:5], signs,
-                                                 w.grad_ce, w.grad_tvd, inplace=True)
-        torch.cuda.synchronize()
-    finally:
-        binding.set_forward_cluster(prev)
+    opts = binding.options(ctas_per_row=cluster)
+    st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    f1 = binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, dev_status=st1, options=opts)
+    g1 = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, *f1[2:], w.grad_ce,
+                                       w.grad_tvd, dev_status=st1)
+    f2 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, dev_status=st2,
+                                            options=opts)
+    signs = f2[5]
+    g2 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f2[2:5], signs,
+                                             w.grad_ce, w.grad_tvd, dev_status=st2)
+    s_in = same_layout_clone(w.student)
+    g3 = binding.fused_ce_tvd_backward_signs(s_in, w.teacher, w.target, *f2[2:5], signs,
+                                             w.grad_ce, w.grad_tvd, inplace=True)
+    torch.cuda.synchronize()
     assert st1.item() == st2.item() == binding.FCT_DEV_TARGET_OUT_OF_RANGE
 
     def bits(x):  # compare bit patterns: the out-of-range row holds NaN
@@ -545,14 +539,11 @@ def test_randomized_layouts_all_paths(k):
     for key in f1:
         assert torch.equal(f1[key], f2[key]), key
     assert torch.equal(g1, g2)
-    prev = binding.set_forward_cluster(cluster)
-    try:
-        f3 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target)
-        g3 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f3[2:5], f3[5],
-                                                 w.grad_ce, w.grad_tvd)
-        torch.cuda.synchronize()
-    finally:
-        binding.set_forward_cluster(prev)
+    f3 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target,
+                                            options=binding.options(ctas_per_row=cluster))
+    g3 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f3[2:5], f3[5],
+                                             w.grad_ce, w.grad_tvd)
+    torch.cuda.synchronize()
     for key, x in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), f3[:5]):
         assert torch.equal(f1[key], x), key
     assert torch.equal(g1, g3)
@@ -562,17 +553,13 @@ def test_randomized_layouts_all_paths(k):
 # ------------------------------------------------------------------ single launch
 
 def run_single(w, cluster=0, inplace=False, grads=None):
-    prev = binding.set_forward_cluster(cluster)
-    try:
-        status = torch.zeros(1, dtype=torch.int32, device=DEV)
-        s_in = same_layout_clone(w.student) if inplace else w.student
-        gce, gtvd = grads if grads is not None else (w.grad_ce, w.grad_tvd)
-        ce, tvd, ls, lt, sg, grad = binding.fused_ce_tvd_forward_backward(
-            s_in, w.teacher, w.target, gce, gtvd, w.ignore_index, inplace=inplace,
-            dev_status=status)
-        torch.cuda.synchronize()
-    finally:
-        binding.set_forward_cluster(prev)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    s_in = same_layout_clone(w.student) if inplace else w.student
+    gce, gtvd = grads if grads is not None else (w.grad_ce, w.grad_tvd)
+    ce, tvd, ls, lt, sg, grad = binding.fused_ce_tvd_forward_backward(
+        s_in, w.teacher, w.target, gce, gtvd, w.ignore_index, inplace=inplace,
+        dev_status=status, options=binding.options(ctas_per_row=cluster))
+    torch.cuda.synchronize()
     fwd = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
     return fwd, grad, int(status.item())
 
@@ -661,9 +648,9 @@ def test_single_launch_parity_and_status():
 
 
 
-@pytest.mark.parametrize("name", ["bt8192_v151936_bf16", "bt4096_v256000_f32"])
+@pytest.mark.parametrize("name", FULL)
 def test_full_size_single_launch_every_row(name):
-    """The bench's workloads in the bench's launch (one forward + backward
+    """Each full-size workload in the bench's launch (one forward + backward
     launch per step, all rows): bitwise equal to forward then backward, and
     every per-row output and every gradient element against the oracle,
     streamed by row blocks."""
@@ -757,20 +744,77 @@ def test_mean_front_end_all_ignored():
     assert n.item() == 0 and gce.item() == 0 and gtvd.item() == 0 and loss.item() == 0
 
 
-def test_from_host_streaming_equals_device_call():
-    w = workloads.make("bt1024_v32000_bf16", DEV, rows=70, V=32000, seed=51)
-    f1, g1, _ = run_single(w)
-    hs, ht = w.student.cpu().pin_memory(), w.teacher.cpu().pin_memory()
-    htg = w.target.cpu().pin_memory()
-    ds, dt = torch.empty_like(w.student), torch.empty_like(w.teacher)
-    dtg = torch.empty_like(w.target)
-    out = binding.fused_ce_tvd_forward_backward_from_host(
-        hs, ht, htg, w.grad_ce, w.grad_tvd, ds, dt, dtg, w.ignore_index, block_rows=16)
-    torch.cuda.synchronize()
-    for k, v in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), out[:5]):
-        assert torch.equal(f1[k], v), k
-    assert torch.equal(g1, out[5])
+def _bits(x):
+    x = x.contiguous()
+    return x.view(torch.int32 if x.element_size() == 4 else torch.int16)
 
+
+@pytest.mark.parametrize("dtype,V,host_ld,block_rows,scalar", [
+    (torch.bfloat16, 32000, None, 16, False),
+    (torch.bfloat16, 32003, 32010, 7, True),      # ragged V, padded host rows, broadcast grads
+    (torch.float32, 9001, None, 64, False),       # block larger than the batch
+    (torch.bfloat16, 151936, None, 32, False),
+])
+def test_host_entry_point_equals_device_call(dtype, V, host_ld, block_rows, scalar):
+    """The host-buffer entry point (copies in and out on its own streams, row
+    blocks through a three-slot device ring) gives bit for bit the device
+    single launch's outputs, the gradient included, and the status bits."""
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=45, V=V, dtype=dtype, seed=51)
+    w.target[3] = w.ignore_index
+    w.target[9] = V + 4                       # out of range: NaN row, status bit
+    w.teacher[5] = w.student[5]               # exact ties
+    grads = (0.125, 0.5) if scalar else (w.grad_ce, w.grad_tvd)
+    # the device reference on rows padded to a 16-byte stride, as the
+    # entry point's device slots are (the same kernel and reduction order)
+    vec = 16 // w.student.element_size()
+    ld_dev = (V + vec - 1) // vec * vec
+    ref_w = padded(w, ld_dev, 0) if ld_dev != V else w
+    f1, g1, st1 = run_single(ref_w, grads=grads)
+    assert st1 == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+
+    def host(x, ld=None):
+        if ld is None:
+            return x.cpu().pin_memory()
+        buf = torch.full((x.shape[0], ld), 3.0, dtype=x.dtype).pin_memory()
+        buf[:, :x.shape[1]] = x.cpu()
+        return buf[:, :x.shape[1]]
+
+    hs, ht = host(w.student, host_ld), host(w.teacher, host_ld)
+    htg = w.target.cpu().pin_memory()
+    if scalar:
+        hgce, hgtvd = torch.tensor([0.125]), torch.tensor([0.5])
+    else:
+        hgce, hgtvd = w.grad_ce.cpu().pin_memory(), w.grad_tvd.cpu().pin_memory()
+    status = torch.zeros(1, dtype=torch.int32).pin_memory()
+    grad_h = torch.full((45, host_ld or V), 9.0, dtype=dtype).pin_memory()[:, :V]
+    out = binding.fused_ce_tvd_forward_backward_host(
+        hs, ht, htg, hgce, hgtvd, w.ignore_index, block_rows=block_rows, grad_student=grad_h,
+        status=status)
+    torch.cuda.synchronize()
+    assert status.item() == st1
+    for k, v in zip(("ce", "tvd", "student_lse", "teacher_lse", "sigma"), out[:5]):
+        assert torch.equal(_bits(f1[k].cpu()), _bits(v)), k
+    assert torch.equal(_bits(g1.cpu()), _bits(out[5]))
+    if host_ld is not None:  # the padding of the host gradient rows is untouched
+        assert torch.all(grad_h.as_strided((45, host_ld - V), (host_ld, 1), V) == 9.0)
+
+
+def test_host_entry_point_without_gradient_and_tiny_workspace_checks():
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=10, V=4000, seed=52)
+    f1, _, _ = run_single(w)
+    hs, ht, htg = (x.cpu().pin_memory() for x in (w.student, w.teacher, w.target))
+    hg = w.grad_ce.cpu().pin_memory(), w.grad_tvd.cpu().pin_memory()
+    out = binding.fused_ce_tvd_forward_backward_host(hs, ht, htg, *hg, want_grad=False,
+                                                     block_rows=3)
+    torch.cuda.synchronize()
+    assert out[5] is None
+    assert torch.equal(_bits(f1["ce"].cpu()), _bits(out[0]))
+    need = binding.fused_ce_tvd_host_workspace_size(4000, torch.bfloat16, 3)
+    small = torch.empty(need - 256, device=DEV, dtype=torch.uint8)
+    with pytest.raises(binding.FctError) as e:
+        binding.fused_ce_tvd_forward_backward_host(hs, ht, htg, *hg, block_rows=3,
+                                                   workspace=small)
+    assert e.value.status == 1
 
 
 # ------------------------------------------------------------------ fused linear (chunked)
