@@ -321,7 +321,7 @@ def main():
                     help="headline step: one fused forward+backward launch, or the forward "
                          "and backward launches")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--e2e-block-rows", type=int, default=512,
+    ap.add_argument("--e2e-block-rows", type=int, default=256,
                     help="row block of the host-buffer entry point")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
@@ -329,6 +329,9 @@ def main():
     ap.add_argument("--no-other", action="store_true", help="skip timing the other path")
     ap.add_argument("--cluster", type=int, default=0,
                     help="CTAs per row in the fused forward (0 = automatic)")
+    ap.add_argument("--ring", type=int, default=0, choices=[0, 1, 2],
+                    help="shared-memory staging of the multi-pass kernels: 0 automatic, "
+                         "1 per-thread cp.async ring, 2 producer-warp TMA bulk-copy ring")
     args = ap.parse_args()
 
     if args.impl == "reference":
@@ -345,7 +348,11 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
-    opts = binding.options(ctas_per_row=args.cluster)
+    opts = binding.options(ctas_per_row=args.cluster, ring=args.ring)
+    # the other staging of the single launch, timed beside the headline (the
+    # automatic choice is the bulk-copy ring where a row belongs to one CTA)
+    alt_ring = binding.RING_TMA if args.ring == binding.RING_CP_ASYNC else binding.RING_CP_ASYNC
+    opts_alt = binding.options(ctas_per_row=args.cluster, ring=alt_ring)
     # each rank holds its own batch of the workload (weak scaling, no exchange)
     seed = workloads.WORKLOADS[args.workload]["seed"] + 1000 * rank
     w = workloads.make(args.workload, dev, rows=args.rows, seed=seed)
@@ -373,6 +380,12 @@ def main():
                                               w.grad_tvd, w.ignore_index, ce=ce, tvd=tvd,
                                               student_lse=ls, teacher_lse=lt, sigma=sg,
                                               grad_student=grad, stream=stream, options=opts)
+
+    def single_alt():
+        binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                              w.grad_tvd, w.ignore_index, ce=ce, tvd=tvd,
+                                              student_lse=ls, teacher_lse=lt, sigma=sg,
+                                              grad_student=grad, stream=stream, options=opts_alt)
 
     ce_lse = torch.empty_like(ce)
     signs = torch.empty(BT, binding.fused_ce_tvd_signs_row_bytes(V, w.student.dtype), device=dev,
@@ -405,6 +418,7 @@ def main():
     paths = {
         "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
         "single": [("forward_backward", single, 3 * BT * V * elem)],
+        "single_alt_ring": [("forward_backward_alt_ring", single_alt, 3 * BT * V * elem)],
         "ce": [("ce_forward", ce_fwd, BT * V * elem), ("ce_backward", ce_bwd, 2 * BT * V * elem)],
         "ce_single": [("ce_forward_backward", ce_single, 2 * BT * V * elem)],
         # two launches with sign words: the backward reads the student and the
@@ -454,6 +468,7 @@ def main():
     other = None
     ce_path = None
     signs_path = None
+    alt_ring_path = None
     if not args.no_other:
         oms, okern = time_path(other_name, K)
         other = {"path": other_name, "ms_per_step": oms, "value": world * BT / (oms * 1e-3),
@@ -468,6 +483,11 @@ def main():
         sms_, skern = time_path("two_signs", K)
         signs_path = {"path": "two_signs", "ms_per_step": sms_,
                       "value": world * BT / (sms_ * 1e-3), "unit": "tokens/s", "kernels": skern}
+        ams, akern = time_path("single_alt_ring", K)
+        alt_ring_path = {"path": "single", "ring": ("tma" if alt_ring == binding.RING_TMA
+                                                    else "cp.async"),
+                         "ms_per_step": ams, "value": world * BT / (ams * 1e-3),
+                         "unit": "tokens/s", "kernels": akern}
 
     peaks = measured_peaks()
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
@@ -545,6 +565,7 @@ def main():
                        "path": args.path,
                        "parallelism": f"replicas{world}" if world > 1 else "single",
                        "forward_ctas_per_row": args.cluster or "auto",
+                       "ring": {0: "auto", 1: "cp.async", 2: "tma"}[args.ring],
                        "l2": "no flush: each step streams >= 7.4 GB, far above the 129 MB L2"
                        if args.rows is None else "reduced rows"},
             # GB/s of the bytes a step must move (3 V e per row in one launch) and the
@@ -561,6 +582,7 @@ def main():
             "other_path": other,
             "ce_path": ce_path,
             "signs_path": signs_path,
+            "alt_ring_path": alt_ring_path,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary() if clocks else None,

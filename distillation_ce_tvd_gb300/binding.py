@@ -37,14 +37,19 @@ EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_forward_ex", "fused_ce_tvd_back
 class Options(ctypes.Structure):
     """fct_options: launch options of one call (see include/fused_ce_tvd.h)."""
     _fields_ = [("ctas_per_row", ctypes.c_int32), ("l2_keep", ctypes.c_int32),
-                ("stagger", ctypes.c_float), ("reserved", ctypes.c_int32)]
+                ("stagger", ctypes.c_float), ("ring", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 4)]
 
 
-def options(ctas_per_row: int = 0, l2_keep: int = 0, stagger: float = 0.0) -> Options | None:
+RING_AUTO, RING_CP_ASYNC, RING_TMA = 0, 1, 2
+
+
+def options(ctas_per_row: int = 0, l2_keep: int = 0, stagger: float = 0.0,
+            ring: int = RING_AUTO) -> Options | None:
     """An fct_options value, or None when every field is automatic."""
-    if ctas_per_row == 0 and l2_keep == 0 and stagger == 0.0:
+    if ctas_per_row == 0 and l2_keep == 0 and stagger == 0.0 and ring == RING_AUTO:
         return None
-    return Options(int(ctas_per_row), int(l2_keep), float(stagger), 0)
+    return Options(int(ctas_per_row), int(l2_keep), float(stagger), int(ring))
 
 
 class FctError(RuntimeError):

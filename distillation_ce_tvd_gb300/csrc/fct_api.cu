@@ -103,7 +103,10 @@ int check_options(const fct_options* o) {
   const int c = o->ctas_per_row;
   if (c != 0 && c != 1 && c != 2 && c != 4 && c != 8) return FCT_ERR_INVALID_ARG;
   if (o->l2_keep != 0 && o->l2_keep != 1) return FCT_ERR_INVALID_ARG;
-  if (!(o->stagger <= 4.0f) || o->reserved != 0) return FCT_ERR_INVALID_ARG;  // rejects NaN too
+  if (!(o->stagger <= 4.0f)) return FCT_ERR_INVALID_ARG;  // rejects NaN too
+  if (o->ring < 0 || o->ring > 2) return FCT_ERR_INVALID_ARG;
+  for (int32_t r : o->reserved)
+    if (r != 0) return FCT_ERR_INVALID_ARG;
   return FCT_OK;
 }
 
@@ -123,8 +126,9 @@ constexpr double kDefaultStagger = 0.5;
 // or the student alone (cross-entropy in one launch, ce_grad).
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec,
                           bool ce_grad = false, const fct_options* opts = nullptr) {
-  fct::FwdPlan plan{vec, 1, 0, false, kDefaultStagger};
+  fct::FwdPlan plan{vec, 1, 0, false, kDefaultStagger, 0};
   if (opts != nullptr) {
+    plan.ring = opts->ring;
     plan.keep_normal = opts->l2_keep == 1;
     if (opts->stagger > 0.f) plan.stagger = opts->stagger;
     if (opts->stagger < 0.f) plan.stagger = 0.0;

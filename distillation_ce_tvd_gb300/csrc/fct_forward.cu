@@ -68,30 +68,42 @@ __device__ __forceinline__ void cluster_sync_all() {
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Barrier of the NT threads that take part in a row's reductions: the whole
+// CTA, or (kNamed) the consumer warps of a kernel whose producer warp runs on
+// its own, on named barrier 1.
+template <int NT, bool kNamed>
+__device__ __forceinline__ void rows_sync() {
+  if constexpr (kNamed) {
+    asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+  } else {
+    __syncthreads();
+  }
+}
+
 // Block-wide merge of two Lse2 states.  Every warp folds the per-warp
 // partials in the same order, so every thread ends with identical values.
-// `buf` must not be rewritten before the next __syncthreads of the caller.
-template <int NT>
+// `buf` must not be rewritten before the caller's next barrier.
+template <int NT, bool kNamed = false>
 __device__ __forceinline__ void block_merge2(Lse2& a, Lse2& b, float4* buf) {
   constexpr int kWarps = NT / 32;
   a = warp_merge(a);
   b = warp_merge(b);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) buf[warp] = make_float4(a.m2, a.s, b.m2, b.s);
-  __syncthreads();
+  rows_sync<NT, kNamed>();
   float4 w = (lane < kWarps) ? buf[lane] : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
   a = warp_merge(Lse2{w.x, w.y});
   b = warp_merge(Lse2{w.z, w.w});
 }
 
-template <int NT>
+template <int NT, bool kNamed = false>
 __device__ __forceinline__ void block_sum2(float& x, float& y, float2* buf) {
   constexpr int kWarps = NT / 32;
   x = warp_sum(x);
   y = warp_sum(y);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) buf[warp] = make_float2(x, y);
-  __syncthreads();
+  rows_sync<NT, kNamed>();
   float2 w = (lane < kWarps) ? buf[lane] : make_float2(0.f, 0.f);
   x = warp_sum(w.x);
   y = warp_sum(w.y);
@@ -381,6 +393,54 @@ __device__ __forceinline__ void lse_step(Lse2x& st, const uint4* cell, N n) {
       if (u < int(n)) {
         float x[VE];
         unpack_raw<T, VE>(cell[u * NT], x);
+        vm = fmaxf(vm, vec_max(x));
+      }
+    }
+    const float m2n = vm * kLog2e;
+    if (m2n > st.m2) {
+      const float sc = ex2(st.m2 - m2n);
+      st.s.x *= sc;
+      st.s.y *= sc;
+      st.m2 = m2n;
+    }
+    if (st.m2 == -INFINITY) {  // every value so far is -inf: nothing to add
+      acc = make_float2(0.f, 0.f);
+    } else {
+      sum_exp(-st.m2);
+    }
+  }
+  st.s = __fadd2_rn(st.s, acc);
+}
+
+// lse_step on a step's vectors given by an accessor, cell(u) for u < n (the
+// same arithmetic and order as lse_step).
+template <typename T, int VE, class Get, class N>
+__device__ __forceinline__ void lse_step_get(Lse2x& st, Get&& cell, N n) {
+  float2 acc = make_float2(0.f, 0.f);
+  auto sum_exp = [&](float nm) {
+    acc = make_float2(0.f, 0.f);
+    const float2 L2 = make_float2(kLog2e, kLog2e), nm2 = make_float2(nm, nm);
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) {
+      if (u < int(n)) {
+        float x[VE];
+        unpack_raw<T, VE>(cell(u), x);
+#pragma unroll
+        for (int j = 0; j < VE; j += 2) {
+          const float2 e = __ffma2_rn(make_float2(x[j], x[j + 1]), L2, nm2);
+          acc = __fadd2_rn(acc, make_float2(ex2(e.x), ex2(e.y)));
+        }
+      }
+    }
+  };
+  sum_exp(-st.m2);
+  if (!(acc.x + acc.y < 0x1p64f)) {
+    float vm = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kPerStep; ++u) {
+      if (u < int(n)) {
+        float x[VE];
+        unpack_raw<T, VE>(cell(u), x);
         vm = fmaxf(vm, vec_max(x));
       }
     }
@@ -774,6 +834,492 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
   if constexpr (C > 1) cluster_sync_all();
 }
 
+// ===================================================================== bulk-copy (TMA) ring path
+//
+// The same three passes with a CTA-wide ring filled by the TMA unit: one
+// producer lane issues, per step, one cp.async.bulk per tensor (the step's
+// kPerStep * NT contiguous 16-byte vectors, 32 KB) into a ring slot and
+// arms the slot's "full" mbarrier with the byte count; the NT consumer
+// threads wait on it, read their cells exactly where the per-thread ring
+// puts them (vector u*NT + tid of the step), and each consumer warp arrives
+// on the slot's "empty" mbarrier when done, which lets the producer refill
+// it.  The consumers issue no copy instructions and keep no feed state.  A
+// row belongs to one CTA (no cluster).  The arithmetic is that of
+// forward_pipelined with one CTA per row; step 1 folds its partial sums once
+// per step of kPS vectors, so the per-row outputs equal forward_pipelined's
+// to rounding (bit for bit when kPS == kPerStep), and the forward alone and
+// the single launch of this ring agree bit for bit with each other (the
+// backward reads only their per-row outputs).  In step 3 the target
+// element's gradient is written by the
+// thread that owns it after its vector stores (same thread, same address,
+// so the later store wins), which takes the target test out of the
+// per-vector loop.
+//
+// Every mbarrier wait is bounded (about 2 s of clock): a wait that runs out
+// sets a CTA-wide abort flag, after which every wait returns at once, the
+// producer stops issuing, and the kernel ORs FCT_DEV_WAIT_TIMEOUT into the
+// status word (the outputs are then invalid).
+
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Whether the phase of `bar` with parity `parity` has completed (may suspend
+// the thread for a short hardware-defined time before answering no).
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for a phase.  Gives up after kWaitLimitCycles (setting *abort)
+// or at once when *abort is already set and `heed_abort`.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            bool heed_abort) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (heed_abort && *abort) return false;
+    if (mbar_try(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) break;
+  }
+  *abort = 1;
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          bool heed_abort = true) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, heed_abort);
+}
+
+// Bulk copy of `bytes` (a multiple of 16) from global `src` into this CTA's
+// shared memory at `dst` (both 16-byte aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "{\n\t.reg .u64 g;\n\tcvta.to.global.u64 g, %1;\n\t"
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [g], %2, [%3], %4;\n\t}" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(pol)
+      : "memory");
+}
+
+// The producer lane: walks the consumers' sequence (rows of this CTA that
+// are not ignored; per row kPasses passes of n_steps steps; the teacher in
+// the first passes_t passes) and fills ring slot t % kST for step t.  In the
+// first pass (from HBM) it also asks L2 for the chunks kPref steps ahead, so
+// more of the row is on its way than the ring holds.
+template <int NT, int kPasses, int kPS, int kST, int kPref, typename T>
+__device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_bar,
+                            uint64_t* empty_bar, volatile int* abort, int64_t nvec, int n_steps,
+                            int passes_t) {
+  constexpr int kStepVecs = kPS * NT;
+  constexpr uint32_t kTensorBytes = kStepVecs * 16;
+  const uint64_t keep = p.keep_normal ? policy_evict_normal() : policy_evict_last();
+  const uint64_t drop = policy_evict_first();
+  const uint32_t ring = smem_addr(ring_mem);
+  if (p.stagger > 0) {  // interleaved start groups, as in forward_pipelined
+    const long long wait =
+        static_cast<long long>(p.stagger * (blockIdx.x % kStaggerGroups) / kStaggerGroups);
+    const long long t0 = clock64();
+    for (int it = 0; it < (1 << 22) && clock64() - t0 < wait; ++it) {
+    }
+  }
+  auto chunk_bytes = [&](int q) {
+    const int64_t v0 = int64_t(q) * kStepVecs;
+    return static_cast<uint32_t>(((nvec - v0 < kStepVecs) ? nvec - v0 : kStepVecs) * 16);
+  };
+  uint32_t t = 0;
+  bool ok = n_steps > 0;
+  for (int64_t row = blockIdx.x; ok && row < p.BT; row += gridDim.x) {
+    if (p.target[row] == p.ignore_index) continue;
+    const char* srow = static_cast<const char*>(p.student) + row * p.ld_s * int64_t(sizeof(T));
+    const char* trow = static_cast<const char*>(p.teacher) + row * p.ld_t * int64_t(sizeof(T));
+    if constexpr (kPref > 0) {  // the first chunks of the first pass
+      for (int q = 0; q < kPref && q < n_steps; ++q) {
+        prefetch_l2(srow + int64_t(q) * kTensorBytes, chunk_bytes(q), keep);
+        prefetch_l2(trow + int64_t(q) * kTensorBytes, chunk_bytes(q), keep);
+      }
+    }
+    for (int pass = 0; ok && pass < kPasses; ++pass) {
+      const bool with_t = pass < passes_t;
+      // keep each row in L2 until its last pass reads it
+      const uint64_t pol_s = (pass + 1 < kPasses) ? keep : drop;
+      const uint64_t pol_t = (pass + 1 < passes_t) ? keep : drop;
+      for (int q = 0; q < n_steps; ++q) {
+        const uint32_t slot = t % kST, fill = t / kST;
+        if (fill > 0 && !mbar_wait(&empty_bar[slot], (fill - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        const int64_t off = int64_t(q) * kTensorBytes;
+        const uint32_t bytes = chunk_bytes(q);
+        mbar_arrive_expect_tx(&full_bar[slot], with_t ? 2 * bytes : bytes);
+        const uint32_t dst = ring + slot * (2 * kTensorBytes);
+        bulk_load(dst, srow + off, bytes, &full_bar[slot], pol_s);
+        if (with_t) bulk_load(dst + kTensorBytes, trow + off, bytes, &full_bar[slot], pol_t);
+        if constexpr (kPref > 0) {
+          if (pass == 0 && q + kPref < n_steps) {
+            const int64_t pf = int64_t(q + kPref) * kTensorBytes;
+            prefetch_l2(srow + pf, chunk_bytes(q + kPref), keep);
+            prefetch_l2(trow + pf, chunk_bytes(q + kPref), keep);
+          }
+        }
+        ++t;
+      }
+    }
+  }
+  // No copy may still be landing when this CTA exits: wait (bounded, even
+  // after an abort) for the last fills.
+  for (uint32_t i = (t > uint32_t(kST) ? t - kST : 0); i < t; ++i)
+    mbar_wait(&full_bar[i % kST], (i / kST) & 1, abort, /*heed_abort=*/false);
+}
+
+// kPS: 16-byte vectors per thread per tensor in one step (a step moves
+// kPS * NT contiguous vectors of each tensor); kST: ring slots; kPref: L2
+// prefetch distance of the first pass, in steps (0 = none).
+// kEarly: 1 = in every pass, 2 = in the first pass only (the one fed from
+// HBM), each warp copies its cells of a step into registers and releases the
+// slot before computing on them, so the slot can be refilling while the
+// warps compute; 0 = release after computing.
+// kSigns: the forward alone also stores each element's sign bit and a per-row
+// tie flag for the backward (sign words, as forward_pipelined does).
+template <typename T, int VE, bool kGrad, int NT, typename TG, int kPS, int kST, int kPref,
+          int kEarly, bool kSigns = false>
+__global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
+  static_assert(kPS >= 1 && kPS <= kPerStep, "steps of at most kPerStep vectors per thread");
+  static_assert(!kSigns || !kGrad, "sign words come from the forward alone");
+  constexpr bool kWord = kGrad || kSigns;  // step 2 builds sign words
+  constexpr int kPasses = kGrad ? 3 : 2;
+  constexpr int kStepVecs = kPS * NT;       // 16-byte vectors per tensor per step
+  constexpr int kSlotVecs = 2 * kStepVecs;  // student then teacher
+  // step 2's sign bits: kBits per step, kSpw steps per 32-bit word
+  constexpr int kBits = kPS * VE;
+  static_assert(32 % kBits == 0, "whole steps per sign word");
+  constexpr int kSpw = 32 / kBits;
+  extern __shared__ __align__(128) uint4 bulk_ring[];
+  __shared__ __align__(8) uint64_t full_bar[kST];
+  __shared__ __align__(8) uint64_t empty_bar[kST];
+  __shared__ float4 red_lse[kMaxWarps];
+  __shared__ float2 red_sum[kMaxWarps];
+  __shared__ int abort_flag;
+
+  const int tid = threadIdx.x;
+  const int64_t nvec = p.V / VE;
+  const int64_t tail0 = nvec * VE;
+  const int n_steps = static_cast<int>((nvec + kStepVecs - 1) / kStepVecs);
+  const bool use_bits = kGrad && n_steps <= kMaxSignWords * kSpw;
+  const int passes_t = use_bits ? 2 : kPasses;  // passes that stage the teacher
+
+  if (tid == 0) {
+    for (int s = 0; s < kST; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], NT / 32);
+    }
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();  // the last CTA-wide barrier: from here the producer runs on its own
+  if (tid >= NT) {
+    if (tid == NT)
+      tma_produce<NT, kPasses, kPS, kST, kPref, T>(p, bulk_ring, full_bar, empty_bar,
+                                                  &abort_flag, nvec, n_steps, passes_t);
+    return;
+  }
+
+  // ---- consumers
+  const int lane = tid & 31;
+  // this thread's vectors in the last step of a pass (all kPS in the others)
+  const int64_t n_last = nvec - int64_t(n_steps > 0 ? n_steps - 1 : 0) * kStepVecs;
+  const int64_t cnt_all = (n_last > tid) ? (n_last - tid + NT - 1) / NT : 0;
+  const int cnt_last = static_cast<int>(cnt_all < kPS ? cnt_all : kPS);
+  const uint4* mine = bulk_ring + tid;
+  uint32_t* sbits = reinterpret_cast<uint32_t*>(bulk_ring + kST * kSlotVecs);
+  uint32_t slot = 0, parity = 0;
+  // One pass over the row: fn(cell_s, cell_t, n, q) for each step q, with
+  // this thread's n vectors of the step as cell_s(u) (student) and cell_t(u)
+  // (teacher, when the pass stages it), u < n.
+  struct Regs {  // a step's cells copied into registers
+    uint4 v[2 * kPS];
+  };
+  auto pass = [&](bool with_t, auto early, auto&& fn) {
+    for (int q = 0; q < n_steps; ++q) {
+      mbar_wait(&full_bar[slot], parity, &abort_flag);
+      const uint4* cells = mine + slot * kSlotVecs;
+      const bool full = q + 1 < n_steps || cnt_last == kPS;
+      if constexpr (decltype(early)::value) {
+        Regs r;
+#pragma unroll
+        for (int u = 0; u < kPS; ++u) {
+          if (full || u < cnt_last) {
+            r.v[u] = cells[u * NT];
+            if (with_t) r.v[kPS + u] = cells[kStepVecs + u * NT];
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+        auto cs = [&](int u) { return r.v[u]; };
+        auto ct = [&](int u) { return r.v[kPS + u]; };
+        if (full) {
+          fn(cs, ct, Count<kPS>{}, q);
+        } else {
+          fn(cs, ct, cnt_last, q);
+        }
+      } else {
+        auto cs = [&](int u) { return cells[u * NT]; };
+        auto ct = [&](int u) { return cells[kStepVecs + u * NT]; };
+        if (full) {
+          fn(cs, ct, Count<kPS>{}, q);
+        } else {
+          fn(cs, ct, cnt_last, q);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      }
+      if (++slot == kST) {
+        slot = 0;
+        parity ^= 1u;
+      }
+    }
+  };
+
+  const T* S = static_cast<const T*>(p.student);
+  const T* Tt = static_cast<const T*>(p.teacher);
+  const uint64_t drop = policy_evict_first();
+  const float2 L2 = make_float2(kLog2e, kLog2e);
+
+  for (int64_t row = blockIdx.x; row < p.BT; row += gridDim.x) {
+    const int64_t tg = p.target[row];
+    const T* srow = S + row * p.ld_s;
+    const T* trow = Tt + row * p.ld_t;
+    if (tg == p.ignore_index) {
+      if (tid == 0) write_ignored<true>(p, row);
+      if constexpr (kGrad) {  // a zero gradient row
+        TG* grow = static_cast<TG*>(p.grad) + row * p.ld_g;
+        const float zero[VE] = {};
+        for (int64_t v = tid; v < nvec; v += NT) store_grad<T, TG, VE>(grow + v * VE, zero, drop);
+        if (tail0 + tid < p.V) Elem<TG>::store1(grow + tail0 + tid, 0.f);
+      }
+      continue;  // the producer skips this row too
+    }
+    const bool bad = (tg < 0 || tg >= p.V);
+    // Logits read before any gradient of this row can overwrite them (in
+    // place): the target logit for ce, and (single launch) the target
+    // element's student and teacher logits for the thread that owns it.
+    const float s_tg = (tid == 0 && !bad) ? Elem<T>::load1(srow + tg) : 0.f;
+    const bool owner = kGrad && !bad && tg < tail0 && ((tg / VE) % NT) == tid;
+    // The row's tie flag starts clear; threads that meet a tie set it after
+    // step 2 (past the consumers' barrier in step 1's merge).
+    uint32_t* tie_flag = nullptr;
+    if constexpr (kSigns) {
+      tie_flag = reinterpret_cast<uint32_t*>(p.signs + row * p.ld_signs);
+      if (tid == 0) *tie_flag = 0u;
+    }
+    float xs_tg = 0.f, xt_tg = 0.f;
+    if (owner) {
+      xs_tg = Elem<T>::load1(srow + tg);
+      xt_tg = Elem<T>::load1(trow + tg);
+    }
+
+    // ---- step 1: log-sum-exp of both rows
+    Lse2x a = lse2x_empty(), b = lse2x_empty();
+    pass(true, std::integral_constant<bool, kEarly != 0>{}, [&](auto&& cs, auto&& ct, auto n, int) {
+      lse_step_get<T, VE>(a, cs, n);
+      lse_step_get<T, VE>(b, ct, n);
+    });
+    Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
+    if (tail0 + tid < p.V) {
+      float xs[1] = {Elem<T>::load1(srow + tail0 + tid)};
+      float xt[1] = {Elem<T>::load1(trow + tail0 + tid)};
+      lse2_update(fa, xs);
+      lse2_update(fb, xt);
+    }
+    block_merge2<NT, true>(fa, fb, red_lse);
+    const float lse_s = lse2_finish(fa);
+    const float lse_t = lse2_finish(fb);
+    const float ns2 = -(lse_s * kLog2e);
+    const float nt2 = -(lse_t * kLog2e);
+    const float2 nst = make_float2(ns2, nt2);
+
+    // ---- step 2: sigma and tau (sum |p - q| = sigma - tau), sign bits
+    const float2 ns22 = make_float2(ns2, ns2), nt22 = make_float2(nt2, nt2);
+    const float2 minus1 = make_float2(-1.f, -1.f);
+    float2 sp2 = make_float2(0.f, 0.f), sq2 = make_float2(0.f, 0.f);
+    uint32_t tie_and = 0xffffffffu;
+    [[maybe_unused]] uint32_t packed = 0;  // sign bits of the steps of the current word
+    pass(true, std::integral_constant<bool, kEarly == 1>{}, [&](auto&& cs, auto&& ct, auto n, int q) {
+      [[maybe_unused]] uint32_t word = 0;
+#pragma unroll
+      for (int u = 0; u < kPS; ++u) {
+        if (u < int(n)) {
+          float xs[VE], xt[VE];
+          unpack_raw<T, VE>(cs(u), xs);
+          unpack_raw<T, VE>(ct(u), xt);
+#pragma unroll
+          for (int j = 0; j < VE; j += 2) {
+            const float2 es = __ffma2_rn(make_float2(xs[j], xs[j + 1]), L2, ns22);
+            const float2 et = __ffma2_rn(make_float2(xt[j], xt[j + 1]), L2, nt22);
+            const float2 pp = make_float2(ex2(es.x), ex2(es.y));
+            const float2 qq = make_float2(ex2(et.x), ex2(et.y));
+            const float2 sg = __ffma2_rn(lt_pq2(pp, qq), minus1, gt_pq2(pp, qq));  // gt - lt
+            sp2 = __ffma2_rn(pp, sg, sp2);
+            sq2 = __ffma2_rn(qq, sg, sq2);
+            if constexpr (kWord) {
+              const uint32_t b0 = __float_as_uint(sg.x);
+              const uint32_t b1 = __float_as_uint(sg.y);
+              word = __funnelshift_l(b1, __funnelshift_l(b0, word, 1), 1);
+              tie_and &= b0 & b1;
+            }
+          }
+        }
+      }
+      if constexpr (kWord) {
+        // a short step's bits move up to the full step's positions
+        if (int(n) < kPS) word <<= (kPS - int(n)) * VE;
+      }
+      if constexpr (kSigns) {
+        // one byte per vector: its VE bits, element j at bit VE-1-j
+        uint8_t* dst = p.signs + row * p.ld_signs + 4 + tid + int64_t(q) * kStepVecs;
+#pragma unroll
+        for (int u = 0; u < kPS; ++u)
+          if (u < int(n))
+            dst[u * NT] = static_cast<uint8_t>((word >> (kBits - VE * (u + 1))) & ((1u << VE) - 1u));
+      }
+      if constexpr (kGrad) {
+        // the steps of a word go in from the top (first step highest), and a
+        // row's last word is shifted as if it were full
+        if constexpr (kSpw == 1) {
+          packed = word;
+        } else {
+          packed = (packed << kBits) | word;
+        }
+        const int i = q % kSpw;
+        if (use_bits && (i == kSpw - 1 || q + 1 == n_steps)) {
+          if constexpr (kSpw > 1) packed <<= (kSpw - 1 - i) * kBits;
+          sbits[(q / kSpw) * NT + tid] = packed;
+          packed = 0;
+        }
+      }
+    });
+    if constexpr (kSigns) {
+      if ((tie_and & 0x3f800000u) != 0x3f800000u) atomicOr(tie_flag, 1u);
+    }
+    float sig_p = sp2.x + sp2.y;
+    float sig_q = sq2.x + sq2.y;
+    if (tail0 + tid < p.V) {
+      const float2 e = __ffma2_rn(make_float2(Elem<T>::load1(srow + tail0 + tid),
+                                              Elem<T>::load1(trow + tail0 + tid)),
+                                  L2, nst);
+      const float pp = ex2(e.x), qq = ex2(e.y);
+      const float sg = sgn_pq(pp, qq);
+      sig_p = fmaf(pp, sg, sig_p);
+      sig_q = fmaf(qq, sg, sig_q);
+    }
+    float abs_sum = sig_p - sig_q;
+    float sig = sig_p;
+    block_sum2<NT, true>(abs_sum, sig, red_sum);
+    if (tid == 0) write_row<true>(p, row, tg, lse_s, lse_t, abs_sum, sig, s_tg);
+
+    if constexpr (kGrad) {
+      // ---- step 3: grad = p * c(sign) - grad_ce * [v == target], the
+      // backward kernel's expressions
+      const float gce = p.grad_ce[row * p.grad_stride];
+      const float h = 0.5f * p.grad_tvd[row * p.grad_stride];
+      const float c0 = gce - h * sig;
+      const float c_plus = fmaf(h, 1.f, c0), c_minus = fmaf(h, -1.f, c0);
+      TG* grow = static_cast<TG*>(p.grad) + row * p.ld_g;
+      TG* gmine = grow + int64_t(tid) * VE;
+      const T* tmine = trow + int64_t(tid) * VE;
+      const bool from_bits = use_bits && (tie_and & 0x3f800000u) == 0x3f800000u;
+      // p * c rounded on its own (never fused with a later subtraction), as
+      // the backward kernel's product is
+      auto grad_of = [&](float xs, float xt) {
+        const float2 e = __ffma2_rn(make_float2(xs, xt), L2, nst);
+        const float pp = ex2(e.x);
+        return __fmul_rn(pp, fmaf(h, sgn_pq(pp, ex2(e.y)), c0));
+      };
+      pass(!use_bits, std::integral_constant<bool, kEarly == 1>{},
+           [&](auto&& cs, auto&& ct, auto n, int q) {
+        TG* gq = gmine + int64_t(q) * kStepVecs * VE;
+        if (bad) {  // out-of-range target: the whole gradient row is NaN
+          float nan[VE];
+#pragma unroll
+          for (int j = 0; j < VE; ++j) nan[j] = __uint_as_float(0x7fc00000u);
+#pragma unroll
+          for (int u = 0; u < kPS; ++u)
+            if (u < int(n)) store_grad<T, TG, VE>(gq + u * NT * VE, nan, drop);
+          return;
+        }
+        if (from_bits) {
+          // this step's bits at the top of the word's slot for it
+          const uint32_t word = sbits[(q / kSpw) * NT + tid] << ((q % kSpw) * kBits);
+#pragma unroll
+          for (int u = 0; u < kPS; ++u) {
+            if (u < int(n)) {
+              float xs[VE], g[VE];
+              unpack_raw<T, VE>(cs(u), xs);
+#pragma unroll
+              for (int j = 0; j < VE; j += 2) {
+                const float2 e = __ffma2_rn(make_float2(xs[j], xs[j + 1]), L2, ns22);
+                const int b0 = 31 - (u * VE + j);
+                const float ca = ((word >> b0) & 1u) ? c_minus : c_plus;
+                const float cb = ((word >> (b0 - 1)) & 1u) ? c_minus : c_plus;
+                const float2 gg =
+                    __fmul2_rn(make_float2(ex2(e.x), ex2(e.y)), make_float2(ca, cb));
+                g[j] = gg.x;
+                g[j + 1] = gg.y;
+              }
+              store_grad<T, TG, VE>(gq + u * NT * VE, g, drop);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < kPS; ++u) {
+            if (u < int(n)) {
+              // the teacher comes from the ring unless step 3 was planned on
+              // sign bits (then it was not staged: read it from L2 / HBM)
+              const uint4 wt = use_bits ? load_raw<T, VE>(tmine + int64_t(q * kPS + u) * NT * VE, drop)
+                                        : ct(u);
+              float xs[VE], xt[VE], g[VE];
+              unpack_raw<T, VE>(cs(u), xs);
+              unpack_raw<T, VE>(wt, xt);
+#pragma unroll
+              for (int j = 0; j < VE; ++j) g[j] = grad_of(xs[j], xt[j]);
+              store_grad<T, TG, VE>(gq + u * NT * VE, g, drop);
+            }
+          }
+        }
+      });
+      if (tail0 + tid < p.V) {
+        const int64_t v = tail0 + tid;
+        float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
+        if (v == tg) g = __fsub_rn(g, gce);
+        Elem<TG>::store1(grow + v, bad ? __uint_as_float(0x7fc00000u) : g);
+      }
+      // the target element, after this thread's vector store of it
+      if (owner) Elem<TG>::store1(grow + tg, __fsub_rn(grad_of(xs_tg, xt_tg), gce));
+    }
+  }
+  if (tid == 0 && abort_flag && p.dev_status) atomicOr(p.dev_status, FCT_DEV_WAIT_TIMEOUT);
+}
+
 // ===================================================================== scalar path
 //
 // Rows whose pointers or strides are not 16-byte aligned: plain element
@@ -957,6 +1503,45 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, double stagger, cudaStr
   return launch_cluster(kernel, C, NT, kSmem, n, b, st);
 }
 
+// The bulk-copy ring form: one CTA per row, 512 consumers plus a producer
+// warp; steps of 4 vectors per thread and tensor (32 KB per tensor), 3 slots,
+// each released after the warps have computed on it; the forward alone asks
+// L2 for its first pass 4 steps ahead of the ring (measured at 8192 x 151936
+// bf16: forward 0.956 -> 0.942 ms; the single launch was 1% slower with it).
+// Smaller steps with more slots, releasing slots before computing, and 480
+// consumers were all measured slower or equal.
+constexpr int kTmaThreads = 512, kTmaPerStep = 4, kTmaStages = 3;
+constexpr int kTmaEarly = 0;
+
+template <typename T, bool kGrad, typename TG = T, bool kSigns = false>
+cudaError_t run_tma(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  constexpr int NT = kTmaThreads;
+  constexpr int VE = Elem<T>::kVec;
+  constexpr size_t kSmem = size_t(kTmaStages) * 2 * kTmaPerStep * NT * 16 +
+                           (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
+  constexpr int kPref = kGrad ? 0 : 4;
+  auto kernel =
+      forward_tma<T, VE, kGrad, NT, TG, kTmaPerStep, kTmaStages, kPref, kTmaEarly, kSigns>;
+  static PerDevice cache;
+  const int n_max = per_device(cache, [&] {
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kSmem)) != cudaSuccess) {
+      cudaGetLastError();
+      return -1;
+    }
+    return max_clusters(kernel, 1, NT + 32, kSmem);
+  });
+  if (n_max < 0) return cudaErrorInvalidConfiguration;
+  int n = n_max;
+  if (plan.slots > 0 && n > plan.slots) n = plan.slots;
+  if (n > a.BT) n = static_cast<int>(a.BT);
+  FwdArgs b = a;
+  if (a.BT >= int64_t(kStaggerMinRows) * n)
+    b.stagger = static_cast<int64_t>(plan.stagger * kStaggerCyclesPerByte * 2.0 * double(a.V) *
+                                     double(sizeof(T)));
+  return launch_cluster(kernel, 1, NT + 32, kSmem, n, b, st);
+}
+
 template <typename T, int C, bool kTvd>
 cudaError_t run_scalar(const FwdArgs& a, int n_slots, cudaStream_t st) {
   auto kernel = forward_scalar<T, C, kTvd>;
@@ -993,6 +1578,21 @@ cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  if (plan.ring != 1 && plan.vec && plan.cluster == 1 && a.tvd) {
+    // the fused forward (alone, with sign words, or with its backward) on the
+    // bulk-copy ring: the automatic choice where a row belongs to one CTA
+    if (a.signs) {
+      if (a.grad) return cudaErrorInvalidValue;
+      return a.dtype == FCT_BF16 ? run_tma<bf16_t, false, bf16_t, true>(a, plan, st)
+                                 : run_tma<float, false, float, true>(a, plan, st);
+    }
+    if (a.dtype == FCT_BF16)
+      return a.grad ? run_tma<bf16_t, true>(a, plan, st) : run_tma<bf16_t, false>(a, plan, st);
+    if (a.grad)
+      return a.grad_bf16 ? run_tma<float, true, bf16_t>(a, plan, st)
+                         : run_tma<float, true>(a, plan, st);
+    return run_tma<float, false>(a, plan, st);
+  }
   if (a.signs) {  // the forward alone with sign words (vector path only)
     if (!plan.vec || !a.tvd || a.grad) return cudaErrorInvalidValue;
     return a.dtype == FCT_BF16 ? run_c<bf16_t, true, false, bf16_t, true>(a, plan, st)

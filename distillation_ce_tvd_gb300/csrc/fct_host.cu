@@ -6,7 +6,8 @@
 // streams: block i is copied in on a copy-in stream while block i-1 is
 // computed on the caller's stream and block i-2's gradient and per-row
 // outputs are copied back on a copy-out stream.  Every copy is one
-// cudaMemcpy2DAsync or cudaMemcpyAsync; events order the three streams.  Each
+// cudaMemcpyAsync (or cudaMemcpy2DAsync for padded rows); events order the
+// three streams.  Each
 // block's gradient is computed in place over its student slot (the
 // single-launch kernel's in-place mode) and copied out from there, so a slot
 // holds two logit blocks and a few per-row vectors.  Rows are independent,
@@ -52,6 +53,15 @@ bool sizes_ok(int64_t V, int64_t rows) {
 }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// One copy of `rows` rows of `width` bytes: a plain copy when both sides are
+// contiguous (the copy engines then move one linear range), else a pitched
+// copy.
+cudaError_t copy_rows(void* dst, size_t dpitch, const void* src, size_t spitch, size_t width,
+                      size_t rows, cudaMemcpyKind kind, cudaStream_t st) {
+  if (dpitch == width && spitch == width) return cudaMemcpyAsync(dst, src, width * rows, kind, st);
+  return cudaMemcpy2DAsync(dst, dpitch, src, spitch, width, rows, kind, st);
+}
 
 // Streams and events of one call, released when the call returns (the
 // runtime defers the release until their work is done).
@@ -165,12 +175,12 @@ int fused_ce_tvd_forward_backward_host(
 
     // copy in (after the copy-out of the block that last used this slot)
     ok = (i < kSlots || cudaStreamWaitEvent(P.in, P.returned[j], 0) == cudaSuccess) &&
-         cudaMemcpy2DAsync(s_dev, dpitch, S + size_t(r0) * size_t(ld_student) * e,
-                           size_t(ld_student) * e, width, size_t(R), cudaMemcpyHostToDevice,
-                           P.in) == cudaSuccess &&
-         cudaMemcpy2DAsync(t_dev, dpitch, T + size_t(r0) * size_t(ld_teacher) * e,
-                           size_t(ld_teacher) * e, width, size_t(R), cudaMemcpyHostToDevice,
-                           P.in) == cudaSuccess &&
+         copy_rows(s_dev, dpitch, S + size_t(r0) * size_t(ld_student) * e,
+                   size_t(ld_student) * e, width, size_t(R), cudaMemcpyHostToDevice,
+                   P.in) == cudaSuccess &&
+         copy_rows(t_dev, dpitch, T + size_t(r0) * size_t(ld_teacher) * e,
+                   size_t(ld_teacher) * e, width, size_t(R), cudaMemcpyHostToDevice,
+                   P.in) == cudaSuccess &&
          cudaMemcpyAsync(tg_dev, target + r0, size_t(R) * 8, cudaMemcpyHostToDevice, P.in) ==
              cudaSuccess &&
          cudaMemcpyAsync(gce_dev, grad_ce + up0, size_t(n_up) * 4, cudaMemcpyHostToDevice,
@@ -193,9 +203,8 @@ int fused_ce_tvd_forward_backward_host(
     ok = cudaEventRecord(P.computed[j], st) == cudaSuccess &&
          cudaStreamWaitEvent(P.out, P.computed[j], 0) == cudaSuccess;
     if (ok && G)
-      ok = cudaMemcpy2DAsync(G + size_t(r0) * size_t(ld_grad) * e, size_t(ld_grad) * e, s_dev,
-                             dpitch, width, size_t(R), cudaMemcpyDeviceToHost,
-                             P.out) == cudaSuccess;
+      ok = copy_rows(G + size_t(r0) * size_t(ld_grad) * e, size_t(ld_grad) * e, s_dev, dpitch,
+                     width, size_t(R), cudaMemcpyDeviceToHost, P.out) == cudaSuccess;
     for (int k = 0; ok && k < 5; ++k)
       if (outs[k])
         ok = cudaMemcpyAsync(outs[k] + r0, out_dev[k], size_t(R) * 4, cudaMemcpyDeviceToHost,

@@ -44,6 +44,7 @@ struct FwdPlan {
   int slots;    // rows in flight across the GPU (clusters launched), 0 = as many as fit
   bool keep_normal;  // L2 policy for rows that are read again (tuning)
   double stagger;    // start stagger, fraction of an estimated row time (0: none)
+  int ring = 0;      // 0 automatic, 1 per-thread cp.async ring, 2 TMA bulk-copy ring
 };
 
 struct BwdArgs {

@@ -68,6 +68,7 @@ typedef enum {
 
 /* Bits OR-ed into *dev_status by the kernels. */
 #define FCT_DEV_TARGET_OUT_OF_RANGE 0x1
+#define FCT_DEV_WAIT_TIMEOUT 0x2 /* a bounded wait in a kernel gave up; outputs invalid */
 
 /*
  * Launch options of the multi-pass forward kernels (a tuning and measurement
@@ -91,12 +92,28 @@ typedef enum {
  *                  an estimated row time: 0 = automatic (0.5), > 0 = that
  *                  fraction (at most 4), < 0 = none.  Results do not depend
  *                  on it.
+ *   ring         : how the fused forward kernels (alone, with sign words,
+ *                  or with the backward) stage logits in shared memory:
+ *                  2 = one producer warp fills a CTA-wide ring with TMA bulk
+ *                  copies (cp.async.bulk, mbarrier completion), available
+ *                  where a row belongs to one CTA; 1 = each thread copies its
+ *                  own 16-byte vectors (cp.async) into a private ring, the
+ *                  only form for rows split over a cluster; 0 = automatic
+ *                  (2 where available, else 1).  A call asking for 2 where
+ *                  it is not available takes 1.  The cross-entropy subset
+ *                  always takes 1.  The two rings group the
+ *                  first pass's partial sums differently, so (as with
+ *                  ctas_per_row) results can differ in the last bits between
+ *                  them; compare a forward with a backward or single launch
+ *                  of the same ring.
+ *   reserved     : must be 0.
  */
 typedef struct {
   int32_t ctas_per_row;
   int32_t l2_keep;
   float stagger;
-  int32_t reserved; /* must be 0 */
+  int32_t ring;
+  int32_t reserved[4];
 } fct_options;
 
 /*

@@ -84,8 +84,11 @@ def test_options_are_checked_per_call(lib):
     assert call(binding.Options(2, 2, 0.0, 0)) == INVALID     # l2_keep
     assert call(binding.Options(2, 0, 5.0, 0)) == INVALID     # stagger above 4
     assert call(binding.Options(2, 0, float("nan"), 0)) == INVALID
-    assert call(binding.Options(2, 0, 0.0, 1)) == INVALID     # reserved
-    assert call(binding.Options(8, 1, -1.0, 0)) == OK
+    assert call(binding.Options(2, 0, 0.0, 3)) == INVALID     # ring
+    bad = binding.Options(2, 0, 0.0, 2)
+    bad.reserved[3] = 1
+    assert call(bad) == INVALID                               # reserved
+    assert call(binding.Options(8, 1, -1.0, 2)) == OK
     assert lib.fused_ce_tvd_forward_ex(*args, None, None, None) == OK   # NULL = automatic
     fb = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 0, 100, -100,
           base, base + 256, 1, base + 512, base + 768, base + 1024, base + 1280, base + 1536,
@@ -98,6 +101,7 @@ def test_options_are_checked_per_call(lib):
                                       None) == INVALID
     assert binding.options() is None
     assert binding.options(ctas_per_row=2).ctas_per_row == 2
+    assert binding.options(ring=binding.RING_TMA).ring == 2
 
 
 def test_host_entry_point_sizes_and_argument_checks(lib):

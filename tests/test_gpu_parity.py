@@ -33,10 +33,10 @@ def same_layout_clone(x):
     return y
 
 
-def run(w, cluster=0, inplace=False, stream=None):
+def run(w, cluster=0, inplace=False, stream=None, ring=0):
     """Forward + backward of a workload on the GPU (cluster: CTAs per row of
-    the forward, 0 = automatic)."""
-    opts = binding.options(ctas_per_row=cluster)
+    the forward, ring: its staging, 0 = automatic)."""
+    opts = binding.options(ctas_per_row=cluster, ring=ring)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     ce, tvd, ls, lt, sg = binding.fused_ce_tvd_forward(
         w.student, w.teacher, w.target, w.ignore_index, dev_status=status, stream=stream,
@@ -552,13 +552,13 @@ def test_randomized_layouts_all_paths(k):
 
 # ------------------------------------------------------------------ single launch
 
-def run_single(w, cluster=0, inplace=False, grads=None):
+def run_single(w, cluster=0, inplace=False, grads=None, ring=0):
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     s_in = same_layout_clone(w.student) if inplace else w.student
     gce, gtvd = grads if grads is not None else (w.grad_ce, w.grad_tvd)
     ce, tvd, ls, lt, sg, grad = binding.fused_ce_tvd_forward_backward(
         s_in, w.teacher, w.target, gce, gtvd, w.ignore_index, inplace=inplace,
-        dev_status=status, options=binding.options(ctas_per_row=cluster))
+        dev_status=status, options=binding.options(ctas_per_row=cluster, ring=ring))
     torch.cuda.synchronize()
     fwd = {"ce": ce, "tvd": tvd, "student_lse": ls, "teacher_lse": lt, "sigma": sg}
     return fwd, grad, int(status.item())
@@ -574,20 +574,23 @@ def run_single(w, cluster=0, inplace=False, grads=None):
     ("bt1024_v32000_bf16", 9, 5, torch.float32, None),
 ])
 @pytest.mark.parametrize("cluster", [0, 2, 8])
-def test_single_launch_equals_forward_then_backward(name, rows, V, dtype, ld, cluster):
+@pytest.mark.parametrize("ring", [0, 1])
+def test_single_launch_equals_forward_then_backward(name, rows, V, dtype, ld, cluster, ring):
     w = workloads.make(name, DEV, rows=rows, V=V, dtype=dtype, seed=31)
     if ld is not None:
         w = padded(w, ld, 0)
     if rows > 3:
         w.target[1] = w.ignore_index
-    f1, g1, st1 = run(w, cluster=cluster)
-    f2, g2, st2 = run_single(w, cluster=cluster)
+    f1, g1, st1 = run(w, cluster=cluster, ring=ring)
+    f2, g2, st2 = run_single(w, cluster=cluster, ring=ring)
     assert st1 == st2 == 0
     for k in f1:
         assert torch.equal(f1[k], f2[k]), k
     assert torch.equal(g1, g2)
-    _, g3, _ = run_single(w, cluster=cluster, inplace=True)
+    _, g3, _ = run_single(w, cluster=cluster, inplace=True, ring=ring)
     assert torch.equal(g1, g3)
+    if cluster == 0 and ring == 1:  # the per-thread ring at one CTA per row: the oracle too
+        compare(w, f2, g2, what=f"cp.async {name} ")
 
 
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
@@ -698,6 +701,80 @@ def test_full_size_single_launch_every_row(name):
             masks, mass, probs = tie_info(s[rows], t[rows])
             check_grad(gb[rows].numpy(), G[rows], gtvd_all[r0:r1][rows], masks, mass, probs,
                        tg[rows], w.ignore_index, f"{name} rows {r0}+{rows[:5]} ", dtype)
+
+
+# ------------------------------------------------------------------ bulk-copy (TMA) ring
+
+@pytest.mark.parametrize("dtype,V,ld,rows", [
+    (torch.bfloat16, 151936, None, 40),
+    (torch.bfloat16, 20003, 20008, 21),     # ragged tail, aligned rows
+    (torch.float32, 9001, 9004, 17),        # fp32, ragged tail
+    (torch.bfloat16, 300003, 300008, 6),    # more steps than sign words: teacher re-read
+    (torch.bfloat16, 5, 8, 9),              # no full vector at all
+    (torch.float32, 3, 4, 9),
+    (torch.bfloat16, 4100, None, 200),      # several rows per CTA
+    (torch.bfloat16, 1000, None, 5000),     # enough rows per CTA for the start stagger
+])
+def test_tma_ring_single_launch_equals_forward_then_backward(dtype, V, ld, rows):
+    """The producer-warp bulk-copy ring: its single launch equals its forward
+    followed by the backward bit for bit (out of place and in place), both
+    rings agree with the oracle, and with each other within the tolerances
+    (their step-1 partial sums are grouped differently)."""
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=rows, V=V, dtype=dtype, seed=61)
+    if ld is not None:
+        w = padded(w, ld, 0)
+    w.teacher[2] = w.student[2]                                   # exact ties
+    w.teacher[3] = (w.student[3].float() + 1.0).to(dtype)         # near ties
+    w.target[1] = w.ignore_index
+    w.target[4] = V + 3                                           # out of range
+    names = ("ce", "tvd", "student_lse", "teacher_lse", "sigma")
+    opts = binding.options(ctas_per_row=1, ring=binding.RING_TMA)
+    st1 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    st2 = torch.zeros(1, dtype=torch.int32, device=DEV)
+    single = binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                                   w.grad_tvd, dev_status=st1, options=opts)
+    s_in = same_layout_clone(w.student)
+    inplace = binding.fused_ce_tvd_forward_backward(s_in, w.teacher, w.target, w.grad_ce,
+                                                    w.grad_tvd, inplace=True, options=opts)
+    fwd = binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, dev_status=st2,
+                                       options=opts)
+    g2 = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, *fwd[2:], w.grad_ce,
+                                       w.grad_tvd, dev_status=st2)
+    torch.cuda.synchronize()
+    assert st1.item() == st2.item() == binding.FCT_DEV_TARGET_OUT_OF_RANGE
+    for x, y in zip(single[:5], fwd):
+        assert torch.equal(_bits(x), _bits(y))
+    assert torch.equal(_bits(single[5]), _bits(g2))
+    assert torch.equal(_bits(single[5]), _bits(inplace[5]))
+    for x, y in zip(single[:5], inplace[:5]):
+        assert torch.equal(_bits(x), _bits(y))
+    # the sign-word pair on the same ring
+    f3 = binding.fused_ce_tvd_forward_signs(w.student, w.teacher, w.target, options=opts)
+    g3 = binding.fused_ce_tvd_backward_signs(w.student, w.teacher, w.target, *f3[2:5], f3[5],
+                                             w.grad_ce, w.grad_tvd)
+    torch.cuda.synchronize()
+    for x, y in zip(single[:5], f3[:5]):
+        assert torch.equal(_bits(x), _bits(y))
+    assert torch.equal(_bits(single[5]), _bits(g3))
+    compare(w, dict(zip(names, single[:5])), single[5], what=f"tma {V} ")
+    # the per-thread ring on the same rows: the oracle's tolerances apart at most
+    fa, ga, _ = run_single(w, cluster=1, ring=binding.RING_CP_ASYNC)
+    compare(w, fa, ga, what=f"cp.async {V} ")
+    if V >= 8 and rows == 40:  # same tie pattern, so identical NaN and zero rows
+        assert torch.equal(torch.isnan(ga.float()), torch.isnan(single[5].float()))
+
+
+def test_tma_ring_falls_back_on_clusters():
+    # A row split over a cluster has no bulk-copy form: the call takes the
+    # per-thread ring and gives its results.
+    w = workloads.make("bt4096_v256000_f32", DEV, rows=10, V=20011, seed=62)
+    r1 = binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                               w.grad_tvd, options=binding.options(2, ring=1))
+    r2 = binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                               w.grad_tvd, options=binding.options(2, ring=2))
+    torch.cuda.synchronize()
+    for x, y in zip(r1, r2):
+        assert torch.equal(x, y)
 
 
 # ------------------------------------------------------------------ mean over tokens
