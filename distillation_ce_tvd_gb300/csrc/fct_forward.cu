@@ -63,8 +63,17 @@ namespace {
 
 constexpr int kMaxWarps = 32;
 
+// Cluster barrier.  Every exchange here has one writer per CTA (thread 0
+// stores the CTA's partials in its own shared memory before the barrier; the
+// peers read them after it), so only that thread fences its writes to
+// cluster scope and every thread arrives relaxed: a release arrive by all
+// threads made each of them wait for its own outstanding loads (the ring's
+// copies in flight), measured as membar stalls.  Reads of peers' partials
+// are consumed before the thread's next arrive, so the next write cannot
+// overtake them.
 __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+  if (threadIdx.x == 0) asm volatile("fence.acq_rel.cluster;" ::: "memory");
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
