@@ -38,7 +38,7 @@ sys.path.insert(0, ROOT)
 
 import torch  # noqa: E402
 
-from distillation_ce_tvd_gb300 import binding, sharding, workloads  # noqa: E402
+from distillation_ce_tvd_gb300 import binding, sharding, vocab_parallel, workloads  # noqa: E402
 
 METRIC = "fused CE+TVD fwd+bwd tokens/s and HBM GB/s (% of peak), V=151936 bf16, 1 GB300"
 DEFAULT_WORKLOAD = "bt8192_v151936_bf16"
@@ -387,6 +387,10 @@ def main():
                                               student_lse=ls, teacher_lse=lt, sigma=sg,
                                               grad_student=grad, stream=stream, options=opts_alt)
 
+    def vocab_shards():  # the vocabulary-parallel step with 2 shards on this GPU
+        vocab_parallel.forward_backward_local(w.student, w.teacher, w.target, 2, w.grad_ce,
+                                              w.grad_tvd, w.ignore_index, stream=stream)
+
     ce_lse = torch.empty_like(ce)
     signs = torch.empty(BT, binding.fused_ce_tvd_signs_row_bytes(V, w.student.dtype), device=dev,
                         dtype=torch.uint8)
@@ -419,6 +423,9 @@ def main():
         "two": [("forward", fwd, 2 * BT * V * elem), ("backward", bwd, 3 * BT * V * elem)],
         "single": [("forward_backward", single, 3 * BT * V * elem)],
         "single_alt_ring": [("forward_backward_alt_ring", single_alt, 3 * BT * V * elem)],
+        # vocabulary shards: passes 1 and 2 read both tensors, pass 3 reads both
+        # and writes the gradient (7 V e per row), plus the merges
+        "vocab2": [("vocab_parallel_2_shards", vocab_shards, 7 * BT * V * elem)],
         "ce": [("ce_forward", ce_fwd, BT * V * elem), ("ce_backward", ce_bwd, 2 * BT * V * elem)],
         "ce_single": [("ce_forward_backward", ce_single, 2 * BT * V * elem)],
         # two launches with sign words: the backward reads the student and the
@@ -469,6 +476,7 @@ def main():
     ce_path = None
     signs_path = None
     alt_ring_path = None
+    vocab_path = None
     if not args.no_other:
         oms, okern = time_path(other_name, K)
         other = {"path": other_name, "ms_per_step": oms, "value": world * BT / (oms * 1e-3),
@@ -483,6 +491,9 @@ def main():
         sms_, skern = time_path("two_signs", K)
         signs_path = {"path": "two_signs", "ms_per_step": sms_,
                       "value": world * BT / (sms_ * 1e-3), "unit": "tokens/s", "kernels": skern}
+        vms, vkern = time_path("vocab2", max(1, K // 4))
+        vocab_path = {"path": "vocab2", "shards": 2, "ms_per_step": vms,
+                      "value": world * BT / (vms * 1e-3), "unit": "tokens/s", "kernels": vkern}
         ams, akern = time_path("single_alt_ring", K)
         alt_ring_path = {"path": "single", "ring": ("tma" if alt_ring == binding.RING_TMA
                                                     else "cp.async"),
@@ -583,6 +594,7 @@ def main():
             "ce_path": ce_path,
             "signs_path": signs_path,
             "alt_ring_path": alt_ring_path,
+            "vocab_path": vocab_path,
             "e2e": e2e,
             "cpu_baseline": cpu,
             "clocks": clocks.summary() if clocks else None,

@@ -20,7 +20,7 @@ LIB_NAME = "libfused_ce_tvd.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu", "fct_linear.cu",
-           "fct_noalloc.cu", "fct_host.cu"]
+           "fct_noalloc.cu", "fct_host.cu", "fct_vocab.cu"]
 HEADERS = ["fct_common.cuh", "fct_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -31,6 +31,8 @@ EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_forward_ex", "fused_ce_tvd_back
            "ce_forward_backward_ex", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fused_linear_ce_tvd_forward_backward_noalloc",
+           "fused_ce_tvd_vp_lse", "fused_ce_tvd_vp_merge_lse", "fused_ce_tvd_vp_tvd",
+           "fused_ce_tvd_vp_merge_tvd", "fused_ce_tvd_vp_backward",
            "fct_status_string", "fct_version")
 
 
@@ -127,6 +129,15 @@ def load(path: str | None = None) -> ctypes.CDLL:
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
                   "ce_forward", "ce_backward", "fused_ce_tvd_mean_upstream",
                   "fused_ce_tvd_mean_loss"):
+            getattr(lib, f).restype = i32
+        lib.fused_ce_tvd_vp_lse.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64, i64, vp, vp]
+        lib.fused_ce_tvd_vp_merge_lse.argtypes = [vp, i64, vp, i64, i64, i64, vp, vp, vp, vp, vp]
+        lib.fused_ce_tvd_vp_tvd.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64, vp, vp, vp, vp]
+        lib.fused_ce_tvd_vp_merge_tvd.argtypes = [vp, i64, vp, i64, i64, vp, vp, vp]
+        lib.fused_ce_tvd_vp_backward.argtypes = [vp, i64, vp, i64, i32, vp, i64, i64, i64, i64, i64,
+                                                 vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
+        for f in ("fused_ce_tvd_vp_lse", "fused_ce_tvd_vp_merge_lse", "fused_ce_tvd_vp_tvd",
+                  "fused_ce_tvd_vp_merge_tvd", "fused_ce_tvd_vp_backward"):
             getattr(lib, f).restype = i32
         lib.fct_status_string.argtypes = [i32]
         lib.fct_status_string.restype = ctypes.c_char_p
@@ -577,6 +588,120 @@ def fused_ce_tvd_forward_backward_host(student, teacher, target, grad_ce, grad_t
             workspace.numel() * workspace.element_size(), rows, _ptr(status), _stream(stream))
     _check(rc, "fused_ce_tvd_forward_backward_host")
     return (*outs, grad_student)
+
+
+# ------------------------------------------------------------------ vocabulary shards
+
+def _pair(student, teacher):
+    code, ld_s = _logits(student, "student")
+    code_t, ld_t = _logits(teacher, "teacher")
+    if code != code_t or student.shape != teacher.shape:
+        raise ValueError("student and teacher shards must share shape and dtype")
+    return code, ld_s, ld_t
+
+
+def _parts(x, k, name):
+    if not x.is_cuda or x.dtype != torch.float32 or x.dim() != 3 or x.shape[2] != k or \
+            not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous (n_shards, BT, {k}) float32 CUDA tensor")
+    return x
+
+
+def fused_ce_tvd_vp_lse(student, teacher, target, v_begin, ignore_index=IGNORE_INDEX, *,
+                        part=None, stream=None):
+    """Pass 1 on one vocabulary shard: (BT, 3) float32 of the shard's student
+    lse, teacher lse and the student logit at the target when the shard holds
+    it.  ``student``/``teacher`` are the shard's (BT, V_shard) columns;
+    ``v_begin`` their first column in the full vocabulary."""
+    code, ld_s, ld_t = _pair(student, teacher)
+    BT, Vs = student.shape
+    _rows(target, BT, "target", torch.int64)
+    if part is None:
+        part = torch.empty(BT, 3, device=student.device, dtype=torch.float32)
+    rc = load().fused_ce_tvd_vp_lse(_ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target),
+                                    BT, Vs, int(v_begin), int(ignore_index), _ptr(part),
+                                    _stream(stream))
+    _check(rc, "fused_ce_tvd_vp_lse")
+    return part
+
+
+def fused_ce_tvd_vp_merge_lse(parts, target, V, ignore_index=IGNORE_INDEX, *, ce=None,
+                              student_lse=None, teacher_lse=None, dev_status=None, stream=None):
+    """Merge of pass 1 over the shards (``parts``: (n_shards, BT, 3), shard
+    order): (ce, student_lse, teacher_lse)."""
+    _parts(parts, 3, "parts")
+    n, BT = parts.shape[0], parts.shape[1]
+    _rows(target, BT, "target", torch.int64)
+    dev = parts.device
+    outs = [_out(x, BT, dev, nm) for x, nm in ((ce, "ce"), (student_lse, "student_lse"),
+                                               (teacher_lse, "teacher_lse"))]
+    rc = load().fused_ce_tvd_vp_merge_lse(_ptr(parts), n, _ptr(target), BT, int(V),
+                                          int(ignore_index), *map(_ptr, outs), _ptr(dev_status),
+                                          _stream(stream))
+    _check(rc, "fused_ce_tvd_vp_merge_lse")
+    return tuple(outs)
+
+
+def fused_ce_tvd_vp_tvd(student, teacher, target, student_lse, teacher_lse,
+                        ignore_index=IGNORE_INDEX, *, part=None, stream=None):
+    """Pass 2 on one shard: (BT, 2) float32 of the shard's sum of p*sign(p - q)
+    and q*sign(p - q), p and q from the merged lse values."""
+    code, ld_s, ld_t = _pair(student, teacher)
+    BT, Vs = student.shape
+    _rows(target, BT, "target", torch.int64)
+    _rows(student_lse, BT, "student_lse")
+    _rows(teacher_lse, BT, "teacher_lse")
+    if part is None:
+        part = torch.empty(BT, 2, device=student.device, dtype=torch.float32)
+    rc = load().fused_ce_tvd_vp_tvd(_ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT,
+                                    Vs, int(ignore_index), _ptr(student_lse), _ptr(teacher_lse),
+                                    _ptr(part), _stream(stream))
+    _check(rc, "fused_ce_tvd_vp_tvd")
+    return part
+
+
+def fused_ce_tvd_vp_merge_tvd(parts, target, ignore_index=IGNORE_INDEX, *, tvd=None, sigma=None,
+                              stream=None):
+    """Merge of pass 2 over the shards (``parts``: (n_shards, BT, 2)): (tvd, sigma)."""
+    _parts(parts, 2, "parts")
+    n, BT = parts.shape[0], parts.shape[1]
+    _rows(target, BT, "target", torch.int64)
+    dev = parts.device
+    outs = [_out(x, BT, dev, nm) for x, nm in ((tvd, "tvd"), (sigma, "sigma"))]
+    rc = load().fused_ce_tvd_vp_merge_tvd(_ptr(parts), n, _ptr(target), BT, int(ignore_index),
+                                          *map(_ptr, outs), _stream(stream))
+    _check(rc, "fused_ce_tvd_vp_merge_tvd")
+    return tuple(outs)
+
+
+def fused_ce_tvd_vp_backward(student, teacher, target, v_begin, V, student_lse, teacher_lse, sigma,
+                             grad_ce, grad_tvd, ignore_index=IGNORE_INDEX, *, grad_student=None,
+                             inplace=False, dev_status=None, stream=None):
+    """Pass 3 on one shard: the gradient of the shard's columns."""
+    code, ld_s, ld_t = _pair(student, teacher)
+    BT, Vs = student.shape
+    dev = student.device
+    _rows(target, BT, "target", torch.int64)
+    for x, nm in ((student_lse, "student_lse"), (teacher_lse, "teacher_lse"), (sigma, "sigma")):
+        _rows(x, BT, nm)
+    gce, stride_ce = _upstream(grad_ce, BT, dev, "grad_ce")
+    gtvd, stride_tvd = _upstream(grad_tvd, BT, dev, "grad_tvd")
+    if stride_ce != stride_tvd:
+        gce, gtvd = gce.expand(BT).contiguous(), gtvd.expand(BT).contiguous()
+    stride = max(stride_ce, stride_tvd)
+    if inplace:
+        grad_student = student
+    elif grad_student is None:
+        grad_student = torch.empty(BT, Vs, device=dev, dtype=student.dtype)
+    code_g, ld_g = _logits(grad_student, "grad_student")
+    if code_g != code or grad_student.shape != student.shape:
+        raise ValueError("grad_student must match the shard's shape and dtype")
+    rc = load().fused_ce_tvd_vp_backward(
+        _ptr(student), ld_s, _ptr(teacher), ld_t, code, _ptr(target), BT, Vs, int(v_begin), int(V),
+        int(ignore_index), _ptr(student_lse), _ptr(teacher_lse), _ptr(sigma), _ptr(gce),
+        _ptr(gtvd), stride, _ptr(grad_student), ld_g, _ptr(dev_status), _stream(stream))
+    _check(rc, "fused_ce_tvd_vp_backward")
+    return grad_student
 
 
 def _logits_dtype(dtype) -> int:

@@ -229,7 +229,8 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
                   const float* lse_s, const float* lse_t, const float* sigma,
                   const float* grad_ce, const float* grad_tvd, int64_t grad_stride,
                   void* grad, int64_t ld_g, int32_t* dev_status, void* stream,
-                  const uint8_t* signs = nullptr, int64_t ld_signs = 0) {
+                  const uint8_t* signs = nullptr, int64_t ld_signs = 0, int64_t tg_base = 0,
+                  int64_t V_full = 0) {
   const bool fused = (teacher != nullptr) || (lse_t != nullptr);
   if (signs != nullptr && !fused) return FCT_ERR_INVALID_ARG;
   if (BT < 0) return FCT_ERR_INVALID_ARG;
@@ -276,6 +277,8 @@ int backward_impl(const void* student, int64_t ld_s, const void* teacher, int64_
     a.signs = signs;
     a.ld_signs = ld_signs;
   }
+  a.tg_base = tg_base;
+  a.V_full = V_full;
   if (fct::launch_backward(a, vec, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
@@ -469,6 +472,78 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
                  logits_dtype};
   const fct::FwdPlan plan = plan_forward(d, V, logits_dtype, true, true);
   if (fct::launch_linear(a, plan, dev, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
+// Vocabulary shards: one pass over a shard's columns (pass 1 or pass 2).
+int vp_pass_impl(const void* student, int64_t ld_s, const void* teacher, int64_t ld_t, int dtype,
+                 const int64_t* target, int64_t BT, int64_t V_shard, int64_t v_begin,
+                 int64_t ignore_index, const float* lse_s, const float* lse_t, float* part,
+                 bool tvd_pass, void* stream) {
+  if (BT < 0 || v_begin < 0) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  int rc = check_common(dtype, target, BT, V_shard);
+  if (rc != FCT_OK) return rc;
+  if ((rc = check_logits(student, ld_s, dtype, V_shard, BT)) != FCT_OK) return rc;
+  if ((rc = check_logits(teacher, ld_t, dtype, V_shard, BT)) != FCT_OK) return rc;
+  if (part == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(part, 4)) return FCT_ERR_ALIGNMENT;
+  if (tvd_pass) {
+    if (lse_s == nullptr || lse_t == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(lse_s, 4) || !aligned(lse_t, 4)) return FCT_ERR_ALIGNMENT;
+  }
+  const size_t e = elem_size(dtype);
+  const Range out = vec_range(part, BT * (tvd_pass ? 2 : 3), 4);
+  if (overlap(out, mat_range(student, BT, ld_s, V_shard, e)) ||
+      overlap(out, mat_range(teacher, BT, ld_t, V_shard, e)) ||
+      overlap(out, vec_range(target, BT, 8)) ||
+      (tvd_pass && (overlap(out, vec_range(lse_s, BT, 4)) || overlap(out, vec_range(lse_t, BT, 4)))))
+    return FCT_ERR_INVALID_ARG;
+  DeviceInfo d;
+  if ((rc = current_device(&d)) != FCT_OK) return rc;
+  fct::VpArgs a{student, teacher, ld_s, ld_t, dtype, target, BT, V_shard, v_begin, ignore_index,
+                lse_s, lse_t, part};
+  const bool vec = vec_ok(student, ld_s, dtype) && vec_ok(teacher, ld_t, dtype);
+  if (fct::launch_vp_pass(a, vec, tvd_pass, d.sms, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
+int vp_merge_impl(const float* parts, int64_t n_shards, const int64_t* target, int64_t BT,
+                  int64_t V, int64_t ignore_index, float* ce, float* lse_s, float* lse_t,
+                  float* tvd, float* sigma, int32_t* dev_status, bool tvd_merge, void* stream) {
+  if (BT < 0 || n_shards < 1) return FCT_ERR_INVALID_ARG;
+  if (BT == 0) return FCT_OK;
+  if (!tvd_merge && V <= 0) return FCT_ERR_INVALID_ARG;
+  if (n_shards > (int64_t(1) << 20) || BT > (int64_t(1) << 40)) return FCT_ERR_UNSUPPORTED;
+  if (parts == nullptr || target == nullptr) return FCT_ERR_INVALID_ARG;
+  if (!aligned(parts, 4) || !aligned(target, 8) || (dev_status && !aligned(dev_status, 4)))
+    return FCT_ERR_ALIGNMENT;
+  float* outs[3] = {ce, lse_s, lse_t};
+  if (tvd_merge) {
+    outs[0] = tvd;
+    outs[1] = sigma;
+    outs[2] = nullptr;
+  }
+  const int n_out = tvd_merge ? 2 : 3;
+  const Range rp = vec_range(parts, n_shards * BT * (tvd_merge ? 2 : 3), 4);
+  const Range rt = vec_range(target, BT, 8);
+  for (int i = 0; i < n_out; ++i) {
+    if (outs[i] == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(outs[i], 4)) return FCT_ERR_ALIGNMENT;
+    const Range r = vec_range(outs[i], BT, 4);
+    if (overlap(r, rp) || overlap(r, rt)) return FCT_ERR_INVALID_ARG;
+    for (int j = i + 1; j < n_out; ++j)
+      if (overlap(r, vec_range(outs[j], BT, 4))) return FCT_ERR_INVALID_ARG;
+  }
+  DeviceInfo d;
+  const int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  fct::VpMergeArgs a{parts, n_shards, target, BT, V, ignore_index, ce, lse_s, lse_t,
+                     tvd, sigma, dev_status};
+  if (fct::launch_vp_merge(a, tvd_merge, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
 }
@@ -711,6 +786,54 @@ int fused_ce_tvd_mean_loss(const float* ce, const float* tvd, const int64_t* tar
                   loss, nullptr, nullptr, nullptr};
   return fct::launch_mean(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? FCT_OK
                                                                                 : FCT_ERR_CUDA;
+}
+
+int fused_ce_tvd_vp_lse(const void* student, int64_t ld_student, const void* teacher,
+                        int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
+                        int64_t V_shard, int64_t v_begin, int64_t ignore_index, float* part,
+                        void* stream) {
+  return vp_pass_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V_shard,
+                      v_begin, ignore_index, nullptr, nullptr, part, false, stream);
+}
+
+int fused_ce_tvd_vp_merge_lse(const float* parts, int64_t n_shards, const int64_t* target,
+                              int64_t BT, int64_t V, int64_t ignore_index, float* ce,
+                              float* student_lse, float* teacher_lse, int32_t* dev_status,
+                              void* stream) {
+  return vp_merge_impl(parts, n_shards, target, BT, V, ignore_index, ce, student_lse,
+                       teacher_lse, nullptr, nullptr, dev_status, false, stream);
+}
+
+int fused_ce_tvd_vp_tvd(const void* student, int64_t ld_student, const void* teacher,
+                        int64_t ld_teacher, fct_dtype dtype, const int64_t* target, int64_t BT,
+                        int64_t V_shard, int64_t ignore_index, const float* student_lse,
+                        const float* teacher_lse, float* part, void* stream) {
+  return vp_pass_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V_shard, 0,
+                      ignore_index, student_lse, teacher_lse, part, true, stream);
+}
+
+int fused_ce_tvd_vp_merge_tvd(const float* parts, int64_t n_shards, const int64_t* target,
+                              int64_t BT, int64_t ignore_index, float* tvd, float* sigma,
+                              void* stream) {
+  return vp_merge_impl(parts, n_shards, target, BT, 1, ignore_index, nullptr, nullptr, nullptr,
+                       tvd, sigma, nullptr, true, stream);
+}
+
+int fused_ce_tvd_vp_backward(const void* student, int64_t ld_student, const void* teacher,
+                             int64_t ld_teacher, fct_dtype dtype, const int64_t* target,
+                             int64_t BT, int64_t V_shard, int64_t v_begin, int64_t V,
+                             int64_t ignore_index, const float* student_lse,
+                             const float* teacher_lse, const float* sigma, const float* grad_ce,
+                             const float* grad_tvd, int64_t grad_stride, void* grad_student,
+                             int64_t ld_grad, int32_t* dev_status, void* stream) {
+  if (v_begin < 0 || V_shard <= 0 || V < V_shard || v_begin > V - V_shard)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  if (teacher == nullptr || teacher_lse == nullptr || sigma == nullptr || grad_tvd == nullptr)
+    return BT == 0 ? FCT_OK : FCT_ERR_INVALID_ARG;
+  return backward_impl(student, ld_student, teacher, ld_teacher, dtype, target, BT, V_shard,
+                       ignore_index, student_lse, teacher_lse, sigma, grad_ce, grad_tvd,
+                       grad_stride, grad_student, ld_grad, dev_status, stream, nullptr, 0,
+                       v_begin, V);
 }
 
 const char* fct_status_string(int status) {

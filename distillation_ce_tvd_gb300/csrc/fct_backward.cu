@@ -61,13 +61,15 @@ __global__ void __launch_bounds__(kThreads) backward_kernel(BwdArgs a) {
     const bool last_seg = (seg == nseg - 1);
     const int64_t v0 = seg * kSeg;
     const int64_t v1 = min(nvec, v0 + kSeg);
-    const int64_t tg = a.target[row];
+    const int64_t tg_full = a.target[row];
+    const int64_t tg = tg_full - a.tg_base;  // in this row's columns (a vocabulary shard's)
     const T* srow = S + row * a.ld_s;
     const T* trow = kTvd ? Tt + row * a.ld_t : nullptr;
     T* grow = G + row * a.ld_g;
 
-    const bool ignored = (tg == a.ignore_index);
-    if (ignored || tg < 0 || tg >= a.V) {
+    const bool ignored = (tg_full == a.ignore_index);
+    const int64_t v_all = a.V_full > 0 ? a.V_full : a.V;
+    if (ignored || tg_full < 0 || tg_full >= v_all) {
       // Ignored rows get a zero gradient; out-of-range targets get NaN and
       // raise the status bit.  Neither reads the logits.
       const float fill = ignored ? 0.f : __uint_as_float(0x7fc00000u);

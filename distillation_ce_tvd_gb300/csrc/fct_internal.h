@@ -66,6 +66,12 @@ struct BwdArgs {
   // the forward's sign words (see FwdArgs::signs), or nullptr
   const uint8_t* signs = nullptr;
   int64_t ld_signs = 0;
+  // vocabulary shards: the logits are columns [tg_base, tg_base + V) of a
+  // vocabulary of V_full entries (0: no shard).  Targets index the full
+  // vocabulary; one outside this shard adds no -grad_ce term here, and only
+  // one outside [0, V_full) is out of range.
+  int64_t tg_base = 0;
+  int64_t V_full = 0;
 };
 
 struct LossArgs {
@@ -119,6 +125,38 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
 // element type logits_dtype) on the calling thread's current device, with
 // that device's index and SM count.  Returns an fct_status.
 int plan_linear_forward(int64_t V, int logits_dtype, FwdPlan* plan, int* device, int* sms);
+
+// Vocabulary shards (fct_vocab.cu): the passes over one shard's columns.
+struct VpArgs {
+  const void* student;  // the shard's first column of row 0
+  const void* teacher;
+  int64_t ld_s, ld_t;
+  int dtype;
+  const int64_t* target;  // indices into the full vocabulary
+  int64_t BT, V;          // V: the shard's columns
+  int64_t v_begin;        // the shard's first column in the full vocabulary
+  int64_t ignore_index;
+  const float* lse_s;     // pass 2: the merged lse values
+  const float* lse_t;
+  float* part;            // (BT, 3) after pass 1, (BT, 2) after pass 2
+};
+
+struct VpMergeArgs {
+  const float* parts;  // (n_shards, BT, 3) or (n_shards, BT, 2)
+  int64_t n_shards;
+  const int64_t* target;
+  int64_t BT, V;  // V: the full vocabulary
+  int64_t ignore_index;
+  float* ce;
+  float* lse_s;
+  float* lse_t;
+  float* tvd;
+  float* sigma;
+  int32_t* dev_status;
+};
+
+cudaError_t launch_vp_pass(const VpArgs& a, bool vec, bool tvd_pass, int sms, cudaStream_t st);
+cudaError_t launch_vp_merge(const VpMergeArgs& a, bool tvd_merge, cudaStream_t st);
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);

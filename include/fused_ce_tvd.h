@@ -482,6 +482,78 @@ int fused_ce_tvd_mean_loss(const float* ce, const float* tvd,
                            int64_t ignore_index, double alpha, double beta,
                            float* loss, void* stream);
 
+/*
+ * Vocabulary-parallel split: the loss when the vocabulary is divided into
+ * column ranges ("shards") across devices, each holding every row's columns
+ * [v_begin, v_begin + V_shard) of the student and teacher logits.  A row's
+ * log-sum-exp, TVD and sigma are sums over the vocabulary (PR #1384
+ * analysis, "Forward Pass" steps 1 and 2; "Backward Pass"), so they split
+ * into per-shard partials and a merge; distributing a model's vocabulary
+ * this way is this library's addition.  One step, on every shard:
+ *
+ *   1. fused_ce_tvd_vp_lse          -> this shard's part1 (BT, 3)
+ *   2. exchange: every device gathers all shards' part1 into
+ *      parts1 (n_shards, BT, 3), in shard order (an all-gather)
+ *   3. fused_ce_tvd_vp_merge_lse    -> ce, student_lse, teacher_lse (BT,)
+ *   4. fused_ce_tvd_vp_tvd          -> this shard's part2 (BT, 2)
+ *   5. exchange: parts2 (n_shards, BT, 2), in shard order
+ *   6. fused_ce_tvd_vp_merge_tvd    -> tvd, sigma (BT,)
+ *   7. fused_ce_tvd_vp_backward     -> the gradient of this shard's columns
+ *
+ * The merges fold the shards in shard order, so every device computes
+ * bit-identical per-row values from the same gathered partials.  Only
+ * 5 floats per row and shard cross devices.  Conventions as above, with:
+ *
+ *   student, teacher : the shard's first column of row 0 (row stride ld_*,
+ *                      in elements, >= V_shard).
+ *   target           : (BT,) int64 indices into the full vocabulary of V
+ *                      entries; a target in another shard contributes no
+ *                      -grad_ce term to this shard's gradient, and only a
+ *                      target outside [0, V) (not ignore_index) is out of
+ *                      range: the merge then writes NaN ce and sets
+ *                      FCT_DEV_TARGET_OUT_OF_RANGE, and every shard's
+ *                      backward writes that row's gradient as NaN.
+ *   part (pass 1)    : (BT, 3) fp32: the shard's student lse, teacher lse,
+ *                      and the student logit at the target when this shard
+ *                      holds it (0 otherwise).  Ignored rows: zeros.
+ *   part (pass 2)    : (BT, 2) fp32: the shard's sum of p*sign(p - q) and of
+ *                      q*sign(p - q), p and q from the merged lse values.
+ *   parts            : the n_shards partials stacked (shard k at k * BT rows).
+ *   ce ... sigma     : as written by fused_ce_tvd_forward; ignored rows 0.
+ *   grad_student     : the shard's (BT, V_shard) gradient columns; in place
+ *                      over the shard's student columns when equal (same ld).
+ */
+int fused_ce_tvd_vp_lse(const void* student, int64_t ld_student,
+                        const void* teacher, int64_t ld_teacher,
+                        fct_dtype dtype, const int64_t* target, int64_t BT,
+                        int64_t V_shard, int64_t v_begin, int64_t ignore_index,
+                        float* part, void* stream);
+int fused_ce_tvd_vp_merge_lse(const float* parts, int64_t n_shards,
+                              const int64_t* target, int64_t BT, int64_t V,
+                              int64_t ignore_index, float* ce,
+                              float* student_lse, float* teacher_lse,
+                              int32_t* dev_status, void* stream);
+int fused_ce_tvd_vp_tvd(const void* student, int64_t ld_student,
+                        const void* teacher, int64_t ld_teacher,
+                        fct_dtype dtype, const int64_t* target, int64_t BT,
+                        int64_t V_shard, int64_t ignore_index,
+                        const float* student_lse, const float* teacher_lse,
+                        float* part, void* stream);
+int fused_ce_tvd_vp_merge_tvd(const float* parts, int64_t n_shards,
+                              const int64_t* target, int64_t BT,
+                              int64_t ignore_index, float* tvd, float* sigma,
+                              void* stream);
+int fused_ce_tvd_vp_backward(const void* student, int64_t ld_student,
+                             const void* teacher, int64_t ld_teacher,
+                             fct_dtype dtype, const int64_t* target, int64_t BT,
+                             int64_t V_shard, int64_t v_begin, int64_t V,
+                             int64_t ignore_index, const float* student_lse,
+                             const float* teacher_lse, const float* sigma,
+                             const float* grad_ce, const float* grad_tvd,
+                             int64_t grad_stride, void* grad_student,
+                             int64_t ld_grad, int32_t* dev_status,
+                             void* stream);
+
 /* Human-readable name of a fct_status value (static storage). */
 const char* fct_status_string(int status);
 

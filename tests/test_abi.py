@@ -360,3 +360,51 @@ def test_plain_c_client_links_and_runs(tmp_path, lib):
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.startswith("ok ")
+
+
+def test_vocab_shard_argument_checks(lib):
+    base = FAKE + (3 << 30)
+    # pass 1: (student, ld, teacher, ld, dtype, target, BT, V_shard, v_begin, ignore, part, stream)
+    p1 = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 4, 100, 0, -100, base, None]
+
+    def call(f, args, **kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    f1 = lib.fused_ce_tvd_vp_lse
+    assert call(f1, p1, a6=0) == OK
+    assert call(f1, p1, a6=-1) == INVALID
+    assert call(f1, p1, a8=-5) == INVALID           # v_begin
+    assert call(f1, p1, a7=0) == INVALID            # V_shard
+    assert call(f1, p1, a4=3) == UNSUPPORTED
+    assert call(f1, p1, a10=None) == INVALID
+    assert call(f1, p1, a10=base + 2) == ALIGN
+    assert call(f1, p1, a10=FAKE + 64) == INVALID   # partials inside the student shard
+    assert call(f1, p1, a1=99) == INVALID           # ld < V_shard
+    # merge of pass 1: (parts, n_shards, target, BT, V, ignore, ce, lse_s, lse_t, status, stream)
+    m1 = [base, 2, FAKE + (2 << 30), 4, 200, -100, base + 4096, base + 8192, base + 12288, None,
+          None]
+    fm = lib.fused_ce_tvd_vp_merge_lse
+    assert call(fm, m1, a3=0) == OK
+    assert call(fm, m1, a1=0) == INVALID            # no shard
+    assert call(fm, m1, a4=0) == INVALID            # V
+    assert call(fm, m1, a6=base + 16) == INVALID    # ce inside the partials
+    assert call(fm, m1, a7=base + 4096) == INVALID  # two outputs alias
+    assert call(fm, m1, a0=base + 1) == ALIGN
+    # merge of pass 2: (parts, n_shards, target, BT, ignore, tvd, sigma, stream)
+    m2 = [base, 3, FAKE + (2 << 30), 4, -100, base + 4096, base + 8192, None]
+    ft = lib.fused_ce_tvd_vp_merge_tvd
+    assert call(ft, m2, a3=0) == OK
+    assert call(ft, m2, a6=None) == INVALID
+    assert call(ft, m2, a6=base + 4096) == INVALID
+    # backward: the shard must lie inside the vocabulary
+    b4 = FAKE + (4 << 30)
+    bw = [FAKE, 128, FAKE + (1 << 30), 128, 1, FAKE + (2 << 30), 4, 100, 0, 200, -100,
+          b4, b4 + 4096, b4 + 8192, b4 + 12288, b4 + 16384, 1, FAKE + (5 << 30), 128, None, None]
+    fb = lib.fused_ce_tvd_vp_backward
+    assert call(fb, bw, a6=0) == OK
+    assert call(fb, bw, a8=150) == INVALID          # v_begin + V_shard > V
+    assert call(fb, bw, a9=50) == INVALID           # V < V_shard
+    assert call(fb, bw, a8=-1) == INVALID
+    assert call(fb, bw, a16=2) == INVALID           # grad_stride

@@ -8,8 +8,8 @@ import torch
 
 import oracle
 from distillation_ce_tvd_gb300 import binding, workloads
-from parity_util import (check_forward, check_grad, grad_tol, oracle_rows, row_atol, tie_info,
-                         to_host_rows)
+from parity_util import (check_every_row, check_forward, check_grad, grad_tol, oracle_rows,
+                         row_atol, tie_info, to_host_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -665,42 +665,7 @@ def test_full_size_single_launch_every_row(name):
         assert torch.equal(f1[k], f2[k]), k
     assert torch.equal(g1, g2)
     del f1, g1
-    dtype = w.student.dtype
-    atol = row_atol(dtype)
-    # A lower bound of the gradient tolerance (1e-6 + 2e-3 |ref|, plus half a
-    # bf16 ulp of the reference, which is at least 2^-9 of it, for bf16):
-    # elements within it pass; any other element's row is checked exactly
-    # (with the near-tie widening) by check_grad.
-    rel_lo = 2e-3 + (2.0 ** -9 if dtype == torch.bfloat16 else 0.0)
-    tg_all = w.target.cpu().numpy()
-    gce_all, gtvd_all = w.grad_ce.cpu().numpy(), w.grad_tvd.cpu().numpy()
-    got_all = {k: v.cpu().numpy() for k, v in f2.items()}
-    step = 256
-    for r0 in range(0, w.BT, step):
-        r1 = min(r0 + step, w.BT)
-        s, t = w.student[r0:r1].cpu(), w.teacher[r0:r1].cpu()
-        tg = tg_all[r0:r1]
-        ref, G = oracle_rows(s, t, tg, gce_all[r0:r1], gtvd_all[r0:r1], w.ignore_index)
-        ign = tg == w.ignore_index
-        for k, gk in got_all.items():
-            g = gk[r0:r1].astype(np.float64)
-            assert np.all(g[ign] == 0.0), f"{name} {k}: ignored rows"
-            err = np.abs(g - ref[k])
-            bad = np.nonzero(err > atol)[0]
-            if bad.size and k == "sigma":  # near-ties may move sigma (and only sigma)
-                _, mass, _ = tie_info(s[bad], t[bad])
-                bad = bad[err[bad] > atol + 2.0 * mass]
-            assert bad.size == 0, f"{name} {k}: rows {(bad + r0)[:5]} err {err[bad].max():.3e}"
-        gb = g2[r0:r1].cpu().double()
-        Gt = torch.from_numpy(G)
-        assert torch.all(gb[torch.from_numpy(ign)] == 0), f"{name}: ignored gradient rows"
-        err = (gb - Gt).abs_()
-        lo = Gt.abs().mul_(rel_lo).add_(1e-6)
-        rows = torch.nonzero((err > lo).any(dim=1)).flatten().numpy()
-        if rows.size:
-            masks, mass, probs = tie_info(s[rows], t[rows])
-            check_grad(gb[rows].numpy(), G[rows], gtvd_all[r0:r1][rows], masks, mass, probs,
-                       tg[rows], w.ignore_index, f"{name} rows {r0}+{rows[:5]} ", dtype)
+    check_every_row(w, f2, g2, name)
 
 
 # ------------------------------------------------------------------ bulk-copy (TMA) ring
