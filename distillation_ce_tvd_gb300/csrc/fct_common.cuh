@@ -366,4 +366,59 @@ __device__ __forceinline__ float warp_sum(float a) {
   return a;
 }
 
+// ---------------------------------------------------------------- mbarriers
+//
+// Every wait is bounded: after kWaitLimitCycles of SM clock (about 2 s) it
+// gives up and sets the caller's abort flag, so a kernel whose producer stalls
+// returns (with an error bit) instead of hanging.
+
+constexpr long long kWaitLimitCycles = 4000000000LL;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(ptr));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+// Whether the phase of `bar` with parity `parity` has completed (may suspend
+// the thread for a short hardware-defined time before answering no).
+__device__ __forceinline__ bool mbar_try(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Bounded wait for a phase.  Gives up after kWaitLimitCycles (setting *abort)
+// or at once when *abort is already set and `heed_abort`.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                            bool heed_abort) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (heed_abort && *abort) return false;
+    if (mbar_try(bar, parity)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) break;
+  }
+  *abort = 1;
+  return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          bool heed_abort = true) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort, heed_abort);
+}
+
 }  // namespace fct
