@@ -20,7 +20,7 @@ LIB_NAME = "libfused_ce_tvd.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 
 SOURCES = ["fct_api.cu", "fct_forward.cu", "fct_backward.cu", "fct_loss.cu", "fct_linear.cu",
-           "fct_noalloc.cu", "fct_host.cu", "fct_vocab.cu"]
+           "fct_noalloc.cu", "fct_host.cu", "fct_vocab.cu", "fct_gemm.cu"]
 HEADERS = ["fct_common.cuh", "fct_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -70,7 +70,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     libdir = _cuda_lib_dir(nvcc)
-    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs, "-lcublas",
+    cmd = [nvcc, *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", f"-rpath,{libdir}"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:

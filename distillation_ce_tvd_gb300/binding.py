@@ -30,7 +30,7 @@ EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_forward_ex", "fused_ce_tvd_back
            "ce_forward", "ce_forward_ex", "ce_backward", "ce_forward_backward",
            "ce_forward_backward_ex", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
-           "fused_linear_ce_tvd_forward_backward_noalloc",
+           "fused_linear_ce_tvd_forward_backward_noalloc", "fct_gemm_bf16",
            "fused_ce_tvd_vp_lse", "fused_ce_tvd_vp_merge_lse", "fused_ce_tvd_vp_tvd",
            "fused_ce_tvd_vp_merge_tvd", "fused_ce_tvd_vp_backward",
            "fct_status_string", "fct_version")
@@ -124,6 +124,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
             vp, i64, vp, i64, i64, vp, i64, vp, i64, i64, vp, i64, i64, i64, vp, vp, i64,
             vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
         lib.fused_linear_ce_tvd_forward_backward_noalloc.restype = i32
+        lib.fct_gemm_bf16.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i32, i64, i64, i64,
+                                      vp, vp]
+        lib.fct_gemm_bf16.restype = i32
         lib.fused_ce_tvd_mean_upstream.argtypes = [vp, i64, i64, dbl, dbl, vp, vp, vp, vp]
         lib.fused_ce_tvd_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp]
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
@@ -775,6 +778,53 @@ def fused_linear_ce_tvd_forward_backward(h_student, w_student, h_teacher, w_teac
         _ptr(dev_status), _stream(stream))
     _check(rc, "fused_linear_ce_tvd_forward_backward")
     return (*outs, grad_h, grad_w)
+
+
+GEMM_F32, GEMM_BF16, GEMM_ADD_F32 = 0, 1, 2
+
+
+def _operand(x: torch.Tensor, name: str):
+    """(ld, mn_major) of a 2-D bf16 operand viewed as given: row-major
+    (stride (ld, 1)) is K-major, column-major (stride (1, ld)) MN-major."""
+    if not x.is_cuda or x.dtype != torch.bfloat16 or x.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D bfloat16 CUDA tensor")
+    if x.stride(1) == 1:
+        return int(x.stride(0)), 0
+    if x.stride(0) == 1:
+        return int(x.stride(1)), 1
+    raise ValueError(f"{name} needs one unit stride")
+
+
+def fct_gemm_bf16(a, b, c=None, *, accumulate=False, out_dtype=torch.float32, dev_status=None,
+                  stream=None):
+    """C = a @ b.T (or C += a @ b.T into an fp32 c) on the library's tcgen05 GEMM.
+
+    a (M, K) and b (N, K) are bf16 CUDA tensors with one unit stride each
+    (b.T of a row-major (K, N) tensor is the MN-major case); c is (M, N),
+    row-major, fp32 or bf16 (bf16 only without accumulate)."""
+    lda, a_mn = _operand(a, "a")
+    ldb, b_mn = _operand(b, "b")
+    M, K = a.shape
+    N, K2 = b.shape
+    if K != K2:
+        raise ValueError("a and b differ in K")
+    if c is None:
+        if accumulate:
+            raise ValueError("accumulate needs c")
+        c = torch.empty(M, N, device=a.device, dtype=out_dtype)
+    if c.dim() != 2 or tuple(c.shape) != (M, N) or (N > 1 and c.stride(1) != 1):
+        raise ValueError("c must be a row-major (M, N) tensor")
+    if c.dtype == torch.bfloat16 and not accumulate:
+        kind = GEMM_BF16
+    elif c.dtype == torch.float32:
+        kind = GEMM_ADD_F32 if accumulate else GEMM_F32
+    else:
+        raise ValueError("c must be float32, or bfloat16 without accumulate")
+    rc = load().fct_gemm_bf16(_ptr(a), lda, a_mn, _ptr(b), ldb, b_mn, _ptr(c),
+                              int(c.stride(0)) if M > 1 else N, kind, M, N, K,
+                              _ptr(dev_status), _stream(stream))
+    _check(rc, "fct_gemm_bf16")
+    return c
 
 
 def fused_linear_ce_tvd_forward_backward_noalloc(h_student, w_student, h_teacher, w_teacher,

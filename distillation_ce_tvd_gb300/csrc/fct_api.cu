@@ -420,7 +420,7 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
       (grad_h_s && !span_fits(BT, ld_ghs, d_s, 2)) ||
       (grad_w_s && !span_fits(V, ld_gws, d_s, 4)) || !span_fits(1, BT, BT, 8))
     return FCT_ERR_UNSUPPORTED;
-  const int64_t kInt = 2147483647;  // cuBLAS takes int sizes and strides
+  const int64_t kInt = 2147483647;  // the GEMM's tile coordinates are 32-bit
   if (V > kInt || d_s > kInt || d_t > kInt || ld_hs > kInt || ld_ws > kInt || ld_ht > kInt ||
       ld_wt > kInt || ld_ghs > kInt || ld_gws > kInt || chunk_rows > kInt)
     return FCT_ERR_UNSUPPORTED;
@@ -430,9 +430,11 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
   if (grad_h_s && ld_ghs < d_s) return FCT_ERR_INVALID_ARG;
   if (grad_w_s && ld_gws < d_s) return FCT_ERR_INVALID_ARG;
   if (grad_stride != 0 && grad_stride != 1) return FCT_ERR_INVALID_ARG;
-  const void* bf[6] = {h_s, w_s, h_t, w_t, grad_h_s, nullptr};
-  for (const void* q : bf)
-    if (q && !aligned(q, 2)) return FCT_ERR_ALIGNMENT;
+  // the GEMM operands are TMA tiles: 16-byte aligned rows
+  if (!fct::gemm_operand_ok(h_s, ld_hs) || !fct::gemm_operand_ok(w_s, ld_ws) ||
+      !fct::gemm_operand_ok(h_t, ld_ht) || !fct::gemm_operand_ok(w_t, ld_wt) ||
+      (grad_h_s && !aligned(grad_h_s, 2)))
+    return FCT_ERR_ALIGNMENT;
   if (!aligned(target, 8) || !aligned(grad_ce, 4) || !aligned(grad_tvd, 4) ||
       (grad_w_s && !aligned(grad_w_s, 4)) || !aligned(workspace, 256) ||
       (dev_status && !aligned(dev_status, 4)))
@@ -472,6 +474,43 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
                  logits_dtype};
   const fct::FwdPlan plan = plan_forward(d, V, logits_dtype, true, true);
   if (fct::launch_linear(a, plan, dev, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return FCT_ERR_CUDA;
+  return FCT_OK;
+}
+
+int gemm_impl(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t ldb, int32_t b_mn,
+              void* C, int64_t ldc, int32_t c_kind, int64_t M, int64_t N, int64_t K,
+              int32_t* dev_status, void* stream) {
+  if (c_kind != FCT_GEMM_F32 && c_kind != FCT_GEMM_BF16 && c_kind != FCT_GEMM_ADD_F32)
+    return FCT_ERR_UNSUPPORTED;
+  if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return FCT_ERR_INVALID_ARG;
+  if (M < 0 || N < 0 || K < 1) return FCT_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) return FCT_OK;
+  // TMA coordinates and box origins are 32-bit
+  const int64_t kMax = int64_t(1) << 31;
+  if (M >= kMax || N >= kMax || K >= kMax) return FCT_ERR_UNSUPPORTED;
+  if (!A || !B || !C) return FCT_ERR_INVALID_ARG;
+  // A: M x K, B: N x K; each stored as lines of its contiguous extent
+  const int64_t a_lines = a_mn ? K : M, a_cols = a_mn ? M : K;
+  const int64_t b_lines = b_mn ? K : N, b_cols = b_mn ? N : K;
+  const size_t ce = c_kind == FCT_GEMM_BF16 ? 2 : 4;
+  if (lda < a_cols || ldb < b_cols || ldc < N) return FCT_ERR_INVALID_ARG;
+  if (!span_fits(a_lines, lda, a_cols, 2) || !span_fits(b_lines, ldb, b_cols, 2) ||
+      !span_fits(M, ldc, N, static_cast<int64_t>(ce)))
+    return FCT_ERR_UNSUPPORTED;
+  if (!fct::gemm_operand_ok(A, lda) || !fct::gemm_operand_ok(B, ldb) || !aligned(C, ce) ||
+      (dev_status && !aligned(dev_status, 4)))
+    return FCT_ERR_ALIGNMENT;
+  const Range c = mat_range(C, M, ldc, N, ce);
+  if (overlap(c, mat_range(A, a_lines, lda, a_cols, 2)) ||
+      overlap(c, mat_range(B, b_lines, ldb, b_cols, 2)))
+    return FCT_ERR_INVALID_ARG;
+  DeviceInfo d;
+  const int rc = current_device(&d);
+  if (rc != FCT_OK) return rc;
+  if (fct::launch_gemm(fct::GemmOperand{A, lda, a_mn != 0}, fct::GemmOperand{B, ldb, b_mn != 0}, C,
+                       ldc, c_kind, M, N, K, dev_status, d.sms,
+                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
 }
@@ -845,6 +884,13 @@ const char* fct_status_string(int status) {
     case FCT_ERR_CUDA: return "FCT_ERR_CUDA: CUDA runtime or launch error";
     default: return "unknown fct_status";
   }
+}
+
+int fct_gemm_bf16(const void* A, int64_t lda, int32_t a_mn_major, const void* B, int64_t ldb,
+                  int32_t b_mn_major, void* C, int64_t ldc, int32_t c_kind, int64_t M, int64_t N,
+                  int64_t K, int32_t* dev_status, void* stream) {
+  return gemm_impl(A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_kind, M, N, K, dev_status,
+                   stream);
 }
 
 int fct_version(void) { return 400; }  // 0.4.0: per-call fct_options, no process-wide knob

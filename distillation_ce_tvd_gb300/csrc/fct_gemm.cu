@@ -1,0 +1,512 @@
+// bf16 GEMM on the fifth-generation tensor cores: C (+)= A * B^T.
+//
+// The fused-linear loss computes logits from hidden states and lm_head
+// weights and, backwards, the gradients of both: dense contractions (the
+// Liger-Kernel overview's fused linear cross-entropy computes logits block by
+// block and never holds the whole (BT, V) logit matrix).  This kernel is
+// their GB300 form:
+//   * operands: A is M x K and B is N x K (C(m, n) = sum_k A(m, k) B(n, k)),
+//     bf16, each either K-major (A(m, k) at a[m * ld + k]) or MN-major
+//     (A(m, k) at a[k * ld + m]), so the products with a transposed operand
+//     (d hidden = G W, d weight = G^T H) need no transposed copies;
+//   * a cluster of two CTAs on an SM pair computes one 256 x 256 tile of C
+//     with tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16 per
+//     instruction, bf16 x bf16, fp32 accumulate): each CTA stages, by TMA
+//     (cp.async.bulk.tensor, 128-byte swizzle), its own 128 rows of A and its
+//     half (128 rows) of B, 64 K-columns per stage, 6 stages deep, and holds
+//     the accumulator of its 128 rows in its own tensor memory.  Against one
+//     CTA computing 128 x 256 alone, each SM stages 32 KB per K block
+//     instead of 48 KB for the same tensor-core work;
+//   * two accumulators of 256 columns per CTA (512 columns), so the epilogue
+//     of one tile overlaps the MMAs of the next; four warps per CTA read
+//     theirs with tcgen05.ld (each its 32-lane quarter, one output row per
+//     thread) and store fp32 or bf16 rows, or add into an fp32 C;
+//   * a persistent grid of as many pairs as fit, walking the tiles with the
+//     M tiles of one N column consecutive, so pairs working at once share B
+//     tiles (and the small A operand) through L2.
+// Per CTA: warp 0 issues TMA, warp 1 owns the tensor memory (and, in the
+// pair's rank-0 CTA, issues the MMAs), warps 2-5 run the epilogue.  Every
+// mbarrier wait is bounded: a wait that runs out sets an abort flag, the
+// roles stop, the last copies and MMAs are waited for (bounded) before the
+// tensor memory is freed, and the kernel ORs FCT_DEV_WAIT_TIMEOUT into the
+// status word.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "fct_common.cuh"
+#include "fct_internal.h"
+
+namespace fct {
+
+namespace {
+
+constexpr int kCtaRows = 128;  // rows of A and of B each CTA of a pair stages
+constexpr int kBM = 256, kBN = 256, kBK = 64;  // the pair's tile
+constexpr int kGStages = 6;
+constexpr int kGemmThreads = 192;
+constexpr uint32_t kHalfBytes = kCtaRows * kBK * 2;  // 16 KB: one operand's rows of a CTA
+constexpr uint32_t kGStageBytes = 2 * kHalfBytes;     // A and B rows of a CTA
+constexpr uint32_t kBoxBytes = 64 * kBK * 2;          // one 64 x 64 box of an MN-major operand
+constexpr uint32_t kTmemCols = 2 * kBN;               // two fp32 accumulators of 256 columns
+constexpr size_t kGemmSmem = size_t(kGStages) * kGStageBytes + 1024;  // + room to align to 1 KB
+
+enum COut { kOutF32 = 0, kOutBf16 = 1, kOutAddF32 = 2 };
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
+// 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), A and B major-ness
+// (bits 15 and 16: 0 K-major, 1 MN-major), N / 8 at bits 17-22, M / 16 at
+// bits 24-28.
+template <bool kAmn, bool kBmn>
+__host__ __device__ constexpr uint32_t idesc() {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(kAmn) << 15) | (uint32_t(kBmn) << 16) |
+         (uint32_t(kBN >> 3) << 17) | (uint32_t(kBM >> 4) << 24);
+}
+
+// Shared-memory matrix descriptor of a tile written by TMA with 128-byte
+// swizzle (8-row atoms of 128-byte rows, 1024 bytes): start address, leading
+// and stride byte offsets in 16-byte units, version 1 (bits 46-47), swizzle
+// mode 2 = 128-byte (bits 61-63).
+//   K-major: rows are the M (N) index, 64 K elements per row; atoms of 8
+//   rows are 1024 bytes apart (stride offset); the leading offset is unused.
+//   A K step of 16 advances the start by 32 bytes inside the atom.
+//   MN-major: rows are the K index, 64 M (N) elements per row; atoms of 8 K
+//   rows are 1024 bytes apart (stride offset), the next 64 M (N) elements
+//   start one 64 x 64 box later (leading offset 8192 bytes).  A K step of 16
+//   advances the start by 16 rows = 2048 bytes.
+template <bool kMn>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  uint64_t d = uint64_t((saddr & 0x3FFFFu) >> 4);
+  d |= uint64_t(kMn ? (kBoxBytes >> 4) : 1u) << 16;
+  d |= uint64_t(1024 >> 4) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(2) << 61;
+  return d;
+}
+template <bool kMn>
+__host__ __device__ constexpr uint64_t desc_k_step() {  // one K step of 16 elements, in 16-byte units
+  return kMn ? (16 * 128) >> 4 : (16 * 2) >> 4;
+}
+
+// A 2-D TMA load into this CTA's shared memory whose completion is counted
+// on the mbarrier at cluster address `bar` (the pair's rank-0 CTA's).
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+// A CTA's rows of an operand for k block kb: rows r0 .. r0 + 127 of the M (N)
+// index.  K-major: one box {64 K, 128}.  MN-major: two boxes {64 M (N),
+// 64 K}, 8 KB apart.
+template <bool kMn>
+__device__ __forceinline__ void load_rows(uint32_t dst, const CUtensorMap* map, int r0, int kb,
+                                          uint32_t bar) {
+  if constexpr (kMn) {
+#pragma unroll
+    for (int j = 0; j < kCtaRows / 64; ++j)
+      tma_load_2d(dst + j * kBoxBytes, map, r0 + 64 * j, kb * kBK, bar);
+  } else {
+    tma_load_2d(dst, map, kb * kBK, r0, bar);
+  }
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The cluster address of this CTA's shared variable at `saddr` in CTA `rank`.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <uint32_t kIdesc>
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(kIdesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrives once on the mbarrier at `bar`'s offset in both CTAs of the pair
+// when every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void umma_commit_pair(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_addr(bar)),
+      "h"(static_cast<uint16_t>(3))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns of tensor memory: thread i of the
+// warp receives lane (lane base + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+struct GemmArgs {
+  int64_t M, N, K;
+  void* C;
+  int64_t ldc;
+  int vec;  // C's rows start on 16-byte boundaries: vector stores
+  int32_t* status;
+};
+
+// Stores (or adds) 32 consecutive fp32 results of one C row, columns
+// [col0, col0 + 32) clipped to N.
+template <int kOut>
+__device__ __forceinline__ void store_row32(const GemmArgs& g, int64_t row, int64_t col0,
+                                            const uint32_t (&r)[32]) {
+  if constexpr (kOut == kOutBf16) {
+    uint16_t* crow = static_cast<uint16_t*>(g.C) + row * g.ldc + col0;
+    if (g.vec && col0 + 32 <= g.N) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 8) {
+        const uint4 v = make_uint4(pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])),
+                                   pack_bf16x2(__uint_as_float(r[j + 2]), __uint_as_float(r[j + 3])),
+                                   pack_bf16x2(__uint_as_float(r[j + 4]), __uint_as_float(r[j + 5])),
+                                   pack_bf16x2(__uint_as_float(r[j + 6]), __uint_as_float(r[j + 7])));
+        *reinterpret_cast<uint4*>(crow + j) = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (col0 + j < g.N)
+          crow[j] = static_cast<uint16_t>(pack_bf16x2(__uint_as_float(r[j]), 0.f) & 0xffffu);
+    }
+  } else {
+    float* crow = static_cast<float*>(g.C) + row * g.ldc + col0;
+    if (g.vec && col0 + 32 <= g.N) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 v = make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                               __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        if constexpr (kOut == kOutAddF32) {
+          const float4 o = *reinterpret_cast<const float4*>(crow + j);
+          v.x = o.x + v.x;
+          v.y = o.y + v.y;
+          v.z = o.z + v.z;
+          v.w = o.w + v.w;
+        }
+        *reinterpret_cast<float4*>(crow + j) = v;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (col0 + j >= g.N) continue;
+        const float v = __uint_as_float(r[j]);
+        crow[j] = (kOut == kOutAddF32) ? crow[j] + v : v;
+      }
+    }
+  }
+}
+
+template <bool kAmn, bool kBmn, int kOut>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                GemmArgs g) {
+  extern __shared__ __align__(1024) uint8_t gemm_smem[];
+  // full_bar: used in the rank-0 CTA only (both CTAs' copies count on it);
+  // acc_empty: rank 0's counts the epilogue warps of both CTAs
+  __shared__ __align__(8) uint64_t full_bar[kGStages], empty_bar[kGStages];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], done_bar;
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = rank == 0;
+  const int64_t pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const uint32_t smem0 = (smem_addr(gemm_smem) + 1023u) & ~1023u;
+  const int64_t m_tiles = (g.M + kBM - 1) / kBM, n_tiles = (g.N + kBN - 1) / kBN;
+  const int64_t tiles = m_tiles * n_tiles;
+  const int k_iters = static_cast<int>((g.K + kBK - 1) / kBK);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGStages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 8);
+    }
+    mbar_init(&done_bar, 1);
+    abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA allocates the pair's tensor memory
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(&tmem_base)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any copy or arrive
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const uint32_t full0 = map_to_rank(smem_addr(&full_bar[0]), 0);
+  const uint32_t acc_empty0 = map_to_rank(smem_addr(&acc_empty[0]), 0);
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      bool ok = true;
+      for (int64_t t = pair; ok && t < tiles; t += n_pairs) {
+        const int m0 = static_cast<int>((t % m_tiles) * kBM) + int(rank) * kCtaRows;
+        const int n0 = static_cast<int>((t / m_tiles) * kBN) + int(rank) * kCtaRows;
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (leader) mbar_arrive_expect_tx(&full_bar[stage], 2 * kGStageBytes);
+          const uint32_t sa = smem0 + stage * kGStageBytes;
+          load_rows<kAmn>(sa, &tmA, m0, kb, full0 + 8u * stage);
+          load_rows<kBmn>(sa + kHalfBytes, &tmB, n0, kb, full0 + 8u * stage);
+          ++issued;
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      // the last fills of both CTAs have landed before the leader's producer
+      // leaves (its full barriers count the peer's bytes too; bounded, even
+      // after an abort)
+      if (leader)
+        for (uint32_t i = (issued > uint32_t(kGStages) ? issued - kGStages : 0); i < issued; ++i)
+          mbar_wait(&full_bar[i % kGStages], (i / kGStages) & 1u, &abort_flag, false);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {  // ---- MMA issuer for the pair
+      constexpr uint32_t kId = idesc<kAmn, kBmn>();
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      int64_t local = 0;
+      for (int64_t t = pair; ok && t < tiles; t += n_pairs, ++local) {
+        const int acc = static_cast<int>(local & 1);
+        const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+        if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, &abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + uint32_t(acc * kBN);
+        for (int kb = 0; kb < k_iters; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem0 + stage * kGStageBytes;
+          const uint64_t adesc = smem_desc<kAmn>(sa), bdesc = smem_desc<kBmn>(sa + kHalfBytes);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16<kId>(d, adesc + kk * desc_k_step<kAmn>(), bdesc + kk * desc_k_step<kBmn>(),
+                           (kb | kk) != 0);
+          umma_commit_pair(&empty_bar[stage]);  // both CTAs' stages are free once these are done
+          if (++stage == kGStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) umma_commit_pair(&acc_full[acc]);
+      }
+      umma_commit_pair(&done_bar);  // every MMA issued has completed
+    }
+  } else {  // ---- epilogue: warps 2-5 of each CTA, each its 32-lane quarter
+    const int q = warp & 3;
+    int64_t local = 0;
+    for (int64_t t = pair; t < tiles; t += n_pairs, ++local) {
+      const int acc = static_cast<int>(local & 1);
+      const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
+      // the warp agrees on the outcome, so the .sync.aligned loads below run
+      // converged even if a wait ran out on some lanes only
+      if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, &abort_flag))) break;
+      tc_fence_after();
+      const int64_t m0 = (t % m_tiles) * kBM + int64_t(rank) * kCtaRows;
+      const int64_t n0 = (t / m_tiles) * kBN;
+      const int64_t row = m0 + q * 32 + lane;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN + c * 32), r);
+        const int64_t col0 = n0 + c * 32;
+        if (row < g.M && col0 < g.N) store_row32<kOut>(g, row, col0, r);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  // the pair's MMAs have all completed before either CTA frees its tensor
+  // memory or leaves (the peer's MMAs read this CTA's shared memory)
+  if (warp == 1 && lane == 0) mbar_wait(&done_bar, 0, &abort_flag, false);
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+  if (threadIdx.x == 0 && abort_flag && g.status) atomicOr(g.status, FCT_DEV_WAIT_TIMEOUT);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Tensor map of a bf16 operand: `inner` contiguous elements per line, `outer`
+// lines ld elements apart; boxes of 64 x box_outer, 128-byte swizzle, zero
+// fill outside the matrix.
+bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, int64_t ld,
+              uint32_t box_outer) {
+  auto encode = encode_fn();
+  if (encode == nullptr) return false;
+  const cuuint64_t dims[2] = {cuuint64_t(inner), cuuint64_t(outer)};
+  const cuuint64_t strides[1] = {cuuint64_t(ld) * 2};
+  const cuuint32_t box[2] = {64u, box_outer};
+  const cuuint32_t elem[2] = {1, 1};
+  return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The operand's map: K-major rows x K with boxes {64 K, tile rows};
+// MN-major K lines of `rows` elements with boxes {64, 64}.
+bool operand_map(CUtensorMap* map, const GemmOperand& x, int64_t rows, int64_t K,
+                 uint32_t tile_rows) {
+  return x.mn_major ? make_map(map, x.ptr, rows, K, x.ld, 64)
+                    : make_map(map, x.ptr, K, rows, x.ld, tile_rows);
+}
+
+template <bool kAmn, bool kBmn, int kOut>
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, int sms,
+                     cudaStream_t st) {
+  auto kernel = gemm_kernel<kAmn, kBmn, kOut>;
+  static std::once_flag once[64];
+  static cudaError_t set_err[64];
+  static int pairs[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kGemmThreads);
+  cfg.dynamicSmemBytes = kGemmSmem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  std::call_once(once[dev], [&] {
+    set_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(kGemmSmem));
+    if (set_err[dev] != cudaSuccess) return;
+    // as many pairs as can be resident at once: the grid is persistent
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(2 * 64);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    pairs[dev] = n;
+  });
+  if (set_err[dev] != cudaSuccess) return set_err[dev];
+  if (pairs[dev] <= 0) return cudaErrorInvalidConfiguration;
+  const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + kBN - 1) / kBN);
+  int64_t n = tiles < pairs[dev] ? tiles : pairs[dev];
+  if (n > sms / 2) n = sms / 2 > 0 ? sms / 2 : 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+  cfg.stream = st;
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, g);
+}
+
+template <int kOut>
+cudaError_t dispatch_major(bool a_mn, bool b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
+                           const GemmArgs& g, int sms, cudaStream_t st) {
+  if (a_mn) return b_mn ? run_gemm<true, true, kOut>(ma, mb, g, sms, st)
+                        : run_gemm<true, false, kOut>(ma, mb, g, sms, st);
+  return b_mn ? run_gemm<false, true, kOut>(ma, mb, g, sms, st)
+              : run_gemm<false, false, kOut>(ma, mb, g, sms, st);
+}
+
+}  // namespace
+
+bool gemm_operand_ok(const void* p, int64_t ld) {
+  return (reinterpret_cast<uintptr_t>(p) % 16) == 0 && ld > 0 && ld % 8 == 0;
+}
+
+cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
+                        int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
+                        cudaStream_t st) {
+  if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (!gemm_operand_ok(A.ptr, A.ld) || !gemm_operand_ok(B.ptr, B.ld) || sms <= 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap ma, mb;
+  if (!operand_map(&ma, A, M, K, kCtaRows) || !operand_map(&mb, B, N, K, kCtaRows))
+    return cudaErrorInvalidValue;
+  const size_t es = c_kind == kOutBf16 ? 2 : 4;
+  const GemmArgs g{M, N, K, C, ldc,
+                   (reinterpret_cast<uintptr_t>(C) % 16 == 0 && (size_t(ldc) * es) % 16 == 0),
+                   status};
+  switch (c_kind) {
+    case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
+    case kOutBf16: return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
+    case kOutAddF32: return dispatch_major<kOutAddF32>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace fct

@@ -158,6 +158,21 @@ struct VpMergeArgs {
 cudaError_t launch_vp_pass(const VpArgs& a, bool vec, bool tvd_pass, int sms, cudaStream_t st);
 cudaError_t launch_vp_merge(const VpMergeArgs& a, bool tvd_merge, cudaStream_t st);
 
+// bf16 GEMM on the tensor cores (fct_gemm.cu): C(m, n) (+)= sum_k A(m, k) B(n, k).
+// An operand is K-major (element (i, k) at ptr[i * ld + k]) or MN-major
+// (element (i, k) at ptr[k * ld + i]); its base must be 16-byte aligned and
+// ld a positive multiple of 8 (gemm_operand_ok).  c_kind: 0 fp32 C, 1 bf16
+// C (rounded to nearest even), 2 fp32 C accumulated into.
+struct GemmOperand {
+  const void* ptr;
+  int64_t ld;
+  bool mn_major;
+};
+bool gemm_operand_ok(const void* p, int64_t ld);
+cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
+                        int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
+                        cudaStream_t st);
+
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs& a, bool vec, int sms, cudaStream_t st);

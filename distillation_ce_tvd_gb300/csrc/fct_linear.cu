@@ -3,41 +3,21 @@
 // The loss of the PR #1384 analysis takes logits; a model produces them as
 // hidden states times an lm_head weight.  Materialising the (BT, V) logits
 // of student and teacher costs 2*BT*V elements of memory and traffic.  Here
-// the rows go through in blocks of R: per block, two plain GEMMs (cuBLAS,
-// bf16 inputs, fp32 accumulate) write the block's student and teacher logits
-// into the caller's workspace, the single-launch forward + backward kernel
-// reads them and writes the block's logit gradient as bf16, and two more
-// GEMMs give the block's d loss / d hidden and accumulate d loss / d weight.
-// The logit blocks are fp32 (the GEMMs' own precision), or bf16 (rounded once
-// by the GEMM, as a model's bf16 lm_head produces them), which halves their
-// bytes and lets the gradient overwrite the student block in place.  Only the
-// block's logits and gradient exist at a time.  The teacher is frozen (no
-// gradients).
-#include <cublas_v2.h>
-
-#include <mutex>
-
+// the rows go through in blocks of R: per block, two GEMMs (the library's
+// tcgen05 GEMM, bf16 inputs, fp32 accumulate) write the block's student and
+// teacher logits into the caller's workspace, the single-launch forward +
+// backward kernel reads them and writes the block's logit gradient as bf16,
+// and two more GEMMs give the block's d loss / d hidden and accumulate
+// d loss / d weight (their transposed operands are read in place, as
+// MN-major tiles).  The logit blocks are fp32 (the GEMMs' own precision), or
+// bf16 (rounded once by the GEMM, as a model's bf16 lm_head produces them),
+// which halves their bytes and lets the gradient overwrite the student block
+// in place.  Only the block's logits and gradient exist at a time.  The
+// teacher is frozen (no gradients).
 #include "fct_common.cuh"
 #include "fct_internal.h"
 
 namespace fct {
-
-namespace {
-
-std::mutex g_blas_mu;
-cublasHandle_t g_blas[64] = {};
-
-cublasStatus_t gemm(cublasHandle_t h, cublasOperation_t ta, cublasOperation_t tb, int64_t m,
-                    int64_t n, int64_t k, const void* A, int64_t lda, const void* B, int64_t ldb,
-                    float beta, void* C, cudaDataType ctype, int64_t ldc) {
-  const float alpha = 1.f;
-  return cublasGemmEx(h, ta, tb, static_cast<int>(m), static_cast<int>(n), static_cast<int>(k),
-                      &alpha, A, CUDA_R_16BF, static_cast<int>(lda), B, CUDA_R_16BF,
-                      static_cast<int>(ldb), &beta, C, ctype, static_cast<int>(ldc),
-                      CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-}
-
-}  // namespace
 
 int64_t linear_logits_ld(int64_t V) { return (V + 7) / 8 * 8; }
 
@@ -51,15 +31,7 @@ size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows, int logits_dtype) {
 
 cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,
                           cudaStream_t st) {
-  (void)sms;
-  std::lock_guard<std::mutex> lk(g_blas_mu);  // one cuBLAS handle per device, one caller at a time
-  if (g_blas[device] == nullptr && cublasCreate(&g_blas[device]) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorInitializationError;
-  cublasHandle_t h = g_blas[device];
-  if (cublasSetStream(h, st) != CUBLAS_STATUS_SUCCESS) return cudaErrorInvalidValue;
-  if (cublasSetMathMode(h, CUBLAS_DEFAULT_MATH) != CUBLAS_STATUS_SUCCESS)
-    return cudaErrorInvalidValue;
-
+  (void)device;
   // logit rows padded to a multiple of 8 elements: 16-byte (bf16) or 32-byte
   // (fp32) row strides, so the loss kernel's vector path applies
   const int64_t ldl = linear_logits_ld(a.V);
@@ -71,39 +43,44 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
   // after the two fp32 blocks
   void* G = bf16 ? static_cast<void*>(Ls) : static_cast<void*>(Lt + block_bytes);
   const int64_t ldg = ldl;
-  const cudaDataType ltype = bf16 ? CUDA_R_16BF : CUDA_R_32F;
+  const int lkind = bf16 ? FCT_GEMM_BF16 : FCT_GEMM_F32;
   const auto* Hs = static_cast<const uint16_t*>(a.h_s);
   const auto* Ht = static_cast<const uint16_t*>(a.h_t);
+  const GemmOperand Ws{a.w_s, a.ld_ws, false}, Wt{a.w_t, a.ld_wt, false};
+  cudaError_t e;
 
   for (int64_t r0 = 0; r0 < a.BT; r0 += a.chunk_rows) {
     const int64_t R = (a.BT - r0 < a.chunk_rows) ? a.BT - r0 : a.chunk_rows;
-    // logits (row-major R x V) = H (R x D) * W^T, as column-major V x R
-    if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, a.V, R, a.d_s, a.w_s, a.ld_ws, Hs + r0 * a.ld_hs,
-             a.ld_hs, 0.f, Ls, ltype, ldl) != CUBLAS_STATUS_SUCCESS)
-      return cudaErrorLaunchFailure;
-    if (gemm(h, CUBLAS_OP_T, CUBLAS_OP_N, a.V, R, a.d_t, a.w_t, a.ld_wt, Ht + r0 * a.ld_ht,
-             a.ld_ht, 0.f, Lt, ltype, ldl) != CUBLAS_STATUS_SUCCESS)
-      return cudaErrorLaunchFailure;
+    // logits (R x V) = H (R x D) W^T: both operands K-major
+    const GemmOperand Hsb{Hs + r0 * a.ld_hs, a.ld_hs, false}, Htb{Ht + r0 * a.ld_ht, a.ld_ht, false};
+    if ((e = launch_gemm(Hsb, Ws, Ls, ldl, lkind, R, a.V, a.d_s, a.dev_status, sms, st)) !=
+        cudaSuccess)
+      return e;
+    if ((e = launch_gemm(Htb, Wt, Lt, ldl, lkind, R, a.V, a.d_t, a.dev_status, sms, st)) !=
+        cudaSuccess)
+      return e;
     // the loss on the block; its logit gradient, as bf16, into G
     FwdArgs f{Ls, Lt, ldl, ldl, bf16 ? FCT_BF16 : FCT_F32, a.target + r0, R, a.V, a.ignore_index,
               a.ce + r0, a.tvd + r0, a.lse_s + r0, a.lse_t + r0, a.sigma + r0, a.dev_status,
               G, ldg, a.grad_ce + (a.grad_stride ? r0 : 0),
               a.grad_tvd + (a.grad_stride ? r0 : 0), a.grad_stride, plan.keep_normal ? 1 : 0,
               /*grad_bf16=*/bf16 ? 0 : 1};
-    cudaError_t e = launch_forward(f, plan, st);
-    if (e != cudaSuccess) return e;
+    if ((e = launch_forward(f, plan, st)) != cudaSuccess) return e;
     if (a.grad_h_s == nullptr && a.grad_w_s == nullptr) continue;
-    // d hidden (row-major R x D) = G (R x V) * W (V x D), as column-major D x R
+    // d hidden (R x D, bf16) = G (R x V) W (V x D): C(r, d) = sum_v G(r, v) W(v, d),
+    // G K-major, W read as the MN-major (D x V) operand
     if (a.grad_h_s &&
-        gemm(h, CUBLAS_OP_N, CUBLAS_OP_N, a.d_s, R, a.V, a.w_s, a.ld_ws, G, ldg, 0.f,
-             static_cast<uint16_t*>(a.grad_h_s) + r0 * a.ld_ghs, CUDA_R_16BF,
-             a.ld_ghs) != CUBLAS_STATUS_SUCCESS)
-      return cudaErrorLaunchFailure;
-    // d weight (row-major V x D, fp32) += G^T (V x R) * H (R x D), as column-major D x V
+        (e = launch_gemm(GemmOperand{G, ldg, false}, GemmOperand{a.w_s, a.ld_ws, true},
+                         static_cast<uint16_t*>(a.grad_h_s) + r0 * a.ld_ghs, a.ld_ghs,
+                         FCT_GEMM_BF16, R, a.d_s, a.V, a.dev_status, sms, st)) != cudaSuccess)
+      return e;
+    // d weight (V x D, fp32) += G^T H: C(v, d) += sum_r G(r, v) H(r, d), both
+    // operands MN-major
     if (a.grad_w_s &&
-        gemm(h, CUBLAS_OP_N, CUBLAS_OP_T, a.d_s, a.V, R, Hs + r0 * a.ld_hs, a.ld_hs, G, ldg, 1.f,
-             a.grad_w_s, CUDA_R_32F, a.ld_gws) != CUBLAS_STATUS_SUCCESS)
-      return cudaErrorLaunchFailure;
+        (e = launch_gemm(GemmOperand{G, ldg, true}, GemmOperand{Hs + r0 * a.ld_hs, a.ld_hs, true},
+                         a.grad_w_s, a.ld_gws, FCT_GEMM_ADD_F32, a.V, a.d_s, R, a.dev_status, sms,
+                         st)) != cudaSuccess)
+      return e;
   }
   return cudaGetLastError();
 }

@@ -409,6 +409,48 @@ int fused_linear_ce_tvd_forward_backward_noalloc(
     void* stream);
 
 /*
+ * The bf16 GEMM that the fused-linear entry point above runs its four
+ * products on (logits = H W^T, d hidden = G W, d weight += G^T H; the
+ * Liger-Kernel overview's fused linear cross-entropy computes the logits of
+ * a row block by such a product and never holds the whole logit matrix),
+ * exported as an operation of its own.  Hand-written for sm_103a: TMA tile
+ * loads, tcgen05.mma with the accumulator in tensor memory, one persistent
+ * CTA per SM.
+ *
+ *   C(m, n)  = sum_k A(m, k) B(n, k)   c_kind FCT_GEMM_F32 (fp32 C) or
+ *                                      FCT_GEMM_BF16 (bf16 C, the fp32 sum
+ *                                      rounded to nearest even);
+ *   C(m, n) += sum_k A(m, k) B(n, k)   c_kind FCT_GEMM_ADD_F32 (fp32 C).
+ *   Anything else: FCT_ERR_UNSUPPORTED.
+ *
+ *   A (M x K), B (N x K): bf16.  a_mn_major = 0: A(m, k) at A[m * lda + k]
+ *            (K contiguous); 1: A(m, k) at A[k * lda + m] (M contiguous).
+ *            Likewise b_mn_major for B.  Other values: FCT_ERR_INVALID_ARG.
+ *            Both 16-byte aligned with lda, ldb multiples of 8 (the tile
+ *            loads are TMA copies), else FCT_ERR_ALIGNMENT; lda, ldb at
+ *            least the contiguous extent, else FCT_ERR_INVALID_ARG.
+ *   C        : row-major M x N, row stride ldc >= N, aligned to its element;
+ *            must not overlap A or B (FCT_ERR_INVALID_ARG).
+ *   M, N >= 0 (0: nothing to do, FCT_OK), K >= 1; M, N, K < 2^31, else
+ *            FCT_ERR_UNSUPPORTED.
+ * The tensor cores accumulate in fp32, K in blocks of 16 in increasing
+ * order; every element goes through the same sequence of instructions, so a
+ * result depends only on its row of A and its row of B (not on M, N or the
+ * tile it falls in), and repeated calls give identical bits.  Sums of
+ * products that are exact in fp32 are exact.
+ * dev_status (optional): FCT_DEV_WAIT_TIMEOUT is ORed in if
+ * a pipeline wait in the kernel ran out (C is then invalid).
+ */
+#define FCT_GEMM_F32 0
+#define FCT_GEMM_BF16 1
+#define FCT_GEMM_ADD_F32 2
+
+int fct_gemm_bf16(const void* A, int64_t lda, int32_t a_mn_major,
+                  const void* B, int64_t ldb, int32_t b_mn_major, void* C,
+                  int64_t ldc, int32_t c_kind, int64_t M, int64_t N, int64_t K,
+                  int32_t* dev_status, void* stream);
+
+/*
  * Cross-entropy alone: the CE half of "Forward Pass" (one log-sum-exp pass,
  * ce = lse - logits[target]).  ce, lse: (BT,) fp32 outputs.
  */

@@ -318,6 +318,52 @@ def test_fused_linear_workspace_sizes_and_argument_checks(lib):
     assert call(a11=0) == OK                          # empty batch
 
 
+def test_gemm_argument_checks(lib):
+    f = lib.fct_gemm_bf16
+    A, B, C = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
+    # A: M x K = 100 x 64 K-major (ld 64); B: N x K = 300 x 64 K-major; C: 100 x 300 fp32
+    args = [A, 64, 0, B, 64, 0, C, 300, 0, 100, 300, 64, None, None]
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a8=3) == UNSUPPORTED                  # unknown output kind
+    assert call(a2=2) == INVALID                      # major flag is 0 or 1
+    assert call(a11=0) == INVALID                     # K >= 1
+    assert call(a9=-1) == INVALID
+    assert call(a9=0) == OK and call(a10=0) == OK     # empty output: nothing to do
+    assert call(a0=None) == INVALID
+    assert call(a1=60) == INVALID                     # lda < K
+    assert call(a2=1, a1=96) == INVALID               # MN-major A needs lda >= M = 100
+    assert call(a4=68) == ALIGN                       # ldb not a multiple of 8
+    assert call(a0=A + 8) == ALIGN                    # A not 16-byte aligned
+    assert call(a6=C + 2) == ALIGN                    # fp32 C not 4-byte aligned
+    assert call(a7=299) == INVALID                    # ldc < N
+    assert call(a6=A + 64) == INVALID                 # C overlaps A
+    assert call(a11=1 << 31) == UNSUPPORTED           # 32-bit tile coordinates
+
+
+def test_fused_linear_needs_tma_aligned_operands(lib):
+    f = lib.fused_linear_ce_tvd_forward_backward
+    base = FAKE + (6 << 30)
+    args = [FAKE, 64, FAKE + (1 << 30), 64, 64, FAKE + (2 << 30), 64, FAKE + (3 << 30), 64, 64,
+            FAKE + (4 << 30), 4, 100, -100, base, base + 256, 1,
+            base + 512, base + 768, base + 1024, base + 1280, base + 1536,
+            FAKE + (5 << 30), 64, FAKE + (7 << 30), 64, 1, FAKE + (8 << 30), 4 * 104 * 4, 4,
+            None, None]
+
+    def call(**kw):
+        a = list(args)
+        for i, v in kw.items():
+            a[int(i[1:])] = v
+        return f(*a)
+    assert call(a1=68, a4=60) == ALIGN                # h_student row stride of 136 bytes
+    assert call(a2=FAKE + (1 << 30) + 8) == ALIGN     # w_student 8 bytes off
+    assert call(a7=FAKE + (3 << 30) + 2) == ALIGN     # w_teacher 2 bytes off
+
+
 def test_binding_refuses_host_tensors(lib):
     import torch
     x = torch.zeros(2, 8)
