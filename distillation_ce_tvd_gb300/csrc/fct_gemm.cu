@@ -21,9 +21,10 @@
 //     of one tile overlaps the MMAs of the next; four warps per CTA read
 //     theirs with tcgen05.ld (each its 32-lane quarter, one output row per
 //     thread) and store fp32 or bf16 rows, or add into an fp32 C;
-//   * a persistent grid of as many pairs as fit, walking the tiles with the
-//     M tiles of one N column consecutive, so pairs working at once share B
-//     tiles (and the small A operand) through L2.
+//   * a persistent grid of as many pairs as fit, walking the tiles along the
+//     index of the smaller operand first (M tiles of one N column when A is
+//     the smaller one), so pairs working at once share the larger operand's
+//     tile through L2 and the smaller operand stays there whole.
 // Per CTA: warp 0 issues TMA, warp 1 owns the tensor memory (and, in the
 // pair's rank-0 CTA, issues the MMAs), warps 2-5 run the epilogue.  Every
 // mbarrier wait is bounded: a wait that runs out sets an abort flag, the
@@ -33,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "fct_common.cuh"
@@ -50,7 +52,13 @@ constexpr uint32_t kHalfBytes = kCtaRows * kBK * 2;  // 16 KB: one operand's row
 constexpr uint32_t kGStageBytes = 2 * kHalfBytes;     // A and B rows of a CTA
 constexpr uint32_t kBoxBytes = 64 * kBK * 2;          // one 64 x 64 box of an MN-major operand
 constexpr uint32_t kTmemCols = 2 * kBN;               // two fp32 accumulators of 256 columns
-constexpr size_t kGemmSmem = size_t(kGStages) * kGStageBytes + 1024;  // + room to align to 1 KB
+// Epilogue staging: per epilogue warp two buffers of 32 rows x 128 bytes
+// (32 fp32 or 64 bf16 columns), written in the 128-byte swizzle of the C
+// tensor map and sent out by TMA.
+constexpr uint32_t kOutBufBytes = 32 * 128;
+constexpr uint32_t kEpiBytes = 4 * 2 * kOutBufBytes;  // 32 KB
+constexpr size_t kGemmSmem =
+    size_t(kGStages) * kGStageBytes + kEpiBytes + 1024;  // + room to align to 1 KB
 
 enum COut { kOutF32 = 0, kOutBf16 = 1, kOutAddF32 = 2 };
 
@@ -181,9 +189,69 @@ struct GemmArgs {
   int64_t M, N, K;
   void* C;
   int64_t ldc;
-  int vec;  // C's rows start on 16-byte boundaries: vector stores
+  int vec;    // C's rows start on 16-byte boundaries: vector stores
+  int tma_c;  // C written through its tensor map (TMA store / reduce-add)
+  int n_fast; // tile walk: N index fastest (A is the larger operand) or M fastest
   int32_t* status;
 };
+
+// Tile t's (M tile, N tile).  Pairs working at once take consecutive t, so
+// they share the operand tile of the slow index through L2; the fast index
+// runs over the smaller operand, which stays in L2 as a whole.
+__device__ __forceinline__ void tile_mn(const GemmArgs& g, int64_t t, int64_t m_tiles,
+                                        int64_t n_tiles, int64_t& tm, int64_t& tn) {
+  if (g.n_fast) {
+    tn = t % n_tiles;
+    tm = t / n_tiles;
+  } else {
+    tm = t % m_tiles;
+    tn = t / m_tiles;
+  }
+}
+
+// TMA from this CTA's shared memory to C: a plain store, or an fp32 add
+// performed at L2 (the read-modify-write of an accumulated C never reaches
+// the SM).  Completion is tracked per thread in bulk groups.
+template <bool kAdd>
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
+  if constexpr (kAdd)
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(src)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(src)
+        : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Waits until at most one (none) of this thread's bulk groups still reads
+// shared memory.
+__device__ __forceinline__ void bulk_wait_read_1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// One thread's 128-byte row of a staging buffer, 16-byte chunk j at chunk
+// position j ^ (row % 8): the 128-byte swizzle of the C tensor map, which
+// also spreads a warp's chunk stores over all banks.
+__device__ __forceinline__ void stage_row(uint32_t buf, int row, const uint32_t (&w)[32]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = buf + uint32_t(row) * 128u + uint32_t((j ^ (row & 7)) * 16);
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(w[4 * j]),
+                 "r"(w[4 * j + 1]), "r"(w[4 * j + 2]), "r"(w[4 * j + 3])
+                 : "memory");
+  }
+}
 
 // Stores (or adds) 32 consecutive fp32 results of one C row, columns
 // [col0, col0 + 32) clipped to N.
@@ -237,8 +305,8 @@ __device__ __forceinline__ void store_row32(const GemmArgs& g, int64_t row, int6
 template <bool kAmn, bool kBmn, int kOut>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                GemmArgs g) {
-  extern __shared__ __align__(1024) uint8_t gemm_smem[];
+                const __grid_constant__ CUtensorMap tmC, GemmArgs g) {
+  extern __shared__ uint8_t gemm_smem[];
   // full_bar: used in the rank-0 CTA only (both CTAs' copies count on it);
   // acc_empty: rank 0's counts the epilogue warps of both CTAs
   __shared__ __align__(8) uint64_t full_bar[kGStages], empty_bar[kGStages];
@@ -289,8 +357,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0, issued = 0;
       bool ok = true;
       for (int64_t t = pair; ok && t < tiles; t += n_pairs) {
-        const int m0 = static_cast<int>((t % m_tiles) * kBM) + int(rank) * kCtaRows;
-        const int n0 = static_cast<int>((t / m_tiles) * kBN) + int(rank) * kCtaRows;
+        int64_t tm, tn;
+        tile_mn(g, t, m_tiles, n_tiles, tm, tn);
+        const int m0 = static_cast<int>(tm * kBM) + int(rank) * kCtaRows;
+        const int n0 = static_cast<int>(tn * kBN) + int(rank) * kCtaRows;
         for (int kb = 0; kb < k_iters; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
             ok = false;
@@ -352,6 +422,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else {  // ---- epilogue: warps 2-5 of each CTA, each its 32-lane quarter
     const int q = warp & 3;
     int64_t local = 0;
+    bool last_sent = false;  // lane 0: whether the previous block committed a bulk group
     for (int64_t t = pair; t < tiles; t += n_pairs, ++local) {
       const int acc = static_cast<int>(local & 1);
       const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
@@ -359,20 +430,71 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // converged even if a wait ran out on some lanes only
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, &abort_flag))) break;
       tc_fence_after();
-      const int64_t m0 = (t % m_tiles) * kBM + int64_t(rank) * kCtaRows;
-      const int64_t n0 = (t / m_tiles) * kBN;
-      const int64_t row = m0 + q * 32 + lane;
+      int64_t tm, tn;
+      tile_mn(g, t, m_tiles, n_tiles, tm, tn);
+      const int64_t m0 = tm * kBM + int64_t(rank) * kCtaRows;
+      const int64_t n0 = tn * kBN;
+      const uint32_t tq = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN);
+      if (g.tma_c) {
+        // 32-row blocks of 128 bytes per row through two staging buffers
+        const uint32_t buf0 = smem0 + kGStages * kGStageBytes + uint32_t(q) * 2 * kOutBufBytes;
+        constexpr int kCols = (kOut == kOutBf16) ? 64 : 32;
+        const int y = static_cast<int>(m0 + q * 32);
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN + c * 32), r);
-        const int64_t col0 = n0 + c * 32;
-        if (row < g.M && col0 < g.N) store_row32<kOut>(g, row, col0, r);
+        for (int c = 0; c < kBN / kCols; ++c) {
+          uint32_t w[32];
+          if constexpr (kOut == kOutBf16) {
+            uint32_t r[32];
+            tmem_ld32(tq + uint32_t(c * 64), r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              w[j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+            tmem_ld32(tq + uint32_t(c * 64 + 32), r);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              w[16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+          } else {
+            tmem_ld32(tq + uint32_t(c * 32), w);
+          }
+          if (c == kBN / kCols - 1) {  // the accumulator is read: release it
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
+          }
+          // buffers alternate (kBN / kCols is even, so also across tiles);
+          // the store that last used this one has finished reading it
+          const uint32_t buf = buf0 + uint32_t(c & 1) * kOutBufBytes;
+          if (lane == 0) {
+            if (last_sent)
+              bulk_wait_read_1();
+            else
+              bulk_wait_read_0();
+          }
+          __syncwarp();
+          stage_row(buf, lane, w);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            last_sent = n0 + c * kCols < g.N && y < g.M;
+            if (last_sent)
+              tma_store_2d<kOut == kOutAddF32>(&tmC, static_cast<int>(n0) + c * kCols, y, buf);
+          }
+        }
+      } else {
+        const int64_t row = m0 + q * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tq + uint32_t(c * 32), r);
+          const int64_t col0 = n0 + c * 32;
+          if (row < g.M && col0 < g.N) store_row32<kOut>(g, row, col0, r);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
     }
+    if (lane == 0) bulk_wait_all();  // C is written before the kernel ends
   }
   tc_fence_before();
   __syncthreads();
@@ -422,6 +544,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t inner, int64_t outer, 
                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// C's map for the epilogue's stores: M rows of N elements, ldc apart, boxes
+// of 32 rows x 128 bytes (32 fp32 or 64 bf16), 128-byte swizzle.
+bool make_c_map(CUtensorMap* map, void* C, int64_t M, int64_t N, int64_t ldc, bool bf16) {
+  auto encode = encode_fn();
+  if (encode == nullptr) return false;
+  const size_t es = bf16 ? 2 : 4;
+  const cuuint64_t dims[2] = {cuuint64_t(N), cuuint64_t(M)};
+  const cuuint64_t strides[1] = {cuuint64_t(ldc) * es};
+  const cuuint32_t box[2] = {cuuint32_t(128 / es), 32u};
+  const cuuint32_t elem[2] = {1, 1};
+  return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                C, dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The operand's map: K-major rows x K with boxes {64 K, tile rows};
 // MN-major K lines of `rows` elements with boxes {64, 64}.
 bool operand_map(CUtensorMap* map, const GemmOperand& x, int64_t rows, int64_t K,
@@ -431,8 +569,8 @@ bool operand_map(CUtensorMap* map, const GemmOperand& x, int64_t rows, int64_t K
 }
 
 template <bool kAmn, bool kBmn, int kOut>
-cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArgs& g, int sms,
-                     cudaStream_t st) {
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                     const GemmArgs& g, int sms, cudaStream_t st) {
   auto kernel = gemm_kernel<kAmn, kBmn, kOut>;
   static std::once_flag once[64];
   static cudaError_t set_err[64];
@@ -470,16 +608,16 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmArg
   if (n > sms / 2) n = sms / 2 > 0 ? sms / 2 : 1;
   cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
   cfg.stream = st;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, g);
+  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, g);
 }
 
 template <int kOut>
 cudaError_t dispatch_major(bool a_mn, bool b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
-                           const GemmArgs& g, int sms, cudaStream_t st) {
-  if (a_mn) return b_mn ? run_gemm<true, true, kOut>(ma, mb, g, sms, st)
-                        : run_gemm<true, false, kOut>(ma, mb, g, sms, st);
-  return b_mn ? run_gemm<false, true, kOut>(ma, mb, g, sms, st)
-              : run_gemm<false, false, kOut>(ma, mb, g, sms, st);
+                           const CUtensorMap& mc, const GemmArgs& g, int sms, cudaStream_t st) {
+  if (a_mn) return b_mn ? run_gemm<true, true, kOut>(ma, mb, mc, g, sms, st)
+                        : run_gemm<true, false, kOut>(ma, mb, mc, g, sms, st);
+  return b_mn ? run_gemm<false, true, kOut>(ma, mb, mc, g, sms, st)
+              : run_gemm<false, false, kOut>(ma, mb, mc, g, sms, st);
 }
 
 }  // namespace
@@ -498,13 +636,20 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
   if (!operand_map(&ma, A, M, K, kCtaRows) || !operand_map(&mb, B, N, K, kCtaRows))
     return cudaErrorInvalidValue;
   const size_t es = c_kind == kOutBf16 ? 2 : 4;
-  const GemmArgs g{M, N, K, C, ldc,
-                   (reinterpret_cast<uintptr_t>(C) % 16 == 0 && (size_t(ldc) * es) % 16 == 0),
-                   status};
+  const bool aligned16 =
+      reinterpret_cast<uintptr_t>(C) % 16 == 0 && (size_t(ldc) * es) % 16 == 0;
+  // TMA stores clip a row at 16-byte granularity: a row whose width is not
+  // a multiple of 16 bytes would get the next few elements written too
+  CUtensorMap mc;
+  memset(&mc, 0, sizeof(mc));
+  const bool tma_c = aligned16 && (size_t(N) * es) % 16 == 0 &&
+                     make_c_map(&mc, C, M, N, ldc, c_kind == kOutBf16);
+  const GemmArgs g{M, N, K, C, ldc, aligned16 ? 1 : 0, tma_c ? 1 : 0, M > N ? 1 : 0, status};
   switch (c_kind) {
-    case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
-    case kOutBf16: return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
-    case kOutAddF32: return dispatch_major<kOutAddF32>(A.mn_major, B.mn_major, ma, mb, g, sms, st);
+    case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
+    case kOutBf16: return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
+    case kOutAddF32:
+      return dispatch_major<kOutAddF32>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
     default: return cudaErrorInvalidValue;
   }
 }

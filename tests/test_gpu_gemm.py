@@ -35,17 +35,20 @@ def round8(n: int) -> int:
     return (n + 7) // 8 * 8
 
 
-def operand(x_rowmajor: torch.Tensor, mn_major: bool, pad: int = 0) -> torch.Tensor:
+def operand(x_rowmajor: torch.Tensor, mn_major: bool, pad: int = 0,
+            fill=float("nan")) -> torch.Tensor:
     """The (rows, K) operand x as a K-major view (row-major, row stride
     round8(K) + pad) or an MN-major one (the transpose of a row-major
     (K, rows) tensor with row stride round8(rows) + pad); pad is a multiple
-    of 8, so the strides meet the 16-byte rule."""
+    of 8, so the strides meet the 16-byte rule.  The padding holds NaN: a
+    tile load that read past the matrix instead of filling zeros would turn
+    the result into NaN."""
     rows, K = x_rowmajor.shape
     if mn_major:
-        base = torch.zeros(K, round8(rows) + pad, dtype=x_rowmajor.dtype, device=DEV)
+        base = torch.full((K, round8(rows) + pad), fill, dtype=x_rowmajor.dtype, device=DEV)
         base[:, :rows] = x_rowmajor.t()
         return base[:, :rows].t()
-    base = torch.zeros(rows, round8(K) + pad, dtype=x_rowmajor.dtype, device=DEV)
+    base = torch.full((rows, round8(K) + pad), fill, dtype=x_rowmajor.dtype, device=DEV)
     base[:, :K] = x_rowmajor
     return base[:, :K]
 
@@ -109,21 +112,27 @@ def test_gemm_is_deterministic_and_tile_independent():
     assert torch.equal(c1[170:171, 300:], c3)
 
 
-def test_gemm_ragged_output_leaves_neighbours_alone():
-    # C as a view inside a larger buffer: nothing outside M x N is written
+@pytest.mark.parametrize("r0,c0", [(3, 5), (8, 8)])
+def test_gemm_ragged_output_leaves_neighbours_alone(r0, c0):
+    # C as a view inside a larger buffer: nothing outside M x N is written.
+    # At (3, 5) the view is not 16-byte aligned (per-thread stores); at
+    # (8, 8) it is, and C goes out through TMA stores whose last boxes are
+    # clipped at the view's edge.
     g = torch.Generator(device=DEV).manual_seed(9)
     a = dyadic((130, 72), 3, 4.0, g)
     b = dyadic((259, 72), 7, 16.0, g)
+    ref64 = a.double() @ b.double().T
     for dtype in (torch.float32, torch.bfloat16):
-        big = torch.full((140, 272), 7.0, device=DEV, dtype=dtype)
-        view = big[3:133, 5:264]
-        binding.fct_gemm_bf16(a, b, view)
-        torch.cuda.synchronize()
-        ref = (a.double() @ b.double().T).to(dtype)
-        assert torch.equal(view, ref)
-        mask = torch.ones_like(big, dtype=torch.bool)
-        mask[3:133, 5:264] = False
-        assert torch.all(big[mask] == 7.0)
+        for accumulate in ((False, True) if dtype == torch.float32 else (False,)):
+            big = torch.full((140, 272), 7.0, device=DEV, dtype=dtype)
+            view = big[r0:r0 + 130, c0:c0 + 259]
+            binding.fct_gemm_bf16(a, b, view, accumulate=accumulate)
+            torch.cuda.synchronize()
+            ref = (ref64 + (7.0 if accumulate else 0.0)).to(dtype)
+            assert torch.equal(view, ref), (dtype, accumulate)
+            mask = torch.ones_like(big, dtype=torch.bool)
+            mask[r0:r0 + 130, c0:c0 + 259] = False
+            assert torch.all(big[mask] == 7.0), (dtype, accumulate)
 
 
 def test_gemm_fused_linear_shapes_sampled():
