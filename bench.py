@@ -242,7 +242,7 @@ def run_reference(args, world, rank):
 def run_linear(args, world, rank, local):
     """Fused-linear CE + TVD: hidden states and lm_head weights in, the loss and
     the student's hidden and weight gradients out, logits only in row blocks.
-    Dominated by four GEMMs per block (tensor cores, cuBLAS)."""
+    Dominated by four GEMMs per block (the library's tcgen05 GEMM)."""
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     binding.load()
@@ -298,7 +298,8 @@ def run_linear(args, world, rank, local):
             "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak,
                          "unit": "TFLOP/s", "frac": tflops / peak, "traffic": None,
                          "peak_source": "measured cuBLAS bf16, sustained"},
-            "gpu_launches": None,
+            # per row block: two logit GEMMs, the loss kernel, d hidden, d weight
+            "gpu_launches": K * ((BT + rows - 1) // rows) * 5,
             "clocks": clocks.summary() if clocks else None,
         }))
 

@@ -31,6 +31,7 @@ EXPORTS = ("fused_ce_tvd_forward", "fused_ce_tvd_forward_ex", "fused_ce_tvd_back
            "ce_forward_backward_ex", "fused_ce_tvd_mean_upstream", "fused_ce_tvd_mean_loss",
            "fused_linear_ce_tvd_workspace_size", "fused_linear_ce_tvd_forward_backward",
            "fused_linear_ce_tvd_forward_backward_noalloc", "fct_gemm_bf16",
+           "fct_gemm_bf16_workspace_size",
            "fused_ce_tvd_vp_lse", "fused_ce_tvd_vp_merge_lse", "fused_ce_tvd_vp_tvd",
            "fused_ce_tvd_vp_merge_tvd", "fused_ce_tvd_vp_backward",
            "fct_status_string", "fct_version")
@@ -125,8 +126,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
             vp, vp, vp, vp, vp, vp, i64, vp, i64, vp, vp]
         lib.fused_linear_ce_tvd_forward_backward_noalloc.restype = i32
         lib.fct_gemm_bf16.argtypes = [vp, i64, i32, vp, i64, i32, vp, i64, i32, i64, i64, i64,
-                                      vp, vp]
+                                      vp, ctypes.c_size_t, vp, vp]
         lib.fct_gemm_bf16.restype = i32
+        lib.fct_gemm_bf16_workspace_size.argtypes = [i64, i64]
+        lib.fct_gemm_bf16_workspace_size.restype = ctypes.c_size_t
         lib.fused_ce_tvd_mean_upstream.argtypes = [vp, i64, i64, dbl, dbl, vp, vp, vp, vp]
         lib.fused_ce_tvd_mean_loss.argtypes = [vp, vp, vp, i64, i64, dbl, dbl, vp, vp]
         for f in ("fused_ce_tvd_forward", "fused_ce_tvd_backward", "fused_ce_tvd_forward_backward",
@@ -795,13 +798,19 @@ def _operand(x: torch.Tensor, name: str):
     raise ValueError(f"{name} needs one unit stride")
 
 
-def fct_gemm_bf16(a, b, c=None, *, accumulate=False, out_dtype=torch.float32, dev_status=None,
-                  stream=None):
+def fct_gemm_bf16_workspace_size(M: int, N: int) -> int:
+    return int(load().fct_gemm_bf16_workspace_size(int(M), int(N)))
+
+
+def fct_gemm_bf16(a, b, c=None, *, accumulate=False, out_dtype=torch.float32, workspace=None,
+                  dev_status=None, stream=None):
     """C = a @ b.T (or C += a @ b.T into an fp32 c) on the library's tcgen05 GEMM.
 
     a (M, K) and b (N, K) are bf16 CUDA tensors with one unit stride each
     (b.T of a row-major (K, N) tensor is the MN-major case); c is (M, N),
-    row-major, fp32 or bf16 (bf16 only without accumulate)."""
+    row-major, fp32 or bf16 (bf16 only without accumulate).  ``workspace``
+    (a CUDA tensor, optional) lets a product with few output tiles and a long
+    K split K; see fct_gemm_bf16_workspace_size."""
     lda, a_mn = _operand(a, "a")
     ldb, b_mn = _operand(b, "b")
     M, K = a.shape
@@ -820,9 +829,10 @@ def fct_gemm_bf16(a, b, c=None, *, accumulate=False, out_dtype=torch.float32, de
         kind = GEMM_ADD_F32 if accumulate else GEMM_F32
     else:
         raise ValueError("c must be float32, or bfloat16 without accumulate")
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     rc = load().fct_gemm_bf16(_ptr(a), lda, a_mn, _ptr(b), ldb, b_mn, _ptr(c),
                               int(c.stride(0)) if M > 1 else N, kind, M, N, K,
-                              _ptr(dev_status), _stream(stream))
+                              _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
     _check(rc, "fct_gemm_bf16")
     return c
 

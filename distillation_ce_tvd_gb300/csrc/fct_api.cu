@@ -480,7 +480,7 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
 
 int gemm_impl(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t ldb, int32_t b_mn,
               void* C, int64_t ldc, int32_t c_kind, int64_t M, int64_t N, int64_t K,
-              int32_t* dev_status, void* stream) {
+              void* workspace, size_t workspace_bytes, int32_t* dev_status, void* stream) {
   if (c_kind != FCT_GEMM_F32 && c_kind != FCT_GEMM_BF16 && c_kind != FCT_GEMM_ADD_F32)
     return FCT_ERR_UNSUPPORTED;
   if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return FCT_ERR_INVALID_ARG;
@@ -505,12 +505,21 @@ int gemm_impl(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t l
   if (overlap(c, mat_range(A, a_lines, lda, a_cols, 2)) ||
       overlap(c, mat_range(B, b_lines, ldb, b_cols, 2)))
     return FCT_ERR_INVALID_ARG;
+  if (workspace_bytes > 0) {
+    if (workspace == nullptr) return FCT_ERR_INVALID_ARG;
+    if (!aligned(workspace, 16)) return FCT_ERR_ALIGNMENT;
+    const Range w = vec_range(workspace, static_cast<int64_t>(workspace_bytes), 1);
+    if (overlap(w, c) || overlap(w, mat_range(A, a_lines, lda, a_cols, 2)) ||
+        overlap(w, mat_range(B, b_lines, ldb, b_cols, 2)))
+      return FCT_ERR_INVALID_ARG;
+  }
   DeviceInfo d;
   const int rc = current_device(&d);
   if (rc != FCT_OK) return rc;
   if (fct::launch_gemm(fct::GemmOperand{A, lda, a_mn != 0}, fct::GemmOperand{B, ldb, b_mn != 0}, C,
                        ldc, c_kind, M, N, K, dev_status, d.sms,
-                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
+                       static_cast<cudaStream_t>(stream), workspace_bytes ? workspace : nullptr,
+                       workspace_bytes) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
 }
@@ -888,9 +897,15 @@ const char* fct_status_string(int status) {
 
 int fct_gemm_bf16(const void* A, int64_t lda, int32_t a_mn_major, const void* B, int64_t ldb,
                   int32_t b_mn_major, void* C, int64_t ldc, int32_t c_kind, int64_t M, int64_t N,
-                  int64_t K, int32_t* dev_status, void* stream) {
-  return gemm_impl(A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_kind, M, N, K, dev_status,
-                   stream);
+                  int64_t K, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                  void* stream) {
+  return gemm_impl(A, lda, a_mn_major, B, ldb, b_mn_major, C, ldc, c_kind, M, N, K, workspace,
+                   workspace_bytes, dev_status, stream);
+}
+
+size_t fct_gemm_bf16_workspace_size(int64_t M, int64_t N) {
+  if (M <= 0 || N <= 0 || M >= (int64_t(1) << 31) || N >= (int64_t(1) << 31)) return 0;
+  return fct::gemm_split_workspace_bytes(M, N);
 }
 
 int fct_version(void) { return 400; }  // 0.4.0: per-call fct_options, no process-wide knob

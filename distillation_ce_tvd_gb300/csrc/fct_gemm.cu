@@ -34,6 +34,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <cmath>
 #include <cstring>
 #include <mutex>
 
@@ -192,6 +193,12 @@ struct GemmArgs {
   int vec;    // C's rows start on 16-byte boundaries: vector stores
   int tma_c;  // C written through its tensor map (TMA store / reduce-add)
   int n_fast; // tile walk: N index fastest (A is the larger operand) or M fastest
+  // split K: unit u covers tile u % tiles and the K blocks of part
+  // u / tiles; part s writes its fp32 partial tile to rows
+  // s * slab_rows + m of C (slab_rows >= the M tiles' extent)
+  int splits;
+  int k_per;  // K blocks per part
+  int64_t slab_rows;
   int32_t* status;
 };
 
@@ -321,6 +328,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const uint32_t smem0 = (smem_addr(gemm_smem) + 1023u) & ~1023u;
   const int64_t m_tiles = (g.M + kBM - 1) / kBM, n_tiles = (g.N + kBN - 1) / kBN;
   const int64_t tiles = m_tiles * n_tiles;
+  const int64_t units = tiles * g.splits;
   const int k_iters = static_cast<int>((g.K + kBK - 1) / kBK);
 
   if (threadIdx.x == 0) {
@@ -356,12 +364,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       bool ok = true;
-      for (int64_t t = pair; ok && t < tiles; t += n_pairs) {
+      for (int64_t u = pair; ok && u < units; u += n_pairs) {
         int64_t tm, tn;
-        tile_mn(g, t, m_tiles, n_tiles, tm, tn);
+        tile_mn(g, u % tiles, m_tiles, n_tiles, tm, tn);
         const int m0 = static_cast<int>(tm * kBM) + int(rank) * kCtaRows;
         const int n0 = static_cast<int>(tn * kBN) + int(rank) * kCtaRows;
-        for (int kb = 0; kb < k_iters; ++kb) {
+        const int kb0 = static_cast<int>(u / tiles) * g.k_per;
+        const int kb1 = min(k_iters, kb0 + g.k_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, &abort_flag)) {
             ok = false;
             break;
@@ -391,13 +401,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       int64_t local = 0;
-      for (int64_t t = pair; ok && t < tiles; t += n_pairs, ++local) {
+      for (int64_t u = pair; ok && u < units; u += n_pairs, ++local) {
         const int acc = static_cast<int>(local & 1);
         const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
         if (!mbar_wait(&acc_empty[acc], acc_phase ^ 1u, &abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem + uint32_t(acc * kBN);
-        for (int kb = 0; kb < k_iters; ++kb) {
+        const int kb0 = static_cast<int>(u / tiles) * g.k_per;
+        const int kb1 = min(k_iters, kb0 + g.k_per);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, &abort_flag)) {
             ok = false;
             break;
@@ -408,7 +420,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16<kId>(d, adesc + kk * desc_k_step<kAmn>(), bdesc + kk * desc_k_step<kBmn>(),
-                           (kb | kk) != 0);
+                           (kb > kb0 || kk > 0) ? 1u : 0u);
           umma_commit_pair(&empty_bar[stage]);  // both CTAs' stages are free once these are done
           if (++stage == kGStages) {
             stage = 0;
@@ -423,7 +435,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int q = warp & 3;
     int64_t local = 0;
     bool last_sent = false;  // lane 0: whether the previous block committed a bulk group
-    for (int64_t t = pair; t < tiles; t += n_pairs, ++local) {
+    for (int64_t u = pair; u < units; u += n_pairs, ++local) {
       const int acc = static_cast<int>(local & 1);
       const uint32_t acc_phase = static_cast<uint32_t>((local >> 1) & 1);
       // the warp agrees on the outcome, so the .sync.aligned loads below run
@@ -431,15 +443,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&acc_full[acc], acc_phase, &abort_flag))) break;
       tc_fence_after();
       int64_t tm, tn;
-      tile_mn(g, t, m_tiles, n_tiles, tm, tn);
+      tile_mn(g, u % tiles, m_tiles, n_tiles, tm, tn);
       const int64_t m0 = tm * kBM + int64_t(rank) * kCtaRows;
       const int64_t n0 = tn * kBN;
+      const int64_t slab = (u / tiles) * g.slab_rows;  // 0 without split K
       const uint32_t tq = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN);
       if (g.tma_c) {
         // 32-row blocks of 128 bytes per row through two staging buffers
         const uint32_t buf0 = smem0 + kGStages * kGStageBytes + uint32_t(q) * 2 * kOutBufBytes;
         constexpr int kCols = (kOut == kOutBf16) ? 64 : 32;
-        const int y = static_cast<int>(m0 + q * 32);
+        const int y = static_cast<int>(slab + m0 + q * 32);
+        const int64_t rows_end = slab + (g.splits > 1 ? g.slab_rows : g.M);
 #pragma unroll 1
         for (int c = 0; c < kBN / kCols; ++c) {
           uint32_t w[32];
@@ -475,7 +489,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
-            last_sent = n0 + c * kCols < g.N && y < g.M;
+            last_sent = n0 + c * kCols < g.N && y < rows_end;
             if (last_sent)
               tma_store_2d<kOut == kOutAddF32>(&tmC, static_cast<int>(n0) + c * kCols, y, buf);
           }
@@ -487,7 +501,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           uint32_t r[32];
           tmem_ld32(tq + uint32_t(c * 32), r);
           const int64_t col0 = n0 + c * 32;
-          if (row < g.M && col0 < g.N) store_row32<kOut>(g, row, col0, r);
+          if (row < g.M && col0 < g.N) store_row32<kOut>(g, slab + row, col0, r);
         }
         tc_fence_before();
         __syncwarp();
@@ -568,56 +582,133 @@ bool operand_map(CUtensorMap* map, const GemmOperand& x, int64_t rows, int64_t K
                     : make_map(map, x.ptr, K, rows, x.ld, tile_rows);
 }
 
-template <bool kAmn, bool kBmn, int kOut>
-cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
-                     const GemmArgs& g, int sms, cudaStream_t st) {
-  auto kernel = gemm_kernel<kAmn, kBmn, kOut>;
-  static std::once_flag once[64];
-  static cudaError_t set_err[64];
-  static int pairs[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+// Fills a launch configuration for a kernel of this file: clusters of two,
+// kGemmThreads threads, kGemmSmem bytes of shared memory.
+struct PairLaunch {
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kGemmThreads);
-  cfg.dynamicSmemBytes = kGemmSmem;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  PairLaunch() {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
+// Sets the shared-memory limit of one instantiation on the current device
+// (once) and returns how many of its pairs can be resident at once (0 on
+// failure).
+template <bool kAmn, bool kBmn, int kOut>
+int prepare(int dev) {
+  static std::once_flag once[64];
+  static int pairs[64];
   std::call_once(once[dev], [&] {
-    set_err[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kGemmSmem));
-    if (set_err[dev] != cudaSuccess) return;
-    // as many pairs as can be resident at once: the grid is persistent
-    cudaLaunchConfig_t q = cfg;
-    q.gridDim = dim3(2 * 64);
+    auto kernel = gemm_kernel<kAmn, kBmn, kOut>;
+    pairs[dev] = 0;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGemmSmem)) != cudaSuccess) {
+      cudaGetLastError();
+      return;
+    }
+    PairLaunch l;
+    l.cfg.gridDim = dim3(2 * 64);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kernel, &q) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &l.cfg) != cudaSuccess) {
       cudaGetLastError();
       n = 0;
     }
     pairs[dev] = n;
   });
-  if (set_err[dev] != cudaSuccess) return set_err[dev];
-  if (pairs[dev] <= 0) return cudaErrorInvalidConfiguration;
-  const int64_t tiles = ((g.M + kBM - 1) / kBM) * ((g.N + kBN - 1) / kBN);
-  int64_t n = tiles < pairs[dev] ? tiles : pairs[dev];
-  if (n > sms / 2) n = sms / 2 > 0 ? sms / 2 : 1;
-  cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
-  cfg.stream = st;
-  return cudaLaunchKernelEx(&cfg, kernel, ma, mb, mc, g);
+  return pairs[dev];
+}
+
+template <bool kAmn, bool kBmn, int kOut>
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& mc,
+                     const GemmArgs& g, int max_pairs, cudaStream_t st) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int pairs = prepare<kAmn, kBmn, kOut>(dev);
+  if (pairs <= 0) return cudaErrorInvalidConfiguration;
+  const int64_t units = ((g.M + kBM - 1) / kBM) * ((g.N + kBN - 1) / kBN) * g.splits;
+  int64_t n = units < pairs ? units : pairs;
+  if (n > max_pairs) n = max_pairs;
+  PairLaunch l;
+  l.cfg.gridDim = dim3(static_cast<unsigned>(2 * n));
+  l.cfg.stream = st;
+  return cudaLaunchKernelEx(&l.cfg, gemm_kernel<kAmn, kBmn, kOut>, ma, mb, mc, g);
 }
 
 template <int kOut>
 cudaError_t dispatch_major(bool a_mn, bool b_mn, const CUtensorMap& ma, const CUtensorMap& mb,
-                           const CUtensorMap& mc, const GemmArgs& g, int sms, cudaStream_t st) {
-  if (a_mn) return b_mn ? run_gemm<true, true, kOut>(ma, mb, mc, g, sms, st)
-                        : run_gemm<true, false, kOut>(ma, mb, mc, g, sms, st);
-  return b_mn ? run_gemm<false, true, kOut>(ma, mb, mc, g, sms, st)
-              : run_gemm<false, false, kOut>(ma, mb, mc, g, sms, st);
+                           const CUtensorMap& mc, const GemmArgs& g, int max_pairs,
+                           cudaStream_t st) {
+  if (a_mn) return b_mn ? run_gemm<true, true, kOut>(ma, mb, mc, g, max_pairs, st)
+                        : run_gemm<true, false, kOut>(ma, mb, mc, g, max_pairs, st);
+  return b_mn ? run_gemm<false, true, kOut>(ma, mb, mc, g, max_pairs, st)
+              : run_gemm<false, false, kOut>(ma, mb, mc, g, max_pairs, st);
+}
+
+// C (M x N, fp32 or bf16) = the sum of `splits` fp32 partial slabs, added in
+// slab order (so the result does not depend on which pair computed which
+// part).  Slab s holds row m at slabs[(s * slab_rows + m) * slab_ld].
+template <bool kBf16>
+__global__ void __launch_bounds__(256)
+    split_sum_kernel(const float* __restrict__ slabs, int64_t slab_ld, int64_t slab_rows,
+                     int splits, void* C, int64_t ldc, int64_t M, int64_t N) {
+  const int64_t per_row = (N + 3) / 4;  // groups of four columns
+  const int64_t total = M * per_row;
+  const int64_t stride_s = slab_rows * slab_ld;
+  for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+       i += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t m = i / per_row, n = (i - m * per_row) * 4;
+    const float* p = slabs + m * slab_ld + n;  // slab rows are 16-byte aligned
+    float4 acc = *reinterpret_cast<const float4*>(p);
+    for (int sp = 1; sp < splits; ++sp) {
+      const float4 v = *reinterpret_cast<const float4*>(p + sp * stride_s);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    const float r[4] = {acc.x, acc.y, acc.z, acc.w};
+    const int cnt = N - n < 4 ? static_cast<int>(N - n) : 4;
+    if constexpr (kBf16) {
+      uint16_t* c = static_cast<uint16_t*>(C) + m * ldc + n;
+      for (int j = 0; j < cnt; ++j)
+        c[j] = static_cast<uint16_t>(pack_bf16x2(r[j], 0.f) & 0xffffu);
+    } else {
+      float* c = static_cast<float*>(C) + m * ldc + n;
+      for (int j = 0; j < cnt; ++j) c[j] = r[j];
+    }
+  }
+}
+
+// Parts of K for a GEMM of `tiles` pair tiles: split when the tiles alone
+// leave pairs idle in the last round (under 90% of the rounds busy), each
+// part keeping at least 16 K blocks, the slabs fitting the workspace, and
+// only for a gain of at least 4 points of busy rounds.
+int plan_splits(int64_t tiles, int k_iters, int pairs, size_t ws_bytes, size_t slab_bytes) {
+  if (pairs <= 0 || slab_bytes == 0) return 1;
+  auto busy = [&](int S) {
+    const double w = double(tiles) * S / pairs;
+    return w / std::ceil(w);
+  };
+  int best = 1;
+  double best_busy = busy(1);
+  if (best_busy >= 0.9) return 1;
+  for (int S = 2; S <= 8; ++S) {
+    if (k_iters < 16 * S || size_t(S) * slab_bytes > ws_bytes) break;
+    const double b = busy(S);
+    if (b > best_busy + 0.04) {
+      best = S;
+      best_busy = b;
+    }
+  }
+  return best;
 }
 
 }  // namespace
@@ -628,13 +719,54 @@ bool gemm_operand_ok(const void* p, int64_t ld) {
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
                         int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
-                        cudaStream_t st) {
+                        cudaStream_t st, void* split_ws, size_t split_ws_bytes) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (!gemm_operand_ok(A.ptr, A.ld) || !gemm_operand_ok(B.ptr, B.ld) || sms <= 0)
     return cudaErrorInvalidValue;
+  if (c_kind != kOutF32 && c_kind != kOutBf16 && c_kind != kOutAddF32) return cudaErrorInvalidValue;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   CUtensorMap ma, mb;
   if (!operand_map(&ma, A, M, K, kCtaRows) || !operand_map(&mb, B, N, K, kCtaRows))
     return cudaErrorInvalidValue;
+  const int max_pairs = sms / 2 > 0 ? sms / 2 : 1;
+  const int64_t m_tiles = (M + kBM - 1) / kBM, n_tiles = (N + kBN - 1) / kBN;
+  const int k_iters = static_cast<int>((K + kBK - 1) / kBK);
+
+  // split K into parts whose fp32 partial tiles go to slabs in split_ws
+  int splits = 1;
+  const int64_t slab_rows = m_tiles * kBM, slab_ld = (N + 3) / 4 * 4;
+  if (c_kind != kOutAddF32 && split_ws != nullptr &&
+      reinterpret_cast<uintptr_t>(split_ws) % 16 == 0) {
+    int pairs = prepare<false, false, kOutF32>(dev);
+    if (pairs > max_pairs) pairs = max_pairs;
+    splits = plan_splits(m_tiles * n_tiles, k_iters, pairs, split_ws_bytes,
+                         size_t(slab_rows) * size_t(slab_ld) * sizeof(float));
+  }
+  if (splits > 1) {
+    const int k_per = (k_iters + splits - 1) / splits;
+    splits = (k_iters + k_per - 1) / k_per;  // every part gets at least one K block
+    CUtensorMap ms;
+    // padded slab rows and row ends: a box clipped at N or at the M tiles'
+    // extent stays inside its own slab
+    if (!make_c_map(&ms, split_ws, splits * slab_rows, N, slab_ld, false))
+      return cudaErrorInvalidValue;
+    const GemmArgs g{M, N, K, split_ws, slab_ld, 1, 1, M > N ? 1 : 0, splits, k_per, slab_rows,
+                     status};
+    cudaError_t e = dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, ms, g, max_pairs, st);
+    if (e != cudaSuccess) return e;
+    const int64_t groups = M * ((N + 3) / 4);
+    int64_t blocks = (groups + 255) / 256;
+    if (blocks > int64_t(sms) * 8) blocks = int64_t(sms) * 8;
+    if (c_kind == kOutBf16)
+      split_sum_kernel<true><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+          static_cast<const float*>(split_ws), slab_ld, slab_rows, splits, C, ldc, M, N);
+    else
+      split_sum_kernel<false><<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+          static_cast<const float*>(split_ws), slab_ld, slab_rows, splits, C, ldc, M, N);
+    return cudaGetLastError();
+  }
+
   const size_t es = c_kind == kOutBf16 ? 2 : 4;
   const bool aligned16 =
       reinterpret_cast<uintptr_t>(C) % 16 == 0 && (size_t(ldc) * es) % 16 == 0;
@@ -644,14 +776,20 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
   memset(&mc, 0, sizeof(mc));
   const bool tma_c = aligned16 && (size_t(N) * es) % 16 == 0 &&
                      make_c_map(&mc, C, M, N, ldc, c_kind == kOutBf16);
-  const GemmArgs g{M, N, K, C, ldc, aligned16 ? 1 : 0, tma_c ? 1 : 0, M > N ? 1 : 0, status};
+  const GemmArgs g{M, N, K, C, ldc, aligned16 ? 1 : 0, tma_c ? 1 : 0, M > N ? 1 : 0, 1, k_iters,
+                   0, status};
   switch (c_kind) {
-    case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
-    case kOutBf16: return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
-    case kOutAddF32:
-      return dispatch_major<kOutAddF32>(A.mn_major, B.mn_major, ma, mb, mc, g, sms, st);
-    default: return cudaErrorInvalidValue;
+    case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, mc, g, max_pairs, st);
+    case kOutBf16:
+      return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, mc, g, max_pairs, st);
+    default:
+      return dispatch_major<kOutAddF32>(A.mn_major, B.mn_major, ma, mb, mc, g, max_pairs, st);
   }
+}
+
+size_t gemm_split_workspace_bytes(int64_t M, int64_t N) {
+  const int64_t m_tiles = (M + kBM - 1) / kBM;
+  return size_t(8) * size_t(m_tiles * kBM) * size_t((N + 3) / 4 * 4) * sizeof(float);
 }
 
 }  // namespace fct

@@ -168,10 +168,16 @@ struct GemmOperand {
   int64_t ld;
   bool mn_major;
 };
+// split_ws (optional, 16-byte aligned): room for fp32 partial sums; a GEMM
+// with too few output tiles to keep every SM pair busy and a long K may then
+// split K (c_kind 0 and 1 only) and add the parts in a fixed order.
+// gemm_split_workspace_bytes(M, N) is the most any split of an M x N result
+// uses.
 bool gemm_operand_ok(const void* p, int64_t ld);
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
                         int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
-                        cudaStream_t st);
+                        cudaStream_t st, void* split_ws = nullptr, size_t split_ws_bytes = 0);
+size_t gemm_split_workspace_bytes(int64_t M, int64_t N);
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);
 cudaError_t launch_mean(const LossArgs& a, cudaStream_t st);

@@ -68,11 +68,14 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
     if ((e = launch_forward(f, plan, st)) != cudaSuccess) return e;
     if (a.grad_h_s == nullptr && a.grad_w_s == nullptr) continue;
     // d hidden (R x D, bf16) = G (R x V) W (V x D): C(r, d) = sum_v G(r, v) W(v, d),
-    // G K-major, W read as the MN-major (D x V) operand
+    // G K-major, W read as the MN-major (D x V) operand.  Few output tiles
+    // and a K of V: the GEMM may split K, with its partial sums in the
+    // teacher block, which the loss kernel has finished reading.
     if (a.grad_h_s &&
         (e = launch_gemm(GemmOperand{G, ldg, false}, GemmOperand{a.w_s, a.ld_ws, true},
                          static_cast<uint16_t*>(a.grad_h_s) + r0 * a.ld_ghs, a.ld_ghs,
-                         FCT_GEMM_BF16, R, a.d_s, a.V, a.dev_status, sms, st)) != cudaSuccess)
+                         FCT_GEMM_BF16, R, a.d_s, a.V, a.dev_status, sms, st, Lt,
+                         size_t(block_bytes))) != cudaSuccess)
       return e;
     // d weight (V x D, fp32) += G^T H: C(v, d) += sum_r G(r, v) H(r, d), both
     // operands MN-major

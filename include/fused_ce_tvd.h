@@ -433,11 +433,21 @@ int fused_linear_ce_tvd_forward_backward_noalloc(
  *            must not overlap A or B (FCT_ERR_INVALID_ARG).
  *   M, N >= 0 (0: nothing to do, FCT_OK), K >= 1; M, N, K < 2^31, else
  *            FCT_ERR_UNSUPPORTED.
+ *   workspace, workspace_bytes: optional (NULL, 0) device memory, 16-byte
+ *            aligned, not overlapping A, B or C.  With it, a product whose
+ *            output tiles (256 x 256) are too few to keep every SM pair
+ *            busy and whose K is long may split K into parts: each part's
+ *            fp32 partial sums go to the workspace and a second kernel adds
+ *            them in part order (c_kind FCT_GEMM_F32 and FCT_GEMM_BF16
+ *            only).  fct_gemm_bf16_workspace_size(M, N) bytes let every
+ *            split happen; fewer allow fewer parts.
  * The tensor cores accumulate in fp32, K in blocks of 16 in increasing
- * order; every element goes through the same sequence of instructions, so a
- * result depends only on its row of A and its row of B (not on M, N or the
- * tile it falls in), and repeated calls give identical bits.  Sums of
- * products that are exact in fp32 are exact.
+ * order.  Without a split every element goes through the same sequence of
+ * instructions, so a result depends only on its row of A and its row of B
+ * (not on M, N or the tile it falls in); with one, also on the number of
+ * parts, which is fixed by M, N, K, the workspace size and the device.
+ * Repeated calls give identical bits either way.  Sums of products that are
+ * exact in fp32 are exact.
  * dev_status (optional): FCT_DEV_WAIT_TIMEOUT is ORed in if
  * a pipeline wait in the kernel ran out (C is then invalid).
  */
@@ -448,7 +458,11 @@ int fused_linear_ce_tvd_forward_backward_noalloc(
 int fct_gemm_bf16(const void* A, int64_t lda, int32_t a_mn_major,
                   const void* B, int64_t ldb, int32_t b_mn_major, void* C,
                   int64_t ldc, int32_t c_kind, int64_t M, int64_t N, int64_t K,
-                  int32_t* dev_status, void* stream);
+                  void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                  void* stream);
+/* Bytes of workspace for every K split of an M x N product; 0 for M or N
+ * outside [1, 2^31). */
+size_t fct_gemm_bf16_workspace_size(int64_t M, int64_t N);
 
 /*
  * Cross-entropy alone: the CE half of "Forward Pass" (one log-sum-exp pass,

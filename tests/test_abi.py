@@ -322,7 +322,7 @@ def test_gemm_argument_checks(lib):
     f = lib.fct_gemm_bf16
     A, B, C = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
     # A: M x K = 100 x 64 K-major (ld 64); B: N x K = 300 x 64 K-major; C: 100 x 300 fp32
-    args = [A, 64, 0, B, 64, 0, C, 300, 0, 100, 300, 64, None, None]
+    args = [A, 64, 0, B, 64, 0, C, 300, 0, 100, 300, 64, None, 0, None, None]
 
     def call(**kw):
         a = list(args)
@@ -343,6 +343,12 @@ def test_gemm_argument_checks(lib):
     assert call(a7=299) == INVALID                    # ldc < N
     assert call(a6=A + 64) == INVALID                 # C overlaps A
     assert call(a11=1 << 31) == UNSUPPORTED           # 32-bit tile coordinates
+    assert call(a13=1024) == INVALID                  # workspace bytes without a workspace
+    assert call(a12=FAKE + (3 << 30) + 8, a13=1024) == ALIGN
+    assert call(a12=C + 64, a13=1024) == INVALID      # workspace overlaps C
+    # every split of a 300 x 1003 product: 8 parts of 512 padded rows x 1004 fp32
+    assert lib.fct_gemm_bf16_workspace_size(300, 1003) == 8 * 512 * 1004 * 4
+    assert lib.fct_gemm_bf16_workspace_size(0, 5) == 0
 
 
 def test_fused_linear_needs_tma_aligned_operands(lib):

@@ -160,3 +160,54 @@ def test_gemm_fused_linear_shapes_sampled():
     assert torch.equal(dh[rows_d][:, dcols_d].cpu().double(), ref_dh)
     ref_dw = G[:, vrows_d].cpu().double().T @ h[:, dcols_d].cpu().double()
     assert torch.equal(dw[vrows_d][:, dcols_d].cpu().double(), ref_dw)
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 1003, 4000), (64, 256, 8192), (513, 520, 3000)])
+def test_gemm_split_k_exact_and_deterministic(M, N, K):
+    # Few output tiles and a long K: with a workspace the GEMM splits K and
+    # adds the parts' fp32 slabs in order.  Exact operands: every split gives
+    # the exact product; random operands: repeated calls give the same bits.
+    g = torch.Generator(device=DEV).manual_seed(M + N + K)
+    a = dyadic((M, K), 3, 4.0, g)
+    b = dyadic((N, K), 7, 16.0, g)
+    ws = torch.empty(binding.fct_gemm_bf16_workspace_size(M, N), dtype=torch.uint8, device=DEV)
+    ref = a.double().cpu() @ b.double().cpu().T
+    big = torch.full((M + 16, N + 24), 7.0, device=DEV)
+    view = big[8:8 + M, 8:8 + N]
+    binding.fct_gemm_bf16(a, operand(b, True), view, workspace=ws)
+    cb = binding.fct_gemm_bf16(a, b, out_dtype=torch.bfloat16, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(view.cpu().double(), ref)
+    assert torch.equal(cb.cpu(), ref.float().bfloat16())
+    mask = torch.ones_like(big, dtype=torch.bool)
+    mask[8:8 + M, 8:8 + N] = False
+    assert torch.all(big[mask] == 7.0)
+
+    x = torch.randn(M, K, generator=g, device=DEV).bfloat16()
+    y = torch.randn(N, K, generator=g, device=DEV).bfloat16()
+    c1 = binding.fct_gemm_bf16(x, y, workspace=ws)
+    c2 = binding.fct_gemm_bf16(x, y, workspace=ws)
+    c0 = binding.fct_gemm_bf16(x, y)
+    torch.cuda.synchronize()
+    assert torch.equal(c1, c2)
+    X, Y = x.double().cpu().numpy(), y.double().cpu().numpy()
+    bound = K * 2.0 ** -23 * (np.abs(X) @ np.abs(Y).T) + 1e-30
+    for c in (c0, c1):
+        assert np.all(np.abs(c.cpu().double().numpy() - X @ Y.T) <= bound)
+
+
+def test_gemm_split_k_fused_linear_d_hidden_shape():
+    # d hidden of a 2048-row block: 8 x 16 output tiles over K = 151936
+    g = torch.Generator(device=DEV).manual_seed(31)
+    R, D, V = 2048, 4096, 151936
+    w = dyadic((V, D), 7, 64.0, g)
+    G = dyadic((R, V), 3, 256.0, g)
+    ws = torch.empty(binding.fct_gemm_bf16_workspace_size(R, D), dtype=torch.uint8, device=DEV)
+    dh = binding.fct_gemm_bf16(G, w.t(), out_dtype=torch.bfloat16, workspace=ws)
+    dh32 = binding.fct_gemm_bf16(G, w.t(), workspace=ws)
+    torch.cuda.synchronize()
+    rows = torch.tensor([0, 255, 256, 1999, 2047], device=DEV)
+    cols = torch.tensor([0, 127, 128, 4000, 4095], device=DEV)
+    ref = G[rows].cpu().double() @ w[:, cols].cpu().double()
+    assert torch.equal(dh32[rows][:, cols].cpu().double(), ref)
+    assert torch.equal(dh[rows][:, cols].cpu(), ref.float().bfloat16())
