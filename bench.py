@@ -304,6 +304,57 @@ def run_linear(args, world, rank, local):
         }))
 
 
+# ---------------------------------------------------------------- GEMM alone
+
+GEMM_PRODUCTS = {
+    # the fused-linear path's products for one row block of R rows
+    "logits": "C (R x V, bf16) = H (R x D) W^T",
+    "d_hidden": "C (R x D, bf16) = G (R x V) W (V x D), W read MN-major, split K",
+    "d_weight": "C (V x D, fp32) += G^T (V x R) H (R x D), both MN-major",
+}
+
+
+def run_gemm(args):
+    """Times one of the fused-linear path's GEMMs on the library's tcgen05
+    kernel (profiling and tuning; not the headline)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    binding.load()
+    R, D, V = (int(x) for x in args.gemm_shape.split(","))
+    g = torch.Generator(device=dev).manual_seed(3)
+    h = torch.randn(R, D, generator=g, device=dev).bfloat16()
+    w = (torch.randn(V, D, generator=g, device=dev) * 0.03).bfloat16()
+    G = (torch.randn(R, V, generator=g, device=dev) * 1e-4).bfloat16()
+    if args.gemm == "logits":
+        c = torch.empty(R, V, device=dev, dtype=torch.bfloat16)
+        ws = None
+        fn = lambda: binding.fct_gemm_bf16(h, w, c)  # noqa: E731
+    elif args.gemm == "d_hidden":
+        c = torch.empty(R, D, device=dev, dtype=torch.bfloat16)
+        ws = torch.empty(binding.fct_gemm_bf16_workspace_size(R, D), device=dev,
+                         dtype=torch.uint8)
+        fn = lambda: binding.fct_gemm_bf16(G, w.t(), c, workspace=ws)  # noqa: E731
+    else:
+        c = torch.zeros(V, D, device=dev)
+        fn = lambda: binding.fct_gemm_bf16(G.t(), h.t(), c, accumulate=True)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    tflops = 2.0 * R * D * V / (ms * 1e-3) / 1e12
+    peaks_path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    peak = json.load(open(peaks_path))["bf16_tflops"] if os.path.exists(peaks_path) else 1900.0
+    print(json.dumps({"gemm": args.gemm, "product": GEMM_PRODUCTS[args.gemm], "R": R, "D": D,
+                      "V": V, "ms": ms, "tflops": tflops, "peak_burst": peak,
+                      "frac": tflops / peak}))
+
+
 # ---------------------------------------------------------------- our arm
 
 def main():
@@ -333,8 +384,14 @@ def main():
     ap.add_argument("--ring", type=int, default=0, choices=[0, 1, 2],
                     help="shared-memory staging of the multi-pass kernels: 0 automatic, "
                          "1 per-thread cp.async ring, 2 producer-warp TMA bulk-copy ring")
+    ap.add_argument("--gemm", default=None, choices=sorted(GEMM_PRODUCTS),
+                    help="time one fused-linear GEMM alone (R,D,V from --gemm-shape)")
+    ap.add_argument("--gemm-shape", default="2048,4096,151936")
     args = ap.parse_args()
 
+    if args.gemm:
+        run_gemm(args)
+        return
     if args.impl == "reference":
         # the oracle runs on rank 0's host cores only; other ranks exit at once
         run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
