@@ -1,8 +1,7 @@
 // Fused-linear CE + TVD for callers that must not allocate device memory.
 //
 // The regular fused-linear entry point needs a caller-provided workspace for
-// its logit blocks and a cuBLAS handle, whose creation allocates device
-// memory.  Some callers can do neither at call time: a serving or training
+// its logit blocks.  Some callers can do neither at call time: a serving or training
 // process whose memory is fixed up front (a caching allocator or a KV cache
 // that owns all free HBM, so a cudaMalloc outside it fails or fragments it),
 // and code on a path that must not synchronise the device, which cudaMalloc
@@ -12,8 +11,9 @@
 //     this file's module (kScratchBytes below; the driver reserves it on each
 //     device when the module loads there and keeps it until the process
 //     exits);
-//   * its three GEMMs run on a tiled CUDA-core kernel of its own (fp32
-//     accumulation) instead of cuBLAS;
+//   * its GEMMs run on the library's tensor-core GEMM (which allocates
+//     nothing) when the hidden states and weights have 16-byte aligned rows,
+//     else on a tiled CUDA-core kernel of its own (fp32 accumulation);
 //   * the loss itself is the same single-launch forward + backward kernel
 //     as every other path, and the logit gradient is rounded to bf16 the same
 //     way before the gradient GEMMs.
@@ -170,8 +170,13 @@ __global__ void __launch_bounds__(kConvThreads) to_bf16(const float* src, uint16
 
 // ------------------------------------------------------------------ block loop
 
+// The block loop's GEMMs: the tensor-core GEMM of fct_gemm.cu (no
+// allocation either) when every bf16 operand has 16-byte aligned rows, the
+// tiled kernel above otherwise.
 cudaError_t run_blocks(const fct::LinArgs& a, const fct::FwdPlan& plan, int sms,
                        cudaStream_t st) {
+  const bool tc = fct::gemm_operand_ok(a.h_s, a.ld_hs) && fct::gemm_operand_ok(a.w_s, a.ld_ws) &&
+                  fct::gemm_operand_ok(a.h_t, a.ld_ht) && fct::gemm_operand_ok(a.w_t, a.ld_wt);
   const int64_t ldl = fct::linear_logits_ld(a.V);
   float* Ls = static_cast<float*>(a.workspace);
   float* Lt = Ls + a.chunk_rows * ldl;
@@ -184,14 +189,24 @@ cudaError_t run_blocks(const fct::LinArgs& a, const fct::FwdPlan& plan, int sms,
   for (int64_t r0 = 0; r0 < a.BT; r0 += a.chunk_rows) {
     const int64_t R = (a.BT - r0 < a.chunk_rows) ? a.BT - r0 : a.chunk_rows;
     // logits (R x V): A(r, d) = H[r0 + r, d], B(d, v) = W[v, d]
-    if ((e = gemm<false>(Gemm{Hs + r0 * a.ld_hs, a.ld_hs, 1, Ws, 1, a.ld_ws, Ls, ldl, 1, R, a.V,
-                              a.d_s, 0.f},
-                         st)) != cudaSuccess)
-      return e;
-    if ((e = gemm<false>(Gemm{Ht + r0 * a.ld_ht, a.ld_ht, 1, Wt, 1, a.ld_wt, Lt, ldl, 1, R, a.V,
-                              a.d_t, 0.f},
-                         st)) != cudaSuccess)
-      return e;
+    if (tc) {
+      if ((e = fct::launch_gemm(fct::GemmOperand{Hs + r0 * a.ld_hs, a.ld_hs, false},
+                                fct::GemmOperand{Ws, a.ld_ws, false}, Ls, ldl, FCT_GEMM_F32, R,
+                                a.V, a.d_s, a.dev_status, sms, st)) != cudaSuccess ||
+          (e = fct::launch_gemm(fct::GemmOperand{Ht + r0 * a.ld_ht, a.ld_ht, false},
+                                fct::GemmOperand{Wt, a.ld_wt, false}, Lt, ldl, FCT_GEMM_F32, R,
+                                a.V, a.d_t, a.dev_status, sms, st)) != cudaSuccess)
+        return e;
+    } else {
+      if ((e = gemm<false>(Gemm{Hs + r0 * a.ld_hs, a.ld_hs, 1, Ws, 1, a.ld_ws, Ls, ldl, 1, R,
+                                a.V, a.d_s, 0.f},
+                           st)) != cudaSuccess)
+        return e;
+      if ((e = gemm<false>(Gemm{Ht + r0 * a.ld_ht, a.ld_ht, 1, Wt, 1, a.ld_wt, Lt, ldl, 1, R,
+                                a.V, a.d_t, 0.f},
+                           st)) != cudaSuccess)
+        return e;
+    }
     // the loss on the block, its logit gradient written over Ls
     fct::FwdArgs f{Ls, Lt, ldl, ldl, FCT_F32, a.target + r0, R, a.V, a.ignore_index,
                    a.ce + r0, a.tvd + r0, a.lse_s + r0, a.lse_t + r0, a.sigma + r0,
@@ -205,17 +220,23 @@ cudaError_t run_blocks(const fct::LinArgs& a, const fct::FwdPlan& plan, int sms,
     to_bf16<<<static_cast<unsigned>(blocks), kConvThreads, 0, st>>>(Ls, G, ldl, R, a.V);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // d hidden (R x D, bf16): A(r, v) = G[r, v], B(v, d) = W[v, d]
+    uint16_t* gh = static_cast<uint16_t*>(a.grad_h_s) + r0 * a.ld_ghs;
     if (a.grad_h_s &&
-        (e = gemm<true>(Gemm{G, ldl, 1, Ws, a.ld_ws, 1,
-                             static_cast<uint16_t*>(a.grad_h_s) + r0 * a.ld_ghs, a.ld_ghs, 1, R,
-                             a.d_s, a.V, 0.f},
-                        st)) != cudaSuccess)
+        (e = tc ? fct::launch_gemm(fct::GemmOperand{G, ldl, false},
+                                   fct::GemmOperand{Ws, a.ld_ws, true}, gh, a.ld_ghs,
+                                   FCT_GEMM_BF16, R, a.d_s, a.V, a.dev_status, sms, st)
+                : gemm<true>(Gemm{G, ldl, 1, Ws, a.ld_ws, 1, gh, a.ld_ghs, 1, R, a.d_s, a.V, 0.f},
+                             st)) != cudaSuccess)
       return e;
     // d weight (V x D, fp32) += A(v, r) = G[r, v] times B(r, d) = H[r0 + r, d]
     if (a.grad_w_s &&
-        (e = gemm<false>(Gemm{G, 1, ldl, Hs + r0 * a.ld_hs, a.ld_hs, 1, a.grad_w_s, a.ld_gws, 1,
-                              a.V, a.d_s, R, 1.f},
-                         st)) != cudaSuccess)
+        (e = tc ? fct::launch_gemm(fct::GemmOperand{G, ldl, true},
+                                   fct::GemmOperand{Hs + r0 * a.ld_hs, a.ld_hs, true},
+                                   a.grad_w_s, a.ld_gws, FCT_GEMM_ADD_F32, a.V, a.d_s, R,
+                                   a.dev_status, sms, st)
+                : gemm<false>(Gemm{G, 1, ldl, Hs + r0 * a.ld_hs, a.ld_hs, 1, a.grad_w_s,
+                                   a.ld_gws, 1, a.V, a.d_s, R, 1.f},
+                              st)) != cudaSuccess)
       return e;
   }
   return cudaGetLastError();

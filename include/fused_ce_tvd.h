@@ -21,9 +21,9 @@
  *    in the host-buffer entry point, which says which of its pointers are
  *    host memory).  The library allocates no device memory and keeps no
  *    state between calls that changes results or launches (it caches device
- *    properties and per-kernel occupancy; the fused-linear entry point below
- *    keeps one cuBLAS handle per device; its no-allocation variant uses a
- *    fixed device array of the library).
+ *    properties, per-kernel occupancy and the driver's tensor-map encoder;
+ *    the no-allocation fused-linear variant uses a fixed device array of
+ *    the library).
  *  - Logit matrices are row-major (BT, V) with a row stride `ld` (in
  *    elements, ld >= V).  Student and teacher share one element type.
  *  - `target` is int64 (BT,).  A row whose target equals `ignore_index`
@@ -312,8 +312,9 @@ int fused_ce_tvd_forward_backward_host(
 /*
  * Fused-linear CE + TVD: the loss from hidden states and lm_head weights,
  * without ever holding the (BT, V) logits.  Rows go through in blocks of
- * chunk_rows: per block, cuBLAS GEMMs (bf16 in, fp32 accumulate) write the
- * block's student and teacher logits into `workspace`, the single-launch
+ * chunk_rows: per block, the library's tensor-core GEMMs (fct_gemm_bf16:
+ * bf16 in, fp32 accumulate) write the block's student and teacher logits
+ * into `workspace`, the single-launch
  * forward + backward of the PR #1384 analysis's loss runs on them and writes
  * their logit gradient as bf16 (also in `workspace`), and two more GEMMs
  * give d loss / d h_student for the block and accumulate d loss / d
@@ -323,7 +324,11 @@ int fused_ce_tvd_forward_backward_host(
  * CE + TVD is this library's addition.)  The teacher is frozen.
  *
  *   h_student (BT, d_student), w_student (V, d_student),
- *   h_teacher (BT, d_teacher), w_teacher (V, d_teacher): bf16, row strides ld_*.
+ *   h_teacher (BT, d_teacher), w_teacher (V, d_teacher): bf16, row strides
+ *                    ld_*; 16-byte aligned with ld_* multiples of 8 (the
+ *                    GEMMs' tile loads are TMA copies), else
+ *                    FCT_ERR_ALIGNMENT (the no-allocation variant below
+ *                    accepts any layout).
  *   target, grad_ce, grad_tvd, grad_stride, ce ... sigma: as for
  *                    fused_ce_tvd_forward_backward.
  *   grad_h_student : (BT, d_student) bf16 output, or NULL.
@@ -340,9 +345,9 @@ int fused_ce_tvd_forward_backward_host(
  *                    chunk_rows, logits_dtype) bytes, 256-byte aligned;
  *                    clobbered.  fused_linear_ce_tvd_workspace_size returns
  *                    0 for V <= 0, chunk_rows <= 0 or an unknown dtype.
- *
- * The library keeps one cuBLAS handle per device (created on first use);
- * calls on one device are serialised by a lock.
+ * The d hidden GEMM (few output tiles, K = V) may split K, with its fp32
+ * partial sums in the teacher block of the workspace, which the loss has
+ * finished reading by then.
  */
 size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows,
                                           fct_dtype logits_dtype);
@@ -369,7 +374,7 @@ int fused_linear_ce_tvd_forward_backward(
  * cache that owns all free HBM, where a cudaMalloc outside it fails or
  * fragments it) and code that must not synchronise the device, which
  * cudaMalloc and cudaFree may do.  The entry point above needs a caller
- * workspace and a cuBLAS handle, whose creation allocates.  This one takes
+ * workspace.  This one takes
  * the same arguments minus logits_dtype, workspace, workspace_bytes and
  * chunk_rows, and computes the outputs of the entry point above with
  * logits_dtype = FCT_F32, with:
@@ -378,9 +383,11 @@ int fused_linear_ce_tvd_forward_backward(
  *     __device__ array): the driver reserves it on each device when the
  *     library's module holding it is loaded there and keeps it until the
  *     process exits;
- *   - its GEMMs on a tiled CUDA-core kernel of the library (fp32
- *     accumulation) instead of cuBLAS, so it is much slower than the entry
- *     point above at large sizes;
+ *   - its GEMMs on the library's tensor-core GEMM (fct_gemm_bf16, without
+ *     a K split) when h_* and w_* have 16-byte aligned rows (ld a multiple
+ *     of 8), else on a tiled CUDA-core kernel of the library (fp32
+ *     accumulation; much slower at large sizes), so unaligned layouts are
+ *     accepted here;
  *   - the same loss kernel and the same bf16 rounding of the logit gradient.
  * Rows go through in blocks of FCT_NOALLOC_SCRATCH_BYTES /
  * (8 * round_up(V, 8)) rows.  V up to 8,388,608 is supported; a larger V

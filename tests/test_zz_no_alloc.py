@@ -195,3 +195,23 @@ def test_noalloc_rejects_vocab_beyond_scratch():
     assert e.value.status == FCT_ERR_UNSUPPORTED
     torch.cuda.synchronize()
     assert all(bool((o == 7.0).all()) for o in outs)
+
+
+def test_noalloc_takes_unaligned_layouts_the_regular_entry_refuses():
+    # Hidden size 100 (rows of 200 bytes): not a TMA layout, so the regular
+    # entry point refuses it with FCT_ERR_ALIGNMENT and this one runs its
+    # CUDA-core GEMMs; the results still meet the oracle's tolerances.
+    BT, ds, dt, V = 40, 100, 60, 1003
+    case = _case(BT, ds, dt, V, seed=91)
+    hs, ws, ht, wt, tg, gce, gtvd = case
+    outs, grad_h, grad_w = _outputs(BT, V, ds)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = binding.fused_linear_ce_tvd_forward_backward_noalloc(
+        hs, ws, ht, wt, tg, gce, gtvd, *outs, grad_h=grad_h, grad_w=grad_w, dev_status=status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    tgc, ref64, tols = _reference(case)
+    _compare(got, ref64, tgc, tols, what="unaligned: ")
+    with pytest.raises(binding.FctError) as e:
+        binding.fused_linear_ce_tvd_forward_backward(hs, ws, ht, wt, tg, gce, gtvd)
+    assert e.value.status == 3  # FCT_ERR_ALIGNMENT
