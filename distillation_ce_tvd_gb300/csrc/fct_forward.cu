@@ -961,13 +961,18 @@ __device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_ba
 // warps compute; 0 = release after computing.
 // kSigns: the forward alone also stores each element's sign bit and a per-row
 // tie flag for the backward (sign words, as forward_pipelined does).
+// kLseIn: the single launch with step 1's per-row states given as partials
+// (FwdArgs::lse_part_s/t): two passes over the row, the first one fed from
+// HBM, and the teacher only in the first when step 3 runs on sign bits, so
+// L2 holds just the student between the passes.
 template <typename T, int VE, bool kGrad, int NT, typename TG, int kPS, int kST, int kPref,
-          int kEarly, bool kSigns = false>
+          int kEarly, bool kSigns = false, bool kLseIn = false>
 __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
   static_assert(kPS >= 1 && kPS <= kPerStep, "steps of at most kPerStep vectors per thread");
   static_assert(!kSigns || !kGrad, "sign words come from the forward alone");
+  static_assert(!kLseIn || kGrad, "given log-sum-exp states: the single launch only");
   constexpr bool kWord = kGrad || kSigns;  // step 2 builds sign words
-  constexpr int kPasses = kGrad ? 3 : 2;
+  constexpr int kPasses = (kGrad ? 3 : 2) - (kLseIn ? 1 : 0);
   constexpr int kStepVecs = kPS * NT;       // 16-byte vectors per tensor per step
   constexpr int kSlotVecs = 2 * kStepVecs;  // student then teacher
   // step 2's sign bits: kBits per step, kSpw steps per 32-bit word
@@ -986,7 +991,7 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
   const int64_t tail0 = nvec * VE;
   const int n_steps = static_cast<int>((nvec + kStepVecs - 1) / kStepVecs);
   const bool use_bits = kGrad && n_steps <= kMaxSignWords * kSpw;
-  const int passes_t = use_bits ? 2 : kPasses;  // passes that stage the teacher
+  const int passes_t = use_bits ? kPasses - 1 : kPasses;  // passes that stage the teacher
 
   if (tid == 0) {
     for (int s = 0; s < kST; ++s) {
@@ -1099,17 +1104,34 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
     }
 
     // ---- step 1: log-sum-exp of both rows
-    Lse2x a = lse2x_empty(), b = lse2x_empty();
-    pass(true, std::integral_constant<bool, kEarly != 0>{}, [&](auto&& cs, auto&& ct, auto n, int) {
-      lse_step_get<T, VE>(a, cs, n);
-      lse_step_get<T, VE>(b, ct, n);
-    });
-    Lse2 fa = lse2x_fold(a), fb = lse2x_fold(b);
-    if (tail0 + tid < p.V) {
-      float xs[1] = {Elem<T>::load1(srow + tail0 + tid)};
-      float xt[1] = {Elem<T>::load1(trow + tail0 + tid)};
-      lse2_update(fa, xs);
-      lse2_update(fb, xt);
+    Lse2 fa, fb;
+    if constexpr (kLseIn) {
+      // the given partial states, thread by thread in index order, then
+      // across the threads in the fixed order of block_merge2
+      fa = lse2_empty();
+      fb = lse2_empty();
+      const float2* ps = p.lse_part_s + row * p.lse_ld;
+      const float2* pt = p.lse_part_t + row * p.lse_ld;
+      for (int64_t j = tid; j < p.lse_n; j += NT) {
+        const float2 u = ps[j], w = pt[j];
+        fa = lse2_merge(fa, Lse2{u.x, u.y});
+        fb = lse2_merge(fb, Lse2{w.x, w.y});
+      }
+    } else {
+      Lse2x a = lse2x_empty(), b = lse2x_empty();
+      pass(true, std::integral_constant<bool, kEarly != 0>{},
+           [&](auto&& cs, auto&& ct, auto n, int) {
+             lse_step_get<T, VE>(a, cs, n);
+             lse_step_get<T, VE>(b, ct, n);
+           });
+      fa = lse2x_fold(a);
+      fb = lse2x_fold(b);
+      if (tail0 + tid < p.V) {
+        float xs[1] = {Elem<T>::load1(srow + tail0 + tid)};
+        float xt[1] = {Elem<T>::load1(trow + tail0 + tid)};
+        lse2_update(fa, xs);
+        lse2_update(fb, xt);
+      }
     }
     block_merge2<NT, true>(fa, fb, red_lse);
     const float lse_s = lse2_finish(fa);
@@ -1473,15 +1495,15 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, double stagger, cudaStr
 constexpr int kTmaThreads = 512, kTmaPerStep = 4, kTmaStages = 3;
 constexpr int kTmaEarly = 0;
 
-template <typename T, bool kGrad, typename TG = T, bool kSigns = false>
+template <typename T, bool kGrad, typename TG = T, bool kSigns = false, bool kLseIn = false>
 cudaError_t run_tma(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr int NT = kTmaThreads;
   constexpr int VE = Elem<T>::kVec;
   constexpr size_t kSmem = size_t(kTmaStages) * 2 * kTmaPerStep * NT * 16 +
                            (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
   constexpr int kPref = kGrad ? 0 : 4;
-  auto kernel =
-      forward_tma<T, VE, kGrad, NT, TG, kTmaPerStep, kTmaStages, kPref, kTmaEarly, kSigns>;
+  auto kernel = forward_tma<T, VE, kGrad, NT, TG, kTmaPerStep, kTmaStages, kPref, kTmaEarly,
+                            kSigns, kLseIn>;
   static PerDevice cache;
   const int n_max = per_device(cache, [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1538,6 +1560,15 @@ cudaError_t run_c(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
+  if (a.lse_part_s != nullptr) {
+    // step 1 given: the two-pass single launch (one CTA per row: L2 holds
+    // only the student between its passes)
+    if (!a.grad || !a.tvd || !plan.vec || a.signs || a.lse_part_t == nullptr || a.lse_n <= 0)
+      return cudaErrorInvalidValue;
+    if (a.dtype == FCT_BF16) return run_tma<bf16_t, true, bf16_t, false, true>(a, plan, st);
+    return a.grad_bf16 ? run_tma<float, true, bf16_t, false, true>(a, plan, st)
+                       : run_tma<float, true, float, false, true>(a, plan, st);
+  }
   if (plan.ring != 1 && plan.vec && plan.cluster == 1 && a.tvd) {
     // the fused forward (alone, with sign words, or with its backward) on the
     // bulk-copy ring: the automatic choice where a row belongs to one CTA

@@ -61,7 +61,14 @@ constexpr uint32_t kEpiBytes = 4 * 2 * kOutBufBytes;  // 32 KB
 constexpr size_t kGemmSmem =
     size_t(kGStages) * kGStageBytes + kEpiBytes + 1024;  // + room to align to 1 KB
 
-enum COut { kOutF32 = 0, kOutBf16 = 1, kOutAddF32 = 2 };
+// Output kinds: fp32 C, bf16 C, fp32 C accumulated into, and fp32 or bf16
+// C with each row's base-2 log-sum-exp state over each 256-column tile
+// (GemmArgs::lse_part), taken on the values as stored.
+enum COut { kOutF32 = 0, kOutBf16 = 1, kOutAddF32 = 2, kOutF32Lse = 3, kOutBf16Lse = 4 };
+template <int kOut>
+constexpr bool kBf16C = kOut == kOutBf16 || kOut == kOutBf16Lse;
+template <int kOut>
+constexpr bool kLseC = kOut == kOutF32Lse || kOut == kOutBf16Lse;
 
 // Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator (bits
 // 4-5 = 1), A and B bf16 (bits 7-9 and 10-12 = 1), A and B major-ness
@@ -200,7 +207,50 @@ struct GemmArgs {
   int k_per;  // K blocks per part
   int64_t slab_rows;
   int32_t* status;
+  // lse kinds: row r's state over tile column block t at lse_part[r * lse_ld + t]
+  float2* lse_part;
+  int64_t lse_ld;
 };
+
+// Folds n values (n <= kN; the first n are columns inside C) into a running
+// base-2 log-sum-exp state (m2, s): the same representation and rounding
+// steps as the loss kernel's step 1 (m2 = max x * log2 e, s = sum of
+// 2^(x log2 e - m2)), one rescale per call.  Full groups (n == kN, all but
+// a row's last tile) take three-input maxima and packed f32x2 FMAs and adds.
+template <int kN>
+__device__ __forceinline__ void lse_fold(float& m2, float& s, const float (&x)[kN], int n) {
+  static_assert(kN % 4 == 0, "groups of four");
+  float vm = -INFINITY;
+  if (n >= kN) {
+#pragma unroll
+    for (int j = 0; j < kN; j += 2) vm = max3(vm, x[j], x[j + 1]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < kN; ++j)
+      if (j < n) vm = fmaxf(vm, x[j]);
+  }
+  const float m2n = vm * kLog2e;
+  if (m2n > m2) {
+    s *= ex2(m2 - m2n);
+    m2 = m2n;
+  }
+  const float2 L2 = make_float2(kLog2e, kLog2e), nm = make_float2(-m2, -m2);
+  float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+  if (n >= kN) {
+#pragma unroll
+    for (int j = 0; j < kN; j += 4) {
+      const float2 e0 = __ffma2_rn(make_float2(x[j], x[j + 1]), L2, nm);
+      const float2 e1 = __ffma2_rn(make_float2(x[j + 2], x[j + 3]), L2, nm);
+      a0 = __fadd2_rn(a0, make_float2(ex2(e0.x), ex2(e0.y)));
+      a1 = __fadd2_rn(a1, make_float2(ex2(e1.x), ex2(e1.y)));
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kN; ++j)
+      if (j < n) a0.x += ex2(fmaf(x[j], kLog2e, -m2));
+  }
+  s += (a0.x + a0.y) + (a1.x + a1.y);
+}
 
 // Tile t's (M tile, N tile).  Pairs working at once take consecutive t, so
 // they share the operand tile of the slow index through L2; the fast index
@@ -265,7 +315,7 @@ __device__ __forceinline__ void stage_row(uint32_t buf, int row, const uint32_t 
 template <int kOut>
 __device__ __forceinline__ void store_row32(const GemmArgs& g, int64_t row, int64_t col0,
                                             const uint32_t (&r)[32]) {
-  if constexpr (kOut == kOutBf16) {
+  if constexpr (kBf16C<kOut>) {
     uint16_t* crow = static_cast<uint16_t*>(g.C) + row * g.ldc + col0;
     if (g.vec && col0 + 32 <= g.N) {
 #pragma unroll
@@ -448,16 +498,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int64_t n0 = tn * kBN;
       const int64_t slab = (u / tiles) * g.slab_rows;  // 0 without split K
       const uint32_t tq = tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kBN);
+      // lse kinds: this thread's row over the tile's columns
+      [[maybe_unused]] float lse_m2 = -INFINITY, lse_s = 0.f;
       if (g.tma_c) {
         // 32-row blocks of 128 bytes per row through two staging buffers
         const uint32_t buf0 = smem0 + kGStages * kGStageBytes + uint32_t(q) * 2 * kOutBufBytes;
-        constexpr int kCols = (kOut == kOutBf16) ? 64 : 32;
+        constexpr int kCols = kBf16C<kOut> ? 64 : 32;
         const int y = static_cast<int>(slab + m0 + q * 32);
         const int64_t rows_end = slab + (g.splits > 1 ? g.slab_rows : g.M);
 #pragma unroll 1
         for (int c = 0; c < kBN / kCols; ++c) {
           uint32_t w[32];
-          if constexpr (kOut == kOutBf16) {
+          if constexpr (kBf16C<kOut>) {
             uint32_t r[32];
             tmem_ld32(tq + uint32_t(c * 64), r);
 #pragma unroll
@@ -469,6 +521,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
               w[16 + j] = pack_bf16x2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
           } else {
             tmem_ld32(tq + uint32_t(c * 32), w);
+          }
+          if constexpr (kLseC<kOut>) {
+            const int64_t nv = g.N - (n0 + c * kCols);
+            float x[kCols];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if constexpr (kBf16C<kOut>) {
+                x[2 * j] = __uint_as_float(w[j] << 16);
+                x[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+              } else {
+                x[j] = __uint_as_float(w[j]);
+              }
+            }
+            lse_fold<kCols>(lse_m2, lse_s, x, nv < kCols ? static_cast<int>(nv) : kCols);
           }
           if (c == kBN / kCols - 1) {  // the accumulator is read: release it
             tc_fence_before();
@@ -502,10 +568,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           tmem_ld32(tq + uint32_t(c * 32), r);
           const int64_t col0 = n0 + c * 32;
           if (row < g.M && col0 < g.N) store_row32<kOut>(g, slab + row, col0, r);
+          if constexpr (kLseC<kOut>) {
+            const int64_t nv = g.N - col0;
+            float x[32];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              if constexpr (kBf16C<kOut>) {  // the values as stored
+                const uint32_t b = pack_bf16x2(__uint_as_float(r[j]), __uint_as_float(r[j + 1]));
+                x[j] = __uint_as_float(b << 16);
+                x[j + 1] = __uint_as_float(b & 0xffff0000u);
+              } else {
+                x[j] = __uint_as_float(r[j]);
+                x[j + 1] = __uint_as_float(r[j + 1]);
+              }
+            }
+            lse_fold<32>(lse_m2, lse_s, x, nv < 32 ? static_cast<int>(nv) : 32);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(acc_empty0 + 8u * acc);
+      }
+      if constexpr (kLseC<kOut>) {
+        const int64_t row = m0 + q * 32 + lane;
+        if (row < g.M) g.lse_part[row * g.lse_ld + tn] = make_float2(lse_m2, lse_s);
       }
     }
     if (lane == 0) bulk_wait_all();  // C is written before the kernel ends
@@ -719,11 +805,15 @@ bool gemm_operand_ok(const void* p, int64_t ld) {
 
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
                         int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
-                        cudaStream_t st, void* split_ws, size_t split_ws_bytes) {
+                        cudaStream_t st, void* split_ws, size_t split_ws_bytes, float2* lse_part,
+                        int64_t lse_ld) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
   if (!gemm_operand_ok(A.ptr, A.ld) || !gemm_operand_ok(B.ptr, B.ld) || sms <= 0)
     return cudaErrorInvalidValue;
-  if (c_kind != kOutF32 && c_kind != kOutBf16 && c_kind != kOutAddF32) return cudaErrorInvalidValue;
+  if (c_kind < kOutF32 || c_kind > kOutBf16Lse) return cudaErrorInvalidValue;
+  const bool lse = c_kind == kOutF32Lse || c_kind == kOutBf16Lse;
+  if (lse && (lse_part == nullptr || lse_ld < (N + kBN - 1) / kBN || A.mn_major || B.mn_major))
+    return cudaErrorInvalidValue;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   CUtensorMap ma, mb;
@@ -736,7 +826,7 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
   // split K into parts whose fp32 partial tiles go to slabs in split_ws
   int splits = 1;
   const int64_t slab_rows = m_tiles * kBM, slab_ld = (N + 3) / 4 * 4;
-  if (c_kind != kOutAddF32 && split_ws != nullptr &&
+  if (c_kind != kOutAddF32 && !lse && split_ws != nullptr &&
       reinterpret_cast<uintptr_t>(split_ws) % 16 == 0) {
     int pairs = prepare<false, false, kOutF32>(dev);
     if (pairs > max_pairs) pairs = max_pairs;
@@ -752,7 +842,7 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
     if (!make_c_map(&ms, split_ws, splits * slab_rows, N, slab_ld, false))
       return cudaErrorInvalidValue;
     const GemmArgs g{M, N, K, split_ws, slab_ld, 1, 1, M > N ? 1 : 0, splits, k_per, slab_rows,
-                     status};
+                     status, nullptr, 0};
     cudaError_t e = dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, ms, g, max_pairs, st);
     if (e != cudaSuccess) return e;
     const int64_t groups = M * ((N + 3) / 4);
@@ -767,7 +857,8 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
     return cudaGetLastError();
   }
 
-  const size_t es = c_kind == kOutBf16 ? 2 : 4;
+  const bool bf16 = c_kind == kOutBf16 || c_kind == kOutBf16Lse;
+  const size_t es = bf16 ? 2 : 4;
   const bool aligned16 =
       reinterpret_cast<uintptr_t>(C) % 16 == 0 && (size_t(ldc) * es) % 16 == 0;
   // TMA stores clip a row at 16-byte granularity: a row whose width is not
@@ -775,10 +866,13 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
   CUtensorMap mc;
   memset(&mc, 0, sizeof(mc));
   const bool tma_c = aligned16 && (size_t(N) * es) % 16 == 0 &&
-                     make_c_map(&mc, C, M, N, ldc, c_kind == kOutBf16);
+                     make_c_map(&mc, C, M, N, ldc, bf16);
   const GemmArgs g{M, N, K, C, ldc, aligned16 ? 1 : 0, tma_c ? 1 : 0, M > N ? 1 : 0, 1, k_iters,
-                   0, status};
+                   0, status, lse_part, lse_ld};
   switch (c_kind) {
+    // the logits product only: both operands K-major
+    case kOutF32Lse: return run_gemm<false, false, kOutF32Lse>(ma, mb, mc, g, max_pairs, st);
+    case kOutBf16Lse: return run_gemm<false, false, kOutBf16Lse>(ma, mb, mc, g, max_pairs, st);
     case kOutF32: return dispatch_major<kOutF32>(A.mn_major, B.mn_major, ma, mb, mc, g, max_pairs, st);
     case kOutBf16:
       return dispatch_major<kOutBf16>(A.mn_major, B.mn_major, ma, mb, mc, g, max_pairs, st);

@@ -36,6 +36,13 @@ struct FwdArgs {
   // start stagger (set by the launcher): cluster i of n waits stagger * i / n
   // clock cycles before its first load
   int64_t stagger = 0;
+  // single launch with the row's log-sum-exp given as partials (the fused-
+  // linear logits GEMM's epilogue writes them): per row lse_n base-2 states
+  // (m2, s) at lse_part_s[row * lse_ld + j]; step 1 merges them instead of
+  // reading the row (nullptr: step 1 reads the row)
+  const float2* lse_part_s = nullptr;
+  const float2* lse_part_t = nullptr;
+  int64_t lse_ld = 0, lse_n = 0;
 };
 
 struct FwdPlan {
@@ -174,9 +181,15 @@ struct GemmOperand {
 // gemm_split_workspace_bytes(M, N) is the most any split of an M x N result
 // uses.
 bool gemm_operand_ok(const void* p, int64_t ld);
+// c_kind 3 (fp32 C) and 4 (bf16 C), both operands K-major only: also each
+// row's base-2 log-sum-exp state (m2, s) over each 256-column tile t of C,
+// at lse_part[row * lse_ld + t] (lse_ld >= the number of tiles), on the
+// values as stored.
+constexpr int kGemmLseTile = 256;
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
                         int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
-                        cudaStream_t st, void* split_ws = nullptr, size_t split_ws_bytes = 0);
+                        cudaStream_t st, void* split_ws = nullptr, size_t split_ws_bytes = 0,
+                        float2* lse_part = nullptr, int64_t lse_ld = 0);
 size_t gemm_split_workspace_bytes(int64_t M, int64_t N);
 
 cudaError_t launch_forward(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st);

@@ -12,7 +12,10 @@
 // MN-major tiles).  The logit blocks are fp32 (the GEMMs' own precision), or
 // bf16 (rounded once by the GEMM, as a model's bf16 lm_head produces them),
 // which halves their bytes and lets the gradient overwrite the student block
-// in place.  Only the block's logits and gradient exist at a time.  The
+// in place.  The logits GEMMs' epilogue also folds each row's values into
+// base-2 log-sum-exp states per 256-column tile, so the loss kernel merges
+// those instead of reading the block for its step 1: two passes over the
+// block instead of three, and only the student stays in L2 between them.  Only the block's logits and gradient exist at a time.  The
 // teacher is frozen (no gradients).
 #include "fct_common.cuh"
 #include "fct_internal.h"
@@ -21,12 +24,17 @@ namespace fct {
 
 int64_t linear_logits_ld(int64_t V) { return (V + 7) / 8 * 8; }
 
+// Log-sum-exp partial states per logit row: one per 256-column tile.
+int64_t linear_lse_parts(int64_t V) { return (V + kGemmLseTile - 1) / kGemmLseTile; }
+
 size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows, int logits_dtype) {
   // fp32: student and teacher logits, then the bf16 logit gradient;
-  // bf16: student and teacher logits, the gradient written over the student's
+  // bf16: student and teacher logits, the gradient written over the student's;
+  // then the student's and the teacher's log-sum-exp partials
   const size_t per_entry = logits_dtype == FCT_BF16 ? 2 * sizeof(uint16_t)
                                                     : 2 * sizeof(float) + sizeof(uint16_t);
-  return size_t(chunk_rows) * size_t(linear_logits_ld(V)) * per_entry;
+  return size_t(chunk_rows) * size_t(linear_logits_ld(V)) * per_entry +
+         2 * size_t(chunk_rows) * size_t(linear_lse_parts(V)) * sizeof(float2);
 }
 
 cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,
@@ -43,7 +51,13 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
   // after the two fp32 blocks
   void* G = bf16 ? static_cast<void*>(Ls) : static_cast<void*>(Lt + block_bytes);
   const int64_t ldg = ldl;
-  const int lkind = bf16 ? FCT_GEMM_BF16 : FCT_GEMM_F32;
+  // the logits GEMMs also write each row's log-sum-exp partials, so the loss
+  // kernel starts at step 2
+  const int lkind = bf16 ? 4 : 3;
+  const int64_t n_parts = linear_lse_parts(a.V);
+  const int64_t grad_bytes = bf16 ? 0 : a.chunk_rows * ldl * 2;  // the separate bf16 gradient
+  float2* Ps = reinterpret_cast<float2*>(Ls + 2 * block_bytes + grad_bytes);
+  float2* Pt = Ps + a.chunk_rows * n_parts;
   const auto* Hs = static_cast<const uint16_t*>(a.h_s);
   const auto* Ht = static_cast<const uint16_t*>(a.h_t);
   const GemmOperand Ws{a.w_s, a.ld_ws, false}, Wt{a.w_t, a.ld_wt, false};
@@ -53,11 +67,11 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
     const int64_t R = (a.BT - r0 < a.chunk_rows) ? a.BT - r0 : a.chunk_rows;
     // logits (R x V) = H (R x D) W^T: both operands K-major
     const GemmOperand Hsb{Hs + r0 * a.ld_hs, a.ld_hs, false}, Htb{Ht + r0 * a.ld_ht, a.ld_ht, false};
-    if ((e = launch_gemm(Hsb, Ws, Ls, ldl, lkind, R, a.V, a.d_s, a.dev_status, sms, st)) !=
-        cudaSuccess)
+    if ((e = launch_gemm(Hsb, Ws, Ls, ldl, lkind, R, a.V, a.d_s, a.dev_status, sms, st, nullptr,
+                         0, Ps, n_parts)) != cudaSuccess)
       return e;
-    if ((e = launch_gemm(Htb, Wt, Lt, ldl, lkind, R, a.V, a.d_t, a.dev_status, sms, st)) !=
-        cudaSuccess)
+    if ((e = launch_gemm(Htb, Wt, Lt, ldl, lkind, R, a.V, a.d_t, a.dev_status, sms, st, nullptr,
+                         0, Pt, n_parts)) != cudaSuccess)
       return e;
     // the loss on the block; its logit gradient, as bf16, into G
     FwdArgs f{Ls, Lt, ldl, ldl, bf16 ? FCT_BF16 : FCT_F32, a.target + r0, R, a.V, a.ignore_index,
@@ -65,6 +79,10 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
               G, ldg, a.grad_ce + (a.grad_stride ? r0 : 0),
               a.grad_tvd + (a.grad_stride ? r0 : 0), a.grad_stride, plan.keep_normal ? 1 : 0,
               /*grad_bf16=*/bf16 ? 0 : 1};
+    f.lse_part_s = Ps;
+    f.lse_part_t = Pt;
+    f.lse_ld = n_parts;
+    f.lse_n = n_parts;
     if ((e = launch_forward(f, plan, st)) != cudaSuccess) return e;
     if (a.grad_h_s == nullptr && a.grad_w_s == nullptr) continue;
     // d hidden (R x D, bf16) = G (R x V) W (V x D): C(r, d) = sum_v G(r, v) W(v, d),

@@ -345,9 +345,12 @@ int fused_ce_tvd_forward_backward_host(
  *                    chunk_rows, logits_dtype) bytes, 256-byte aligned;
  *                    clobbered.  fused_linear_ce_tvd_workspace_size returns
  *                    0 for V <= 0, chunk_rows <= 0 or an unknown dtype.
- * The d hidden GEMM (few output tiles, K = V) may split K, with its fp32
- * partial sums in the teacher block of the workspace, which the loss has
- * finished reading by then.
+ * The logits GEMMs' epilogue also writes each row's log-sum-exp as base-2
+ * (max, sum) states per 256 logit columns (in the workspace), so the loss
+ * kernel takes step 1 of "Forward Pass" from those states and reads each
+ * logit block twice instead of three times.  The d hidden GEMM (few output
+ * tiles, K = V) may split K, with its fp32 partial sums in the teacher block
+ * of the workspace, which the loss has finished reading by then.
  */
 size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows,
                                           fct_dtype logits_dtype);
