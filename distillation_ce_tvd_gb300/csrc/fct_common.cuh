@@ -77,18 +77,22 @@ __device__ __forceinline__ float sgn_pq(float p, float q) {
   return gt - lt;
 }
 
-// Per lane of two (p, q) pairs: 1.0 where p > q (resp. p < q), else 0.0.
-__device__ __forceinline__ float2 gt_pq2(float2 p, float2 q) {
-  float2 r;
-  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(r.x) : "f"(p.x), "f"(q.x));
-  asm("set.gt.f32.f32 %0, %1, %2;" : "=f"(r.y) : "f"(p.y), "f"(q.y));
+// sign(p - q) of two (p, q) pairs on the FMA pipe instead of four compares
+// on the ALU pipe (which step 2 is bound by): d = p - q rounded once, then
+// 2 sat(d * 2^126 + 1/2) - 1.  That is exactly +1 or -1 for |d| >= 2^-127,
+// i.e. for every nonzero difference except a subnormal one, and exactly 0
+// at p == q (the zero subgradient at ties).  A nonzero subnormal difference
+// gives a value strictly between -1 and 1; its bit pattern then fails the
+// callers' tie test like a tie does, so sign bits are never taken from it.
+__device__ __forceinline__ float sat_ramp(float d) {
+  float r;
+  asm("fma.rn.sat.f32 %0, %1, 0f7E800000, 0f3F000000;" : "=f"(r) : "f"(d));
   return r;
 }
-__device__ __forceinline__ float2 lt_pq2(float2 p, float2 q) {
-  float2 r;
-  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r.x) : "f"(p.x), "f"(q.x));
-  asm("set.lt.f32.f32 %0, %1, %2;" : "=f"(r.y) : "f"(p.y), "f"(q.y));
-  return r;
+__device__ __forceinline__ float2 sgn_pq2(float2 p, float2 q) {
+  const float2 d = __ffma2_rn(q, make_float2(-1.f, -1.f), p);
+  return __ffma2_rn(make_float2(sat_ramp(d.x), sat_ramp(d.y)), make_float2(2.f, 2.f),
+                    make_float2(-1.f, -1.f));
 }
 
 // max(a, b, c) in one instruction (sm_100+).

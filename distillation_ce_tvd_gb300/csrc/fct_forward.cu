@@ -674,21 +674,21 @@ __global__ void __launch_bounds__(NT, 1) forward_pipelined(FwdArgs p) {
       // op (neighbours of one tensor come out of the unpack side by side);
       // sigma and tau run as two packed partial sums.
       const float2 ns22 = make_float2(ns2, ns2), nt22 = make_float2(nt2, nt2);
-      const float2 minus1 = make_float2(-1.f, -1.f);
       float2 sp2 = make_float2(0.f, 0.f), sq2 = make_float2(0.f, 0.f);
       auto tvd_two = [&](float s0, float s1, float t0, float t1) {
         const float2 es = __ffma2_rn(make_float2(s0, s1), L2, ns22);
         const float2 et = __ffma2_rn(make_float2(t0, t1), L2, nt22);
         const float2 pp = make_float2(ex2(es.x), ex2(es.y));
         const float2 qq = make_float2(ex2(et.x), ex2(et.y));
-        const float2 sg = __ffma2_rn(lt_pq2(pp, qq), minus1, gt_pq2(pp, qq));  // gt - lt, exact
+        const float2 sg = sgn_pq2(pp, qq);
         sp2 = __ffma2_rn(pp, sg, sp2);
         sq2 = __ffma2_rn(qq, sg, sq2);
         return sg;
       };
       // Single launch: the sign bit of each element (1 for p < q), shifted in
       // element order into one word per step, and the AND of all signs' bit
-      // patterns, whose exponent bits clear at a tie (sign +0; NaN gives 0 too).
+      // patterns, whose exponent bits clear at a tie (sign +0) and at a
+      // subnormal difference (a sign strictly between -1 and 1).
       uint32_t tie_and = 0xffffffffu;
       consume_pass<NT, F::kTensors>(f, slot, p, n_clusters, mine, n_full, rem,
                                     [&](const uint4* cell, auto n, int k0) {
@@ -1142,7 +1142,6 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
 
     // ---- step 2: sigma and tau (sum |p - q| = sigma - tau), sign bits
     const float2 ns22 = make_float2(ns2, ns2), nt22 = make_float2(nt2, nt2);
-    const float2 minus1 = make_float2(-1.f, -1.f);
     float2 sp2 = make_float2(0.f, 0.f), sq2 = make_float2(0.f, 0.f);
     uint32_t tie_and = 0xffffffffu;
     [[maybe_unused]] uint32_t packed = 0;  // sign bits of the steps of the current word
@@ -1160,7 +1159,7 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
             const float2 et = __ffma2_rn(make_float2(xt[j], xt[j + 1]), L2, nt22);
             const float2 pp = make_float2(ex2(es.x), ex2(es.y));
             const float2 qq = make_float2(ex2(et.x), ex2(et.y));
-            const float2 sg = __ffma2_rn(lt_pq2(pp, qq), minus1, gt_pq2(pp, qq));  // gt - lt
+            const float2 sg = sgn_pq2(pp, qq);
             sp2 = __ffma2_rn(pp, sg, sp2);
             sq2 = __ffma2_rn(qq, sg, sq2);
             if constexpr (kWord) {
