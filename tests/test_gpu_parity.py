@@ -615,6 +615,29 @@ def test_single_launch_ties_equal_forward_then_backward(dtype, cluster):
     assert f2["tvd"][2].item() == 0.0 and f2["sigma"][2].item() == 0.0
 
 
+@pytest.mark.parametrize("cluster", [0, 2])
+def test_subnormal_probability_differences(cluster):
+    # Elements whose p and q are normal floats just above 2^-126 and differ
+    # by a subnormal amount: teacher == student except one ulp up at those
+    # elements, so both rows keep the same lse and p - q is about 1e-43.
+    # Step 2 then takes a fractional sign there and flags the thread for the
+    # exact teacher path in step 3; the outputs stay within the oracle's
+    # near-tie tolerances and the single launch equals forward + backward.
+    w = workloads.make("bt1024_v32000_bf16", DEV, rows=4, V=4096, dtype=torch.float32, seed=35)
+    w.teacher.copy_(w.student)
+    for r, cols in ((0, slice(100, 164)), (1, slice(0, 4096, 37)), (3, slice(4000, 4096))):
+        w.student[r, cols] = -78.0
+        w.teacher[r, cols] = torch.nextafter(w.student[r, cols], torch.zeros_like(w.student[r, cols]))
+    w.teacher[2] = w.student[2] * 0.9 + 0.1  # a plain row beside them
+    f1, g1, st1 = run(w, cluster=cluster)
+    f2, g2, st2 = run_single(w, cluster=cluster)
+    assert st1 == st2 == 0
+    for k in f1:
+        assert torch.equal(f1[k], f2[k]), k
+    assert torch.equal(g1, g2)
+    compare(w, f2, g2, what="subnormal differences ")
+
+
 @pytest.mark.parametrize("dtype,V,ld", [(torch.bfloat16, 300003, 300008),
                                         (torch.float32, 140001, 140004)])
 def test_single_launch_without_sign_words(dtype, V, ld):
