@@ -100,3 +100,64 @@ def test_captured_step_replays_bitwise(path, V):
         for k, (x, y) in enumerate(zip(results, eager)):
             assert torch.equal(x, y), f"{path} output {k}"
     assert status.item() == 0
+
+
+@pytest.mark.parametrize("logits_dtype", [torch.bfloat16, torch.float32])
+def test_captured_fused_linear_step_replays_bitwise(logits_dtype):
+    # The fused-linear entry point: cluster launches of the tensor-core GEMM
+    # with tensor maps built at capture time, the loss started from the
+    # GEMM's log-sum-exp partials, d hidden's K split and d weight's
+    # accumulation (zeroed inside the graph), over 3 row blocks (the last
+    # one ragged).
+    BT, D, V, chunk = 300, 128, 3000, 128
+    g = torch.Generator(device=DEV).manual_seed(71)
+
+    def case():
+        hs = torch.randn(BT, D, generator=g, device=DEV).bfloat16()
+        ht = torch.randn(BT, D, generator=g, device=DEV).bfloat16()
+        ws = (torch.randn(V, D, generator=g, device=DEV) * 0.2).bfloat16()
+        wt = (torch.randn(V, D, generator=g, device=DEV) * 0.2).bfloat16()
+        tg = torch.randint(0, V, (BT,), generator=g, device=DEV)
+        tg[::9] = -100
+        gce = torch.full((BT,), 1.0 / BT, device=DEV)
+        return [hs, ws, ht, wt, tg, gce, gce * 0.5]
+
+    def buffers():
+        ws_bytes = binding.fused_linear_ce_tvd_workspace_size(V, chunk, logits_dtype)
+        return (torch.empty(BT, D, device=DEV, dtype=torch.bfloat16),
+                torch.zeros(V, D, device=DEV),
+                torch.empty(ws_bytes, device=DEV, dtype=torch.uint8),
+                torch.zeros(1, dtype=torch.int32, device=DEV))
+
+    def step_all(inp, bufs):
+        gh, gw, work, status = bufs
+        gw.zero_()
+        # (the per-row outputs come from the caching allocator: inside the
+        # capture, from the graph's own pool)
+        return binding.fused_linear_ce_tvd_forward_backward(
+            *inp, chunk_rows=chunk, logits_dtype=logits_dtype, workspace=work, grad_h=gh,
+            grad_w=gw, dev_status=status)
+
+    cases = [case() for _ in range(2)]
+    inp = [x.clone() for x in cases[0]]
+    bufs = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step_all(inp, bufs)  # eager: per-device set-up outside the capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        results = step_all(inp, bufs)
+
+    for c in (cases[1], cases[0], cases[1]):
+        for dst, src in zip(inp, c):
+            dst.copy_(src)
+        graph.replay()
+        eager = step_all(c, buffers())
+        torch.cuda.synchronize()
+        for k, (x, y) in enumerate(zip(results, eager)):
+            assert torch.equal(x, y), f"output {k}"
+    assert bufs[-1].item() == 0
