@@ -28,11 +28,13 @@ int64_t linear_logits_ld(int64_t V) { return (V + 7) / 8 * 8; }
 int64_t linear_lse_parts(int64_t V) { return (V + kGemmLseTile - 1) / kGemmLseTile; }
 
 size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows, int logits_dtype) {
-  // fp32: student and teacher logits, then the bf16 logit gradient;
-  // bf16: student and teacher logits, the gradient written over the student's;
-  // then the student's and the teacher's log-sum-exp partials
-  const size_t per_entry = logits_dtype == FCT_BF16 ? 2 * sizeof(uint16_t)
-                                                    : 2 * sizeof(float) + sizeof(uint16_t);
+  // bf16: two student blocks (the logit gradient is written over the
+  // student's, and d weight takes two blocks' gradients at once) and the
+  // teacher block; fp32: the student and teacher blocks, then two bf16
+  // logit-gradient blocks; then the student's and the teacher's
+  // log-sum-exp partials
+  const size_t per_entry = logits_dtype == FCT_BF16 ? 3 * sizeof(uint16_t)
+                                                    : 2 * sizeof(float) + 2 * sizeof(uint16_t);
   return size_t(chunk_rows) * size_t(linear_logits_ld(V)) * per_entry +
          2 * size_t(chunk_rows) * size_t(linear_lse_parts(V)) * sizeof(float2);
 }
@@ -45,26 +47,31 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
   const int64_t ldl = linear_logits_ld(a.V);
   const bool bf16 = a.logits_dtype == FCT_BF16;
   const int64_t block_bytes = a.chunk_rows * ldl * (bf16 ? 2 : 4);
-  char* Ls = static_cast<char*>(a.workspace);
-  char* Lt = Ls + block_bytes;
-  // the bf16 logit gradient: over the student block (same type, in place) or
-  // after the two fp32 blocks
-  void* G = bf16 ? static_cast<void*>(Ls) : static_cast<void*>(Lt + block_bytes);
+  const int64_t gblock = a.chunk_rows * ldl;  // elements of one bf16 gradient block
+  char* base = static_cast<char*>(a.workspace);
+  // bf16: student blocks 0 and 1 (block b uses b % 2; its gradient goes over
+  // it), then the teacher block; fp32: student, teacher, gradient blocks 0, 1
+  char* Lt = base + (bf16 ? 2 : 1) * block_bytes;
+  uint16_t* G0 = bf16 ? reinterpret_cast<uint16_t*>(base)
+                      : reinterpret_cast<uint16_t*>(Lt + block_bytes);
   const int64_t ldg = ldl;
   // the logits GEMMs also write each row's log-sum-exp partials, so the loss
   // kernel starts at step 2
   const int lkind = bf16 ? 4 : 3;
   const int64_t n_parts = linear_lse_parts(a.V);
-  const int64_t grad_bytes = bf16 ? 0 : a.chunk_rows * ldl * 2;  // the separate bf16 gradient
-  float2* Ps = reinterpret_cast<float2*>(Ls + 2 * block_bytes + grad_bytes);
+  float2* Ps = reinterpret_cast<float2*>(bf16 ? Lt + block_bytes
+                                              : reinterpret_cast<char*>(G0 + 2 * gblock));
   float2* Pt = Ps + a.chunk_rows * n_parts;
   const auto* Hs = static_cast<const uint16_t*>(a.h_s);
   const auto* Ht = static_cast<const uint16_t*>(a.h_t);
   const GemmOperand Ws{a.w_s, a.ld_ws, false}, Wt{a.w_t, a.ld_wt, false};
   cudaError_t e;
 
-  for (int64_t r0 = 0; r0 < a.BT; r0 += a.chunk_rows) {
+  int64_t b = 0;
+  for (int64_t r0 = 0; r0 < a.BT; r0 += a.chunk_rows, ++b) {
     const int64_t R = (a.BT - r0 < a.chunk_rows) ? a.BT - r0 : a.chunk_rows;
+    uint16_t* G = G0 + (b & 1) * gblock;  // this block's logit gradient
+    void* Ls = bf16 ? static_cast<void*>(G) : static_cast<void*>(base);
     // logits (R x V) = H (R x D) W^T: both operands K-major
     const GemmOperand Hsb{Hs + r0 * a.ld_hs, a.ld_hs, false}, Htb{Ht + r0 * a.ld_ht, a.ld_ht, false};
     if ((e = launch_gemm(Hsb, Ws, Ls, ldl, lkind, R, a.V, a.d_s, a.dev_status, sms, st, nullptr,
@@ -96,12 +103,18 @@ cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int
                          size_t(block_bytes))) != cudaSuccess)
       return e;
     // d weight (V x D, fp32) += G^T H: C(v, d) += sum_r G(r, v) H(r, d), both
-    // operands MN-major
-    if (a.grad_w_s &&
-        (e = launch_gemm(GemmOperand{G, ldg, true}, GemmOperand{Hs + r0 * a.ld_hs, a.ld_hs, true},
-                         a.grad_w_s, a.ld_gws, FCT_GEMM_ADD_F32, a.V, a.d_s, R, a.dev_status, sms,
-                         st)) != cudaSuccess)
-      return e;
+    // operands MN-major, once per two blocks (K = their rows, the gradient
+    // blocks adjacent in the workspace), or for a last block left alone:
+    // one read-modify-write of the fp32 (V, D) gradient per two blocks
+    const bool last = r0 + R >= a.BT;
+    if (a.grad_w_s && ((b & 1) || last)) {
+      const int64_t k0 = (b & 1) ? r0 - a.chunk_rows : r0;  // first row of the pending blocks
+      if ((e = launch_gemm(GemmOperand{G0, ldg, true},
+                           GemmOperand{Hs + k0 * a.ld_hs, a.ld_hs, true}, a.grad_w_s, a.ld_gws,
+                           FCT_GEMM_ADD_F32, a.V, a.d_s, r0 + R - k0, a.dev_status, sms, st)) !=
+          cudaSuccess)
+        return e;
+    }
   }
   return cudaGetLastError();
 }

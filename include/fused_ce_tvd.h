@@ -343,8 +343,12 @@ int fused_ce_tvd_forward_backward_host(
  *                    Anything else: FCT_ERR_UNSUPPORTED.
  *   workspace      : device memory of fused_linear_ce_tvd_workspace_size(V,
  *                    chunk_rows, logits_dtype) bytes, 256-byte aligned;
- *                    clobbered.  fused_linear_ce_tvd_workspace_size returns
- *                    0 for V <= 0, chunk_rows <= 0 or an unknown dtype.
+ *                    clobbered.  It holds the logit blocks and two blocks'
+ *                    logit gradients: d w_student is accumulated once per two
+ *                    row blocks (one read-modify-write of the fp32 (V, d)
+ *                    matrix per 2 * chunk_rows rows).
+ *                    fused_linear_ce_tvd_workspace_size returns 0 for V <= 0,
+ *                    chunk_rows <= 0 or an unknown dtype.
  * The logits GEMMs' epilogue also writes each row's log-sum-exp as base-2
  * (max, sum) states per 256 logit columns (in the workspace), so the loss
  * kernel takes step 1 of "Forward Pass" from those states and reads each

@@ -12,10 +12,10 @@ int main(void) {
   if (fused_ce_tvd_signs_row_bytes(151936, FCT_BF16) != 4 + 18992) return 3;
   /* logit blocks, then 2 x rows x 594 log-sum-exp states of 8 bytes */
   if (fused_linear_ce_tvd_workspace_size(151936, 2, FCT_F32) !=
-      (size_t)2 * 151936 * 10 + (size_t)2 * 2 * 594 * 8)
+      (size_t)2 * 151936 * 12 + (size_t)2 * 2 * 594 * 8)
     return 4;
   if (fused_linear_ce_tvd_workspace_size(151936, 2, FCT_BF16) !=
-      (size_t)2 * 151936 * 4 + (size_t)2 * 2 * 594 * 8)
+      (size_t)2 * 151936 * 6 + (size_t)2 * 2 * 594 * 8)
     return 4;
   if (fused_linear_ce_tvd_workspace_size(151936, 2, (fct_dtype)7) != 0) return 4;
   /* empty batch: a no-op */

@@ -291,14 +291,15 @@ def test_forward_backward_argument_checks(lib):
 
 def test_fused_linear_workspace_sizes_and_argument_checks(lib):
     import torch
-    # fp32 blocks: 2 x 4 bytes of logits + 2 of gradient per padded entry;
-    # bf16 blocks: 2 x 2 (the gradient overwrites the student block); then
-    # per row and tensor one 8-byte log-sum-exp state per 256 columns
+    # fp32 blocks: 2 x 4 bytes of logits + 2 x 2 of gradient (two blocks)
+    # per padded entry; bf16 blocks: 3 x 2 (two student blocks, the gradient
+    # over them, and the teacher's); then per row and tensor one 8-byte
+    # log-sum-exp state per 256 columns
     parts = 2 * 4 * 1 * 8
-    assert binding.fused_linear_ce_tvd_workspace_size(100, 4) == 4 * 104 * 10 + parts
-    assert binding.fused_linear_ce_tvd_workspace_size(100, 4, torch.bfloat16) == 4 * 104 * 4 + parts
+    assert binding.fused_linear_ce_tvd_workspace_size(100, 4) == 4 * 104 * 12 + parts
+    assert binding.fused_linear_ce_tvd_workspace_size(100, 4, torch.bfloat16) == 4 * 104 * 6 + parts
     assert binding.fused_linear_ce_tvd_workspace_size(151936, 2, torch.bfloat16) == \
-        2 * 151936 * 4 + 2 * 2 * 594 * 8
+        2 * 151936 * 6 + 2 * 2 * 594 * 8
     assert lib.fused_linear_ce_tvd_workspace_size(100, 4, 7) == 0
     assert lib.fused_linear_ce_tvd_workspace_size(0, 4, 1) == 0
     f = lib.fused_linear_ce_tvd_forward_backward
@@ -306,7 +307,7 @@ def test_fused_linear_workspace_sizes_and_argument_checks(lib):
     args = [FAKE, 64, FAKE + (1 << 30), 64, 64, FAKE + (2 << 30), 64, FAKE + (3 << 30), 64, 64,
             FAKE + (4 << 30), 4, 100, -100, base, base + 256, 1,
             base + 512, base + 768, base + 1024, base + 1280, base + 1536,
-            FAKE + (5 << 30), 64, FAKE + (7 << 30), 64, 1, FAKE + (8 << 30), 4 * 104 * 4 + 64, 4,
+            FAKE + (5 << 30), 64, FAKE + (7 << 30), 64, 1, FAKE + (8 << 30), 4 * 104 * 6 + 64, 4,
             None, None]
 
     def call(**kw):
@@ -315,8 +316,8 @@ def test_fused_linear_workspace_sizes_and_argument_checks(lib):
             a[int(i[1:])] = v
         return f(*a)
     assert call(a26=7) == UNSUPPORTED                 # unknown logits dtype
-    assert call(a28=4 * 104 * 4 + 63) == INVALID      # bf16 workspace one byte short
-    assert call(a26=0) == INVALID                     # fp32 blocks need 4 * 104 * 10 + 64
+    assert call(a28=4 * 104 * 6 + 63) == INVALID      # bf16 workspace one byte short
+    assert call(a26=0) == INVALID                     # fp32 blocks need 4 * 104 * 12 + 64
     assert call(a27=FAKE + (8 << 30) + 16) == ALIGN   # workspace not 256-byte aligned
     assert call(a11=0, a26=7) == UNSUPPORTED          # the dtype is checked first
     assert call(a11=0) == OK                          # empty batch
@@ -361,7 +362,7 @@ def test_fused_linear_needs_tma_aligned_operands(lib):
     args = [FAKE, 64, FAKE + (1 << 30), 64, 64, FAKE + (2 << 30), 64, FAKE + (3 << 30), 64, 64,
             FAKE + (4 << 30), 4, 100, -100, base, base + 256, 1,
             base + 512, base + 768, base + 1024, base + 1280, base + 1536,
-            FAKE + (5 << 30), 64, FAKE + (7 << 30), 64, 1, FAKE + (8 << 30), 4 * 104 * 4 + 64, 4,
+            FAKE + (5 << 30), 64, FAKE + (7 << 30), 64, 1, FAKE + (8 << 30), 4 * 104 * 6 + 64, 4,
             None, None]
 
     def call(**kw):
