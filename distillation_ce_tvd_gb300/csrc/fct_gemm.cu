@@ -35,6 +35,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 
@@ -64,6 +65,8 @@ constexpr size_t kGemmSmem =
 // Output kinds: fp32 C, bf16 C, fp32 C accumulated into, and fp32 or bf16
 // C with each row's base-2 log-sum-exp state over each 256-column tile
 // (GemmArgs::lse_part), taken on the values as stored.
+static_assert(kBN == kGemmLseTile, "one log-sum-exp state per pair tile column block");
+
 enum COut { kOutF32 = 0, kOutBf16 = 1, kOutAddF32 = 2, kOutF32Lse = 3, kOutBf16Lse = 4 };
 template <int kOut>
 constexpr bool kBf16C = kOut == kOutBf16 || kOut == kOutBf16Lse;
@@ -773,6 +776,15 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// Bytes of one part's fp32 slab of an M x N result: rows padded to the M
+// tiles' extent, row length to a multiple of 4; 0 if that overflows.
+constexpr int kMaxSplits = 8;
+size_t split_slab_bytes(int64_t M, int64_t N) {
+  const uint64_t rows = uint64_t((M + kBM - 1) / kBM) * kBM, cols = uint64_t((N + 3) / 4 * 4);
+  if (rows == 0 || cols == 0 || rows > SIZE_MAX / cols / sizeof(float)) return 0;
+  return size_t(rows * cols * sizeof(float));
+}
+
 // Parts of K for a GEMM of `tiles` pair tiles: split when the tiles alone
 // leave pairs idle in the last round (under 90% of the rounds busy), each
 // part keeping at least 16 K blocks, the slabs fitting the workspace, and
@@ -786,8 +798,8 @@ int plan_splits(int64_t tiles, int k_iters, int pairs, size_t ws_bytes, size_t s
   int best = 1;
   double best_busy = busy(1);
   if (best_busy >= 0.9) return 1;
-  for (int S = 2; S <= 8; ++S) {
-    if (k_iters < 16 * S || size_t(S) * slab_bytes > ws_bytes) break;
+  for (int S = 2; S <= kMaxSplits; ++S) {
+    if (k_iters < 16 * S || slab_bytes > ws_bytes / size_t(S)) break;
     const double b = busy(S);
     if (b > best_busy + 0.04) {
       best = S;
@@ -831,7 +843,7 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
     int pairs = prepare<false, false, kOutF32>(dev);
     if (pairs > max_pairs) pairs = max_pairs;
     splits = plan_splits(m_tiles * n_tiles, k_iters, pairs, split_ws_bytes,
-                         size_t(slab_rows) * size_t(slab_ld) * sizeof(float));
+                         split_slab_bytes(M, N));
   }
   if (splits > 1) {
     const int k_per = (k_iters + splits - 1) / splits;
@@ -882,8 +894,8 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
 }
 
 size_t gemm_split_workspace_bytes(int64_t M, int64_t N) {
-  const int64_t m_tiles = (M + kBM - 1) / kBM;
-  return size_t(8) * size_t(m_tiles * kBM) * size_t((N + 3) / 4 * 4) * sizeof(float);
+  const size_t slab = split_slab_bytes(M, N);
+  return slab <= SIZE_MAX / kMaxSplits ? size_t(kMaxSplits) * slab : 0;
 }
 
 }  // namespace fct

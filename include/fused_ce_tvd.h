@@ -475,7 +475,7 @@ int fct_gemm_bf16(const void* A, int64_t lda, int32_t a_mn_major,
                   void* workspace, size_t workspace_bytes, int32_t* dev_status,
                   void* stream);
 /* Bytes of workspace for every K split of an M x N product; 0 for M or N
- * outside [1, 2^31). */
+ * outside [1, 2^31) or a size that does not fit a size_t. */
 size_t fct_gemm_bf16_workspace_size(int64_t M, int64_t N);
 
 /*

@@ -354,6 +354,7 @@ def test_gemm_argument_checks(lib):
     # every split of a 300 x 1003 product: 8 parts of 512 padded rows x 1004 fp32
     assert lib.fct_gemm_bf16_workspace_size(300, 1003) == 8 * 512 * 1004 * 4
     assert lib.fct_gemm_bf16_workspace_size(0, 5) == 0
+    assert lib.fct_gemm_bf16_workspace_size((1 << 31) - 1, (1 << 31) - 1) == 0  # overflows
 
 
 def test_fused_linear_needs_tma_aligned_operands(lib):
