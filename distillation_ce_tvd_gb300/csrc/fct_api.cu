@@ -621,7 +621,8 @@ size_t fused_linear_ce_tvd_workspace_size(int64_t V, int64_t chunk_rows,
                                           fct_dtype logits_dtype) {
   if (V <= 0 || chunk_rows <= 0) return 0;
   if (logits_dtype != FCT_F32 && logits_dtype != FCT_BF16) return 0;
-  return fct::linear_workspace_bytes(V, chunk_rows, logits_dtype);
+  const size_t b = fct::linear_workspace_bytes(V, chunk_rows, logits_dtype);
+  return b == SIZE_MAX ? 0 : b;
 }
 
 int fused_linear_ce_tvd_forward_backward(

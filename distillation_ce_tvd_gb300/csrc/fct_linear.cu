@@ -17,6 +17,8 @@
 // those instead of reading the block for its step 1: two passes over the
 // block instead of three, and only the student stays in L2 between them.  Only the block's logits and gradient exist at a time.  The
 // teacher is frozen (no gradients).
+#include <cstdint>
+
 #include "fct_common.cuh"
 #include "fct_internal.h"
 
@@ -33,10 +35,14 @@ size_t linear_workspace_bytes(int64_t V, int64_t chunk_rows, int logits_dtype) {
   // teacher block; fp32: the student and teacher blocks, then two bf16
   // logit-gradient blocks; then the student's and the teacher's
   // log-sum-exp partials
-  const size_t per_entry = logits_dtype == FCT_BF16 ? 3 * sizeof(uint16_t)
-                                                    : 2 * sizeof(float) + 2 * sizeof(uint16_t);
-  return size_t(chunk_rows) * size_t(linear_logits_ld(V)) * per_entry +
-         2 * size_t(chunk_rows) * size_t(linear_lse_parts(V)) * sizeof(float2);
+  // SIZE_MAX when the size does not fit a size_t (no workspace can hold it)
+  const uint64_t per_entry = logits_dtype == FCT_BF16 ? 3 * sizeof(uint16_t)
+                                                      : 2 * sizeof(float) + 2 * sizeof(uint16_t);
+  const uint64_t rows = uint64_t(chunk_rows);
+  const uint64_t row_bytes = uint64_t(linear_logits_ld(V)) * per_entry +
+                             2 * uint64_t(linear_lse_parts(V)) * sizeof(float2);
+  if (chunk_rows <= 0 || V <= 0 || row_bytes > SIZE_MAX / rows) return SIZE_MAX;
+  return size_t(rows * row_bytes);
 }
 
 cudaError_t launch_linear(const LinArgs& a, const FwdPlan& plan, int device, int sms,

@@ -348,7 +348,8 @@ int fused_ce_tvd_forward_backward_host(
  *                    row blocks (one read-modify-write of the fp32 (V, d)
  *                    matrix per 2 * chunk_rows rows).
  *                    fused_linear_ce_tvd_workspace_size returns 0 for V <= 0,
- *                    chunk_rows <= 0 or an unknown dtype.
+ *                    chunk_rows <= 0, an unknown dtype or a size that does
+ *                    not fit a size_t.
  * The logits GEMMs' epilogue also writes each row's log-sum-exp as base-2
  * (max, sum) states per 256 logit columns (in the workspace), so the loss
  * kernel takes step 1 of "Forward Pass" from those states and reads each

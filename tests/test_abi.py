@@ -301,6 +301,7 @@ def test_fused_linear_workspace_sizes_and_argument_checks(lib):
     assert binding.fused_linear_ce_tvd_workspace_size(151936, 2, torch.bfloat16) == \
         2 * 151936 * 6 + 2 * 2 * 594 * 8
     assert lib.fused_linear_ce_tvd_workspace_size(100, 4, 7) == 0
+    assert lib.fused_linear_ce_tvd_workspace_size((1 << 31) - 1, (1 << 31) - 1, 1) == 0  # overflows
     assert lib.fused_linear_ce_tvd_workspace_size(0, 4, 1) == 0
     f = lib.fused_linear_ce_tvd_forward_backward
     base = FAKE + (6 << 30)
