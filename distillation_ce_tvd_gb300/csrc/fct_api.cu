@@ -420,9 +420,11 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
       (grad_h_s && !span_fits(BT, ld_ghs, d_s, 2)) ||
       (grad_w_s && !span_fits(V, ld_gws, d_s, 4)) || !span_fits(1, BT, BT, 8))
     return FCT_ERR_UNSUPPORTED;
-  const int64_t kInt = 2147483647;  // the GEMM's tile coordinates are 32-bit
-  if (V > kInt || d_s > kInt || d_t > kInt || ld_hs > kInt || ld_ws > kInt || ld_ht > kInt ||
-      ld_wt > kInt || ld_ghs > kInt || ld_gws > kInt || chunk_rows > kInt)
+  // the GEMMs' dimensions (V, d, and up to two row blocks as K) within the
+  // range of their 32-bit tile coordinates
+  const int64_t kDim = fct::kGemmMaxDim;
+  if (V > kDim || d_s > kDim || d_t > kDim || ld_hs > kDim || ld_ws > kDim || ld_ht > kDim ||
+      ld_wt > kDim || ld_ghs > kDim || ld_gws > kDim || chunk_rows > kDim / 2)
     return FCT_ERR_UNSUPPORTED;
   if (!h_s || !w_s || !h_t || !w_t || !target || !grad_ce || !grad_tvd || !workspace)
     return FCT_ERR_INVALID_ARG;
@@ -487,8 +489,8 @@ int gemm_impl(const void* A, int64_t lda, int32_t a_mn, const void* B, int64_t l
   if (M < 0 || N < 0 || K < 1) return FCT_ERR_INVALID_ARG;
   if (M == 0 || N == 0) return FCT_OK;
   // TMA coordinates and box origins are 32-bit
-  const int64_t kMax = int64_t(1) << 31;
-  if (M >= kMax || N >= kMax || K >= kMax) return FCT_ERR_UNSUPPORTED;
+  if (M > fct::kGemmMaxDim || N > fct::kGemmMaxDim || K > fct::kGemmMaxDim)
+    return FCT_ERR_UNSUPPORTED;
   if (!A || !B || !C) return FCT_ERR_INVALID_ARG;
   // A: M x K, B: N x K; each stored as lines of its contiguous extent
   const int64_t a_lines = a_mn ? K : M, a_cols = a_mn ? M : K;

@@ -820,6 +820,7 @@ cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int
                         cudaStream_t st, void* split_ws, size_t split_ws_bytes, float2* lse_part,
                         int64_t lse_ld) {
   if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+  if (M > kGemmMaxDim || N > kGemmMaxDim || K > kGemmMaxDim) return cudaErrorInvalidValue;
   if (!gemm_operand_ok(A.ptr, A.ld) || !gemm_operand_ok(B.ptr, B.ld) || sms <= 0)
     return cudaErrorInvalidValue;
   if (c_kind < kOutF32 || c_kind > kOutBf16Lse) return cudaErrorInvalidValue;

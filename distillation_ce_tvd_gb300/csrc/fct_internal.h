@@ -186,6 +186,9 @@ bool gemm_operand_ok(const void* p, int64_t ld);
 // at lse_part[row * lse_ld + t] (lse_ld >= the number of tiles), on the
 // values as stored.
 constexpr int kGemmLseTile = 256;
+// Largest M, N or K: tile and box coordinates are 32-bit, and a tile's last
+// rows (up to 1023 past its first) must not wrap.
+constexpr int64_t kGemmMaxDim = (int64_t(1) << 31) - 1024;
 cudaError_t launch_gemm(const GemmOperand& A, const GemmOperand& B, void* C, int64_t ldc,
                         int c_kind, int64_t M, int64_t N, int64_t K, int32_t* status, int sms,
                         cudaStream_t st, void* split_ws = nullptr, size_t split_ws_bytes = 0,

@@ -350,6 +350,8 @@ int fused_ce_tvd_forward_backward_host(
  *                    fused_linear_ce_tvd_workspace_size returns 0 for V <= 0,
  *                    chunk_rows <= 0, an unknown dtype or a size that does
  *                    not fit a size_t.
+ * V, d_*, the row strides and 2 * chunk_rows are GEMM dimensions: at most
+ * 2^31 - 1024 each, else FCT_ERR_UNSUPPORTED.
  * The logits GEMMs' epilogue also writes each row's log-sum-exp as base-2
  * (max, sum) states per 256 logit columns (in the workspace), so the loss
  * kernel takes step 1 of "Forward Pass" from those states and reads each
@@ -446,8 +448,8 @@ int fused_linear_ce_tvd_forward_backward_noalloc(
  *            least the contiguous extent, else FCT_ERR_INVALID_ARG.
  *   C        : row-major M x N, row stride ldc >= N, aligned to its element;
  *            must not overlap A or B (FCT_ERR_INVALID_ARG).
- *   M, N >= 0 (0: nothing to do, FCT_OK), K >= 1; M, N, K < 2^31, else
- *            FCT_ERR_UNSUPPORTED.
+ *   M, N >= 0 (0: nothing to do, FCT_OK), K >= 1; M, N, K at most
+ *            2^31 - 1024, else FCT_ERR_UNSUPPORTED.
  *   workspace, workspace_bytes: optional (NULL, 0) device memory, 16-byte
  *            aligned, not overlapping A, B or C.  With it, a product whose
  *            output tiles (256 x 256) are too few to keep every SM pair

@@ -349,6 +349,7 @@ def test_gemm_argument_checks(lib):
     assert call(a7=299) == INVALID                    # ldc < N
     assert call(a6=A + 64) == INVALID                 # C overlaps A
     assert call(a11=1 << 31) == UNSUPPORTED           # 32-bit tile coordinates
+    assert call(a9=(1 << 31) - 1000) == UNSUPPORTED   # a last tile's rows would wrap
     assert call(a13=1024) == INVALID                  # workspace bytes without a workspace
     assert call(a12=FAKE + (3 << 30) + 8, a13=1024) == ALIGN
     assert call(a12=C + 64, a13=1024) == INVALID      # workspace overlaps C
