@@ -911,6 +911,6 @@ size_t fct_gemm_bf16_workspace_size(int64_t M, int64_t N) {
   return fct::gemm_split_workspace_bytes(M, N);
 }
 
-int fct_version(void) { return 400; }  // 0.4.0: per-call fct_options, no process-wide knob
+int fct_version(void) { return 500; }  // 0.5.0: tensor-core GEMM entry point, lse partials in the fused-linear workspace
 
 }  // extern "C"

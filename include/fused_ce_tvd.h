@@ -633,7 +633,9 @@ const char* fct_status_string(int status);
 /* Library version as 10000*major + 100*minor + patch.  300 and later: the
  * fused-linear entry point and its workspace query take logits_dtype.  400
  * and later: tuning goes through fct_options on the _ex entry points (no
- * process-wide knob). */
+ * process-wide knob).  500 and later: fct_gemm_bf16 and its workspace query;
+ * the fused-linear workspace also holds the log-sum-exp partials of the
+ * logits GEMMs (query its size again). */
 int fct_version(void);
 
 #ifdef __cplusplus

@@ -325,6 +325,7 @@ def test_fused_linear_workspace_sizes_and_argument_checks(lib):
 
 
 def test_gemm_argument_checks(lib):
+    assert binding.version() >= 500  # the GEMM entry point and its workspace query
     f = lib.fct_gemm_bf16
     A, B, C = FAKE, FAKE + (1 << 30), FAKE + (2 << 30)
     # A: M x K = 100 x 64 K-major (ld 64); B: N x K = 300 x 64 K-major; C: 100 x 300 fp32
