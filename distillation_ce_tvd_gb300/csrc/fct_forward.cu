@@ -881,17 +881,41 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Which steps each pass of a row stages in the ring, shared by the producer
+// and the consumers.  The passes by role: 0 = step 1 (log-sum-exp; absent
+// when the states are given), 1 = step 2 (sums and sign bits), 2 = step 3
+// (gradient).  Each pass stages its steps in increasing order, except:
+// * c1: step 1's last c1 steps stay in their slots; step 2 computes them
+//   first and stages only [0, n - c1).
+// * c3: step 2's last c3 staged steps [a3, a3 + c3), a3 = n - c1 - c3, stay
+//   in the slots' student halves; step 3 (student only, on sign bits)
+//   computes them first and stages its other steps into the teacher halves.
+// Each carried step is read from L2 once less per row.
+struct RingPlan {
+  int n;          // steps per pass
+  int c1, c3;     // steps carried from step 1 to 2, from step 2 to 3
+  bool teacher3;  // step 3 stages the teacher (no sign bits)
+  __device__ int a3() const { return n - c1 - c3; }
+  __device__ bool staged3(int q) const { return q < a3() || q >= n - c1; }
+};
+
 // The producer lane: walks the consumers' sequence (rows of this CTA that
-// are not ignored; per row kPasses passes of n_steps steps; the teacher in
-// the first passes_t passes) and fills ring slot t % kST for step t.  In the
-// first pass (from HBM) it also asks L2 for the chunks kPref steps ahead, so
-// more of the row is on its way than the ring holds.
-template <int NT, int kPasses, int kPS, int kST, int kPref, typename T>
+// are not ignored; per row the passes of kRole0..kRoles-1, each staging the
+// steps RingPlan gives) and fills ring slot t % kST for fill t.  In the first
+// pass (from HBM) it also asks L2 for the chunks kPref steps ahead, so more
+// of the row is on its way than the ring holds.  Each tensor's step is read
+// with evict_last (or evict_normal) while a later pass of the row stages it
+// again, else with evict_first.  With c3 > 0 a row's first fill also waits
+// until the consumers have computed the previous row's steps carried into
+// its step 3 (carry_bar): those sit in the student halves the fill would
+// overwrite.
+template <int NT, int kPS, int kST, int kPref, int kRole0, int kRoles, typename T>
 __device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_bar,
-                            uint64_t* empty_bar, volatile int* abort, int64_t nvec, int n_steps,
-                            int passes_t) {
+                            uint64_t* empty_bar, uint64_t* carry_bar, volatile int* abort,
+                            int64_t nvec, RingPlan rp) {
   constexpr int kStepVecs = kPS * NT;
   constexpr uint32_t kTensorBytes = kStepVecs * 16;
+  constexpr bool kStep3 = kRoles == 3;
   const uint64_t keep = p.keep_normal ? policy_evict_normal() : policy_evict_last();
   const uint64_t drop = policy_evict_first();
   const uint32_t ring = smem_addr(ring_mem);
@@ -906,37 +930,42 @@ __device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_ba
     const int64_t v0 = int64_t(q) * kStepVecs;
     return static_cast<uint32_t>(((nvec - v0 < kStepVecs) ? nvec - v0 : kStepVecs) * 16);
   };
-  uint32_t t = 0;
-  bool ok = n_steps > 0;
+  uint32_t t = 0, rows_carried = 0;
+  bool ok = rp.n > 0;
   for (int64_t row = blockIdx.x; ok && row < p.BT; row += gridDim.x) {
     if (p.target[row] == p.ignore_index) continue;
+    if (rows_carried > 0 && !mbar_wait(carry_bar, (rows_carried - 1) & 1, abort)) break;
     const char* srow = static_cast<const char*>(p.student) + row * p.ld_s * int64_t(sizeof(T));
     const char* trow = static_cast<const char*>(p.teacher) + row * p.ld_t * int64_t(sizeof(T));
     if constexpr (kPref > 0) {  // the first chunks of the first pass
-      for (int q = 0; q < kPref && q < n_steps; ++q) {
+      for (int q = 0; q < kPref && q < rp.n; ++q) {
         prefetch_l2(srow + int64_t(q) * kTensorBytes, chunk_bytes(q), keep);
         prefetch_l2(trow + int64_t(q) * kTensorBytes, chunk_bytes(q), keep);
       }
     }
-    for (int pass = 0; ok && pass < kPasses; ++pass) {
-      const bool with_t = pass < passes_t;
-      // keep each row in L2 until its last pass reads it
-      const uint64_t pol_s = (pass + 1 < kPasses) ? keep : drop;
-      const uint64_t pol_t = (pass + 1 < passes_t) ? keep : drop;
-      for (int q = 0; q < n_steps; ++q) {
+    for (int role = kRole0; ok && role < kRoles; ++role) {
+      const bool with_t = role < 2 || rp.teacher3;
+      const bool into_t = role == 2 && rp.c3 > 0;  // the student into the teacher halves
+      const int q_end = role == 1 ? rp.n - rp.c1 : rp.n;
+      for (int q = 0; q < q_end; ++q) {
+        if (role == 2 && !rp.staged3(q)) continue;  // carried from step 2
         const uint32_t slot = t % kST, fill = t / kST;
         if (fill > 0 && !mbar_wait(&empty_bar[slot], (fill - 1) & 1, abort)) {
           ok = false;
           break;
         }
+        // staged again by a later pass of this row?
+        const bool again2 = role == 0 && q < rp.n - rp.c1;
+        const bool s_again = again2 || (kStep3 && role < 2 && rp.staged3(q));
+        const bool t_again = again2 || (kStep3 && role < 2 && rp.teacher3);
         const int64_t off = int64_t(q) * kTensorBytes;
         const uint32_t bytes = chunk_bytes(q);
         mbar_arrive_expect_tx(&full_bar[slot], with_t ? 2 * bytes : bytes);
-        const uint32_t dst = ring + slot * (2 * kTensorBytes);
-        bulk_load(dst, srow + off, bytes, &full_bar[slot], pol_s);
-        if (with_t) bulk_load(dst + kTensorBytes, trow + off, bytes, &full_bar[slot], pol_t);
+        const uint32_t dst = ring + slot * (2 * kTensorBytes) + (into_t ? kTensorBytes : 0);
+        bulk_load(dst, srow + off, bytes, &full_bar[slot], s_again ? keep : drop);
+        if (with_t) bulk_load(dst + kTensorBytes, trow + off, bytes, &full_bar[slot], t_again ? keep : drop);
         if constexpr (kPref > 0) {
-          if (pass == 0 && q + kPref < n_steps) {
+          if (role == kRole0 && q + kPref < rp.n) {
             const int64_t pf = int64_t(q + kPref) * kTensorBytes;
             prefetch_l2(srow + pf, chunk_bytes(q + kPref), keep);
             prefetch_l2(trow + pf, chunk_bytes(q + kPref), keep);
@@ -945,6 +974,7 @@ __device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_ba
         ++t;
       }
     }
+    if (rp.c3 > 0) ++rows_carried;
   }
   // No copy may still be landing when this CTA exits: wait (bounded, even
   // after an abort) for the last fills.
@@ -955,35 +985,42 @@ __device__ void tma_produce(const FwdArgs& p, uint4* ring_mem, uint64_t* full_ba
 // kPS: 16-byte vectors per thread per tensor in one step (a step moves
 // kPS * NT contiguous vectors of each tensor); kST: ring slots; kPref: L2
 // prefetch distance of the first pass, in steps (0 = none).
-// kEarly: 1 = in every pass, 2 = in the first pass only (the one fed from
-// HBM), each warp copies its cells of a step into registers and releases the
-// slot before computing on them, so the slot can be refilling while the
-// warps compute; 0 = release after computing.
 // kSigns: the forward alone also stores each element's sign bit and a per-row
 // tie flag for the backward (sign words, as forward_pipelined does).
 // kLseIn: the single launch with step 1's per-row states given as partials
 // (FwdArgs::lse_part_s/t): two passes over the row, the first one fed from
 // HBM, and the teacher only in the first when step 3 runs on sign bits, so
 // L2 holds just the student between the passes.
+// kCarry1, kCarry3: steps carried from step 1 into step 2 (RingPlan::c1; at
+// most kST - 1, so one slot stays free for step 2's first fill, and only
+// with one step per sign word) and from step 2 into step 3 (RingPlan::c3,
+// when step 3 runs on sign bits).  Carried steps are computed first in the
+// pass they are carried into.  The step order of step 2, and so the rounding
+// of its sums, depends only on the row's length, the same in the forward
+// alone and in the single launch; step 3's order does not change any value.
 template <typename T, int VE, bool kGrad, int NT, typename TG, int kPS, int kST, int kPref,
-          int kEarly, bool kSigns = false, bool kLseIn = false>
+          bool kSigns = false, bool kLseIn = false, int kCarry1 = 0, int kCarry3 = 0>
 __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
   static_assert(kPS >= 1 && kPS <= kPerStep, "steps of at most kPerStep vectors per thread");
   static_assert(!kSigns || !kGrad, "sign words come from the forward alone");
   static_assert(!kLseIn || kGrad, "given log-sum-exp states: the single launch only");
+  static_assert(kCarry1 >= 0 && kCarry1 < kST, "a free slot for step 2's first fill");
+  static_assert(kCarry3 >= 0 && kCarry3 <= kST, "at most one carried step per slot");
   constexpr bool kWord = kGrad || kSigns;  // step 2 builds sign words
-  constexpr int kPasses = (kGrad ? 3 : 2) - (kLseIn ? 1 : 0);
   constexpr int kStepVecs = kPS * NT;       // 16-byte vectors per tensor per step
   constexpr int kSlotVecs = 2 * kStepVecs;  // student then teacher
   // step 2's sign bits: kBits per step, kSpw steps per 32-bit word
   constexpr int kBits = kPS * VE;
   static_assert(32 % kBits == 0, "whole steps per sign word");
   constexpr int kSpw = 32 / kBits;
+  // step 2 out of order only where each step has a sign word of its own
+  constexpr int kC1 = (kLseIn || kSpw != 1) ? 0 : kCarry1;
   extern __shared__ __align__(128) uint4 bulk_ring[];
   __shared__ __align__(8) uint64_t full_bar[kST];
   __shared__ __align__(8) uint64_t empty_bar[kST];
   __shared__ float4 red_lse[kMaxWarps];
   __shared__ float2 red_sum[kMaxWarps];
+  __shared__ __align__(8) uint64_t carry_bar;  // the steps carried into step 3 have been read
   __shared__ int abort_flag;
 
   const int tid = threadIdx.x;
@@ -991,21 +1028,26 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
   const int64_t tail0 = nvec * VE;
   const int n_steps = static_cast<int>((nvec + kStepVecs - 1) / kStepVecs);
   const bool use_bits = kGrad && n_steps <= kMaxSignWords * kSpw;
-  const int passes_t = use_bits ? kPasses - 1 : kPasses;  // passes that stage the teacher
+  RingPlan rp;
+  rp.n = n_steps;
+  rp.c1 = n_steps >= kC1 + kST ? kC1 : 0;
+  rp.c3 = use_bits ? (n_steps - rp.c1 < kCarry3 ? n_steps - rp.c1 : kCarry3) : 0;
+  rp.teacher3 = kGrad && !use_bits;
 
   if (tid == 0) {
     for (int s = 0; s < kST; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], NT / 32);
     }
+    mbar_init(&carry_bar, NT / 32);
     abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();  // the last CTA-wide barrier: from here the producer runs on its own
   if (tid >= NT) {
     if (tid == NT)
-      tma_produce<NT, kPasses, kPS, kST, kPref, T>(p, bulk_ring, full_bar, empty_bar,
-                                                  &abort_flag, nvec, n_steps, passes_t);
+      tma_produce<NT, kPS, kST, kPref, kLseIn ? 1 : 0, kGrad ? 3 : 2, T>(
+          p, bulk_ring, full_bar, empty_bar, &carry_bar, &abort_flag, nvec, rp);
     return;
   }
 
@@ -1017,50 +1059,77 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
   const int cnt_last = static_cast<int>(cnt_all < kPS ? cnt_all : kPS);
   const uint4* mine = bulk_ring + tid;
   uint32_t* sbits = reinterpret_cast<uint32_t*>(bulk_ring + kST * kSlotVecs);
-  uint32_t slot = 0, parity = 0;
-  // One pass over the row: fn(cell_s, cell_t, n, q) for each step q, with
-  // this thread's n vectors of the step as cell_s(u) (student) and cell_t(u)
-  // (teacher, when the pass stages it), u < n.
-  struct Regs {  // a step's cells copied into registers
-    uint4 v[2 * kPS];
+  uint32_t slot = 0, parity = 0;  // the next fill's slot and phase
+  // fn(cell_s, cell_t, n, q) on step q, with this thread's n vectors of the
+  // step as cell_s(u) (student) and cell_t(u) (teacher), u < n
+  auto run = [&](const uint4* cells_s, const uint4* cells_t, int q, auto&& fn) {
+    auto cs = [&](int u) { return cells_s[u * NT]; };
+    auto ct = [&](int u) { return cells_t[u * NT]; };
+    if (q + 1 < n_steps || cnt_last == kPS) {
+      fn(cs, ct, Count<kPS>{}, q);
+    } else {
+      fn(cs, ct, cnt_last, q);
+    }
   };
-  auto pass = [&](bool with_t, auto early, auto&& fn) {
+  auto arrive = [&](uint64_t* bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
+  // the next fill: wait for it, return its slot, move on
+  auto next_fill = [&]() {
+    const uint32_t k = slot;
+    mbar_wait(&full_bar[k], parity, &abort_flag);
+    if (++slot == kST) {
+      slot = 0;
+      parity ^= 1u;
+    }
+    return k;
+  };
+  // slot of the j-th of the last c fills
+  auto recent = [&](int c, int j) { return (slot + kST - c + j) % kST; };
+  auto cells = [&](uint32_t k) { return mine + k * kSlotVecs; };
+  // step 1: every step in order; the last c1 slots are kept for step 2
+  auto pass1 = [&](auto&& fn) {
     for (int q = 0; q < n_steps; ++q) {
-      mbar_wait(&full_bar[slot], parity, &abort_flag);
-      const uint4* cells = mine + slot * kSlotVecs;
-      const bool full = q + 1 < n_steps || cnt_last == kPS;
-      if constexpr (decltype(early)::value) {
-        Regs r;
-#pragma unroll
-        for (int u = 0; u < kPS; ++u) {
-          if (full || u < cnt_last) {
-            r.v[u] = cells[u * NT];
-            if (with_t) r.v[kPS + u] = cells[kStepVecs + u * NT];
-          }
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
-        auto cs = [&](int u) { return r.v[u]; };
-        auto ct = [&](int u) { return r.v[kPS + u]; };
-        if (full) {
-          fn(cs, ct, Count<kPS>{}, q);
-        } else {
-          fn(cs, ct, cnt_last, q);
-        }
-      } else {
-        auto cs = [&](int u) { return cells[u * NT]; };
-        auto ct = [&](int u) { return cells[kStepVecs + u * NT]; };
-        if (full) {
-          fn(cs, ct, Count<kPS>{}, q);
-        } else {
-          fn(cs, ct, cnt_last, q);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      const uint32_t k = next_fill();
+      run(cells(k), cells(k) + kStepVecs, q, fn);
+      if (q < n_steps - rp.c1) arrive(&empty_bar[k]);
+    }
+  };
+  // step 2: step 1's last c1 steps, then the others in order
+  auto pass2 = [&](auto&& fn) {
+    for (int j = 0; j < rp.c1; ++j) {
+      const uint32_t k = recent(rp.c1, j);
+      run(cells(k), cells(k) + kStepVecs, n_steps - rp.c1 + j, fn);
+      arrive(&empty_bar[k]);
+    }
+    for (int q = 0; q < n_steps - rp.c1; ++q) {
+      const uint32_t k = next_fill();
+      run(cells(k), cells(k) + kStepVecs, q, fn);
+      arrive(&empty_bar[k]);
+    }
+  };
+  // step 3: with c3 > 0, step 2's last c3 steps from the slots' student
+  // halves, then the others from the teacher halves (the teacher is not
+  // staged: cell_t is cell_s); else every step in order
+  auto pass3 = [&](auto&& fn) {
+    if (rp.c3 > 0) {
+      for (int j = 0; j < rp.c3; ++j) {
+        const uint4* c = cells(recent(rp.c3, j));
+        run(c, c, rp.a3() + j, fn);
       }
-      if (++slot == kST) {
-        slot = 0;
-        parity ^= 1u;
+      arrive(&carry_bar);
+      for (int q = 0; q < n_steps; ++q) {
+        if (!rp.staged3(q)) continue;
+        const uint32_t k = next_fill();
+        run(cells(k) + kStepVecs, cells(k) + kStepVecs, q, fn);
+        arrive(&empty_bar[k]);
+      }
+    } else {
+      for (int q = 0; q < n_steps; ++q) {
+        const uint32_t k = next_fill();
+        run(cells(k), cells(k) + kStepVecs, q, fn);
+        arrive(&empty_bar[k]);
       }
     }
   };
@@ -1119,11 +1188,10 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
       }
     } else {
       Lse2x a = lse2x_empty(), b = lse2x_empty();
-      pass(true, std::integral_constant<bool, kEarly != 0>{},
-           [&](auto&& cs, auto&& ct, auto n, int) {
-             lse_step_get<T, VE>(a, cs, n);
-             lse_step_get<T, VE>(b, ct, n);
-           });
+      pass1([&](auto&& cs, auto&& ct, auto n, int) {
+        lse_step_get<T, VE>(a, cs, n);
+        lse_step_get<T, VE>(b, ct, n);
+      });
       fa = lse2x_fold(a);
       fb = lse2x_fold(b);
       if (tail0 + tid < p.V) {
@@ -1145,7 +1213,7 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
     float2 sp2 = make_float2(0.f, 0.f), sq2 = make_float2(0.f, 0.f);
     uint32_t tie_and = 0xffffffffu;
     [[maybe_unused]] uint32_t packed = 0;  // sign bits of the steps of the current word
-    pass(true, std::integral_constant<bool, kEarly == 1>{}, [&](auto&& cs, auto&& ct, auto n, int q) {
+    pass2([&](auto&& cs, auto&& ct, auto n, int q) {
       [[maybe_unused]] uint32_t word = 0;
 #pragma unroll
       for (int u = 0; u < kPS; ++u) {
@@ -1236,8 +1304,7 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
         const float pp = ex2(e.x);
         return __fmul_rn(pp, fmaf(h, sgn_pq(pp, ex2(e.y)), c0));
       };
-      pass(!use_bits, std::integral_constant<bool, kEarly == 1>{},
-           [&](auto&& cs, auto&& ct, auto n, int q) {
+      auto step3 = [&](auto&& cs, auto&& ct, auto n, int q) {
         TG* gq = gmine + int64_t(q) * kStepVecs * VE;
         if (bad) {  // out-of-range target: the whole gradient row is NaN
           float nan[VE];
@@ -1287,7 +1354,8 @@ __global__ void __launch_bounds__(NT + 32, 1) forward_tma(FwdArgs p) {
             }
           }
         }
-      });
+      };
+      pass3(step3);
       if (tail0 + tid < p.V) {
         const int64_t v = tail0 + tid;
         float g = grad_of(Elem<T>::load1(srow + v), Elem<T>::load1(trow + v));
@@ -1491,8 +1559,13 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, double stagger, cudaStr
 // bf16: forward 0.956 -> 0.942 ms; the single launch was 1% slower with it).
 // Smaller steps with more slots, releasing slots before computing, and 480
 // consumers were all measured slower or equal.
+// Steps carried between passes (RingPlan): step 2's last 3 steps into step 3
+// (measured at 8192 x 151936 bf16: single launch 1.487 -> 1.474 ms, results
+// unchanged); none from step 1 into step 2 (carrying 1 or 2 steps made the
+// forward alone 0.4-0.8% faster but the single launch 1% slower, and both
+// must share step 2's order to agree bit for bit).
 constexpr int kTmaThreads = 512, kTmaPerStep = 4, kTmaStages = 3;
-constexpr int kTmaEarly = 0;
+constexpr int kTmaCarry1 = 0, kTmaCarry3 = 3;
 
 template <typename T, bool kGrad, typename TG = T, bool kSigns = false, bool kLseIn = false>
 cudaError_t run_tma(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
@@ -1501,8 +1574,8 @@ cudaError_t run_tma(const FwdArgs& a, const FwdPlan& plan, cudaStream_t st) {
   constexpr size_t kSmem = size_t(kTmaStages) * 2 * kTmaPerStep * NT * 16 +
                            (kGrad ? size_t(kMaxSignWords) * NT * 4 : 0);
   constexpr int kPref = kGrad ? 0 : 4;
-  auto kernel = forward_tma<T, VE, kGrad, NT, TG, kTmaPerStep, kTmaStages, kPref, kTmaEarly,
-                            kSigns, kLseIn>;
+  auto kernel = forward_tma<T, VE, kGrad, NT, TG, kTmaPerStep, kTmaStages, kPref, kSigns, kLseIn,
+                            kTmaCarry1, kTmaCarry3>;
   static PerDevice cache;
   const int n_max = per_device(cache, [&] {
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
