@@ -702,6 +702,11 @@ def test_full_size_single_launch_every_row(name):
     (torch.float32, 3, 4, 9),
     (torch.bfloat16, 4100, None, 200),      # several rows per CTA
     (torch.bfloat16, 1000, None, 5000),     # enough rows per CTA for the start stagger
+    # step 3 takes step 2's last 3 steps from the ring: 3 steps (none left
+    # to stage), 4 steps (one), and fp32 with two steps per sign word
+    (torch.bfloat16, 40003, 40008, 400),
+    (torch.bfloat16, 60000, None, 400),
+    (torch.float32, 100003, 100004, 320),
 ])
 def test_tma_ring_single_launch_equals_forward_then_backward(dtype, V, ld, rows):
     """The producer-warp bulk-copy ring: its single launch equals its forward
