@@ -707,6 +707,8 @@ def test_full_size_single_launch_every_row(name):
     (torch.bfloat16, 40003, 40008, 400),
     (torch.bfloat16, 60000, None, 400),
     (torch.float32, 100003, 100004, 320),
+    (torch.bfloat16, 49152, None, 300),     # last step exactly full (3 steps)
+    (torch.float32, 16384, None, 300),      # last step exactly full (2 steps)
 ])
 def test_tma_ring_single_launch_equals_forward_then_backward(dtype, V, ld, rows):
     """The producer-warp bulk-copy ring: its single launch equals its forward
