@@ -759,6 +759,47 @@ def test_tma_ring_single_launch_equals_forward_then_backward(dtype, V, ld, rows)
         assert torch.equal(torch.isnan(ga.float()), torch.isnan(single[5].float()))
 
 
+def test_tma_ring_randomised_shapes():
+    """Seeded random row lengths (many near a step boundary of the ring),
+    dtypes, row strides and row counts: the bulk-copy ring's single launch
+    equals its forward + backward bit for bit, out of place and in place,
+    and the oracle on sampled rows (including an exact-tie row and an
+    ignored row)."""
+    import random
+    rng = random.Random(20261203)
+    opts = binding.options(ctas_per_row=1, ring=binding.RING_TMA)
+    names = ("ce", "tvd", "student_lse", "teacher_lse", "sigma")
+    for i in range(20):
+        dtype = rng.choice([torch.bfloat16, torch.float32])
+        ve = 8 if dtype == torch.bfloat16 else 4
+        if rng.random() < 0.5:
+            V = max(1, rng.randint(1, 20) * 2048 * ve + rng.randint(-9, 9))
+        else:
+            V = rng.randint(1, 320000)
+        ld = (V + ve - 1) // ve * ve + ve * rng.randint(0, 3)
+        rows = rng.randint(4, 600)
+        w = padded(workloads.make("bt1024_v32000_bf16", DEV, rows=rows, V=V, dtype=dtype,
+                                  seed=300 + i), ld, 0)
+        w.teacher[rows // 2] = w.student[rows // 2]
+        w.target[rows // 3] = w.ignore_index
+        single = binding.fused_ce_tvd_forward_backward(w.student, w.teacher, w.target, w.grad_ce,
+                                                       w.grad_tvd, options=opts)
+        s_in = same_layout_clone(w.student)
+        inplace = binding.fused_ce_tvd_forward_backward(s_in, w.teacher, w.target, w.grad_ce,
+                                                        w.grad_tvd, inplace=True, options=opts)
+        fwd = binding.fused_ce_tvd_forward(w.student, w.teacher, w.target, options=opts)
+        g2 = binding.fused_ce_tvd_backward(w.student, w.teacher, w.target, *fwd[2:], w.grad_ce,
+                                           w.grad_tvd)
+        torch.cuda.synchronize()
+        what = f"random {i} (V {V}, ld {ld}, rows {rows}) "
+        for x, y in zip(single[:5], fwd):
+            assert torch.equal(_bits(x), _bits(y)), what
+        assert torch.equal(_bits(single[5]), _bits(g2)), what
+        assert torch.equal(_bits(single[5]), _bits(inplace[5])), what
+        sample = sorted({rows // 2, rows // 3, rows - 1, *rng.sample(range(rows), min(rows, 8))})
+        compare(w, dict(zip(names, single[:5])), single[5], rows=torch.tensor(sample), what=what)
+
+
 def test_tma_ring_falls_back_on_clusters():
     # A row split over a cluster has no bulk-copy form: the call takes the
     # per-thread ring and gives its results.
