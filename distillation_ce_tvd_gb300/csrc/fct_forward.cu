@@ -1512,15 +1512,22 @@ int per_device(PerDevice& c, Init&& init) {
 // spread, in kStaggerGroups interleaved groups, over plan.stagger times an
 // estimate of one row's time (about 0.1 clock cycles per byte a CTA reads in
 // one pass of a row, measured on GB300 for the single launch at V = 151936
-// bf16), when every cluster has at least kStaggerMinRows rows (with fewer,
-// the last group's wait costs more than the spread saves).  Measured at 8192
-// x 151936 bf16, against starting together: a spread of half a row's time in
-// 8 interleaved groups, one launch 1.619 -> 1.582 ms and the forward alone
-// 2.130 -> 2.084 ms with its backward; a whole row's time, 1.579 and 2.100;
-// the same spreads over contiguous ranges of clusters gained about half as
-// much.
+// bf16), when every cluster has at least kStaggerMinRows rows (with one row
+// each, the last group's wait costs more than the spread saves).  Measured
+// at 8192 x 151936 bf16, against starting together: a spread of half a
+// row's time in 8 interleaved groups, one launch 1.619 -> 1.582 ms and the
+// forward alone 2.130 -> 2.084 ms with its backward; a whole row's time,
+// 1.579 and 2.100; the same spreads over contiguous ranges of clusters
+// gained about half as much.  With few rows per CTA (bulk-copy ring, V =
+// 151936 bf16, single launch): 304 rows 0.0865 -> 0.0785 ms, 608 rows
+// 0.159 -> 0.145, 1216 rows 0.281 -> 0.251, 2048 rows 0.443 -> 0.408; one
+// row per CTA (152 rows) 0.0527 -> 0.0564, hence at least 2.
+// Cross-entropy alone on clusters (fp32 rows of V = 256000 on 2-CTA
+// clusters) measured slower staggered at few rows per cluster (304 rows
+// 0.115 -> 0.121 ms, 1024 rows 0.373 -> 0.389), so it keeps the earlier
+// threshold of 32.
 constexpr double kStaggerCyclesPerByte = 0.1;
-constexpr int kStaggerMinRows = 32;
+constexpr int kStaggerMinRows = 2, kStaggerMinRowsCeCluster = 32;
 
 // One (kernel, configuration) instance: shared-memory opt-in and the
 // occupancy query are done once per device.
@@ -1544,7 +1551,8 @@ cudaError_t run_pipelined(const FwdArgs& a, int n_slots, double stagger, cudaStr
   if (n > a.BT) n = static_cast<int>(a.BT);
   FwdArgs b = a;
   if constexpr (kTvd || kGrad) {  // several passes per row: stagger the clusters' start
-    if (a.BT >= int64_t(kStaggerMinRows) * n) {
+    constexpr int kMinRows = (!kTvd && C > 1) ? kStaggerMinRowsCeCluster : kStaggerMinRows;
+    if (a.BT >= int64_t(kMinRows) * n) {
       const double row_bytes = (kTvd ? 2.0 : 1.0) * double(a.V) * double(sizeof(T)) / C;
       b.stagger = static_cast<int64_t>(stagger * kStaggerCyclesPerByte * row_bytes);
     }
