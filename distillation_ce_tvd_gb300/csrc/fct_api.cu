@@ -115,17 +115,24 @@ int check_options(const fct_options* o) {
 // optimum for the single launch at 8192 x 151936 bf16).
 constexpr double kDefaultStagger = 0.5;
 
-// Rows in flight and CTAs per row for the two-pass fused forward.  The
-// second pass re-reads each row from L2, so the rows in flight times the
-// bytes of a student+teacher row must stay inside L2 (80%: measured on
-// GB300, one CTA per row at V = 151936 bf16 beats splitting rows); rows are split
-// over a cluster of C CTAs until every SM still gets at least one CTA.
+// Rows in flight and CTAs per row for the multi-pass forward kernels.  A
+// later pass re-reads each row from L2, so the rows in flight times the
+// bytes of the kept row should stay near the L2 size; rows are split over a
+// cluster of C CTAs until every SM still gets at least one CTA.  The kept
+// row is student + teacher for the fused loss (tvd), the student alone for
+// cross-entropy in one launch (ce_grad), or kept_rows rows when given (the
+// fused-linear loss starts from given states and re-reads only the student).
+// Budget: 1.10 of L2 for the fused loss (measured on GB300 with staggered
+// CTAs, single launch and forward alone: one CTA per row on the bulk-copy
+// ring beats 2-CTA clusters up to 960 KB of student + teacher row, bf16
+// V = 240000 and fp32 V = 121000, by up to 30%, and loses at 1.02 MB; the
+// rows in flight are in different passes, the first one's row still
+// arriving and the third one's shrinking); 0.80 for cross-entropy alone.
 // Depends on V, the element type, the device and the call's options only
 // (never on BT), so results do not depend on how the rows are batched.
-// kept: the row re-read from L2 in a later pass is student + teacher (tvd),
-// or the student alone (cross-entropy in one launch, ce_grad).
 fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, bool vec,
-                          bool ce_grad = false, const fct_options* opts = nullptr) {
+                          bool ce_grad = false, const fct_options* opts = nullptr,
+                          int kept_rows = 0) {
   fct::FwdPlan plan{vec, 1, 0, false, kDefaultStagger, 0};
   if (opts != nullptr) {
     plan.ring = opts->ring;
@@ -134,9 +141,9 @@ fct::FwdPlan plan_forward(const DeviceInfo& d, int64_t V, int dtype, bool tvd, b
     if (opts->stagger < 0.f) plan.stagger = 0.0;
   }
   if (!tvd && !ce_grad) return plan;  // one pass: nothing to keep in L2
-  const double row_bytes =
-      (tvd ? 2.0 : 1.0) * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
-  const double budget = 0.80 * static_cast<double>(d.l2_bytes);
+  const double rows_kept = kept_rows > 0 ? double(kept_rows) : (tvd ? 2.0 : 1.0);
+  const double row_bytes = rows_kept * static_cast<double>(V) * static_cast<double>(elem_size(dtype));
+  const double budget = (tvd ? 1.10 : 0.80) * static_cast<double>(d.l2_bytes);
   int64_t fit = static_cast<int64_t>(budget / row_bytes);
   if (fit < 1) fit = 1;
   int C = opts ? opts->ctas_per_row : 0;
@@ -474,7 +481,10 @@ int linear_impl(const void* h_s, int64_t ld_hs, const void* w_s, int64_t ld_ws, 
                  ignore_index, grad_ce, grad_tvd, grad_stride, ce, tvd, lse_s, lse_t, sigma,
                  grad_h_s, ld_ghs, grad_w_s, ld_gws, workspace, chunk_rows, dev_status,
                  logits_dtype};
-  const fct::FwdPlan plan = plan_forward(d, V, logits_dtype, true, true);
+  // the loss kernel starts from the logits GEMMs' states: only the student
+  // block's row stays in L2 between its two passes (its second pass takes
+  // the signs from sign words, up to V = 262144)
+  const fct::FwdPlan plan = plan_forward(d, V, logits_dtype, true, true, false, nullptr, 1);
   if (fct::launch_linear(a, plan, dev, d.sms, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return FCT_ERR_CUDA;
   return FCT_OK;
