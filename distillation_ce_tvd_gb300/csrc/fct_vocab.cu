@@ -21,10 +21,13 @@
 // kernels (base 2, ex2, the same tie rule).
 //
 // GB300 mapping: passes 1 and 2 are one CTA of 256 threads per row
-// (persistent over rows), 16-byte vector loads (4 in flight per thread per
-// tensor) when the shard's columns start on 16 bytes, plain element loads
-// otherwise, fp32 accumulation, warp-shuffle and shared-memory reductions.
-// The merges are one thread per row.
+// (persistent over rows, as many CTAs as are resident at once), 16-byte
+// vector loads (4 in flight per thread per tensor) when the shard's columns
+// start on 16 bytes, plain element loads otherwise, fp32 accumulation,
+// warp-shuffle and shared-memory reductions.  The merges are one thread per
+// row.
+#include <mutex>
+
 #include "fct_common.cuh"
 #include "fct_internal.h"
 
@@ -237,31 +240,63 @@ __global__ void vp_merge_tvd_kernel(VpMergeArgs a) {
   }
 }
 
-int g_vp_blocks(int sms, int64_t BT) {
-  const int64_t g = int64_t(sms) * 8;  // 8 resident CTAs of 256 threads per SM
-  return static_cast<int>(BT < g ? BT : g);
+// Resident CTAs per SM of a pass kernel on the current device (its register
+// count sets it), queried once per device.  The persistent grid is exactly
+// that many CTAs per SM: with more, the CTAs beyond the resident ones start
+// only as others finish and run their rows at the end at low occupancy
+// (bf16 passes: 48 registers, 5 resident CTAs; the 2-shard step at 8192 x
+// 151936 bf16 took 2.925 ms with a grid of 8 CTAs per SM and 2.710 ms with
+// the resident count, 4096 x 256000 fp32 4.375 and 4.263 ms).
+template <typename K>
+int resident_per_sm(K kernel) {
+  static std::mutex mu;
+  static int value[64];
+  static bool done[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 1;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  if (!done[dev]) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kVpThreads, 0) != cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    value[dev] = n;
+    done[dev] = true;
+  }
+  return value[dev];
+}
+
+template <typename K>
+void launch_pass(K kernel, const VpArgs& a, int sms, cudaStream_t st) {
+  int64_t g = int64_t(sms) * resident_per_sm(kernel);
+  if (g > a.BT) g = a.BT;
+  kernel<<<static_cast<unsigned>(g), kVpThreads, 0, st>>>(a);
 }
 
 }  // namespace
 
 cudaError_t launch_vp_pass(const VpArgs& a, bool vec, bool tvd_pass, int sms, cudaStream_t st) {
   if (a.BT == 0) return cudaSuccess;
-  const int grid = g_vp_blocks(sms, a.BT);
   if (a.dtype == FCT_BF16) {
     if (tvd_pass) {
-      vec ? vp_tvd_kernel<bf16_t, 8><<<grid, kVpThreads, 0, st>>>(a)
-          : vp_tvd_kernel<bf16_t, 1><<<grid, kVpThreads, 0, st>>>(a);
+      vec ? launch_pass(vp_tvd_kernel<bf16_t, 8>, a, sms, st)
+          : launch_pass(vp_tvd_kernel<bf16_t, 1>, a, sms, st);
     } else {
-      vec ? vp_lse_kernel<bf16_t, 8><<<grid, kVpThreads, 0, st>>>(a)
-          : vp_lse_kernel<bf16_t, 1><<<grid, kVpThreads, 0, st>>>(a);
+      vec ? launch_pass(vp_lse_kernel<bf16_t, 8>, a, sms, st)
+          : launch_pass(vp_lse_kernel<bf16_t, 1>, a, sms, st);
     }
   } else {
     if (tvd_pass) {
-      vec ? vp_tvd_kernel<float, 4><<<grid, kVpThreads, 0, st>>>(a)
-          : vp_tvd_kernel<float, 1><<<grid, kVpThreads, 0, st>>>(a);
+      vec ? launch_pass(vp_tvd_kernel<float, 4>, a, sms, st)
+          : launch_pass(vp_tvd_kernel<float, 1>, a, sms, st);
     } else {
-      vec ? vp_lse_kernel<float, 4><<<grid, kVpThreads, 0, st>>>(a)
-          : vp_lse_kernel<float, 1><<<grid, kVpThreads, 0, st>>>(a);
+      vec ? launch_pass(vp_lse_kernel<float, 4>, a, sms, st)
+          : launch_pass(vp_lse_kernel<float, 1>, a, sms, st);
     }
   }
   return cudaGetLastError();
