@@ -99,7 +99,7 @@ class FusedLinearCETVDMeanLoss(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, h_student, w_student, h_teacher, w_teacher, target,
-                ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0, chunk_rows=1024,
+                ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0, chunk_rows=2048,
                 logits_dtype=torch.float32):
         gce, gtvd, _ = binding.fused_ce_tvd_mean_upstream(target, ignore_index, alpha, beta)
         ce, tvd, _, _, _, grad_h, grad_w = binding.fused_linear_ce_tvd_forward_backward(
@@ -121,7 +121,7 @@ class FusedLinearCETVDMeanLoss(torch.autograd.Function):
 
 def fused_linear_ce_tvd_mean_loss(h_student, w_student, h_teacher, w_teacher, target,
                                   ignore_index=binding.IGNORE_INDEX, alpha=1.0, beta=1.0,
-                                  chunk_rows=1024, logits_dtype=torch.float32):
+                                  chunk_rows=2048, logits_dtype=torch.float32):
     """Scalar alpha * mean(ce) + beta * mean(tvd) of the lm_head logits, with
     autograd support for h_student and w_student (2-D bf16 tensors).
     ``logits_dtype`` is the element type of the logit blocks (float32 or
